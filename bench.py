@@ -1,0 +1,549 @@
+#!/usr/bin/env python3
+"""Benchmark of the Purlin copy/reduce datapath on GB300.
+
+One step = one pass of the hot path over the headline workload: ReduceScatter
+then AllGather over R=8 virtual ranks, bf16, 64 MiB per rank input (8
+partitions of 8 MiB), N(0,1) values, binary32 accumulation in rank order.  The
+inputs (512 MiB) are larger than L2, so no flush is needed between steps.
+
+Prints ONE JSON line (rank 0).  ``value`` is effective GB/s: the algorithmic
+bytes (read + written) of all ranks' steps divided by the max-over-ranks device
+time.  Also reported: per-collective GB/s and roofline fraction, the AllReduce
+latency at 4 KiB per rank, the end-to-end figure through host buffers, the CPU
+oracle as a baseline, clocks sampled during the timed region.
+
+``--impl reference`` times the CPU oracle instead (the reference arm: the
+pages publish no code, so the oracle written from them stands in).
+Under torchrun, every rank runs an independent replica on its own GPU
+(the collective does not shard across GPUs).
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "effective HBM GB/s (% of GB300 peak) per collective @R=8; µs at 4 KiB/rank"
+UNIT = "GB/s"
+WORKLOAD = "rs_ag_r8_bf16"
+R = 8
+BYTES_PER_RANK = 64 << 20
+ELEMS_PER_RANK = BYTES_PER_RANK // 2
+PART = ELEMS_PER_RANK // R
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["purlin", "reference"], default="purlin")
+    ap.add_argument("--variant", choices=["zs", "staged"], default="zs")
+    ap.add_argument("--chunk", type=int, default=0, help="SNAC chunk bytes (0 = auto)")
+    ap.add_argument("--depth", type=int, default=0, help="SNAC ring depth (0 = auto)")
+    ap.add_argument("--ctas", type=int, default=0, help="CTAs / channels (0 = auto)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------- environment
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def cpu_model():
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu part")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return os.uname().machine
+
+
+class ClockSampler:
+    """SM clock and clock-event reasons during the timed region (NVML via
+    ctypes every few ms; nvidia-smi as a fallback).  Read-only."""
+
+    REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+               0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+               0x100: "display_clock_setting"}
+
+    def __init__(self, torch_device):
+        self.samples = []
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self._thread = None
+        self._proc = None
+        self._nvml = None
+        self._h = ctypes.c_void_p()
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                raise OSError("nvmlInit failed")
+            got = False
+            bus = self._pci_bus_id(torch_device)
+            if bus:
+                got = nv.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(self._h)) == 0
+            if not got and nv.nvmlDeviceGetHandleByIndex_v2(0, ctypes.byref(self._h)) != 0:
+                raise OSError("no NVML handle")
+            mx = ctypes.c_uint()
+            if nv.nvmlDeviceGetMaxClockInfo(self._h, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = mx.value
+            self._reasons_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(nv, "nvmlDeviceGetCurrentClocksThrottleReasons")
+            self._nvml = nv
+        except (OSError, AttributeError):
+            self._nvml = None
+
+    @staticmethod
+    def _pci_bus_id(dev):
+        try:
+            import torch
+            p = torch.cuda.get_device_properties(dev)
+            return "%08x:%02x:%02x.0" % (p.pci_domain_id, p.pci_bus_id, p.pci_device_id)
+        except Exception:
+            return None
+
+    def _loop(self):
+        mhz = ctypes.c_uint()
+        reasons = ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            if self._nvml.nvmlDeviceGetClockInfo(self._h, 1, ctypes.byref(mhz)) == 0 and \
+                    self._reasons_fn(self._h, ctypes.byref(reasons)) == 0:
+                self.samples.append((mhz.value, reasons.value))
+            self._stop.wait(0.005)
+
+    def start(self):
+        if self._nvml is not None:
+            self._thread = threading.Thread(target=self._loop, daemon=True)
+            self._thread.start()
+        else:
+            try:
+                self._proc = subprocess.Popen(
+                    ["nvidia-smi", "--query-gpu=clocks.sm,clocks.max.sm,clocks_event_reasons.active",
+                     "--format=csv,noheader,nounits", "-lms", "100"],
+                    stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            except OSError:
+                self._proc = None
+
+    def stop(self):
+        if self._thread is not None:
+            self._stop.set()
+            self._thread.join()
+        if self._proc is not None:
+            self._proc.terminate()
+            out, _ = self._proc.communicate()
+            for line in out.splitlines():
+                try:
+                    sm, mx, rs = [v.strip() for v in line.split(",")]
+                    self.samples.append((int(sm), int(rs, 16)))
+                    self.max_mhz = int(mx)
+                except ValueError:
+                    pass
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0}
+        seen = 0
+        for _, rs in self.samples:
+            seen |= rs
+        names = [n for bit, n in self.REASONS.items() if seen & bit and n != "gpu_idle"]
+        return {"sm_mhz": statistics.median(m for m, _ in self.samples),
+                "sm_max_mhz": self.max_mhz, "reasons": names, "samples": len(self.samples)}
+
+
+# ------------------------------------------------------------------ distributed
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def dist_init(world, local, backend):
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group(backend=backend)
+
+
+def barrier(world, device=None):
+    if world > 1:
+        import torch.distributed as dist
+        if device is not None:
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def max_over_ranks(world, value, device=None):
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------- the workload
+
+def step_bytes():
+    """Algorithmic bytes of one step: RS reads R*N*e, writes N*e; AG reads N*e,
+    writes R*N*e (N*e = 64 MiB summed over the 8 partitions)."""
+    rs = (R + 1) * BYTES_PER_RANK
+    ag = (R + 1) * BYTES_PER_RANK
+    return rs, ag
+
+
+def host_bits(t):
+    import numpy as np
+    import torch
+    t = t.detach().cpu().contiguous()
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def run_cpu_oracle(xh, budget_s, max_reps=20):
+    """The oracle as it stands (single-threaded C) on full steps of the
+    workload; repeated until `budget_s` seconds of CPU work."""
+    import oracle
+    counts = [PART] * R
+    reps, t0, y, z = 0, time.perf_counter(), None, None
+    while True:
+        y = oracle.reduce_scatter(xh, counts, dtype="bf16")
+        z = oracle.all_gather(y)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or reps >= max_reps:
+            break
+    rs, ag = step_bytes()
+    return {"value": reps * (rs + ag) / el / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{reps} full step(s) of the workload (RS then AG, R=8, 8 x 64 MiB bf16) "
+                      f"in {el:.1f} s, single-threaded C, {cpu_model()}",
+            "seconds": el}, y, z
+
+
+def bench_reference(args):
+    """The reference arm: the CPU oracle timed on the host cores."""
+    world, rank, local = dist_setup(args)
+    if rank != 0:
+        return
+    import numpy as np
+    import workloads
+    import torch
+    x = workloads.rank_buffers(WORKLOAD, R, ELEMS_PER_RANK, "bf16", device="cpu")
+    xh = [host_bits(t) for t in x]
+    warm = max(0, args.warmup)
+    import oracle
+    oracle.build()
+    for _ in range(min(warm, 1)):
+        run_cpu_oracle(xh, 0.0, max_reps=1)
+    steps = max(1, args.steps)
+    # each timed step is one full step of the workload; bounded to a few minutes
+    steps = min(steps, 60)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        run_cpu_oracle(xh, 0.0, max_reps=1)
+    el = time.perf_counter() - t0
+    rs, ag = step_bytes()
+    value = steps * (rs + ag) / el / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": steps, "warmup": warm, "ms_per_step": el / steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": "ReduceScatter then AllGather, R=8 virtual ranks, bf16, "
+                               "64 MiB per rank, N(0,1)", "R": R, "bytes_per_rank": BYTES_PER_RANK},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"{steps} full step(s), single-threaded C, {cpu_model()}"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "note": "the pages publish no code; the CPU oracle written from them is the reference arm",
+    }
+    print(json.dumps(line), flush=True)
+
+
+def traffic_from_profiles(kernel_key):
+    """Per-launch DRAM bytes of a kernel from the committed ncu summary, if it
+    was taken on the current kernel sources (else None)."""
+    import hashlib
+    src = os.path.join(ROOT, "reduce_datapath_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(src)):
+        with open(os.path.join(src, f), "rb") as fh:
+            h.update(fh.read())
+    digest = h.hexdigest()[:16]
+    pdir = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(pdir):
+        return None, digest
+    for f in sorted(os.listdir(pdir)):
+        if not f.endswith((".md", ".txt")):
+            continue
+        with open(os.path.join(pdir, f)) as fh:
+            for line in fh:
+                # "traffic: <kernel_key> <bytes_per_launch> sources=<digest>"
+                parts = line.strip().strip("`").split()
+                if len(parts) == 4 and parts[0] == "traffic:" and parts[1] == kernel_key \
+                        and parts[3] == f"sources={digest}":
+                    return int(parts[2]), digest
+    return None, digest
+
+
+def bench_purlin(args):
+    import numpy as np
+    import torch
+
+    import reduce_datapath_gb300 as rd
+    import workloads
+
+    world, rank, local = dist_setup(args)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist_init(world, local, "nccl")
+    rd.build() if rank == 0 else None
+    barrier(world, dev)
+    rd.lib()
+
+    peak, peak_kind = measured_peaks()
+    stream = torch.cuda.Stream(device=dev)
+    h = rd.purlin_create(R, 0, local)
+    variant = rd.VARIANT_ZS if args.variant == "zs" else rd.VARIANT_STAGED
+    rd.purlin_set_policy(h, args.chunk, args.depth, args.ctas, variant)
+
+    x = workloads.rank_buffers(WORKLOAD, R, ELEMS_PER_RANK, "bf16", device=dev)
+    y = [torch.empty(PART, dtype=torch.bfloat16, device=dev) for _ in range(R)]
+    z = [torch.empty(ELEMS_PER_RANK, dtype=torch.bfloat16, device=dev) for _ in range(R)]
+    counts = [PART] * R
+    torch.cuda.synchronize()
+
+    def rs():
+        rd.purlin_reduce_scatter(h, x, y, counts, None, "bf16", stream=stream)
+
+    def ag():
+        rd.purlin_all_gather(h, y, z, counts, None, "bf16", stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            rs()
+            ag()
+    torch.cuda.synchronize()
+    rs_info = None
+    rs()
+    rs_info = rd.purlin_last_launch(h)
+    ag()
+    ag_info = rd.purlin_last_launch(h)
+    torch.cuda.synchronize()
+
+    K = max(1, args.steps)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    clocks = ClockSampler(dev)
+    barrier(world, dev)
+    torch.cuda.synchronize()
+    clocks.start()
+    for i in range(K):
+        ev[i][0].record(stream)
+        rs()
+        ev[i][1].record(stream)
+        ag()
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    clocks.stop()
+    barrier(world, dev)
+    total_ms = ev[0][0].elapsed_time(ev[K - 1][2])
+    rs_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
+    ag_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
+    status = rd.purlin_query_status(h)
+    if status != rd.OK:
+        raise RuntimeError("device status: " + rd.purlin_status_string(status))
+    launches = K * (rs_info["kernels"] + ag_info["kernels"])
+    max_ms = max_over_ranks(world, total_ms, dev)
+    rs_b, ag_b = step_bytes()
+    value = world * K * (rs_b + ag_b) / (max_ms / 1e3) / 1e9
+
+    rs_avg = sum(rs_ms) / K
+    ag_avg = sum(ag_ms) / K
+    per = {
+        "reduce_scatter": {"us": rs_avg * 1e3, "gbs": rs_b / (rs_avg / 1e3) / 1e9,
+                           "bytes": rs_b, "grid": rs_info["grid"]},
+        "all_gather": {"us": ag_avg * 1e3, "gbs": ag_b / (ag_avg / 1e3) / 1e9,
+                       "bytes": ag_b, "grid": ag_info["grid"]},
+    }
+    for v in per.values():
+        v["frac_of_peak"] = v["gbs"] / peak
+        v["sm_bound"] = min(v["grid"], rs_info["sms"])
+    dom = "reduce_scatter" if rs_avg >= ag_avg else "all_gather"
+    kernel_key = ("zs_reduce" if dom == "reduce_scatter" else "zs_copy") \
+        if args.variant == "zs" else "snac"
+    traffic, digest = traffic_from_profiles(f"{kernel_key}:{WORKLOAD}")
+    roofline = {"bound": "hbm", "achieved": per[dom]["gbs"], "peak": peak, "unit": "GB/s",
+                "frac": per[dom]["gbs"] / peak, "traffic": traffic, "kernel": dom,
+                "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs, copy burst)"
+                if peak_kind == "measured" else "fallback 6.8 TB/s",
+                "algorithmic_bytes_per_launch": per[dom]["bytes"]}
+
+    # ---- AllReduce latency at 4 KiB per rank (R=8 bf16, 2048 elements)
+    lat = allreduce_latency(rd, torch, dev, stream, variant)
+
+    # ---- end to end: inputs from pinned host memory, outputs back to it
+    e2e = bench_e2e(args, rd, torch, h, x, y, z, counts, stream)
+
+    # ---- CPU oracle baseline and a bit-exact check of this run's result
+    cpu = None
+    parity = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        xh = [host_bits(t) for t in x]
+        cpu, want_y, want_z = run_cpu_oracle(xh, args.cpu_seconds)
+        cpu.pop("seconds", None)
+        rs()
+        ag()
+        torch.cuda.synchronize()
+        parity = all(np.array_equal(host_bits(y[k]), want_y[k]) for k in range(R)) and \
+            all(np.array_equal(host_bits(z[k]), want_z[k]) for k in range(R))
+
+    rd.purlin_destroy(h)
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": max(3, args.warmup), "ms_per_step": max_ms / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "ReduceScatter then AllGather, R=8 virtual ranks, bf16, 64 MiB "
+                               "per rank (8 partitions of 8 MiB), N(0,1), fp32 accumulation "
+                               "in rank order",
+                   "R": R, "bytes_per_rank": BYTES_PER_RANK, "variant": args.variant,
+                   "parallelism": f"replicas x{world}",
+                   "l2": "inputs 512 MiB > L2 per step; no flush"},
+        "roofline": roofline,
+        "per_collective": per,
+        "allreduce_4KiB": lat,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+        "parity_vs_oracle": parity,
+        "gpu_launches": launches,
+        "clocks": clocks.summary(),
+        "sources": digest,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def allreduce_latency(rd, torch, dev, stream, variant):
+    n = 2048   # 4 KiB of bf16 per rank
+    h = rd.purlin_create(R, 0, dev.index)
+    rd.purlin_set_policy(h, 0, 0, 0, variant)
+    x = [torch.randn(n, device=dev).to(torch.bfloat16) for _ in range(R)]
+    o = [torch.empty_like(t) for t in x]
+    with torch.cuda.stream(stream):
+        for _ in range(20):
+            rd.purlin_all_reduce(h, x, o, n, "bf16", stream=stream)
+    torch.cuda.synchronize()
+    # one launch, device time between two events
+    single = []
+    for _ in range(200):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        rd.purlin_all_reduce(h, x, o, n, "bf16", stream=stream)
+        b.record(stream)
+        b.synchronize()
+        single.append(a.elapsed_time(b) * 1e3)
+    # 1000 launches back to back from the host
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(1000):
+        rd.purlin_all_reduce(h, x, o, n, "bf16", stream=stream)
+    b.record(stream)
+    torch.cuda.synchronize()
+    b2b = a.elapsed_time(b) * 1e3 / 1000
+    # CUDA graph of 100 launches, replayed 10 times
+    graph_us = None
+    try:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(100):
+                rd.purlin_all_reduce(h, x, o, n, "bf16")
+        g.replay()
+        torch.cuda.synchronize()
+        a.record(stream)
+        for _ in range(10):
+            g.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        graph_us = a.elapsed_time(b) * 1e3 / 1000
+    except Exception as e:  # capture is optional for the latency figure
+        graph_us = f"capture failed: {e}"
+    torch.cuda.synchronize()
+    rd.purlin_destroy(h)
+    return {"us_graph_per_launch": graph_us, "us_back_to_back": b2b,
+            "us_single_event_median": statistics.median(single), "R": R, "bytes_per_rank": 4096}
+
+
+def bench_e2e(args, rd, torch, h, x, y, z, counts, stream):
+    xh = [torch.empty_like(t, device="cpu").pin_memory() for t in x]
+    zh = [torch.empty_like(t, device="cpu").pin_memory() for t in z]
+    for a, b in zip(xh, x):
+        a.copy_(b)
+    torch.cuda.synchronize()
+
+    def step():
+        for a, b in zip(x, xh):
+            a.copy_(b, non_blocking=True)
+        rd.purlin_reduce_scatter(h, x, y, counts, None, "bf16", stream=stream)
+        rd.purlin_all_gather(h, y, z, counts, None, "bf16", stream=stream)
+        for a, b in zip(zh, z):
+            a.copy_(b, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            step()
+        torch.cuda.synchronize()
+        K = max(1, args.e2e_steps)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(K):
+            step()
+        b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / K
+    rs_b, ag_b = step_bytes()
+    return {"value": (rs_b + ag_b) / (ms / 1e3) / 1e9, "unit": UNIT,
+            "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in xh),
+            "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in zh),
+            "ms_per_step": ms, "steps": K}
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        bench_reference(args)
+    else:
+        bench_purlin(args)
+
+
+if __name__ == "__main__":
+    main()

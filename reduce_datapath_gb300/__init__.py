@@ -1,0 +1,293 @@
+"""Python binding of the Purlin collective datapath C ABI (``include/purlin.h``).
+
+Argument marshalling only: every entry point forwards to ``libpurlin.so``, whose
+CUDA kernels do all the work.  There is no Python or CPU fallback: if the
+library is missing, the first call raises ``PurlinLibraryError``.
+
+The functions keep the C names.  Buffers are passed as sequences of R device
+tensors (anything with ``data_ptr()``) or raw integer device addresses; counts
+and displacements as sequences of ints (R, or R*R for AllToAllV, row-major);
+``dtype`` as ``"f32" | "bf16" | "f16" | "u8"`` or a torch dtype; ``stream`` as a
+``torch.cuda.Stream``, a raw ``cudaStream_t`` integer, or None for torch's current
+stream.  A non-OK status raises ``PurlinError`` carrying the status code.
+
+Page: "Purlin: Separating Orchestration from the Datapath of Collectives"
+(abstract; Figure 4 layouts; Figure 6 composed AllReduce; Table 2 "(V)").
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "lib", "libpurlin.so")
+
+# purlin_status_t
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_OOM = range(6)
+# purlin_dtype_t
+F32, BF16, F16, U8 = range(4)
+DTYPES = {"f32": F32, "bf16": BF16, "f16": F16, "u8": U8}
+ELEM_BYTES = {F32: 4, BF16: 2, F16: 2, U8: 1}
+# purlin_op_t
+OP_COPY, OP_SUM = 0, 1
+# purlin_variant_t
+VARIANT_AUTO, VARIANT_ZS, VARIANT_STAGED = 0, 1, 2
+# purlin_order_t
+ORDER_FIXED, ORDER_TREE = 0, 1
+# purlin_collective_t
+COLL_REDUCE_SCATTER, COLL_ALL_GATHER, COLL_ALL_REDUCE, COLL_ALL_TO_ALL_V = range(4)
+MAX_RANKS = 8
+
+# Every symbol the headers under include/ declare.
+EXPORTED = (
+    "purlin_create", "purlin_destroy", "purlin_reduce_scatter", "purlin_all_gather",
+    "purlin_all_reduce", "purlin_all_to_all", "purlin_all_to_all_v", "purlin_set_policy",
+    "purlin_set_reduce_order", "purlin_set_timeout", "purlin_query_status",
+    "purlin_last_launch", "purlin_status_string", "purlin_version", "purlin_plan_segments",
+    "purlin_debug_inject",
+)
+
+
+class PurlinLibraryError(RuntimeError):
+    """libpurlin.so is missing or does not load."""
+
+
+class PurlinError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_text(status)} (status {status})")
+
+
+class LaunchInfo(ctypes.Structure):
+    _fields_ = [("variant", ctypes.c_int), ("kernels", ctypes.c_int), ("grid", ctypes.c_int),
+                ("block", ctypes.c_int), ("sms", ctypes.c_int), ("depth", ctypes.c_int),
+                ("chunk_bytes", ctypes.c_size_t), ("bytes_moved", ctypes.c_size_t)]
+
+    def as_dict(self):
+        return {f: getattr(self, f) for f, _ in self._fields_}
+
+
+class Segment(ctypes.Structure):
+    _fields_ = [("src_off", ctypes.c_uint64), ("dst_off", ctypes.c_uint64),
+                ("bytes", ctypes.c_uint64), ("src_rank", ctypes.c_int32),
+                ("dst_rank", ctypes.c_int32), ("unit", ctypes.c_int32),
+                ("tile0", ctypes.c_uint32)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile libpurlin.so in-tree (nvcc, sm_103a)."""
+    from . import _build
+    return _build.build(force=force)
+
+
+def lib():
+    """The loaded libpurlin.so (raises PurlinLibraryError if it is not built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise PurlinLibraryError(
+                f"{LIB_PATH} is not built; run reduce_datapath_gb300.build() first")
+        try:
+            L = ctypes.CDLL(LIB_PATH)
+        except OSError as e:
+            raise PurlinLibraryError(f"cannot load {LIB_PATH}: {e}") from e
+        vp, sz, i32, u64 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_uint64
+        pp = ctypes.POINTER(ctypes.c_void_p)
+        szp = ctypes.POINTER(ctypes.c_size_t)
+        u64p = ctypes.POINTER(ctypes.c_uint64)
+        sigs = {
+            "purlin_create": [ctypes.POINTER(vp), i32, sz, i32],
+            "purlin_destroy": [vp],
+            "purlin_reduce_scatter": [vp, pp, pp, szp, szp, i32, i32, vp],
+            "purlin_all_gather": [vp, pp, pp, szp, szp, i32, vp],
+            "purlin_all_reduce": [vp, pp, pp, sz, i32, i32, vp],
+            "purlin_all_to_all": [vp, pp, pp, sz, i32, vp],
+            "purlin_all_to_all_v": [vp, pp, pp, szp, szp, szp, i32, vp],
+            "purlin_set_policy": [vp, sz, i32, i32, i32],
+            "purlin_set_reduce_order": [vp, i32],
+            "purlin_set_timeout": [vp, u64],
+            "purlin_query_status": [vp],
+            "purlin_last_launch": [vp, ctypes.POINTER(LaunchInfo)],
+            "purlin_status_string": [i32],
+            "purlin_version": [],
+            "purlin_plan_segments": [i32, i32, u64p, u64p, szp, szp, szp, sz, i32, i32,
+                                     ctypes.POINTER(Segment), i32, ctypes.POINTER(i32),
+                                     ctypes.POINTER(ctypes.c_uint32)],
+            "purlin_debug_inject": [vp, i32],
+        }
+        for name, args in sigs.items():
+            fn = getattr(L, name)
+            fn.argtypes = args
+            fn.restype = i32
+        L.purlin_status_string.restype = ctypes.c_char_p
+        _lib = L
+        return L
+
+
+def status_text(status: int) -> str:
+    try:
+        return lib().purlin_status_string(int(status)).decode()
+    except PurlinLibraryError:
+        return "status %d" % status
+
+
+# ------------------------------------------------------------------ marshalling
+
+def _check(status: int, where: str):
+    if status != OK:
+        raise PurlinError(status, where)
+
+
+def _ptr(x) -> int:
+    if x is None:
+        return 0
+    if hasattr(x, "data_ptr"):
+        return int(x.data_ptr())
+    return int(x)
+
+
+def _ptrs(bufs):
+    vals = [_ptr(b) for b in bufs]
+    return (ctypes.c_void_p * len(vals))(*vals)
+
+
+def _sizes(vals):
+    if vals is None:
+        return None
+    flat = [int(v) for v in (vals.reshape(-1).tolist() if hasattr(vals, "reshape") else vals)]
+    return (ctypes.c_size_t * len(flat))(*flat)
+
+
+def _dtype(dt) -> int:
+    if isinstance(dt, int):
+        return dt
+    if isinstance(dt, str):
+        return DTYPES[dt]
+    import torch
+    table = {torch.float32: F32, torch.bfloat16: BF16, torch.float16: F16, torch.uint8: U8,
+             torch.int8: U8}
+    fp8 = [getattr(torch, n) for n in ("float8_e4m3fn", "float8_e5m2") if hasattr(torch, n)]
+    for t in fp8:
+        table[t] = U8
+    return table[dt]
+
+
+def _op(op) -> int:
+    if isinstance(op, int):
+        return op
+    return {"sum": OP_SUM, "copy": OP_COPY}[op]
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        import torch
+        return int(torch.cuda.current_stream().cuda_stream)
+    if hasattr(stream, "cuda_stream"):
+        return int(stream.cuda_stream)
+    return int(stream)
+
+
+# ------------------------------------------------------------------- the ABI
+
+def purlin_version() -> int:
+    return lib().purlin_version()
+
+
+def purlin_create(R: int, staging_bytes: int = 0, device: int | None = None) -> int:
+    if device is None:
+        import torch
+        device = torch.cuda.current_device()
+    h = ctypes.c_void_p()
+    _check(lib().purlin_create(ctypes.byref(h), int(R), int(staging_bytes), int(device)),
+           "purlin_create")
+    return h.value
+
+
+def purlin_destroy(h) -> None:
+    _check(lib().purlin_destroy(h), "purlin_destroy")
+
+
+def purlin_reduce_scatter(h, ins, outs, recv_counts, in_displs=None, dtype="bf16", op="sum",
+                          stream=None) -> None:
+    _check(lib().purlin_reduce_scatter(h, _ptrs(ins), _ptrs(outs), _sizes(recv_counts),
+                                       _sizes(in_displs), _dtype(dtype), _op(op),
+                                       _stream(stream)), "purlin_reduce_scatter")
+
+
+def purlin_all_gather(h, ins, outs, counts, out_displs=None, dtype="bf16", stream=None) -> None:
+    _check(lib().purlin_all_gather(h, _ptrs(ins), _ptrs(outs), _sizes(counts),
+                                   _sizes(out_displs), _dtype(dtype), _stream(stream)),
+           "purlin_all_gather")
+
+
+def purlin_all_reduce(h, ins, outs, count, dtype="bf16", op="sum", stream=None) -> None:
+    _check(lib().purlin_all_reduce(h, _ptrs(ins), _ptrs(outs), int(count), _dtype(dtype),
+                                   _op(op), _stream(stream)), "purlin_all_reduce")
+
+
+def purlin_all_to_all(h, ins, outs, count_per_pair, dtype="bf16", stream=None) -> None:
+    _check(lib().purlin_all_to_all(h, _ptrs(ins), _ptrs(outs), int(count_per_pair),
+                                   _dtype(dtype), _stream(stream)), "purlin_all_to_all")
+
+
+def purlin_all_to_all_v(h, ins, outs, send_counts, send_displs=None, recv_displs=None,
+                        dtype="bf16", stream=None) -> None:
+    _check(lib().purlin_all_to_all_v(h, _ptrs(ins), _ptrs(outs), _sizes(send_counts),
+                                     _sizes(send_displs), _sizes(recv_displs), _dtype(dtype),
+                                     _stream(stream)), "purlin_all_to_all_v")
+
+
+def purlin_set_policy(h, chunk_bytes=0, depth=0, ctas=0, variant=VARIANT_AUTO) -> None:
+    _check(lib().purlin_set_policy(h, int(chunk_bytes), int(depth), int(ctas), int(variant)),
+           "purlin_set_policy")
+
+
+def purlin_set_reduce_order(h, order) -> None:
+    _check(lib().purlin_set_reduce_order(h, int(order)), "purlin_set_reduce_order")
+
+
+def purlin_set_timeout(h, timeout_ns) -> None:
+    _check(lib().purlin_set_timeout(h, int(timeout_ns)), "purlin_set_timeout")
+
+
+def purlin_query_status(h) -> int:
+    """Device status word (read and cleared); returns the code, does not raise."""
+    return int(lib().purlin_query_status(h))
+
+
+def purlin_last_launch(h) -> dict:
+    info = LaunchInfo()
+    _check(lib().purlin_last_launch(h, ctypes.byref(info)), "purlin_last_launch")
+    return info.as_dict()
+
+
+def purlin_status_string(status) -> str:
+    return lib().purlin_status_string(int(status)).decode()
+
+
+def purlin_debug_inject(h, what: int) -> None:
+    _check(lib().purlin_debug_inject(h, int(what)), "purlin_debug_inject")
+
+
+def purlin_plan_segments(coll, R, in_addr, out_addr, counts=None, displs_a=None, displs_b=None,
+                         count=0, dtype="bf16", max_unit=32, max_segs=256):
+    """Host-only plan of one collective (no GPU needed); returns (segments, ntiles)."""
+    segs = (Segment * max_segs)()
+    n = ctypes.c_int(0)
+    nt = ctypes.c_uint32(0)
+    ia = (ctypes.c_uint64 * len(in_addr))(*[int(a) for a in in_addr])
+    oa = (ctypes.c_uint64 * len(out_addr))(*[int(a) for a in out_addr])
+    _check(lib().purlin_plan_segments(int(coll), int(R), ia, oa, _sizes(counts),
+                                      _sizes(displs_a), _sizes(displs_b), int(count),
+                                      _dtype(dtype), int(max_unit), segs, max_segs,
+                                      ctypes.byref(n), ctypes.byref(nt)),
+           "purlin_plan_segments")
+    out = [{f: getattr(segs[i], f) for f, _ in Segment._fields_} for i in range(n.value)]
+    return out, nt.value

@@ -1,0 +1,529 @@
+// capi.cpp -- the C ABI (include/purlin.h): argument checks, handle, policy,
+// and dispatch of each collective to the layout module and the Atom kernels.
+//
+// Page "Purlin: Separating Orchestration from the Datapath of Collectives":
+// the layers of Figure 1 map onto this file as
+//   collective naming (abstract, Figure 4)  -> the entry points below,
+//   codesign policies (Figure 1)            -> choose_variant / grid sizing,
+//   SNAC (abstract, Figure 6)               -> snac_kernels.cu,
+//   Atom (abstract, Table 4)                -> atom.cuh, zs_kernels.cu.
+#include "purlin.h"
+#include "purlin_layout.h"
+#include "purlin_debug.h"
+
+#include <algorithm>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+
+#include "internal.h"
+#include "plan.h"
+#include "snac.h"
+
+using namespace purlin;
+
+struct purlin_handle {
+    int R = 0;
+    int device = 0;
+    int sms = 0;
+    size_t l2_bytes = 0;
+    // SNAC staging ring, flags and the device status word (owned).
+    size_t staging_bytes = 0;
+    char* staging = nullptr;
+    uint64_t* flags = nullptr;
+    size_t flag_words = 0;
+    int* status = nullptr;
+    uint64_t call_seq = 0;  // SNAC epoch: grows by one per staged call
+    // policy (0 = automatic)
+    size_t chunk_bytes = 0;
+    int depth = 0;
+    int ctas = 0;
+    int variant = PURLIN_VARIANT_AUTO;
+    int order = PURLIN_ORDER_FIXED;
+    uint64_t timeout_ns = 1000000000ull;
+    int max_unit_log2 = 5;
+    int inject = 0;  // purlin_debug_inject, one staged call
+    purlin_launch_info_t last{};
+};
+
+namespace {
+
+constexpr int kVersionMajor = 1;
+constexpr int kVersionMinor = 0;
+constexpr size_t kDefaultStaging = 32ull << 20;  // well below the 129 MB L2
+constexpr size_t kFlagWords = 8192;
+
+struct DeviceGuard {
+    int prev = -1;
+    bool ok = true;
+    explicit DeviceGuard(int dev)
+    {
+        if (cudaGetDevice(&prev) != cudaSuccess) { ok = false; return; }
+        if (prev != dev && cudaSetDevice(dev) != cudaSuccess) ok = false;
+    }
+    ~DeviceGuard()
+    {
+        int cur = -1;
+        if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+    }
+};
+
+size_t elem_bytes(int dtype)
+{
+    switch (dtype) {
+    case kF32: return 4;
+    case kBF16: return 2;
+    case kF16: return 2;
+    case kU8: return 1;
+    default: return 0;
+    }
+}
+
+bool overlaps(uint64_t a, uint64_t alen, uint64_t b, uint64_t blen)
+{
+    if (alen == 0 || blen == 0) return false;
+    return a < b + blen && b < a + alen;
+}
+
+// Pointer, alignment and aliasing rules of purlin.h for one call.
+purlin_status_t check_buffers(Coll coll, int R, const uint64_t* in, const uint64_t* out,
+                              const uint64_t* in_ext, const uint64_t* out_ext, size_t esz,
+                              bool reduce, const size_t* counts, const size_t* da)
+{
+    for (int r = 0; r < R; ++r) {
+        if ((in_ext[r] && !in[r]) || (out_ext[r] && !out[r])) return PURLIN_ERR_INVALID_ARG;
+        if (in[r] + in_ext[r] < in[r] || out[r] + out_ext[r] < out[r]) return PURLIN_ERR_INVALID_ARG;
+        if (reduce && ((in_ext[r] && in[r] % esz) || (out_ext[r] && out[r] % esz)))
+            return PURLIN_ERR_INVALID_ARG;
+    }
+    // Output blocks inside one buffer must not overlap each other.
+    if (coll == Coll::AllGather) {
+        for (int a = 0; a < R; ++a)
+            for (int b = a + 1; b < R; ++b) {
+                uint64_t sa = (da ? da[a] : 0), sb = (da ? da[b] : 0);
+                if (!da) {
+                    for (int m = 0; m < a; ++m) sa += counts[m];
+                    for (int m = 0; m < b; ++m) sb += counts[m];
+                }
+                if (overlaps(sa, counts[a], sb, counts[b])) return PURLIN_ERR_INVALID_ARG;
+            }
+    }
+    // Outputs are pairwise disjoint.
+    for (int a = 0; a < R; ++a)
+        for (int b = a + 1; b < R; ++b)
+            if (overlaps(out[a], out_ext[a], out[b], out_ext[b])) return PURLIN_ERR_INVALID_ARG;
+    // An output may meet an input only in the in-place forms of purlin.h.
+    for (int r = 0; r < R; ++r)
+        for (int j = 0; j < R; ++j) {
+            if (!overlaps(in[r], in_ext[r], out[j], out_ext[j])) continue;
+            bool allowed = false;
+            if (r == j) {
+                if (coll == Coll::AllReduce) {
+                    allowed = in[r] == out[r];
+                } else if (coll == Coll::ReduceScatter) {
+                    uint64_t d = 0;
+                    if (da) d = da[r];
+                    else for (int m = 0; m < r; ++m) d += counts[m];
+                    allowed = out[r] == in[r] + d * esz;
+                } else if (coll == Coll::AllGather) {
+                    uint64_t d = 0;
+                    if (da) d = da[r];
+                    else for (int m = 0; m < r; ++m) d += counts[m];
+                    allowed = in[r] == out[r] + d * esz;
+                }
+            }
+            if (!allowed) return PURLIN_ERR_INVALID_ARG;
+        }
+    return PURLIN_OK;
+}
+
+template <int MAXSEG>
+purlin_status_t make_params(ZsParams<MAXSEG>& p, const Piece* pieces, int npieces, int R,
+                            const uint64_t* in, const uint64_t* out, size_t esz, bool reduce,
+                            int max_unit_log2)
+{
+    std::memset(&p, 0, sizeof(p));
+    for (int r = 0; r < R; ++r) {
+        p.in[r] = reinterpret_cast<const char*>(in[r]);
+        p.out[r] = reinterpret_cast<char*>(out[r]);
+    }
+    p.R = (uint32_t)R;
+    p.unroll = reduce ? kUnrollReduce : kUnrollCopy;
+    uint32_t ntiles = 0;
+    int n = layout_segments(pieces, npieces, R, in, out, esz, reduce, max_unit_log2, p.seg,
+                            MAXSEG, &ntiles);
+    if (n < 0) return PURLIN_ERR_UNSUPPORTED;
+    p.nseg = (uint32_t)n;
+    p.ntiles = ntiles;
+    return PURLIN_OK;
+}
+
+size_t algorithmic_bytes(Coll coll, int R, const size_t* counts, size_t count, size_t esz)
+{
+    uint64_t total = 0;
+    switch (coll) {
+    case Coll::ReduceScatter:
+        for (int k = 0; k < R; ++k) total += counts[k];
+        return (size_t)((uint64_t)(R + 1) * total * esz);
+    case Coll::AllGather:
+        for (int k = 0; k < R; ++k) total += counts[k];
+        return (size_t)((uint64_t)(R + 1) * total * esz);
+    case Coll::AllReduce:
+        return (size_t)(2ull * R * count * esz);
+    case Coll::AllToAllV:
+        for (int i = 0; i < R * R; ++i) total += counts[i];
+        return (size_t)(2ull * total * esz);
+    }
+    return 0;
+}
+
+int zs_grid(const purlin_handle* h, uint32_t ntiles, int resident)
+{
+    if (ntiles == 0) return 0;
+    long g = h->ctas > 0 ? h->ctas : (long)h->sms * resident;
+    return (int)std::max<long>(1, std::min<long>(g, (long)ntiles));
+}
+
+bool wants_staged(const purlin_handle* h)
+{
+    return h->variant == PURLIN_VARIANT_STAGED;
+}
+
+purlin_status_t run(purlin_handle_t h, Coll coll, const void* const in_[], void* const out_[],
+                    const size_t* counts, const size_t* da, const size_t* db, size_t count,
+                    int dtype, bool reduce, purlin_stream_t stream)
+{
+    if (!h || !in_ || !out_) return PURLIN_ERR_INVALID_ARG;
+    if (coll != Coll::AllReduce && !counts) return PURLIN_ERR_INVALID_ARG;
+    const size_t esz = elem_bytes(dtype);
+    if (esz == 0) return PURLIN_ERR_INVALID_ARG;
+    if (reduce && dtype == kU8) return PURLIN_ERR_UNSUPPORTED;
+    const int R = h->R;
+
+    uint64_t in[kMaxRanks], out[kMaxRanks];
+    for (int r = 0; r < R; ++r) {
+        in[r] = reinterpret_cast<uint64_t>(in_[r]);
+        out[r] = reinterpret_cast<uint64_t>(out_[r]);
+    }
+    Piece pieces[kSegsLarge];
+    int np = layout_pieces(coll, R, counts, da, db, count, esz, pieces, kSegsLarge);
+    if (np < 0) return PURLIN_ERR_INVALID_ARG;
+    uint64_t in_ext[kMaxRanks], out_ext[kMaxRanks];
+    layout_extents(coll, R, counts, da, db, count, esz, in_ext, out_ext);
+    purlin_status_t st = check_buffers(coll, R, in, out, in_ext, out_ext, esz, reduce, counts, da);
+    if (st != PURLIN_OK) return st;
+    if (coll == Coll::AllToAllV) {
+        // received blocks inside one output must not overlap
+        for (int a = 0; a < np; ++a)
+            for (int b = a + 1; b < np; ++b)
+                if (pieces[a].dst == pieces[b].dst &&
+                    overlaps(pieces[a].dst_off, pieces[a].bytes, pieces[b].dst_off, pieces[b].bytes))
+                    return PURLIN_ERR_INVALID_ARG;
+    }
+
+    DeviceGuard guard(h->device);
+    if (!guard.ok) return PURLIN_ERR_CUDA;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+    purlin_launch_info_t info{};
+    info.sms = h->sms;
+    info.block = kThreads;
+    info.bytes_moved = algorithmic_bytes(coll, R, counts, count, esz);
+
+    if (wants_staged(h) && np > 0) {
+        SnacRequest rq{};
+        rq.coll = coll;
+        rq.R = R;
+        rq.dtype = dtype;
+        rq.order = h->order;
+        rq.esz = esz;
+        rq.pieces = pieces;
+        rq.npieces = np;
+        for (int r = 0; r < R; ++r) { rq.in[r] = in[r]; rq.out[r] = out[r]; }
+        SnacConfig cfg{};
+        cfg.staging = h->staging;
+        cfg.staging_bytes = h->staging_bytes;
+        cfg.flags = h->flags;
+        cfg.flag_words = h->flag_words;
+        cfg.status = h->status;
+        cfg.epoch = ++h->call_seq;
+        cfg.chunk_bytes = h->chunk_bytes;
+        cfg.depth = h->depth;
+        cfg.channels = h->ctas;
+        cfg.sms = h->sms;
+        cfg.timeout_ns = h->timeout_ns;
+        cfg.inject_skip_notify = h->inject;
+        h->inject = 0;
+        SnacLaunch sl{};
+        purlin_status_t ss = snac_run(rq, cfg, s, &sl);
+        if (ss != PURLIN_OK) return ss;
+        info.variant = PURLIN_VARIANT_STAGED;
+        info.kernels = sl.kernels;
+        info.grid = sl.grid;
+        info.block = sl.block;
+        info.depth = sl.depth;
+        info.chunk_bytes = sl.chunk_bytes;
+        h->last = info;
+        return PURLIN_OK;
+    }
+
+    info.variant = PURLIN_VARIANT_ZS;
+    cudaError_t ce = cudaSuccess;
+    if (coll == Coll::AllToAllV) {
+        static thread_local ZsParams<kSegsLarge> p;
+        st = make_params(p, pieces, np, R, in, out, esz, false, h->max_unit_log2);
+        if (st != PURLIN_OK) return st;
+        int grid = zs_grid(h, p.ntiles, zs_copy_resident_ctas(true, false));
+        if (grid > 0) ce = zs_copy_launch(p, false, grid, s);
+        info.grid = grid;
+        info.kernels = grid > 0;
+        info.chunk_bytes = tile_bytes(h->max_unit_log2, kUnrollCopy);
+    } else {
+        static thread_local ZsParams<kSegsSmall> p;
+        st = make_params(p, pieces, np, R, in, out, esz, reduce, h->max_unit_log2);
+        if (st != PURLIN_OK) return st;
+        bool fan_all = coll == Coll::AllGather || coll == Coll::AllReduce;
+        int grid;
+        if (reduce) {
+            grid = zs_grid(h, p.ntiles, zs_reduce_resident_ctas(dtype, h->order, fan_all));
+            if (grid > 0) ce = zs_reduce_launch(p, dtype, h->order, fan_all, grid, s);
+            info.chunk_bytes = tile_bytes(h->max_unit_log2, kUnrollReduce);
+        } else {
+            grid = zs_grid(h, p.ntiles, zs_copy_resident_ctas(false, fan_all));
+            if (grid > 0) ce = zs_copy_launch(p, fan_all, grid, s);
+            info.chunk_bytes = tile_bytes(h->max_unit_log2, kUnrollCopy);
+        }
+        info.grid = grid;
+        info.kernels = grid > 0;
+    }
+    if (ce != cudaSuccess) return PURLIN_ERR_CUDA;
+    h->last = info;
+    return PURLIN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int purlin_version(void) { return (kVersionMajor << 16) | kVersionMinor; }
+
+const char* purlin_status_string(purlin_status_t s)
+{
+    switch (s) {
+    case PURLIN_OK: return "ok";
+    case PURLIN_ERR_INVALID_ARG: return "invalid argument";
+    case PURLIN_ERR_UNSUPPORTED: return "unsupported request";
+    case PURLIN_ERR_CUDA: return "CUDA runtime error";
+    case PURLIN_ERR_TIMEOUT: return "device-side wait timed out";
+    case PURLIN_ERR_OOM: return "device out of memory";
+    }
+    return "unknown status";
+}
+
+purlin_status_t purlin_create(purlin_handle_t* out, int R, size_t staging_bytes, int device)
+{
+    if (!out) return PURLIN_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (R < 1 || R > PURLIN_MAX_RANKS || device < 0) return PURLIN_ERR_INVALID_ARG;
+    int ndev = 0;
+    if (cudaGetDeviceCount(&ndev) != cudaSuccess) return PURLIN_ERR_CUDA;
+    if (device >= ndev) return PURLIN_ERR_INVALID_ARG;
+    DeviceGuard guard(device);
+    if (!guard.ok) return PURLIN_ERR_CUDA;
+
+    purlin_handle* h = new (std::nothrow) purlin_handle();
+    if (!h) return PURLIN_ERR_OOM;
+    h->R = R;
+    h->device = device;
+    int l2 = 0;
+    if (cudaDeviceGetAttribute(&h->sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, device) != cudaSuccess) {
+        delete h;
+        return PURLIN_ERR_CUDA;
+    }
+    h->l2_bytes = (size_t)l2;
+    h->staging_bytes = staging_bytes ? (staging_bytes + 255) & ~(size_t)255 : kDefaultStaging;
+    h->flag_words = kFlagWords;
+    if (cudaMalloc(&h->staging, h->staging_bytes) != cudaSuccess ||
+        cudaMalloc(&h->flags, h->flag_words * sizeof(uint64_t)) != cudaSuccess ||
+        cudaMalloc(&h->status, sizeof(int)) != cudaSuccess) {
+        cudaGetLastError();
+        purlin_destroy(h);
+        return PURLIN_ERR_OOM;
+    }
+    if (cudaMemset(h->flags, 0, h->flag_words * sizeof(uint64_t)) != cudaSuccess ||
+        cudaMemset(h->status, 0, sizeof(int)) != cudaSuccess ||
+        cudaDeviceSynchronize() != cudaSuccess) {
+        purlin_destroy(h);
+        return PURLIN_ERR_CUDA;
+    }
+    if (const char* u = std::getenv("PURLIN_MAX_UNIT")) {
+        int v = std::atoi(u);
+        if (v == 16) h->max_unit_log2 = 4;
+        if (v == 32) h->max_unit_log2 = 5;
+    }
+    *out = h;
+    return PURLIN_OK;
+}
+
+purlin_status_t purlin_destroy(purlin_handle_t h)
+{
+    if (!h) return PURLIN_OK;
+    purlin_status_t st = PURLIN_OK;
+    {
+        DeviceGuard guard(h->device);
+        if (cudaDeviceSynchronize() != cudaSuccess) st = PURLIN_ERR_CUDA;
+        if (h->staging) cudaFree(h->staging);
+        if (h->flags) cudaFree(h->flags);
+        if (h->status) cudaFree(h->status);
+    }
+    delete h;
+    return st;
+}
+
+purlin_status_t purlin_reduce_scatter(purlin_handle_t h, const void* const in[], void* const out[],
+                                      const size_t recv_counts[], const size_t in_displs[],
+                                      purlin_dtype_t dtype, purlin_op_t op, purlin_stream_t stream)
+{
+    if (op == PURLIN_OP_COPY) return PURLIN_ERR_UNSUPPORTED;
+    if (op != PURLIN_OP_SUM) return PURLIN_ERR_INVALID_ARG;
+    return run(h, Coll::ReduceScatter, in, out, recv_counts, in_displs, nullptr, 0, dtype, true,
+               stream);
+}
+
+purlin_status_t purlin_all_gather(purlin_handle_t h, const void* const in[], void* const out[],
+                                  const size_t counts[], const size_t out_displs[],
+                                  purlin_dtype_t dtype, purlin_stream_t stream)
+{
+    return run(h, Coll::AllGather, in, out, counts, out_displs, nullptr, 0, dtype, false, stream);
+}
+
+purlin_status_t purlin_all_reduce(purlin_handle_t h, const void* const in[], void* const out[],
+                                  size_t count, purlin_dtype_t dtype, purlin_op_t op,
+                                  purlin_stream_t stream)
+{
+    if (op == PURLIN_OP_COPY) return PURLIN_ERR_UNSUPPORTED;
+    if (op != PURLIN_OP_SUM) return PURLIN_ERR_INVALID_ARG;
+    return run(h, Coll::AllReduce, in, out, nullptr, nullptr, nullptr, count, dtype, true, stream);
+}
+
+purlin_status_t purlin_all_to_all(purlin_handle_t h, const void* const in[], void* const out[],
+                                  size_t count_per_pair, purlin_dtype_t dtype,
+                                  purlin_stream_t stream)
+{
+    if (!h) return PURLIN_ERR_INVALID_ARG;
+    size_t counts[kMaxRanks * kMaxRanks];
+    for (int i = 0; i < h->R * h->R; ++i) counts[i] = count_per_pair;
+    return run(h, Coll::AllToAllV, in, out, counts, nullptr, nullptr, 0, dtype, false, stream);
+}
+
+purlin_status_t purlin_all_to_all_v(purlin_handle_t h, const void* const in[], void* const out[],
+                                    const size_t send_counts[], const size_t send_displs[],
+                                    const size_t recv_displs[], purlin_dtype_t dtype,
+                                    purlin_stream_t stream)
+{
+    return run(h, Coll::AllToAllV, in, out, send_counts, send_displs, recv_displs, 0, dtype, false,
+               stream);
+}
+
+purlin_status_t purlin_set_policy(purlin_handle_t h, size_t chunk_bytes, int depth, int ctas,
+                                  int variant)
+{
+    if (!h) return PURLIN_ERR_INVALID_ARG;
+    if (chunk_bytes % 16 || depth < 0 || depth > 8 || ctas < 0 || ctas > 65535 ||
+        variant < PURLIN_VARIANT_AUTO || variant > PURLIN_VARIANT_STAGED)
+        return PURLIN_ERR_INVALID_ARG;
+    h->chunk_bytes = chunk_bytes;
+    h->depth = depth;
+    h->ctas = ctas;
+    h->variant = variant;
+    return PURLIN_OK;
+}
+
+purlin_status_t purlin_set_reduce_order(purlin_handle_t h, int order)
+{
+    if (!h || (order != PURLIN_ORDER_FIXED && order != PURLIN_ORDER_TREE))
+        return PURLIN_ERR_INVALID_ARG;
+    h->order = order;
+    return PURLIN_OK;
+}
+
+purlin_status_t purlin_set_timeout(purlin_handle_t h, uint64_t timeout_ns)
+{
+    if (!h || timeout_ns == 0) return PURLIN_ERR_INVALID_ARG;
+    h->timeout_ns = timeout_ns;
+    return PURLIN_OK;
+}
+
+purlin_status_t purlin_debug_inject(purlin_handle_t h, int what)
+{
+    if (!h || what < 0 || what > 1) return PURLIN_ERR_INVALID_ARG;
+    h->inject = what;
+    return PURLIN_OK;
+}
+
+purlin_status_t purlin_query_status(purlin_handle_t h)
+{
+    if (!h) return PURLIN_ERR_INVALID_ARG;
+    DeviceGuard guard(h->device);
+    int v = 0;
+    if (cudaMemcpy(&v, h->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return PURLIN_ERR_CUDA;
+    if (v != 0) {
+        const int zero = 0;
+        if (cudaMemcpy(h->status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess ||
+            cudaDeviceSynchronize() != cudaSuccess)
+            return PURLIN_ERR_CUDA;
+    }
+    return (purlin_status_t)v;
+}
+
+purlin_status_t purlin_last_launch(purlin_handle_t h, purlin_launch_info_t* info)
+{
+    if (!h || !info) return PURLIN_ERR_INVALID_ARG;
+    *info = h->last;
+    return PURLIN_OK;
+}
+
+purlin_status_t purlin_plan_segments(purlin_collective_t coll, int R, const uint64_t in_addr[],
+                                     const uint64_t out_addr[], const size_t counts[],
+                                     const size_t displs_a[], const size_t displs_b[],
+                                     size_t count, purlin_dtype_t dtype, int max_unit,
+                                     purlin_segment_t* segs, int max_segs, int* nsegs,
+                                     uint32_t* ntiles)
+{
+    if (R < 1 || R > PURLIN_MAX_RANKS || !in_addr || !out_addr || !segs || !nsegs || !ntiles ||
+        (max_unit != 16 && max_unit != 32) || coll < PURLIN_COLL_REDUCE_SCATTER ||
+        coll > PURLIN_COLL_ALL_TO_ALL_V)
+        return PURLIN_ERR_INVALID_ARG;
+    Coll c = (Coll)coll;
+    if (c != Coll::AllReduce && !counts) return PURLIN_ERR_INVALID_ARG;
+    const size_t esz = elem_bytes(dtype);
+    if (!esz) return PURLIN_ERR_INVALID_ARG;
+    const bool reduce = c == Coll::ReduceScatter || c == Coll::AllReduce;
+    if (reduce && dtype == PURLIN_U8) return PURLIN_ERR_UNSUPPORTED;
+    for (int r = 0; r < R; ++r)
+        if (reduce && (in_addr[r] % esz || out_addr[r] % esz)) return PURLIN_ERR_INVALID_ARG;
+    Piece pieces[kSegsLarge];
+    int np = layout_pieces(c, R, counts, displs_a, displs_b, count, esz, pieces, kSegsLarge);
+    if (np < 0) return PURLIN_ERR_INVALID_ARG;
+    Segment tmp[kSegsLarge];
+    uint32_t nt = 0;
+    int n = layout_segments(pieces, np, R, in_addr, out_addr, esz, reduce, max_unit == 32 ? 5 : 4,
+                            tmp, kSegsLarge, &nt);
+    if (n < 0 || n > max_segs) return PURLIN_ERR_UNSUPPORTED;
+    for (int i = 0; i < n; ++i) {
+        segs[i].src_off = tmp[i].src_off;
+        segs[i].dst_off = tmp[i].dst_off;
+        segs[i].bytes = tmp[i].bytes;
+        segs[i].src_rank = tmp[i].src == kEveryRank ? -1 : tmp[i].src;
+        segs[i].dst_rank = tmp[i].dst == kEveryRank ? -1 : tmp[i].dst;
+        segs[i].unit = 1 << tmp[i].unit_log2;
+        segs[i].tile0 = tmp[i].tile0;
+    }
+    *nsegs = n;
+    *ntiles = nt;
+    return PURLIN_OK;
+}
+
+}  // extern "C"

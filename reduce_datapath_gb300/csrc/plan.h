@@ -1,0 +1,104 @@
+// plan.h -- the per-call plan that the layout module derives from a collective's
+// naming and that the Atom kernels execute.  Shared by host and device code of
+// the CUDA library (never by the oracle).
+//
+// A collective (page "Purlin: Separating Orchestration from the Datapath of
+// Collectives", abstract and Figure 4) is a naming of input and output
+// partitions plus an operation.  The layout module turns it into a list of
+// SEGMENTS: contiguous byte ranges that go from one source buffer (copy) or from
+// the same offset of every source buffer (sum) to one destination buffer or to
+// the same offset of every destination buffer.  Each segment is executed with
+// one access width ("unit"): a 16- or 32-byte vector for aligned bodies, or the
+// element / byte for unaligned heads and tails.  The launch's work is a flat
+// space of TILES (one tile = kThreads threads x unit x unroll); a segment owns
+// the tiles [tile0, tile0 + its tile count).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#if defined(__CUDACC__)
+#define PURLIN_HD __host__ __device__
+#else
+#define PURLIN_HD
+#endif
+
+namespace purlin {
+
+constexpr int kMaxRanks = 8;
+constexpr int kThreads = 256;          // threads per CTA of every Atom kernel
+constexpr uint8_t kEveryRank = 0xff;   // src: sum over all ranks; dst: all outputs
+constexpr int kSegsSmall = 24;         // RS / AG / AR: <= 3 segments per rank
+constexpr int kSegsLarge = 3 * kMaxRanks * kMaxRanks;  // A2AV: <= 3 per pair
+constexpr int kUnrollReduce = 1;       // units per thread per tile, sums
+constexpr int kUnrollCopy = 4;         // units per thread per tile, copies
+
+struct Segment {
+    uint64_t src_off;   // byte offset in the source buffer(s)
+    uint64_t dst_off;   // byte offset in the destination buffer(s)
+    uint64_t bytes;     // length; a multiple of the unit
+    uint32_t tile0;     // first tile of this segment
+    uint8_t src;        // source rank, or kEveryRank (sum over ranks)
+    uint8_t dst;        // destination rank, or kEveryRank (every output)
+    uint8_t unit_log2;  // access width = 1 << unit_log2 bytes (0..5)
+    uint8_t pad;
+};
+static_assert(sizeof(Segment) == 32, "Segment is passed by value to kernels");
+
+// Kernel parameter block of the zero-staging Atom kernels (passed as a
+// __grid_constant__ argument: no host-to-device copy per call).
+template <int MAXSEG>
+struct ZsParams {
+    const char* in[kMaxRanks];
+    char* out[kMaxRanks];
+    uint32_t R;
+    uint32_t nseg;
+    uint32_t ntiles;
+    uint32_t unroll;
+    Segment seg[MAXSEG];
+};
+
+// Tile length in bytes of a segment with this unit.
+PURLIN_HD inline uint64_t tile_bytes(int unit_log2, int unroll)
+{
+    return (uint64_t)kThreads * ((uint64_t)1 << unit_log2) * (uint64_t)unroll;
+}
+
+enum class Coll : int { ReduceScatter = 0, AllGather = 1, AllReduce = 2, AllToAllV = 3 };
+
+// A piece of a collective before alignment splitting.
+struct Piece {
+    uint64_t src_off;
+    uint64_t dst_off;
+    uint64_t bytes;
+    uint8_t src;
+    uint8_t dst;
+};
+
+// ---- layout module (layout.cpp; host only) ---------------------------------
+
+// Logical pieces of a collective from its counts and displacements (elements).
+//   ReduceScatter: counts = recv_counts[R], da = in_displs   (NULL = packed)
+//   AllGather:     counts = counts[R],      da = out_displs  (NULL = packed)
+//   AllReduce:     count
+//   AllToAllV:     counts = send_counts[R*R], da = send_displs, db = recv_displs
+// Returns the number of pieces (zero-length ones dropped), or -1 on overflow
+// of 64-bit byte arithmetic.
+int layout_pieces(Coll coll, int R, const size_t* counts, const size_t* da,
+                  const size_t* db, size_t count, size_t elem_bytes, Piece* out, int max_out);
+
+// Byte extent [0, extent) touched in every input and output buffer.
+void layout_extents(Coll coll, int R, const size_t* counts, const size_t* da,
+                    const size_t* db, size_t count, size_t elem_bytes,
+                    uint64_t in_extent[kMaxRanks], uint64_t out_extent[kMaxRanks]);
+
+// Split pieces into head / body / tail segments by the alignment of the actual
+// addresses, then number the tiles.  `reduce` selects element-wise heads and
+// tails (sums) or byte-wise ones (copies).  max_unit_log2 caps the vector width
+// (4 = 16 B, 5 = 32 B).  Returns the segment count or -1 if max_segs is too
+// small; *ntiles receives the tile count.
+int layout_segments(const Piece* pieces, int npieces, int R, const uint64_t* in_addr,
+                    const uint64_t* out_addr, size_t elem_bytes, bool reduce,
+                    int max_unit_log2, Segment* segs, int max_segs, uint32_t* ntiles);
+
+}  // namespace purlin

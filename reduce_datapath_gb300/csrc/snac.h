@@ -1,0 +1,71 @@
+// snac.h -- host interface of the SNAC (Stage, Notify, And Consume) kernels.
+//
+// Page "Purlin: Separating Orchestration from the Datapath of Collectives":
+// the abstract introduces SNAC as the shared orchestration protocol derived
+// from the collective's layouts; Figure 6 shows the composed AllReduce in which
+// every rank stages chunks incrementally while partition k is reduced and
+// already-reduced chunks are gathered.  On one GPU the protocol runs inside one
+// cooperative launch:
+//   producer CTAs  stage a chunk of every source into a slot of the staging
+//                  ring, then NOTIFY with a release store of the step's tag;
+//   consumer CTAs  acquire the tag (bounded wait), CONSUME the slot -- sum the
+//                  R staged pieces, or copy the staged piece -- into the
+//                  destination(s) or, for AllReduce, into the slot's y part,
+//                  then release the slot back to the producer;
+//   gatherer CTAs  (AllReduce) acquire the y tag and copy the reduced chunk to
+//                  all R outputs (the AllGather half of Figure 6).
+// Each CHANNEL is one producer, one consumer (and one gatherer) with its own
+// ring of `depth` slots; steps (chunks) are dealt to channels round-robin.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "plan.h"
+#include "purlin.h"
+
+namespace purlin {
+
+struct SnacRequest {
+    Coll coll;
+    int R;
+    int dtype;
+    int order;
+    size_t esz;
+    const Piece* pieces;
+    int npieces;
+    uint64_t in[kMaxRanks];
+    uint64_t out[kMaxRanks];
+};
+
+struct SnacConfig {
+    char* staging;          // device ring memory (owned by the caller)
+    size_t staging_bytes;
+    uint64_t* flags;        // device flag words, zeroed once at creation
+    size_t flag_words;
+    int* status;            // device status word (0 = ok)
+    uint64_t epoch;         // > every epoch used before with these flags
+    size_t chunk_bytes;     // 0 = automatic
+    int depth;              // 0 = automatic
+    int channels;           // 0 = automatic
+    int sms;
+    uint64_t timeout_ns;
+    int inject_skip_notify; // testing: channel 0's producer never notifies step 0
+};
+
+struct SnacLaunch {
+    int kernels;
+    int grid;
+    int block;
+    int depth;
+    int channels;
+    size_t chunk_bytes;
+};
+
+purlin_status_t snac_run(const SnacRequest& rq, const SnacConfig& cfg, cudaStream_t stream,
+                         SnacLaunch* launch);
+
+// Channels, chunk and depth that snac_run would use (for introspection/tests).
+purlin_status_t snac_geometry(int R, Coll coll, const SnacConfig& cfg, int resident_per_sm,
+                              size_t* chunk, int* depth, int* channels);
+
+}  // namespace purlin

@@ -1,0 +1,464 @@
+// snac_kernels.cu -- the SNAC (Stage, Notify, And Consume) protocol on one GPU.
+//
+// Page "Purlin: Separating Orchestration from the Datapath of Collectives":
+//   - Abstract: SNAC is a shared orchestration protocol that derives
+//     coordination from the collective's layouts, sitting above the Atom.
+//   - Figure 6: in the composed AllReduce "all ranks stage chunks
+//     incrementally"; rank k reduces chunks of partition k from all ranks while
+//     gathering reduced chunks of other partitions.
+//   - Figure 9 / Figure 16: staging serves "ordinary application buffers";
+//     Figure 10: "Purlin-ZS omits staging" (zs_kernels.cu).
+//   - Table 3: chunks sized to the bandwidth-delay product; Figure 11: pipeline
+//     depth one to eight stages.
+//
+// One cooperative launch holds every role, so each waiting CTA's partner is
+// resident.  Roles by blockIdx.x / channels:
+//   0 producer(ch): for each step dealt to ch, wait until its ring slot is free,
+//     STAGE the step's chunk of every source into the slot, NOTIFY (release).
+//   1 consumer(ch): wait for the step's tag (acquire), CONSUME: sum the R staged
+//     pieces (Atom::reduce) into the destination -- or, for AllReduce, into the
+//     slot's y part -- or copy the staged piece (Atom::copy) to its
+//     destination(s); then free the slot.
+//   2 gatherer(ch), AllReduce only: wait for the y tag, copy the reduced chunk to
+//     all R outputs, free the y part.
+// Steps are the layout's segments cut into chunks of `chunk` bytes per rank;
+// step i belongs to channel i % channels and is that channel's n-th step,
+// n = i / channels, held in slot n % depth.  A flag holds the tag
+// (epoch << 32) | (n + 1); epochs grow by one per call, so flags never need
+// resetting.  Every wait is bounded (time and iteration count) and watches the
+// status word: on a timeout the waiter records PURLIN_ERR_TIMEOUT and every CTA
+// leaves at its next wait.
+#include "atom.cuh"
+#include "internal.h"
+#include "snac.h"
+
+#include <algorithm>
+#include <cstring>
+
+namespace purlin {
+
+namespace {
+
+enum Kind : int { kRS = 0, kAG = 1, kAR = 2, kA2A = 3 };
+enum : int { kReady = 0, kFree = 1, kYReady = 2, kYFree = 3, kFlagsPerSlot = 4 };
+
+constexpr size_t kDefaultChunk = 64 * 1024;
+constexpr int kDefaultDepth = 2;
+constexpr int kMaxChannels = 128;
+
+struct SnacParams {
+    const char* in[kMaxRanks];
+    char* out[kMaxRanks];
+    char* staging;
+    uint64_t* flags;
+    int* status;
+    uint64_t epoch;
+    uint64_t timeout_ns;
+    uint64_t max_spins;
+    uint64_t chunk;        // bytes per rank per step (multiple of 256)
+    uint64_t slot_stride;  // bytes of one ring slot
+    uint64_t chan_stride;  // bytes of one channel's ring
+    uint32_t R;
+    uint32_t nch;
+    uint32_t depth;
+    uint32_t nseg;
+    uint32_t nsteps;
+    uint32_t inject;
+    Segment seg[kSegsLarge];  // tile0 = first step of the segment
+};
+
+__device__ __forceinline__ uint64_t tag_of(const SnacParams& p, uint32_t n)
+{
+    return (p.epoch << 32) | (uint64_t)(n + 1);
+}
+
+__device__ __forceinline__ uint64_t now_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ uint64_t ld_acquire(const uint64_t* f)
+{
+    uint64_t v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(f) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release(uint64_t* f, uint64_t v)
+{
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(f), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ int ld_status(const int* s)
+{
+    int v;
+    asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(s) : "memory");
+    return v;
+}
+
+// Bounded wait of one CTA for *flag >= want.  Thread 0 spins; the verdict is
+// shared through shared memory.  Returns false if the CTA must leave (this
+// wait timed out, or another CTA recorded an error).
+__device__ bool cta_wait(const SnacParams& p, const uint64_t* flag, uint64_t want)
+{
+    __shared__ int go;
+    if (threadIdx.x == 0) {
+        int ok = 1;
+        uint64_t spins = 0, start = 0;
+        while (ld_acquire(flag) < want) {
+            if (ld_status(p.status) != 0) { ok = 0; break; }
+            ++spins;
+            if ((spins & 31) == 0) {
+                uint64_t t = now_ns();
+                if (start == 0) start = t;
+                if (t - start > p.timeout_ns || spins > p.max_spins) {
+                    atomicCAS(p.status, 0, (int)PURLIN_ERR_TIMEOUT);
+                    ok = 0;
+                    break;
+                }
+            }
+            __nanosleep(100);
+        }
+        go = ok;
+    }
+    __syncthreads();
+    const bool ok = go != 0;
+    __syncthreads();  // `go` is rewritten by the next wait
+    return ok;
+}
+
+// Publish this CTA's work of the step: every thread's accesses happen before
+// the release store of the tag.
+__device__ __forceinline__ void cta_notify(uint64_t* flag, uint64_t tag)
+{
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        st_release(flag, tag);
+    }
+}
+
+__device__ __forceinline__ const Segment& step_segment(const SnacParams& p, uint32_t i)
+{
+    int lo = 0, hi = (int)p.nseg - 1;
+    while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if (p.seg[mid].tile0 <= i) lo = mid;
+        else hi = mid - 1;
+    }
+    return p.seg[lo];
+}
+
+__device__ __forceinline__ uint64_t* slot_flags(const SnacParams& p, uint32_t ch, uint32_t slot)
+{
+    return p.flags + ((uint64_t)ch * p.depth + slot) * kFlagsPerSlot;
+}
+
+__device__ __forceinline__ char* slot_data(const SnacParams& p, uint32_t ch, uint32_t slot)
+{
+    return p.staging + (uint64_t)ch * p.chan_stride + (uint64_t)slot * p.slot_stride;
+}
+
+// ------------------------------------------------------- CTA-wide data movers
+
+// Copy len bytes src -> dst (or -> out[r] + dst_off for every r when FAN),
+// in units of B bytes, four units per thread in flight.
+// `skip` (an address, 0 for none): with FAN, a destination range starting there is
+// the source of an in-place AllGather block and is left alone.
+template <int B, bool SRC_CG, bool FAN>
+__device__ __forceinline__ void cta_copy(const SnacParams& p, char* dst, uint64_t dst_off,
+                                         const char* src, uint64_t len, uintptr_t skip)
+{
+    constexpr int U = 4;
+    for (uint64_t base = 0; base < len; base += (uint64_t)kThreads * B * U) {
+        atom::Unit<B> u[U];
+#pragma unroll
+        for (int k = 0; k < U; ++k) {
+            const uint64_t o = base + (uint64_t)(k * kThreads + threadIdx.x) * B;
+            if (o < len) atom::load_unit<B, SRC_CG>(u[k], src + o);
+        }
+#pragma unroll
+        for (int k = 0; k < U; ++k) {
+            const uint64_t o = base + (uint64_t)(k * kThreads + threadIdx.x) * B;
+            if (o >= len) continue;
+            if (FAN) {
+                for (int r = 0; r < (int)p.R; ++r) {
+                    char* d = p.out[r] + dst_off + o;
+                    if ((uintptr_t)d != skip + o) atom::store_unit<B>(d, u[k]);
+                }
+            } else {
+                atom::store_unit<B>(dst + o, u[k]);
+            }
+        }
+    }
+}
+
+template <bool SRC_CG, bool FAN>
+__device__ void cta_copy_any(const SnacParams& p, int unit_log2, char* dst, uint64_t dst_off,
+                             const char* src, uint64_t len, uintptr_t skip)
+{
+    switch (unit_log2) {
+    case 5: cta_copy<32, SRC_CG, FAN>(p, dst, dst_off, src, len, skip); break;
+    case 4: cta_copy<16, SRC_CG, FAN>(p, dst, dst_off, src, len, skip); break;
+    case 3: cta_copy<8, SRC_CG, FAN>(p, dst, dst_off, src, len, skip); break;
+    case 2: cta_copy<4, SRC_CG, FAN>(p, dst, dst_off, src, len, skip); break;
+    case 1: cta_copy<2, SRC_CG, FAN>(p, dst, dst_off, src, len, skip); break;
+    default: cta_copy<1, SRC_CG, FAN>(p, dst, dst_off, src, len, skip); break;
+    }
+}
+
+// Atom::reduce over the R staged pieces (stride `stride` apart) into dst.
+template <typename T, int ORDER, int B>
+__device__ __forceinline__ void cta_reduce_vec(const SnacParams& p, char* dst, const char* staged,
+                                               uint64_t len)
+{
+    const int R = (int)p.R;
+    for (uint64_t o = (uint64_t)threadIdx.x * B; o < len; o += (uint64_t)kThreads * B) {
+        atom::Vec<B> v[kMaxRanks];
+#pragma unroll
+        for (int r = 0; r < kMaxRanks; ++r)
+            if (r < R) atom::load_cg(v[r], staged + r * p.chunk + o);
+        atom::Vec<B> out;
+        atom::reduce_unit<T, ORDER, B>(v, R, out);
+        atom::store(dst + o, out);
+    }
+}
+
+template <typename T, int ORDER>
+__device__ __forceinline__ void cta_reduce_elem(const SnacParams& p, char* dst, const char* staged,
+                                                uint64_t len)
+{
+    const int R = (int)p.R;
+    for (uint64_t o = (uint64_t)threadIdx.x * T::kBytes; o < len; o += (uint64_t)kThreads * T::kBytes) {
+        float v[kMaxRanks];
+#pragma unroll
+        for (int r = 0; r < kMaxRanks; ++r) v[r] = (r < R) ? T::load1_cg(staged + r * p.chunk + o) : 0.0f;
+        T::store1(dst + o, atom::fold<ORDER>(v, R));
+    }
+}
+
+template <typename T, int ORDER>
+__device__ void cta_reduce(const SnacParams& p, int unit_log2, char* dst, const char* staged,
+                           uint64_t len)
+{
+    if (unit_log2 == 5) cta_reduce_vec<T, ORDER, 32>(p, dst, staged, len);
+    else if (unit_log2 == 4) cta_reduce_vec<T, ORDER, 16>(p, dst, staged, len);
+    else cta_reduce_elem<T, ORDER>(p, dst, staged, len);
+}
+
+// ------------------------------------------------------------------ roles
+
+template <int KIND>
+__device__ void producer(const SnacParams& p, uint32_t ch)
+{
+    const bool reduce = KIND == kRS || KIND == kAR;
+    uint32_t n = 0;
+    for (uint32_t i = ch; i < p.nsteps; i += p.nch, ++n) {
+        const uint32_t slot = n % p.depth;
+        uint64_t* f = slot_flags(p, ch, slot);
+        if (n >= p.depth && !cta_wait(p, f + kFree, tag_of(p, n - p.depth))) return;
+        const Segment& s = step_segment(p, i);
+        const uint64_t off = (uint64_t)(i - s.tile0) * p.chunk;
+        const uint64_t len = min(p.chunk, s.bytes - off);
+        char* staged = slot_data(p, ch, slot);
+        if (reduce) {
+            for (int r = 0; r < (int)p.R; ++r)
+                cta_copy_any<false, false>(p, s.unit_log2, staged + r * p.chunk, 0,
+                                           p.in[r] + s.src_off + off, len, 0);
+        } else {
+            cta_copy_any<false, false>(p, s.unit_log2, staged, 0, p.in[s.src] + s.src_off + off,
+                                       len, 0);
+        }
+        if (p.inject && ch == 0 && n == 0) continue;  // testing: this notify never happens
+        cta_notify(f + kReady, tag_of(p, n));
+    }
+}
+
+template <typename T, int ORDER, int KIND>
+__device__ void consumer(const SnacParams& p, uint32_t ch)
+{
+    uint32_t n = 0;
+    for (uint32_t i = ch; i < p.nsteps; i += p.nch, ++n) {
+        const uint32_t slot = n % p.depth;
+        uint64_t* f = slot_flags(p, ch, slot);
+        if (!cta_wait(p, f + kReady, tag_of(p, n))) return;
+        const Segment& s = step_segment(p, i);
+        const uint64_t off = (uint64_t)(i - s.tile0) * p.chunk;
+        const uint64_t len = min(p.chunk, s.bytes - off);
+        char* staged = slot_data(p, ch, slot);
+        if (KIND == kRS) {
+            cta_reduce<T, ORDER>(p, s.unit_log2, p.out[s.dst] + s.dst_off + off, staged, len);
+        } else if (KIND == kAR) {
+            if (n >= p.depth && !cta_wait(p, f + kYFree, tag_of(p, n - p.depth))) return;
+            cta_reduce<T, ORDER>(p, s.unit_log2, staged + (uint64_t)p.R * p.chunk, staged, len);
+        } else if (KIND == kAG) {
+            cta_copy_any<true, true>(p, s.unit_log2, nullptr, s.dst_off + off, staged, len,
+                                     (uintptr_t)(p.in[s.src] + s.src_off + off));
+        } else {
+            cta_copy_any<true, false>(p, s.unit_log2, p.out[s.dst] + s.dst_off + off, 0, staged,
+                                      len, 0);
+        }
+        cta_notify(f + kFree, tag_of(p, n));
+        if (KIND == kAR && threadIdx.x == 0) st_release(f + kYReady, tag_of(p, n));
+    }
+}
+
+__device__ void gatherer(const SnacParams& p, uint32_t ch)
+{
+    uint32_t n = 0;
+    for (uint32_t i = ch; i < p.nsteps; i += p.nch, ++n) {
+        const uint32_t slot = n % p.depth;
+        uint64_t* f = slot_flags(p, ch, slot);
+        if (!cta_wait(p, f + kYReady, tag_of(p, n))) return;
+        const Segment& s = step_segment(p, i);
+        const uint64_t off = (uint64_t)(i - s.tile0) * p.chunk;
+        const uint64_t len = min(p.chunk, s.bytes - off);
+        const char* y = slot_data(p, ch, slot) + (uint64_t)p.R * p.chunk;
+        // In-place AllReduce writes out[r] == in[r]; this step's input range
+        // was staged before the y tag was published, so the writes are safe.
+        cta_copy_any<true, true>(p, s.unit_log2, nullptr, s.dst_off + off, y, len, 0);
+        cta_notify(f + kYFree, tag_of(p, n));
+    }
+}
+
+template <typename T, int ORDER, int KIND>
+__global__ void __launch_bounds__(kThreads, 2) snac_kernel(const __grid_constant__ SnacParams p)
+{
+    const uint32_t role = blockIdx.x / p.nch;
+    const uint32_t ch = blockIdx.x % p.nch;
+    if (role == 0) producer<KIND>(p, ch);
+    else if (role == 1) consumer<T, ORDER, KIND>(p, ch);
+    else if (KIND == kAR) gatherer(p, ch);
+}
+
+using SnacKernel = void (*)(SnacParams);
+
+template <typename T, int KIND>
+SnacKernel pick_order(int order)
+{
+    return order == 0 ? snac_kernel<T, 0, KIND> : snac_kernel<T, 1, KIND>;
+}
+
+template <int KIND>
+SnacKernel pick_dtype(int dtype, int order)
+{
+    if (dtype == kF32) return pick_order<atom::F32, KIND>(order);
+    if (dtype == kBF16) return pick_order<atom::BF16, KIND>(order);
+    return pick_order<atom::F16, KIND>(order);
+}
+
+SnacKernel kernel_for(Coll coll, int dtype, int order)
+{
+    switch (coll) {
+    case Coll::ReduceScatter: return pick_dtype<kRS>(dtype, order);
+    case Coll::AllReduce: return pick_dtype<kAR>(dtype, order);
+    case Coll::AllGather: return snac_kernel<atom::F32, 0, kAG>;
+    default: return snac_kernel<atom::F32, 0, kA2A>;
+    }
+}
+
+int roles_of(Coll coll) { return coll == Coll::AllReduce ? 3 : 2; }
+
+int sub_slots(Coll coll, int R)
+{
+    if (coll == Coll::AllReduce) return R + 1;
+    if (coll == Coll::ReduceScatter) return R;
+    return 1;
+}
+
+}  // namespace
+
+purlin_status_t snac_geometry(int R, Coll coll, const SnacConfig& cfg, int resident_per_sm,
+                              size_t* chunk_out, int* depth_out, int* channels_out)
+{
+    size_t chunk = cfg.chunk_bytes ? cfg.chunk_bytes : kDefaultChunk;
+    chunk = std::max<size_t>(256, (chunk + 255) & ~(size_t)255);
+    const int depth = cfg.depth ? cfg.depth : kDefaultDepth;
+    const size_t slot = (size_t)sub_slots(coll, R) * chunk;
+    const size_t ring = (size_t)depth * slot;
+    const long by_ring = ring ? (long)(cfg.staging_bytes / ring) : 0;
+    const long by_flags = (long)(cfg.flag_words / ((size_t)depth * kFlagsPerSlot));
+    const long by_residency = (long)resident_per_sm * cfg.sms / roles_of(coll);
+    long nch = cfg.channels ? cfg.channels : kMaxChannels;
+    nch = std::min({nch, by_ring, by_flags, by_residency});
+    if (nch < 1) return PURLIN_ERR_UNSUPPORTED;  // ring too small for this chunk/depth
+    *chunk_out = chunk;
+    *depth_out = depth;
+    *channels_out = (int)nch;
+    return PURLIN_OK;
+}
+
+purlin_status_t snac_run(const SnacRequest& rq, const SnacConfig& cfg, cudaStream_t stream,
+                         SnacLaunch* launch)
+{
+    static thread_local SnacParams p;
+    std::memset(&p, 0, sizeof(p));
+    const bool reduce = rq.coll == Coll::ReduceScatter || rq.coll == Coll::AllReduce;
+    uint32_t ntiles = 0;
+    int nseg = layout_segments(rq.pieces, rq.npieces, rq.R, rq.in, rq.out, rq.esz, reduce, 5,
+                               p.seg, kSegsLarge, &ntiles);
+    if (nseg < 0) return PURLIN_ERR_UNSUPPORTED;
+
+    SnacKernel kernel = kernel_for(rq.coll, rq.dtype, rq.order);
+    int resident = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&resident, kernel, kThreads, 0) !=
+            cudaSuccess || resident < 1)
+        return PURLIN_ERR_CUDA;
+    size_t chunk = 0;
+    int depth = 0, nch = 0;
+    purlin_status_t st = snac_geometry(rq.R, rq.coll, cfg, resident, &chunk, &depth, &nch);
+    if (st != PURLIN_OK) return st;
+
+    // Steps: every segment cut into chunks of `chunk` bytes.
+    uint64_t steps = 0;
+    for (int i = 0; i < nseg; ++i) {
+        p.seg[i].tile0 = (uint32_t)steps;
+        steps += (p.seg[i].bytes + chunk - 1) / chunk;
+        if (steps > 0xffffffffull) return PURLIN_ERR_UNSUPPORTED;
+    }
+    if (steps == 0) {
+        *launch = SnacLaunch{0, 0, kThreads, depth, 0, chunk};
+        return PURLIN_OK;
+    }
+    nch = (int)std::min<uint64_t>((uint64_t)nch, steps);
+
+    for (int r = 0; r < rq.R; ++r) {
+        p.in[r] = reinterpret_cast<const char*>(rq.in[r]);
+        p.out[r] = reinterpret_cast<char*>(rq.out[r]);
+    }
+    p.staging = cfg.staging;
+    p.flags = cfg.flags;
+    p.status = cfg.status;
+    p.epoch = cfg.epoch;
+    p.timeout_ns = cfg.timeout_ns;
+    p.max_spins = cfg.timeout_ns / 64 + 65536;
+    p.chunk = chunk;
+    p.slot_stride = (uint64_t)sub_slots(rq.coll, rq.R) * chunk;
+    p.chan_stride = (uint64_t)depth * p.slot_stride;
+    p.R = (uint32_t)rq.R;
+    p.nch = (uint32_t)nch;
+    p.depth = (uint32_t)depth;
+    p.nseg = (uint32_t)nseg;
+    p.nsteps = (uint32_t)steps;
+    p.inject = (uint32_t)cfg.inject_skip_notify;
+
+    const int grid = nch * roles_of(rq.coll);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3((unsigned)grid);
+    lc.blockDim = dim3(kThreads);
+    lc.dynamicSmemBytes = 0;
+    lc.stream = stream;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    cudaError_t ce = cudaLaunchKernelEx(&lc, kernel, p);
+    if (ce != cudaSuccess) return PURLIN_ERR_CUDA;
+    *launch = SnacLaunch{1, grid, kThreads, depth, nch, chunk};
+    return PURLIN_OK;
+}
+
+}  // namespace purlin

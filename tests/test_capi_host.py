@@ -1,0 +1,232 @@
+"""Host-side tests of the C-ABI library (no GPU, no kernel launches).
+
+* libpurlin.so loads and exports every symbol that include/*.h declares;
+* the layout module's plan (purlin_plan_segments, host only) covers every
+  output byte exactly once, maps it to the right source byte per the Figure 4
+  layouts, and splits pieces so each access unit is aligned for every stream;
+* argument errors are reported as such.
+"""
+import glob
+import os
+import re
+
+import numpy as np
+import pytest
+
+import reduce_datapath_gb300 as rd
+import workloads
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    rd.build()
+    return rd.lib()
+
+
+def declared_symbols():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        names |= set(re.findall(r"PURLIN_API\s+[\w\s\*]+?\b(purlin_\w+)\s*\(", text))
+    return names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_symbols()
+    assert len(names) >= 16
+    for n in names:
+        assert hasattr(lib, n), n
+    assert names == set(rd.EXPORTED)
+
+
+def test_version_and_status_strings(lib):
+    assert rd.purlin_version() >> 16 == 1
+    for s in range(6):
+        assert rd.purlin_status_string(s)
+    assert rd.purlin_status_string(99) == "unknown status"
+
+
+def test_null_handle_is_invalid(lib):
+    assert lib.purlin_set_policy(None, 0, 0, 0, 0) == rd.ERR_INVALID_ARG
+    assert lib.purlin_query_status(None) == rd.ERR_INVALID_ARG
+    assert lib.purlin_destroy(None) == rd.OK
+    assert lib.purlin_all_reduce(None, None, None, 4, rd.F32, rd.OP_SUM, None) == rd.ERR_INVALID_ARG
+
+
+# ----------------------------------------------------------------- plan tests
+
+def _packed(counts):
+    out, s = [], 0
+    for c in counts:
+        out.append(s)
+        s += int(c)
+    return out
+
+
+def expected_map(coll, R, counts, da, db, count, esz):
+    """For every output rank: {dst byte -> (src rank or -1, src byte)} from the
+    Figure 4 definitions, written as plain loops over partitions."""
+    want = [dict() for _ in range(R)]
+    if coll == rd.COLL_REDUCE_SCATTER:
+        d = da if da is not None else _packed(counts)
+        for k in range(R):
+            for i in range(int(counts[k]) * esz):
+                want[k][i] = (-1, int(d[k]) * esz + i)
+    elif coll == rd.COLL_ALL_GATHER:
+        D = da if da is not None else _packed(counts)
+        for j in range(R):
+            for k in range(R):
+                for i in range(int(counts[k]) * esz):
+                    want[j][int(D[k]) * esz + i] = (k, i)
+    elif coll == rd.COLL_ALL_REDUCE:
+        for j in range(R):
+            for i in range(count * esz):
+                want[j][i] = (-1, i)
+    else:
+        C = np.asarray(counts).reshape(R, R)
+        for j in range(R):
+            pos = 0
+            for s in range(R):
+                sd = int(da[s * R + j]) if da is not None else int(sum(C[s, :j]))
+                rdsp = int(db[j * R + s]) if db is not None else pos
+                for i in range(int(C[s, j]) * esz):
+                    want[j][rdsp * esz + i] = (s, sd * esz + i)
+                pos += int(C[s, j])
+    return want
+
+
+def plan_map(segs, R):
+    got = [dict() for _ in range(R)]
+    for s in segs:
+        dsts = range(R) if s["dst_rank"] == -1 else [s["dst_rank"]]
+        for j in dsts:
+            for b in range(s["bytes"]):
+                key = s["dst_off"] + b
+                assert key not in got[j], "output byte written twice"
+                got[j][key] = (s["src_rank"], s["src_off"] + b)
+    return got
+
+
+def check_alignment(segs, R, in_addr, out_addr, reduce, esz):
+    for s in segs:
+        u = s["unit"]
+        assert s["bytes"] % u == 0
+        srcs = [in_addr[r] + s["src_off"] for r in range(R)] if s["src_rank"] == -1 \
+            else [in_addr[s["src_rank"]] + s["src_off"]]
+        dsts = [out_addr[r] + s["dst_off"] for r in range(R)] if s["dst_rank"] == -1 \
+            else [out_addr[s["dst_rank"]] + s["dst_off"]]
+        for a in srcs + dsts:
+            assert a % u == 0, (s, a)
+        if reduce:
+            assert u in (esz, 16, 32)
+
+
+def check_tiles(segs, ntiles, reduce):
+    unroll = 1 if reduce else 4
+    t = 0
+    for s in segs:
+        assert s["tile0"] == t
+        tb = 256 * s["unit"] * unroll
+        t += -(-s["bytes"] // tb)
+    assert t == ntiles
+
+
+def _addrs(rng, R, misalign, esz):
+    base = [(1 << 30) * (r + 1) for r in range(R)]
+    if misalign:
+        base = [b + int(rng.integers(0, 16)) * esz for b in base]
+    return base
+
+
+@pytest.mark.parametrize("seed", range(6))
+@pytest.mark.parametrize("coll", [rd.COLL_REDUCE_SCATTER, rd.COLL_ALL_GATHER,
+                                  rd.COLL_ALL_REDUCE, rd.COLL_ALL_TO_ALL_V])
+@pytest.mark.parametrize("dtype", ["bf16", "f32", "u8"])
+def test_plan_covers_every_output_byte_once(lib, coll, dtype, seed):
+    reduce = coll in (rd.COLL_REDUCE_SCATTER, rd.COLL_ALL_REDUCE)
+    if reduce and dtype == "u8":
+        pytest.skip("sums take float types only")
+    esz = rd.ELEM_BYTES[rd.DTYPES[dtype]]
+    rng = np.random.default_rng(seed)
+    R = int(rng.integers(1, 9))
+    misalign = seed % 2 == 1
+    in_addr = _addrs(rng, R, misalign, esz)
+    out_addr = _addrs(rng, R, misalign, esz)
+    counts = da = db = None
+    count = 0
+    if coll == rd.COLL_ALL_REDUCE:
+        count = int(rng.integers(0, 3000))
+    elif coll == rd.COLL_ALL_TO_ALL_V:
+        counts = workloads.random_pair_counts(R, 300, seed)
+        if seed % 3 == 2:   # explicit displacements: reversed packing
+            C = counts.reshape(R, R)
+            da = np.zeros((R, R), dtype=np.int64)
+            db = np.zeros((R, R), dtype=np.int64)
+            for s in range(R):
+                pos = 0
+                for j in reversed(range(R)):
+                    da[s, j] = pos
+                    pos += C[s, j]
+            for j in range(R):
+                pos = 0
+                for s in reversed(range(R)):
+                    db[j, s] = pos
+                    pos += C[s, j]
+            da, db = da.reshape(-1), db.reshape(-1)
+        counts = counts.reshape(-1)
+    else:
+        counts = workloads.random_counts(R, 700, seed)
+        if seed % 3 == 2:
+            perm = rng.permutation(R)
+            starts = np.zeros(R, dtype=np.int64)
+            pos = 0
+            for k in perm:
+                starts[k] = pos
+                pos += counts[k] + int(rng.integers(0, 5))
+            da = starts
+    segs, ntiles = rd.purlin_plan_segments(coll, R, in_addr, out_addr, counts, da, db, count,
+                                           dtype)
+    check_alignment(segs, R, in_addr, out_addr, reduce, esz)
+    check_tiles(segs, ntiles, reduce)
+    got = plan_map(segs, R)
+    want = expected_map(coll, R, counts, da, db, count, esz)
+    assert got == want
+
+
+def test_aligned_bodies_use_wide_units(lib):
+    R = 8
+    n = 1 << 16
+    in_addr = [(1 << 32) * (r + 1) for r in range(R)]
+    out_addr = [(1 << 32) * (r + 9) for r in range(R)]
+    segs, _ = rd.purlin_plan_segments(rd.COLL_ALL_REDUCE, R, in_addr, out_addr, count=n,
+                                      dtype="bf16")
+    assert len(segs) == 1 and segs[0]["unit"] == 32 and segs[0]["bytes"] == 2 * n
+    segs, _ = rd.purlin_plan_segments(rd.COLL_ALL_REDUCE, R, in_addr, out_addr, count=n,
+                                      dtype="bf16", max_unit=16)
+    assert segs[0]["unit"] == 16
+    # one stream off by one element: sums fall back to element units
+    in_addr[3] += 2
+    segs, _ = rd.purlin_plan_segments(rd.COLL_ALL_REDUCE, R, in_addr, out_addr, count=n,
+                                      dtype="bf16")
+    assert [s["unit"] for s in segs] == [2]
+
+
+def test_plan_rejects_bad_arguments(lib):
+    a = [1 << 20, 2 << 20]
+    with pytest.raises(rd.PurlinError) as e:
+        rd.purlin_plan_segments(rd.COLL_ALL_REDUCE, 9, a * 5, a * 5, count=4, dtype="f32")
+    assert e.value.status == rd.ERR_INVALID_ARG
+    with pytest.raises(rd.PurlinError) as e:   # misaligned sum stream
+        rd.purlin_plan_segments(rd.COLL_ALL_REDUCE, 2, [a[0] + 1, a[1]], a, count=4, dtype="f32")
+    assert e.value.status == rd.ERR_INVALID_ARG
+    with pytest.raises(rd.PurlinError) as e:   # sums of bytes are not served
+        rd.purlin_plan_segments(rd.COLL_ALL_REDUCE, 2, a, a, count=4, dtype="u8")
+    assert e.value.status == rd.ERR_UNSUPPORTED
+    with pytest.raises(rd.PurlinError) as e:   # counts missing
+        rd.purlin_plan_segments(rd.COLL_REDUCE_SCATTER, 2, a, a, None, dtype="f32")
+    assert e.value.status == rd.ERR_INVALID_ARG
+    with pytest.raises(rd.PurlinError) as e:   # byte count overflows 64 bits
+        rd.purlin_plan_segments(rd.COLL_ALL_GATHER, 2, a, a, [2 ** 63, 1], dtype="f32")
+    assert e.value.status == rd.ERR_INVALID_ARG

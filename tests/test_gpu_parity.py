@@ -1,0 +1,362 @@
+"""GPU parity: the CUDA library (through the C ABI) against the CPU oracle.
+
+Every collective, dtype, datapath variant (zero staging and SNAC staged, at
+several chunk sizes / depths / CTA counts) and layout (packed, explicit
+displacements, zero counts, unaligned starts, in-place forms) must match the
+oracle BIT FOR BIT: copies are permutations of bytes, and sums follow one fixed
+rank order with binary32 accumulation and a single rounding.  Every output is
+surrounded by canary guards that must survive.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import reduce_datapath_gb300 as rd
+import workloads
+from helpers import Guarded, handle, host_bits, inputs, same_bits, set_variant, close_handles
+
+pytestmark = pytest.mark.gpu
+
+POLICIES = {
+    "zs": (rd.VARIANT_ZS, 0, 0, 0),
+    "zs_3ctas": (rd.VARIANT_ZS, 0, 0, 3),
+    "snac_tiny_chunks": (rd.VARIANT_STAGED, 256, 2, 3),
+    "snac_default": (rd.VARIANT_STAGED, 0, 0, 0),
+    "snac_deep": (rd.VARIANT_STAGED, 4096, 8, 5),
+}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    rd.build()
+    yield
+    torch.cuda.synchronize()
+    close_handles()
+
+
+def run_ok(h):
+    torch.cuda.synchronize()
+    st = rd.purlin_query_status(h)
+    assert st == rd.OK, rd.purlin_status_string(st)
+
+
+def oracle_in(bufs):
+    return [host_bits(b) for b in bufs]
+
+
+# ------------------------------------------------------------------ AllReduce
+
+@pytest.mark.parametrize("policy", list(POLICIES))
+@pytest.mark.parametrize("dtype", ["bf16", "f32", "f16"])
+@pytest.mark.parametrize("R", [1, 2, 3, 8])
+@pytest.mark.parametrize("n", [0, 1, 7, 33, 4096, 70001])
+def test_all_reduce(policy, dtype, R, n):
+    h = handle(R)
+    set_variant(h, *POLICIES[policy])
+    x = inputs(R, n, dtype, seed=n + 7 * R)
+    outs = [Guarded(n, dtype) for _ in range(R)]
+    rd.purlin_all_reduce(h, x, [o.view for o in outs], n, dtype)
+    run_ok(h)
+    want = oracle.all_reduce(oracle_in(x), dtype=dtype)
+    for j in range(R):
+        assert same_bits(host_bits(outs[j].view), want[j]), (j,)
+        assert outs[j].guards_intact()
+
+
+@pytest.mark.parametrize("policy", ["zs", "snac_tiny_chunks"])
+@pytest.mark.parametrize("offset", [1, 3, 8])
+def test_all_reduce_unaligned_streams(policy, offset):
+    """Streams starting at different offsets force element-wise segments."""
+    R, n, dtype = 4, 5000, "bf16"
+    h = handle(R)
+    set_variant(h, *POLICIES[policy])
+    x = [inputs(1, n, dtype, seed=100 + r, offset=(offset * r) % 16)[0] for r in range(R)]
+    outs = [Guarded(n, dtype, offset=offset) for _ in range(R)]
+    rd.purlin_all_reduce(h, x, [o.view for o in outs], n, dtype)
+    run_ok(h)
+    want = oracle.all_reduce(oracle_in(x), dtype=dtype)
+    for j in range(R):
+        assert same_bits(host_bits(outs[j].view), want[j])
+        assert outs[j].guards_intact()
+
+
+@pytest.mark.parametrize("policy", ["zs", "snac_tiny_chunks"])
+def test_all_reduce_in_place(policy):
+    R, n, dtype = 8, 12345, "f32"
+    h = handle(R)
+    set_variant(h, *POLICIES[policy])
+    x = inputs(R, n, dtype, seed=5)
+    want = oracle.all_reduce(oracle_in(x), dtype=dtype)
+    rd.purlin_all_reduce(h, x, x, n, dtype)
+    run_ok(h)
+    for j in range(R):
+        assert same_bits(host_bits(x[j]), want[j])
+
+
+# ------------------------------------------------------------- ReduceScatter
+
+def _rs_case(R, seed, explicit):
+    counts = workloads.random_counts(R, 3000, seed)
+    if explicit:   # partitions in a shuffled order with gaps
+        rng = np.random.default_rng(seed)
+        displs = np.zeros(R, dtype=np.int64)
+        pos = 0
+        for k in rng.permutation(R):
+            displs[k] = pos
+            pos += counts[k] + int(rng.integers(0, 9))
+        return counts, displs, int(pos)
+    return counts, None, int(counts.sum())
+
+
+@pytest.mark.parametrize("policy", list(POLICIES))
+@pytest.mark.parametrize("dtype", ["bf16", "f32", "f16"])
+@pytest.mark.parametrize("R", [1, 3, 8])
+@pytest.mark.parametrize("explicit", [False, True])
+def test_reduce_scatter_v(policy, dtype, R, explicit):
+    h = handle(R)
+    set_variant(h, *POLICIES[policy])
+    seed = 11 * R + explicit
+    counts, displs, total = _rs_case(R, seed, explicit)
+    x = inputs(R, total, dtype, seed=seed)
+    outs = [Guarded(int(c), dtype) for c in counts]
+    rd.purlin_reduce_scatter(h, x, [o.view for o in outs], counts, displs, dtype)
+    run_ok(h)
+    want = oracle.reduce_scatter(oracle_in(x), counts, displs, dtype=dtype)
+    for k in range(R):
+        assert same_bits(host_bits(outs[k].view), want[k]), k
+        assert outs[k].guards_intact()
+
+
+@pytest.mark.parametrize("policy", ["zs", "snac_tiny_chunks"])
+def test_reduce_scatter_in_place(policy):
+    R, c, dtype = 8, 1001, "bf16"
+    h = handle(R)
+    set_variant(h, *POLICIES[policy])
+    x = inputs(R, R * c, dtype, seed=77)
+    want = oracle.reduce_scatter(oracle_in(x), [c] * R, dtype=dtype)
+    outs = [x[k][k * c:(k + 1) * c] for k in range(R)]
+    rd.purlin_reduce_scatter(h, x, outs, [c] * R, None, dtype)
+    run_ok(h)
+    for k in range(R):
+        assert same_bits(host_bits(outs[k]), want[k])
+
+
+@pytest.mark.parametrize("policy", ["zs", "snac_tiny_chunks"])
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_reduce_scatter_unaligned_partitions(policy, dtype):
+    """Partitions at odd element offsets: heads and tails are element-wise."""
+    R = 5
+    h = handle(R)
+    set_variant(h, *POLICIES[policy])
+    counts = np.array([1023, 1, 0, 517, 2049])
+    displs = np.array([3, 1031, 1040, 1100, 1701])
+    x = inputs(R, 3800, dtype, seed=3, offset=1)
+    outs = [Guarded(int(c), dtype, offset=3) for c in counts]
+    rd.purlin_reduce_scatter(h, x, [o.view for o in outs], counts, displs, dtype)
+    run_ok(h)
+    want = oracle.reduce_scatter(oracle_in(x), counts, displs, dtype=dtype)
+    for k in range(R):
+        assert same_bits(host_bits(outs[k].view), want[k])
+        assert outs[k].guards_intact()
+
+
+# ------------------------------------------------------------------ AllGather
+
+@pytest.mark.parametrize("policy", list(POLICIES))
+@pytest.mark.parametrize("dtype", ["bf16", "f32", "u8"])
+@pytest.mark.parametrize("R", [1, 3, 8])
+@pytest.mark.parametrize("explicit", [False, True])
+def test_all_gather_v(policy, dtype, R, explicit):
+    h = handle(R)
+    set_variant(h, *POLICIES[policy])
+    seed = 13 * R + explicit
+    counts, displs, total = _rs_case(R, seed, explicit)
+    x = [inputs(1, int(c), dtype, seed=seed + k)[0] for k, c in enumerate(counts)]
+    outs = [Guarded(total, dtype) for _ in range(R)]
+    for o in outs:   # gaps between blocks keep their initial value in both sides
+        o.view.zero_()
+    rd.purlin_all_gather(h, x, [o.view for o in outs], counts, displs, dtype)
+    run_ok(h)
+    want = oracle.all_gather(oracle_in(x), counts, displs, out_count=total)
+    for j in range(R):
+        assert same_bits(host_bits(outs[j].view), want[j]), j
+        assert outs[j].guards_intact()
+
+
+@pytest.mark.parametrize("policy", ["zs", "snac_tiny_chunks"])
+def test_all_gather_in_place(policy):
+    R, c, dtype = 8, 999, "bf16"
+    h = handle(R)
+    set_variant(h, *POLICIES[policy])
+    outs = inputs(R, R * c, dtype, seed=9)
+    ins = [outs[k][k * c:(k + 1) * c] for k in range(R)]
+    want = oracle.all_gather([host_bits(i) for i in ins])
+    rd.purlin_all_gather(h, ins, outs, [c] * R, None, dtype)
+    run_ok(h)
+    for j in range(R):
+        assert same_bits(host_bits(outs[j]), want[j])
+
+
+@pytest.mark.parametrize("policy", ["zs", "snac_tiny_chunks"])
+def test_all_gather_bytes_at_odd_offsets(policy):
+    """u8 payloads at odd byte offsets use narrow copy units."""
+    R = 3
+    h = handle(R)
+    set_variant(h, *POLICIES[policy])
+    counts = np.array([4097, 31, 1000])
+    x = [inputs(1, int(c), "u8", seed=k, offset=k + 1)[0] for k, c in enumerate(counts)]
+    outs = [Guarded(int(counts.sum()), "u8", offset=5) for _ in range(R)]
+    rd.purlin_all_gather(h, x, [o.view for o in outs], counts, None, "u8")
+    run_ok(h)
+    want = oracle.all_gather(oracle_in(x), counts)
+    for j in range(R):
+        assert same_bits(host_bits(outs[j].view), want[j])
+        assert outs[j].guards_intact()
+
+
+# ------------------------------------------------------------------ AllToAll(V)
+
+@pytest.mark.parametrize("policy", list(POLICIES))
+@pytest.mark.parametrize("dtype", ["bf16", "u8", "f32"])
+@pytest.mark.parametrize("R", [1, 2, 8])
+@pytest.mark.parametrize("explicit", [False, True])
+def test_all_to_all_v(policy, dtype, R, explicit):
+    h = handle(R)
+    set_variant(h, *POLICIES[policy])
+    seed = 17 * R + explicit
+    C = workloads.random_pair_counts(R, 700, seed)
+    sd = rdsp = None
+    if explicit:   # reversed packing on both sides
+        sd = np.zeros((R, R), dtype=np.int64)
+        rdsp = np.zeros((R, R), dtype=np.int64)
+        for s in range(R):
+            pos = 0
+            for j in reversed(range(R)):
+                sd[s, j] = pos
+                pos += C[s, j]
+        for j in range(R):
+            pos = 0
+            for s in reversed(range(R)):
+                rdsp[j, s] = pos
+                pos += C[s, j]
+    x = [inputs(1, int(C[s].sum()), dtype, seed=seed + s)[0] for s in range(R)]
+    outs = [Guarded(int(C[:, j].sum()), dtype) for j in range(R)]
+    rd.purlin_all_to_all_v(h, x, [o.view for o in outs], C, sd, rdsp, dtype)
+    run_ok(h)
+    want = oracle.all_to_all_v(oracle_in(x), C, sd, rdsp)
+    for j in range(R):
+        assert same_bits(host_bits(outs[j].view), want[j]), j
+        assert outs[j].guards_intact()
+
+
+@pytest.mark.parametrize("policy", ["zs", "snac_tiny_chunks"])
+def test_all_to_all_fixed_twice_is_identity(policy):
+    R, c, dtype = 8, 3001, "bf16"
+    h = handle(R)
+    set_variant(h, *POLICIES[policy])
+    x = inputs(R, R * c, dtype, seed=21)
+    mid = [torch.empty_like(t) for t in x]
+    back = [torch.empty_like(t) for t in x]
+    rd.purlin_all_to_all(h, x, mid, c, dtype)
+    rd.purlin_all_to_all(h, mid, back, c, dtype)
+    run_ok(h)
+    want = oracle.all_to_all_v(oracle_in(x), np.full((R, R), c))
+    for j in range(R):
+        assert same_bits(host_bits(mid[j]), want[j])
+        assert same_bits(host_bits(back[j]), host_bits(x[j]))
+
+
+# ------------------------------------------------------------- tree order
+
+def _as_f64(bits, dtype):
+    if dtype == "f32":
+        return bits.astype(np.float64)
+    return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).double().numpy()
+
+
+@pytest.mark.parametrize("policy", ["zs", "snac_tiny_chunks"])
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("R", [3, 8])
+def test_tree_order(policy, dtype, R):
+    """The pairwise order is bit-exact to the oracle's pairwise fold.  Against
+    the fixed rank order it may differ by the reordering error of binary32 adds,
+    2(R-1) 2^-24 sum|x|, plus one unit in the last place of the output type:
+    1e-6 relative to sum|x| for fp32, 1 ulp plus that for bf16."""
+    h = handle(R)
+    set_variant(h, *POLICIES[policy])
+    c = 4000
+    x = inputs(R, R * c, dtype, seed=31 + R)
+    outs = [torch.empty(c, dtype=x[0].dtype, device="cuda") for _ in range(R)]
+    rd.purlin_set_reduce_order(h, rd.ORDER_TREE)
+    try:
+        rd.purlin_reduce_scatter(h, x, outs, [c] * R, None, dtype)
+        run_ok(h)
+    finally:
+        rd.purlin_set_reduce_order(h, rd.ORDER_FIXED)
+    xin = oracle_in(x)
+    tree = oracle.reduce_scatter(xin, [c] * R, dtype=dtype, order="tree")
+    fixed = oracle.reduce_scatter(xin, [c] * R, dtype=dtype)
+    mag = np.sum([np.abs(_as_f64(a, dtype)) for a in xin], axis=0)
+    for k in range(R):
+        got = host_bits(outs[k])
+        assert same_bits(got, tree[k])
+        g, f = _as_f64(got, dtype), _as_f64(fixed[k], dtype)
+        scale = mag[k * c:(k + 1) * c]
+        reorder = 2 * (R - 1) * 2.0 ** -24 * scale
+        if dtype == "f32":
+            assert np.all(np.abs(g - f) <= 1e-6 * scale + 1e-38)
+        else:
+            ulp = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(f), 2.0 ** -126))) - 7)
+            assert np.all(np.abs(g - f) <= ulp + reorder)
+
+
+# ------------------------------------------------------------ argument errors
+
+def test_argument_errors_enqueue_nothing():
+    R, n = 2, 64
+    h = handle(R)
+    set_variant(h, rd.VARIANT_ZS)
+    x = inputs(R, n, "f32", seed=1)
+    out = [torch.zeros(n, device="cuda") for _ in range(R)]
+    with pytest.raises(rd.PurlinError) as e:   # outputs overlap
+        rd.purlin_all_reduce(h, x, [out[0], out[0]], n, "f32")
+    assert e.value.status == rd.ERR_INVALID_ARG
+    with pytest.raises(rd.PurlinError) as e:   # an output inside another rank's input
+        rd.purlin_all_reduce(h, x, [x[1], out[1]], n, "f32")
+    assert e.value.status == rd.ERR_INVALID_ARG
+    with pytest.raises(rd.PurlinError) as e:   # copy op is not a reduction
+        rd.purlin_all_reduce(h, x, out, n, "f32", op="copy")
+    assert e.value.status == rd.ERR_UNSUPPORTED
+    with pytest.raises(rd.PurlinError) as e:   # misaligned float stream
+        rd.purlin_all_reduce(h, [x[0].data_ptr() + 1, x[1]], out, n - 1, "f32")
+    assert e.value.status == rd.ERR_INVALID_ARG
+    with pytest.raises(rd.PurlinError) as e:   # null buffer with a non-zero count
+        rd.purlin_all_reduce(h, [None, x[1]], out, n, "f32")
+    assert e.value.status == rd.ERR_INVALID_ARG
+    with pytest.raises(rd.PurlinError) as e:   # overlapping AllGather blocks
+        rd.purlin_all_gather(h, x, out, [8, 8], [0, 4], "f32")
+    assert e.value.status == rd.ERR_INVALID_ARG
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(out[0]) == 0 and torch.count_nonzero(out[1]) == 0
+    with pytest.raises(rd.PurlinError) as e:
+        rd.purlin_create(9)
+    assert e.value.status == rd.ERR_INVALID_ARG
+
+
+def test_last_launch_reports_the_call():
+    R, n = 8, 1 << 20
+    h = handle(R)
+    set_variant(h, rd.VARIANT_ZS)
+    x = inputs(R, n, "bf16", seed=2)
+    out = [torch.empty_like(t) for t in x]
+    rd.purlin_all_reduce(h, x, out, n, "bf16")
+    info = rd.purlin_last_launch(h)
+    assert info["variant"] == rd.VARIANT_ZS and info["kernels"] == 1
+    assert info["bytes_moved"] == 2 * R * n * 2
+    assert 1 <= info["grid"] and info["block"] == 256 and info["sms"] > 100
+    set_variant(h, rd.VARIANT_STAGED)
+    rd.purlin_all_reduce(h, x, out, n, "bf16")
+    info = rd.purlin_last_launch(h)
+    assert info["variant"] == rd.VARIANT_STAGED and info["grid"] % 3 == 0
+    run_ok(h)
