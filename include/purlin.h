@@ -190,6 +190,44 @@ PURLIN_API purlin_status_t purlin_all_to_all_v(purlin_handle_t h, const void* co
                                     const size_t send_displs[], const size_t recv_displs[],
                                     purlin_dtype_t dtype, purlin_stream_t stream);
 
+/* AllReduce that allocates nothing.  The paper has no counterpart to this call.
+ *
+ * Some callers cannot call cudaMalloc: a host framework that has reserved the
+ * GPU's memory for its own pool (a direct cudaMalloc would fail or escape its
+ * accounting), a plugin that may not own device memory, or a latency-critical
+ * path that cannot take the synchronization cudaMalloc/cudaFree may cause.  The
+ * handle-based calls above allocate their scratch in purlin_create(); this one
+ * needs no handle.  It runs the staged (SNAC) AllReduce kernel -- same result,
+ * bit for bit, as purlin_all_reduce -- with its staging ring, flags and status
+ * word in one static device array of PURLIN_NOALLOC_SCRATCH_BYTES (8 MiB) that
+ * every GPU which loads this library holds until the process exits.  It calls no
+ * cudaMalloc, cudaFree or other allocating routine.
+ *   in, out      R device pointers each; out[r] == in[r] (in-place) is allowed,
+ *                any other overlap is PURLIN_ERR_INVALID_ARG.
+ *   R            1..PURLIN_MAX_RANKS;  count: elements per rank.
+ *   dtype        PURLIN_F32, PURLIN_BF16 or PURLIN_F16.
+ *   chunk_bytes  staged bytes per rank per pipeline step, a multiple of 256
+ *                (0 = 32 KiB); depth: ring slots, 0..8 (0 = 2).  A ring that
+ *                cannot fit in the static array -- depth * (R + 1) * chunk_bytes
+ *                above PURLIN_NOALLOC_SCRATCH_BYTES - 64 KiB -- is rejected with
+ *                PURLIN_ERR_INVALID_ARG before anything is enqueued.
+ *   device_status  optional DEVICE int: set to 0 on the stream, then to
+ *                PURLIN_ERR_TIMEOUT if a bounded wait of the kernel ran out
+ *                (NULL: the library's own word inside the static array is used
+ *                and not reported).
+ *   stream       runs on the current device, on this stream.
+ * The first call on a device looks up the static array's device address (with
+ * that device current); make that first call before any stream capture.  Every
+ * call on a device shares the one array: calls whose kernels overlap on the GPU
+ * (e.g. on two streams at once) race and produce wrong results; serialize them.
+ * Flags hold per-call epoch tags and the status word is cleared at each call, so
+ * what the last call left behind needs no other clearing. */
+#define PURLIN_NOALLOC_SCRATCH_BYTES (8u << 20)
+PURLIN_API purlin_status_t purlin_all_reduce_noalloc(const void* const in[], void* const out[],
+                                                     int R, size_t count, purlin_dtype_t dtype,
+                                                     size_t chunk_bytes, int depth,
+                                                     int* device_status, purlin_stream_t stream);
+
 /* ------------------------------------------------------------------------- */
 /* Policy, status, introspection                                              */
 /* ------------------------------------------------------------------------- */

@@ -45,7 +45,7 @@ EXPORTED = (
     "purlin_all_reduce", "purlin_all_to_all", "purlin_all_to_all_v", "purlin_set_policy",
     "purlin_set_reduce_order", "purlin_set_timeout", "purlin_query_status",
     "purlin_last_launch", "purlin_status_string", "purlin_version", "purlin_plan_segments",
-    "purlin_debug_inject",
+    "purlin_debug_inject", "purlin_all_reduce_noalloc",
 )
 
 
@@ -121,6 +121,7 @@ def lib():
                                      ctypes.POINTER(Segment), i32, ctypes.POINTER(i32),
                                      ctypes.POINTER(ctypes.c_uint32)],
             "purlin_debug_inject": [vp, i32],
+            "purlin_all_reduce_noalloc": [pp, pp, i32, sz, i32, sz, i32, vp, vp],
         }
         for name, args in sigs.items():
             fn = getattr(L, name)
@@ -274,6 +275,16 @@ def purlin_status_string(status) -> str:
 
 def purlin_debug_inject(h, what: int) -> None:
     _check(lib().purlin_debug_inject(h, int(what)), "purlin_debug_inject")
+
+
+def purlin_all_reduce_noalloc(ins, outs, count, dtype="bf16", chunk_bytes=0, depth=0,
+                              device_status=None, stream=None) -> None:
+    """AllReduce that allocates nothing (see purlin.h): for callers that may not
+    call cudaMalloc.  Scratch is a fixed 8 MiB static device array."""
+    _check(lib().purlin_all_reduce_noalloc(_ptrs(ins), _ptrs(outs), len(ins), int(count),
+                                           _dtype(dtype), int(chunk_bytes), int(depth),
+                                           _ptr(device_status), _stream(stream)),
+           "purlin_all_reduce_noalloc")
 
 
 def purlin_plan_segments(coll, R, in_addr, out_addr, counts=None, displs_a=None, displs_b=None,

@@ -19,7 +19,7 @@ BUILD = os.path.join(HERE, "_build")
 LIBDIR = os.path.join(HERE, "lib")
 LIB = os.path.join(LIBDIR, "libpurlin.so")
 
-SOURCES = ["capi.cpp", "layout.cpp", "zs_kernels.cu", "snac_kernels.cu"]
+SOURCES = ["capi.cpp", "layout.cpp", "zs_kernels.cu", "snac_kernels.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-std=c++17", "-O3", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
           "-Xcompiler", "-fvisibility=hidden",

@@ -1,0 +1,143 @@
+// noalloc.cu -- purlin_all_reduce_noalloc: the staged (SNAC) AllReduce for
+// callers that must not allocate device memory.
+//
+// Some callers cannot call cudaMalloc: a host framework that has reserved the
+// GPU's memory for its own pool allocator (a direct cudaMalloc would fail, or
+// would bypass the framework's accounting), a plugin that is forbidden to own
+// device memory, or a latency-critical path that cannot afford the device-wide
+// synchronization cudaMalloc/cudaFree may imply.  For them this file keeps the
+// scratch memory the staged kernel needs -- its staging ring, its ready/free
+// flags and a status word -- in ONE file-scope __device__ array of fixed size,
+// created when the library is loaded and held by every GPU that loads it until
+// the process exits.  The paper has no counterpart to this entry point.
+//
+// The array's name in host code is only a host-side stand-in, not a device
+// address, so the device address is looked up with cudaGetSymbolAddress once
+// per device (with that device current) and passed to the kernel.
+#include "purlin.h"
+
+#include <atomic>
+#include <cstdint>
+#include <mutex>
+
+#include "internal.h"
+#include "plan.h"
+#include "snac.h"
+
+namespace purlin {
+namespace {
+
+constexpr size_t kScratchBytes = PURLIN_NOALLOC_SCRATCH_BYTES;
+constexpr size_t kStatusOffset = 0;               // one int, padded to 256 bytes
+constexpr size_t kFlagsOffset = 256;
+constexpr size_t kFlagWords = 4096;               // 32 KiB of uint64 flags
+constexpr size_t kStagingOffset = 64 * 1024;      // the rest is the staging ring
+constexpr size_t kStagingBytes = kScratchBytes - kStagingOffset;
+constexpr size_t kDefaultChunk = 32 * 1024;
+constexpr int kDefaultDepth = 2;
+constexpr uint64_t kTimeoutNs = 1000000000ull;
+constexpr int kMaxDevices = 64;
+
+static_assert(kFlagsOffset + kFlagWords * sizeof(uint64_t) <= kStagingOffset, "layout");
+
+// Zero at load time; the flags hold epoch tags, so they never need clearing.
+static __device__ __align__(256) char g_noalloc_scratch[kScratchBytes];
+
+struct DeviceScratch {
+    std::once_flag once;
+    cudaError_t setup_error = cudaSuccess;
+    char* base = nullptr;   // device address of g_noalloc_scratch on this device
+    int sms = 0;
+    std::atomic<uint64_t> epoch{0};
+};
+
+DeviceScratch g_devices[kMaxDevices];
+
+void set_up(DeviceScratch& d, int device)
+{
+    void* ptr = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, device);
+    d.base = static_cast<char*>(ptr);
+    d.setup_error = e;
+}
+
+bool overlaps(uint64_t a, uint64_t alen, uint64_t b, uint64_t blen)
+{
+    return alen && blen && a < b + blen && b < a + alen;
+}
+
+}  // namespace
+}  // namespace purlin
+
+using namespace purlin;
+
+extern "C" PURLIN_API purlin_status_t purlin_all_reduce_noalloc(
+    const void* const in[], void* const out[], int R, size_t count, purlin_dtype_t dtype,
+    size_t chunk_bytes, int depth, int* device_status, purlin_stream_t stream)
+{
+    if (!in || !out || R < 1 || R > PURLIN_MAX_RANKS) return PURLIN_ERR_INVALID_ARG;
+    if (dtype != PURLIN_F32 && dtype != PURLIN_BF16 && dtype != PURLIN_F16)
+        return PURLIN_ERR_INVALID_ARG;
+    if (depth < 0 || depth > 8 || chunk_bytes % 256) return PURLIN_ERR_INVALID_ARG;
+    const size_t chunk = chunk_bytes ? chunk_bytes : kDefaultChunk;
+    const int dep = depth ? depth : kDefaultDepth;
+    // One channel's ring must fit in the static staging area.
+    if (chunk > kStagingBytes / ((size_t)dep * (R + 1))) return PURLIN_ERR_INVALID_ARG;
+    const size_t esz = dtype == PURLIN_F32 ? 4 : 2;
+    if (count > UINT64_MAX / esz) return PURLIN_ERR_INVALID_ARG;
+    const uint64_t bytes = (uint64_t)count * esz;
+    uint64_t inp[kMaxRanks], outp[kMaxRanks];
+    for (int r = 0; r < R; ++r) {
+        inp[r] = reinterpret_cast<uint64_t>(in[r]);
+        outp[r] = reinterpret_cast<uint64_t>(out[r]);
+        if (bytes && (!inp[r] || !outp[r] || inp[r] % esz || outp[r] % esz))
+            return PURLIN_ERR_INVALID_ARG;
+    }
+    for (int a = 0; a < R; ++a)
+        for (int b = 0; b < R; ++b) {
+            if (b > a && overlaps(outp[a], bytes, outp[b], bytes)) return PURLIN_ERR_INVALID_ARG;
+            if (overlaps(inp[a], bytes, outp[b], bytes) && !(a == b && inp[a] == outp[b]))
+                return PURLIN_ERR_INVALID_ARG;   // only out[r] == in[r] may alias
+        }
+
+    int device = 0;
+    if (cudaGetDevice(&device) != cudaSuccess) return PURLIN_ERR_CUDA;
+    if (device < 0 || device >= kMaxDevices) return PURLIN_ERR_UNSUPPORTED;
+    DeviceScratch& d = g_devices[device];
+    std::call_once(d.once, [&d, device] { set_up(d, device); });
+    if (d.setup_error != cudaSuccess || !d.base) return PURLIN_ERR_CUDA;
+
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    int* status = device_status ? device_status
+                                : reinterpret_cast<int*>(d.base + kStatusOffset);
+    if (cudaMemsetAsync(status, 0, sizeof(int), s) != cudaSuccess) return PURLIN_ERR_CUDA;
+    if (bytes == 0) return PURLIN_OK;
+
+    Piece piece{0, 0, bytes, kEveryRank, kEveryRank};
+    SnacRequest rq{};
+    rq.coll = Coll::AllReduce;
+    rq.R = R;
+    rq.dtype = (int)dtype;
+    rq.order = PURLIN_ORDER_FIXED;
+    rq.esz = esz;
+    rq.pieces = &piece;
+    rq.npieces = 1;
+    for (int r = 0; r < R; ++r) { rq.in[r] = inp[r]; rq.out[r] = outp[r]; }
+    SnacConfig cfg{};
+    cfg.staging = d.base + kStagingOffset;
+    cfg.staging_bytes = kStagingBytes;
+    cfg.flags = reinterpret_cast<uint64_t*>(d.base + kFlagsOffset);
+    cfg.flag_words = kFlagWords;
+    cfg.status = status;
+    cfg.epoch = d.epoch.fetch_add(1) + 1;
+    cfg.chunk_bytes = chunk;
+    cfg.depth = dep;
+    cfg.channels = 0;
+    cfg.sms = d.sms;
+    cfg.timeout_ns = kTimeoutNs;
+    cfg.inject_skip_notify = 0;
+    SnacLaunch launch{};
+    return snac_run_on_stack(rq, cfg, s, &launch);
+}

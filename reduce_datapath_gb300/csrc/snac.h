@@ -64,6 +64,11 @@ struct SnacLaunch {
 purlin_status_t snac_run(const SnacRequest& rq, const SnacConfig& cfg, cudaStream_t stream,
                          SnacLaunch* launch);
 
+// Same as snac_run, with the kernel's parameter block on the caller's stack
+// instead of in thread-local storage (no memory is allocated).
+purlin_status_t snac_run_on_stack(const SnacRequest& rq, const SnacConfig& cfg,
+                                  cudaStream_t stream, SnacLaunch* launch);
+
 // Channels, chunk and depth that snac_run would use (for introspection/tests).
 purlin_status_t snac_geometry(int R, Coll coll, const SnacConfig& cfg, int resident_per_sm,
                               size_t* chunk, int* depth, int* channels);

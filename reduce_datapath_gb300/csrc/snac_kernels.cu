@@ -390,10 +390,11 @@ purlin_status_t snac_geometry(int R, Coll coll, const SnacConfig& cfg, int resid
     return PURLIN_OK;
 }
 
-purlin_status_t snac_run(const SnacRequest& rq, const SnacConfig& cfg, cudaStream_t stream,
-                         SnacLaunch* launch)
+namespace {
+
+purlin_status_t run_with(SnacParams& p, const SnacRequest& rq, const SnacConfig& cfg,
+                         cudaStream_t stream, SnacLaunch* launch)
 {
-    static thread_local SnacParams p;
     std::memset(&p, 0, sizeof(p));
     const bool reduce = rq.coll == Coll::ReduceScatter || rq.coll == Coll::AllReduce;
     uint32_t ntiles = 0;
@@ -459,6 +460,22 @@ purlin_status_t snac_run(const SnacRequest& rq, const SnacConfig& cfg, cudaStrea
     if (ce != cudaSuccess) return PURLIN_ERR_CUDA;
     *launch = SnacLaunch{1, grid, kThreads, depth, nch, chunk};
     return PURLIN_OK;
+}
+
+}  // namespace
+
+purlin_status_t snac_run(const SnacRequest& rq, const SnacConfig& cfg, cudaStream_t stream,
+                         SnacLaunch* launch)
+{
+    static thread_local SnacParams p;
+    return run_with(p, rq, cfg, stream, launch);
+}
+
+purlin_status_t snac_run_on_stack(const SnacRequest& rq, const SnacConfig& cfg,
+                                  cudaStream_t stream, SnacLaunch* launch)
+{
+    SnacParams p;
+    return run_with(p, rq, cfg, stream, launch);
 }
 
 }  // namespace purlin
