@@ -55,6 +55,10 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--only", choices=["rs", "ag", "ar", "a2av"], default=None,
+                    help="time one collective alone (profiling runs); prints a short line")
+    ap.add_argument("--bytes-per-rank", type=int, default=BYTES_PER_RANK,
+                    help="with --only: input bytes per rank")
     return ap.parse_args()
 
 
@@ -538,8 +542,73 @@ def bench_e2e(args, rd, torch, h, x, y, z, counts, stream):
             "ms_per_step": ms, "steps": K}
 
 
+def bench_only(args):
+    """One collective of the bench workload's shape, K times (for ncu runs)."""
+    import torch
+
+    import reduce_datapath_gb300 as rd
+    import workloads
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    rd.build()
+    n = args.bytes_per_rank // 2
+    c = n // R
+    h = rd.purlin_create(R, 0, 0)
+    variant = rd.VARIANT_ZS if args.variant == "zs" else rd.VARIANT_STAGED
+    rd.purlin_set_policy(h, args.chunk, args.depth, args.ctas, variant)
+    stream = torch.cuda.Stream(device=dev)
+    if args.only == "rs":
+        x = workloads.rank_buffers(WORKLOAD, R, n, "bf16", device=dev)
+        y = [torch.empty(c, dtype=torch.bfloat16, device=dev) for _ in range(R)]
+        fn = lambda: rd.purlin_reduce_scatter(h, x, y, [c] * R, None, "bf16", stream=stream)
+        nbytes = (R + 1) * c * R * 2
+    elif args.only == "ag":
+        y = workloads.rank_buffers(WORKLOAD, R, c, "bf16", device=dev)
+        z = [torch.empty(n, dtype=torch.bfloat16, device=dev) for _ in range(R)]
+        fn = lambda: rd.purlin_all_gather(h, y, z, [c] * R, None, "bf16", stream=stream)
+        nbytes = (R + 1) * c * R * 2
+    elif args.only == "ar":
+        x = workloads.rank_buffers(WORKLOAD, R, n, "bf16", device=dev)
+        o = [torch.empty_like(t) for t in x]
+        fn = lambda: rd.purlin_all_reduce(h, x, o, n, "bf16", stream=stream)
+        nbytes = 2 * R * n * 2
+    else:
+        H = workloads.HIDDEN
+        T = max(1, n // H)
+        C = workloads.zipf_pair_counts(R, T, workloads.ZIPF_S, workloads.seed_for("moe_a2av_r8", 9))
+        x = workloads.rank_buffers("moe_a2av_r8", R, T * H, "bf16", device=dev)
+        o = [torch.empty(int(C[:, j].sum()) * H, dtype=torch.bfloat16, device=dev)
+             for j in range(R)]
+        fn = lambda: rd.purlin_all_to_all_v(h, x, o, C * H, None, None, "bf16", stream=stream)
+        nbytes = 2 * int(C.sum()) * H * 2
+    with torch.cuda.stream(stream):
+        for _ in range(max(1, args.warmup)):
+            fn()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    K = max(1, args.steps)
+    a.record(stream)
+    for _ in range(K):
+        fn()
+    b.record(stream)
+    torch.cuda.synchronize()
+    assert rd.purlin_query_status(h) == rd.OK
+    info = rd.purlin_last_launch(h)
+    rd.purlin_destroy(h)
+    us = a.elapsed_time(b) * 1e3 / K
+    print(json.dumps({"only": args.only, "variant": args.variant,
+                      "bytes_per_rank": args.bytes_per_rank, "us": us,
+                      "gbs": nbytes / (us / 1e6) / 1e9, "algorithmic_bytes": nbytes,
+                      "launch": info}), flush=True)
+
+
 def main():
     args = parse_args()
+    if args.only:
+        bench_only(args)
+        return
     if args.impl == "reference":
         bench_reference(args)
     else:
