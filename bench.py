@@ -212,6 +212,13 @@ def max_over_ranks(world, value, device=None):
     return float(t.item())
 
 
+def whole_job_value(world, steps, bytes_per_step, local_ms, device=None):
+    """Replicas: every rank moved steps * bytes_per_step; the job took the
+    slowest rank's time.  Returns (GB/s of the whole job, max ms)."""
+    max_ms = max_over_ranks(world, local_ms, device)
+    return world * steps * bytes_per_step / (max_ms / 1e3) / 1e9, max_ms
+
+
 # ----------------------------------------------------------------- the workload
 
 def step_bytes():
@@ -381,9 +388,8 @@ def bench_purlin(args):
     if status != rd.OK:
         raise RuntimeError("device status: " + rd.purlin_status_string(status))
     launches = K * (rs_info["kernels"] + ag_info["kernels"])
-    max_ms = max_over_ranks(world, total_ms, dev)
     rs_b, ag_b = step_bytes()
-    value = world * K * (rs_b + ag_b) / (max_ms / 1e3) / 1e9
+    value, max_ms = whole_job_value(world, K, rs_b + ag_b, total_ms, dev)
 
     rs_avg = sum(rs_ms) / K
     ag_avg = sum(ag_ms) / K

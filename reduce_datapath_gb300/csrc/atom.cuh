@@ -56,6 +56,52 @@ __device__ __forceinline__ void store(char* p, const Vec<32>& v)
                  : "memory");
 }
 
+// L2 eviction priority for a whole launch, as a cache-policy operand
+// (createpolicy): a stream read or written exactly once can be marked
+// evict-first so that it does not push out lines another stream will reuse.
+__device__ __forceinline__ uint64_t l2_policy(uint32_t kind)
+{
+    uint64_t pol;
+    if (kind == kL2EvictFirst)
+        asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    else if (kind == kL2EvictLast)
+        asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    else
+        asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+__device__ __forceinline__ void load(Vec<16>& v, const char* p, uint64_t pol)
+{
+    asm volatile("ld.global.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+                 : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3])
+                 : "l"(p), "l"(pol));
+}
+
+__device__ __forceinline__ void load(Vec<32>& v, const char* p, uint64_t pol)
+{
+    asm volatile("ld.global.L1::no_allocate.L2::cache_hint.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7},"
+                 " [%8], %9;"
+                 : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3]),
+                   "=r"(v.w[4]), "=r"(v.w[5]), "=r"(v.w[6]), "=r"(v.w[7])
+                 : "l"(p), "l"(pol));
+}
+
+__device__ __forceinline__ void store(char* p, const Vec<16>& v, uint64_t pol)
+{
+    asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1,%2,%3,%4}, %5;"
+                 :: "l"(p), "r"(v.w[0]), "r"(v.w[1]), "r"(v.w[2]), "r"(v.w[3]), "l"(pol)
+                 : "memory");
+}
+
+__device__ __forceinline__ void store(char* p, const Vec<32>& v, uint64_t pol)
+{
+    asm volatile("st.global.L2::cache_hint.v8.u32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8}, %9;"
+                 :: "l"(p), "r"(v.w[0]), "r"(v.w[1]), "r"(v.w[2]), "r"(v.w[3]),
+                    "r"(v.w[4]), "r"(v.w[5]), "r"(v.w[6]), "r"(v.w[7]), "l"(pol)
+                 : "memory");
+}
+
 // Loads of data another CTA wrote during this kernel (the SNAC staging ring):
 // cached in L2 only (.cg), so no stale L1 line can be returned.
 __device__ __forceinline__ void load_cg(Vec<16>& v, const char* p)

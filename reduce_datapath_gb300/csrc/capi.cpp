@@ -41,7 +41,9 @@ struct purlin_handle {
     int variant = PURLIN_VARIANT_AUTO;
     int order = PURLIN_ORDER_FIXED;
     uint64_t timeout_ns = 1000000000ull;
-    int max_unit_log2 = 5;
+    int max_unit_log2 = 0;   // 0: per collective (AllReduce 4 = 16 B, else 5 = 32 B)
+    int l2_load = -1;        // -1: per collective; else kL2Normal/EvictFirst/EvictLast
+    int l2_store = -1;
     int inject = 0;  // purlin_debug_inject, one staged call
     purlin_launch_info_t last{};
 };
@@ -137,12 +139,43 @@ purlin_status_t check_buffers(Coll coll, int R, const uint64_t* in, const uint64
     return PURLIN_OK;
 }
 
+// Launch-wide knobs of the zero-staging kernels.
+struct ZsKnobs {
+    int max_unit_log2;
+    uint32_t l2_load;
+    uint32_t l2_store;
+};
+
+// Measured on GB300 (64 MiB per rank, R = 8, bf16):
+//  - the fused AllReduce (R loads and R stores per unit) runs best with 16-byte
+//    units (170 vs 174 us), everything else with 32-byte units (ReduceScatter
+//    91 vs 96 us);
+//  - sources that are read exactly once (sums, AllToAll) are loaded
+//    evict-first: in a ReduceScatter -> AllGather step this keeps the reduced
+//    partitions and the previous call's dirty lines in L2 (ReduceScatter
+//    108.8 -> 98.5 us inside the step); AllReduce and AllToAll outputs are
+//    written evict-first.
+ZsKnobs zs_knobs(const purlin_handle* h, Coll coll)
+{
+    ZsKnobs k;
+    k.max_unit_log2 = h->max_unit_log2 ? h->max_unit_log2 : (coll == Coll::AllReduce ? 4 : 5);
+    k.l2_load = h->l2_load >= 0 ? (uint32_t)h->l2_load
+                                : (coll == Coll::AllGather ? kL2Normal : kL2EvictFirst);
+    k.l2_store = h->l2_store >= 0 ? (uint32_t)h->l2_store
+                                  : ((coll == Coll::AllReduce || coll == Coll::AllToAllV)
+                                         ? kL2EvictFirst : kL2Normal);
+    return k;
+}
+
 template <int MAXSEG>
 purlin_status_t make_params(ZsParams<MAXSEG>& p, const Piece* pieces, int npieces, int R,
                             const uint64_t* in, const uint64_t* out, size_t esz, bool reduce,
-                            int max_unit_log2)
+                            const ZsKnobs& k)
 {
+    const int max_unit_log2 = k.max_unit_log2;
     std::memset(&p, 0, sizeof(p));
+    p.l2_load = k.l2_load;
+    p.l2_store = k.l2_store;
     for (int r = 0; r < R; ++r) {
         p.in[r] = reinterpret_cast<const char*>(in[r]);
         p.out[r] = reinterpret_cast<char*>(out[r]);
@@ -269,29 +302,30 @@ purlin_status_t run(purlin_handle_t h, Coll coll, const void* const in_[], void*
 
     info.variant = PURLIN_VARIANT_ZS;
     cudaError_t ce = cudaSuccess;
+    const ZsKnobs knobs = zs_knobs(h, coll);
     if (coll == Coll::AllToAllV) {
         static thread_local ZsParams<kSegsLarge> p;
-        st = make_params(p, pieces, np, R, in, out, esz, false, h->max_unit_log2);
+        st = make_params(p, pieces, np, R, in, out, esz, false, knobs);
         if (st != PURLIN_OK) return st;
         int grid = zs_grid(h, p.ntiles, zs_copy_resident_ctas(true, false));
         if (grid > 0) ce = zs_copy_launch(p, false, grid, s);
         info.grid = grid;
         info.kernels = grid > 0;
-        info.chunk_bytes = tile_bytes(h->max_unit_log2, kUnrollCopy);
+        info.chunk_bytes = tile_bytes(knobs.max_unit_log2, kUnrollCopy);
     } else {
         static thread_local ZsParams<kSegsSmall> p;
-        st = make_params(p, pieces, np, R, in, out, esz, reduce, h->max_unit_log2);
+        st = make_params(p, pieces, np, R, in, out, esz, reduce, knobs);
         if (st != PURLIN_OK) return st;
         bool fan_all = coll == Coll::AllGather || coll == Coll::AllReduce;
         int grid;
         if (reduce) {
             grid = zs_grid(h, p.ntiles, zs_reduce_resident_ctas(dtype, h->order, fan_all));
             if (grid > 0) ce = zs_reduce_launch(p, dtype, h->order, fan_all, grid, s);
-            info.chunk_bytes = tile_bytes(h->max_unit_log2, kUnrollReduce);
+            info.chunk_bytes = tile_bytes(knobs.max_unit_log2, kUnrollReduce);
         } else {
             grid = zs_grid(h, p.ntiles, zs_copy_resident_ctas(false, fan_all));
             if (grid > 0) ce = zs_copy_launch(p, fan_all, grid, s);
-            info.chunk_bytes = tile_bytes(h->max_unit_log2, kUnrollCopy);
+            info.chunk_bytes = tile_bytes(knobs.max_unit_log2, kUnrollCopy);
         }
         info.grid = grid;
         info.kernels = grid > 0;
@@ -357,6 +391,9 @@ purlin_status_t purlin_create(purlin_handle_t* out, int R, size_t staging_bytes,
         purlin_destroy(h);
         return PURLIN_ERR_CUDA;
     }
+    // Tuning knobs for measurements only; the defaults are the measured best.
+    if (const char* u = std::getenv("PURLIN_L2_LOAD")) h->l2_load = std::atoi(u) % 3;
+    if (const char* u = std::getenv("PURLIN_L2_STORE")) h->l2_store = std::atoi(u) % 3;
     if (const char* u = std::getenv("PURLIN_MAX_UNIT")) {
         int v = std::atoi(u);
         if (v == 16) h->max_unit_log2 = 4;

@@ -47,10 +47,15 @@ static_assert(sizeof(Segment) == 32, "Segment is passed by value to kernels");
 
 // Kernel parameter block of the zero-staging Atom kernels (passed as a
 // __grid_constant__ argument: no host-to-device copy per call).
+// L2 eviction priority of a stream (PTX createpolicy).
+enum : uint32_t { kL2Normal = 0, kL2EvictFirst = 1, kL2EvictLast = 2 };
+
 template <int MAXSEG>
 struct ZsParams {
     const char* in[kMaxRanks];
     char* out[kMaxRanks];
+    uint32_t l2_load;   // eviction priority of source loads (kL2*)
+    uint32_t l2_store;  // ... and of destination stores
     uint32_t R;
     uint32_t nseg;
     uint32_t ntiles;

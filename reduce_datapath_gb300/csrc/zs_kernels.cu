@@ -37,22 +37,22 @@ __device__ __forceinline__ const Segment& segment_of(const ZsParams<MAXSEG>& p, 
 
 template <typename T, int ORDER, bool FAN_ALL, int BYTES>
 __device__ __forceinline__ void reduce_vector(const ZsParams<kSegsSmall>& p, const Segment& s,
-                                              uint64_t off, int R)
+                                              uint64_t off, int R, uint64_t lpol, uint64_t spol)
 {
     atom::Vec<BYTES> v[kMaxRanks];
     // All R loads are issued before the first add: R independent requests in
     // flight per thread.
 #pragma unroll
     for (int r = 0; r < kMaxRanks; ++r)
-        if (r < R) atom::load(v[r], p.in[r] + s.src_off + off);
+        if (r < R) atom::load(v[r], p.in[r] + s.src_off + off, lpol);
     atom::Vec<BYTES> o;
     atom::reduce_unit<T, ORDER, BYTES>(v, R, o);
     if (FAN_ALL) {
 #pragma unroll
         for (int r = 0; r < kMaxRanks; ++r)
-            if (r < R) atom::store(p.out[r] + s.dst_off + off, o);
+            if (r < R) atom::store(p.out[r] + s.dst_off + off, o, spol);
     } else {
-        atom::store(p.out[s.dst] + s.dst_off + off, o);
+        atom::store(p.out[s.dst] + s.dst_off + off, o, spol);
     }
 }
 
@@ -78,14 +78,16 @@ __global__ void __launch_bounds__(kThreads, 2)
 zs_reduce_kernel(const __grid_constant__ ZsParams<kSegsSmall> p)
 {
     const int R = (int)p.R;
+    const uint64_t lpol = atom::l2_policy(p.l2_load);
+    const uint64_t spol = atom::l2_policy(p.l2_store);
     for (uint32_t t = blockIdx.x; t < p.ntiles; t += gridDim.x) {
         const Segment& s = segment_of(p, t);
         const int ul = s.unit_log2;
         const uint64_t off = (uint64_t)(t - s.tile0) * tile_bytes(ul, kUnrollReduce) +
                              ((uint64_t)threadIdx.x << ul);
         if (off >= s.bytes) continue;
-        if (ul == 5) reduce_vector<T, ORDER, FAN_ALL, 32>(p, s, off, R);
-        else if (ul == 4) reduce_vector<T, ORDER, FAN_ALL, 16>(p, s, off, R);
+        if (ul == 5) reduce_vector<T, ORDER, FAN_ALL, 32>(p, s, off, R, lpol, spol);
+        else if (ul == 4) reduce_vector<T, ORDER, FAN_ALL, 16>(p, s, off, R, lpol, spol);
         else reduce_element<T, ORDER, FAN_ALL>(p, s, off, R);
     }
 }
@@ -96,11 +98,25 @@ using atom::Unit;
 using atom::load_unit;
 using atom::store_unit;
 
+template <int BYTES>
+__device__ __forceinline__ void load_hinted(Unit<BYTES>& u, const char* p, uint64_t pol)
+{
+    if constexpr (BYTES >= 16) atom::load(u.v, p, pol);
+    else load_unit<BYTES>(u, p);
+}
+
+template <int BYTES>
+__device__ __forceinline__ void store_hinted(char* p, const Unit<BYTES>& u, uint64_t pol)
+{
+    if constexpr (BYTES >= 16) atom::store(p, u.v, pol);
+    else store_unit<BYTES>(p, u);
+}
+
 // Atom::copy of one tile: kUnrollCopy units per thread, each warp access
 // contiguous; every unit loaded once and stored to one or all R outputs.
 template <int BYTES, bool FAN_ALL, int MAXSEG>
 __device__ __forceinline__ void copy_tile(const ZsParams<MAXSEG>& p, const Segment& s,
-                                          uint64_t base)
+                                          uint64_t base, uint64_t lpol, uint64_t spol)
 {
     const uint64_t rem = s.bytes - base;
     const char* src = p.in[s.src] + s.src_off + base;
@@ -108,7 +124,7 @@ __device__ __forceinline__ void copy_tile(const ZsParams<MAXSEG>& p, const Segme
 #pragma unroll
     for (int k = 0; k < kUnrollCopy; ++k) {
         const uint64_t o = (uint64_t)(k * kThreads + threadIdx.x) * BYTES;
-        if (o < rem) load_unit<BYTES>(u[k], src + o);
+        if (o < rem) load_hinted<BYTES>(u[k], src + o, lpol);
     }
 #pragma unroll
     for (int k = 0; k < kUnrollCopy; ++k) {
@@ -117,10 +133,10 @@ __device__ __forceinline__ void copy_tile(const ZsParams<MAXSEG>& p, const Segme
         if (FAN_ALL) {
             for (int r = 0; r < (int)p.R; ++r) {
                 char* dst = p.out[r] + s.dst_off + base + o;
-                if (dst != src + o) store_unit<BYTES>(dst, u[k]);  // in-place block: skip
+                if (dst != src + o) store_hinted<BYTES>(dst, u[k], spol);  // in-place: skip
             }
         } else {
-            store_unit<BYTES>(p.out[s.dst] + s.dst_off + base + o, u[k]);
+            store_hinted<BYTES>(p.out[s.dst] + s.dst_off + base + o, u[k], spol);
         }
     }
 }
@@ -129,17 +145,19 @@ template <bool FAN_ALL, int MAXSEG>
 __global__ void __launch_bounds__(kThreads, 2)
 zs_copy_kernel(const __grid_constant__ ZsParams<MAXSEG> p)
 {
+    const uint64_t lpol = atom::l2_policy(p.l2_load);
+    const uint64_t spol = atom::l2_policy(p.l2_store);
     for (uint32_t t = blockIdx.x; t < p.ntiles; t += gridDim.x) {
         const Segment& s = segment_of(p, t);
         const int ul = s.unit_log2;
         const uint64_t base = (uint64_t)(t - s.tile0) * tile_bytes(ul, kUnrollCopy);
         switch (ul) {
-        case 5: copy_tile<32, FAN_ALL>(p, s, base); break;
-        case 4: copy_tile<16, FAN_ALL>(p, s, base); break;
-        case 3: copy_tile<8, FAN_ALL>(p, s, base); break;
-        case 2: copy_tile<4, FAN_ALL>(p, s, base); break;
-        case 1: copy_tile<2, FAN_ALL>(p, s, base); break;
-        default: copy_tile<1, FAN_ALL>(p, s, base); break;
+        case 5: copy_tile<32, FAN_ALL>(p, s, base, lpol, spol); break;
+        case 4: copy_tile<16, FAN_ALL>(p, s, base, lpol, spol); break;
+        case 3: copy_tile<8, FAN_ALL>(p, s, base, lpol, spol); break;
+        case 2: copy_tile<4, FAN_ALL>(p, s, base, lpol, spol); break;
+        case 1: copy_tile<2, FAN_ALL>(p, s, base, lpol, spol); break;
+        default: copy_tile<1, FAN_ALL>(p, s, base, lpol, spol); break;
         }
     }
 }
