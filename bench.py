@@ -52,6 +52,8 @@ def parse_args():
     ap.add_argument("--chunk", type=int, default=0, help="SNAC chunk bytes (0 = auto)")
     ap.add_argument("--depth", type=int, default=0, help="SNAC ring depth (0 = auto)")
     ap.add_argument("--ctas", type=int, default=0, help="CTAs / channels (0 = auto)")
+    ap.add_argument("--staging", type=int, default=0,
+                    help="SNAC staging ring bytes of the handle (0 = library default)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -338,7 +340,7 @@ def bench_purlin(args):
 
     peak, peak_kind = measured_peaks()
     stream = torch.cuda.Stream(device=dev)
-    h = rd.purlin_create(R, 0, local)
+    h = rd.purlin_create(R, args.staging, local)
     variant = rd.VARIANT_ZS if args.variant == "zs" else rd.VARIANT_STAGED
     rd.purlin_set_policy(h, args.chunk, args.depth, args.ctas, variant)
 
@@ -560,7 +562,7 @@ def bench_only(args):
     rd.build()
     n = args.bytes_per_rank // 2
     c = n // R
-    h = rd.purlin_create(R, 0, 0)
+    h = rd.purlin_create(R, args.staging, 0)
     variant = rd.VARIANT_ZS if args.variant == "zs" else rd.VARIANT_STAGED
     rd.purlin_set_policy(h, args.chunk, args.depth, args.ctas, variant)
     stream = torch.cuda.Stream(device=dev)

@@ -33,6 +33,7 @@
 #include "snac.h"
 
 #include <algorithm>
+#include <cstdlib>
 #include <cstring>
 
 namespace purlin {
@@ -42,7 +43,7 @@ namespace {
 enum Kind : int { kRS = 0, kAG = 1, kAR = 2, kA2A = 3 };
 enum : int { kReady = 0, kFree = 1, kYReady = 2, kYFree = 3, kFlagsPerSlot = 4 };
 
-constexpr size_t kDefaultChunk = 64 * 1024;
+constexpr size_t kDefaultChunk = 16 * 1024;  // measured best at 64 MiB per rank, R = 8
 constexpr int kDefaultDepth = 2;
 constexpr int kMaxChannels = 128;
 
@@ -167,9 +168,24 @@ __device__ __forceinline__ char* slot_data(const SnacParams& p, uint32_t ch, uin
 // in units of B bytes, four units per thread in flight.
 // `skip` (an address, 0 for none): with FAN, a destination range starting there is
 // the source of an in-place AllGather block and is left alone.
+template <int B>
+__device__ __forceinline__ void store_pol(char* d, const atom::Unit<B>& u, uint64_t pol)
+{
+    if constexpr (B >= 16) atom::store(d, u.v, pol);
+    else atom::store_unit<B>(d, u);
+}
+
+template <int B, bool SRC_CG>
+__device__ __forceinline__ void load_pol(atom::Unit<B>& u, const char* s, uint64_t pol)
+{
+    if constexpr (B >= 16 && !SRC_CG) atom::load(u.v, s, pol);
+    else atom::load_unit<B, SRC_CG>(u, s);
+}
+
 template <int B, bool SRC_CG, bool FAN>
 __device__ __forceinline__ void cta_copy(const SnacParams& p, char* dst, uint64_t dst_off,
-                                         const char* src, uint64_t len, uintptr_t skip)
+                                         const char* src, uint64_t len, uintptr_t skip,
+                                         uint64_t lpol, uint64_t spol)
 {
     constexpr int U = 4;
     for (uint64_t base = 0; base < len; base += (uint64_t)kThreads * B * U) {
@@ -177,7 +193,7 @@ __device__ __forceinline__ void cta_copy(const SnacParams& p, char* dst, uint64_
 #pragma unroll
         for (int k = 0; k < U; ++k) {
             const uint64_t o = base + (uint64_t)(k * kThreads + threadIdx.x) * B;
-            if (o < len) atom::load_unit<B, SRC_CG>(u[k], src + o);
+            if (o < len) load_pol<B, SRC_CG>(u[k], src + o, lpol);
         }
 #pragma unroll
         for (int k = 0; k < U; ++k) {
@@ -186,10 +202,10 @@ __device__ __forceinline__ void cta_copy(const SnacParams& p, char* dst, uint64_
             if (FAN) {
                 for (int r = 0; r < (int)p.R; ++r) {
                     char* d = p.out[r] + dst_off + o;
-                    if ((uintptr_t)d != skip + o) atom::store_unit<B>(d, u[k]);
+                    if ((uintptr_t)d != skip + o) store_pol<B>(d, u[k], spol);
                 }
             } else {
-                atom::store_unit<B>(dst + o, u[k]);
+                store_pol<B>(dst + o, u[k], spol);
             }
         }
     }
@@ -197,22 +213,55 @@ __device__ __forceinline__ void cta_copy(const SnacParams& p, char* dst, uint64_
 
 template <bool SRC_CG, bool FAN>
 __device__ void cta_copy_any(const SnacParams& p, int unit_log2, char* dst, uint64_t dst_off,
-                             const char* src, uint64_t len, uintptr_t skip)
+                             const char* src, uint64_t len, uintptr_t skip, uint64_t lpol,
+                             uint64_t spol)
 {
     switch (unit_log2) {
-    case 5: cta_copy<32, SRC_CG, FAN>(p, dst, dst_off, src, len, skip); break;
-    case 4: cta_copy<16, SRC_CG, FAN>(p, dst, dst_off, src, len, skip); break;
-    case 3: cta_copy<8, SRC_CG, FAN>(p, dst, dst_off, src, len, skip); break;
-    case 2: cta_copy<4, SRC_CG, FAN>(p, dst, dst_off, src, len, skip); break;
-    case 1: cta_copy<2, SRC_CG, FAN>(p, dst, dst_off, src, len, skip); break;
-    default: cta_copy<1, SRC_CG, FAN>(p, dst, dst_off, src, len, skip); break;
+    case 5: cta_copy<32, SRC_CG, FAN>(p, dst, dst_off, src, len, skip, lpol, spol); break;
+    case 4: cta_copy<16, SRC_CG, FAN>(p, dst, dst_off, src, len, skip, lpol, spol); break;
+    case 3: cta_copy<8, SRC_CG, FAN>(p, dst, dst_off, src, len, skip, lpol, spol); break;
+    case 2: cta_copy<4, SRC_CG, FAN>(p, dst, dst_off, src, len, skip, lpol, spol); break;
+    case 1: cta_copy<2, SRC_CG, FAN>(p, dst, dst_off, src, len, skip, lpol, spol); break;
+    default: cta_copy<1, SRC_CG, FAN>(p, dst, dst_off, src, len, skip, lpol, spol); break;
+    }
+}
+
+// STAGE of a sum's step: the chunk of every source rank into its part of the
+// slot.  All R loads of a unit are in flight before the first staging store,
+// so one step costs about one memory round trip, not R of them.
+template <int B>
+__device__ __forceinline__ void cta_stage_ranks(const SnacParams& p, char* staged,
+                                                uint64_t src_off, uint64_t len, uint64_t lpol)
+{
+    const int R = (int)p.R;
+    for (uint64_t o = (uint64_t)threadIdx.x * B; o < len; o += (uint64_t)kThreads * B) {
+        atom::Unit<B> u[kMaxRanks];
+#pragma unroll
+        for (int r = 0; r < kMaxRanks; ++r)
+            if (r < R) load_pol<B, false>(u[r], p.in[r] + src_off + o, lpol);
+#pragma unroll
+        for (int r = 0; r < kMaxRanks; ++r)
+            if (r < R) atom::store_unit<B>(staged + r * p.chunk + o, u[r]);
+    }
+}
+
+__device__ void cta_stage_any(const SnacParams& p, int unit_log2, char* staged, uint64_t src_off,
+                              uint64_t len, uint64_t lpol)
+{
+    switch (unit_log2) {
+    case 5: cta_stage_ranks<32>(p, staged, src_off, len, lpol); break;
+    case 4: cta_stage_ranks<16>(p, staged, src_off, len, lpol); break;
+    case 3: cta_stage_ranks<8>(p, staged, src_off, len, lpol); break;
+    case 2: cta_stage_ranks<4>(p, staged, src_off, len, lpol); break;
+    case 1: cta_stage_ranks<2>(p, staged, src_off, len, lpol); break;
+    default: cta_stage_ranks<1>(p, staged, src_off, len, lpol); break;
     }
 }
 
 // Atom::reduce over the R staged pieces (stride `stride` apart) into dst.
 template <typename T, int ORDER, int B>
 __device__ __forceinline__ void cta_reduce_vec(const SnacParams& p, char* dst, const char* staged,
-                                               uint64_t len)
+                                               uint64_t len, uint64_t spol)
 {
     const int R = (int)p.R;
     for (uint64_t o = (uint64_t)threadIdx.x * B; o < len; o += (uint64_t)kThreads * B) {
@@ -222,7 +271,7 @@ __device__ __forceinline__ void cta_reduce_vec(const SnacParams& p, char* dst, c
             if (r < R) atom::load_cg(v[r], staged + r * p.chunk + o);
         atom::Vec<B> out;
         atom::reduce_unit<T, ORDER, B>(v, R, out);
-        atom::store(dst + o, out);
+        atom::store(dst + o, out, spol);
     }
 }
 
@@ -241,10 +290,10 @@ __device__ __forceinline__ void cta_reduce_elem(const SnacParams& p, char* dst, 
 
 template <typename T, int ORDER>
 __device__ void cta_reduce(const SnacParams& p, int unit_log2, char* dst, const char* staged,
-                           uint64_t len)
+                           uint64_t len, uint64_t spol)
 {
-    if (unit_log2 == 5) cta_reduce_vec<T, ORDER, 32>(p, dst, staged, len);
-    else if (unit_log2 == 4) cta_reduce_vec<T, ORDER, 16>(p, dst, staged, len);
+    if (unit_log2 == 5) cta_reduce_vec<T, ORDER, 32>(p, dst, staged, len, spol);
+    else if (unit_log2 == 4) cta_reduce_vec<T, ORDER, 16>(p, dst, staged, len, spol);
     else cta_reduce_elem<T, ORDER>(p, dst, staged, len);
 }
 
@@ -254,6 +303,9 @@ template <int KIND>
 __device__ void producer(const SnacParams& p, uint32_t ch)
 {
     const bool reduce = KIND == kRS || KIND == kAR;
+    // Sources are read exactly once: their lines go first, the ring stays.
+    const uint64_t lpol = atom::l2_policy(kL2EvictFirst);
+    const uint64_t spol = atom::l2_policy(kL2Normal);
     uint32_t n = 0;
     for (uint32_t i = ch; i < p.nsteps; i += p.nch, ++n) {
         const uint32_t slot = n % p.depth;
@@ -264,12 +316,10 @@ __device__ void producer(const SnacParams& p, uint32_t ch)
         const uint64_t len = min(p.chunk, s.bytes - off);
         char* staged = slot_data(p, ch, slot);
         if (reduce) {
-            for (int r = 0; r < (int)p.R; ++r)
-                cta_copy_any<false, false>(p, s.unit_log2, staged + r * p.chunk, 0,
-                                           p.in[r] + s.src_off + off, len, 0);
+            cta_stage_any(p, s.unit_log2, staged, s.src_off + off, len, lpol);
         } else {
             cta_copy_any<false, false>(p, s.unit_log2, staged, 0, p.in[s.src] + s.src_off + off,
-                                       len, 0);
+                                       len, 0, lpol, spol);
         }
         if (p.inject && ch == 0 && n == 0) continue;  // testing: this notify never happens
         cta_notify(f + kReady, tag_of(p, n));
@@ -279,6 +329,9 @@ __device__ void producer(const SnacParams& p, uint32_t ch)
 template <typename T, int ORDER, int KIND>
 __device__ void consumer(const SnacParams& p, uint32_t ch)
 {
+    // AllToAll outputs are written once and not read again here: evict-first.
+    const uint64_t lpol = atom::l2_policy(kL2Normal);
+    const uint64_t spol = atom::l2_policy(KIND == kA2A ? kL2EvictFirst : kL2Normal);
     uint32_t n = 0;
     for (uint32_t i = ch; i < p.nsteps; i += p.nch, ++n) {
         const uint32_t slot = n % p.depth;
@@ -289,16 +342,17 @@ __device__ void consumer(const SnacParams& p, uint32_t ch)
         const uint64_t len = min(p.chunk, s.bytes - off);
         char* staged = slot_data(p, ch, slot);
         if (KIND == kRS) {
-            cta_reduce<T, ORDER>(p, s.unit_log2, p.out[s.dst] + s.dst_off + off, staged, len);
+            cta_reduce<T, ORDER>(p, s.unit_log2, p.out[s.dst] + s.dst_off + off, staged, len, spol);
         } else if (KIND == kAR) {
             if (n >= p.depth && !cta_wait(p, f + kYFree, tag_of(p, n - p.depth))) return;
-            cta_reduce<T, ORDER>(p, s.unit_log2, staged + (uint64_t)p.R * p.chunk, staged, len);
+            cta_reduce<T, ORDER>(p, s.unit_log2, staged + (uint64_t)p.R * p.chunk, staged, len,
+                                 spol);
         } else if (KIND == kAG) {
             cta_copy_any<true, true>(p, s.unit_log2, nullptr, s.dst_off + off, staged, len,
-                                     (uintptr_t)(p.in[s.src] + s.src_off + off));
+                                     (uintptr_t)(p.in[s.src] + s.src_off + off), lpol, spol);
         } else {
             cta_copy_any<true, false>(p, s.unit_log2, p.out[s.dst] + s.dst_off + off, 0, staged,
-                                      len, 0);
+                                      len, 0, lpol, spol);
         }
         cta_notify(f + kFree, tag_of(p, n));
         if (KIND == kAR && threadIdx.x == 0) st_release(f + kYReady, tag_of(p, n));
@@ -307,6 +361,9 @@ __device__ void consumer(const SnacParams& p, uint32_t ch)
 
 __device__ void gatherer(const SnacParams& p, uint32_t ch)
 {
+    // The R outputs are written once: evict-first keeps the ring in L2.
+    const uint64_t lpol = atom::l2_policy(kL2Normal);
+    const uint64_t spol = atom::l2_policy(kL2EvictFirst);
     uint32_t n = 0;
     for (uint32_t i = ch; i < p.nsteps; i += p.nch, ++n) {
         const uint32_t slot = n % p.depth;
@@ -318,7 +375,7 @@ __device__ void gatherer(const SnacParams& p, uint32_t ch)
         const char* y = slot_data(p, ch, slot) + (uint64_t)p.R * p.chunk;
         // In-place AllReduce writes out[r] == in[r]; this step's input range
         // was staged before the y tag was published, so the writes are safe.
-        cta_copy_any<true, true>(p, s.unit_log2, nullptr, s.dst_off + off, y, len, 0);
+        cta_copy_any<true, true>(p, s.unit_log2, nullptr, s.dst_off + off, y, len, 0, lpol, spol);
         cta_notify(f + kYFree, tag_of(p, n));
     }
 }
@@ -361,6 +418,16 @@ SnacKernel kernel_for(Coll coll, int dtype, int order)
 
 int roles_of(Coll coll) { return coll == Coll::AllReduce ? 3 : 2; }
 
+// Widest access of the staged kernels (tuning knob for measurements only).
+int snac_unit_log2()
+{
+    static const int u = [] {
+        const char* e = std::getenv("PURLIN_SNAC_UNIT");
+        return (e && std::atoi(e) == 16) ? 4 : 5;
+    }();
+    return u;
+}
+
 int sub_slots(Coll coll, int R)
 {
     if (coll == Coll::AllReduce) return R + 1;
@@ -398,8 +465,8 @@ purlin_status_t run_with(SnacParams& p, const SnacRequest& rq, const SnacConfig&
     std::memset(&p, 0, sizeof(p));
     const bool reduce = rq.coll == Coll::ReduceScatter || rq.coll == Coll::AllReduce;
     uint32_t ntiles = 0;
-    int nseg = layout_segments(rq.pieces, rq.npieces, rq.R, rq.in, rq.out, rq.esz, reduce, 5,
-                               p.seg, kSegsLarge, &ntiles);
+    int nseg = layout_segments(rq.pieces, rq.npieces, rq.R, rq.in, rq.out, rq.esz, reduce,
+                               snac_unit_log2(), p.seg, kSegsLarge, &ntiles);
     if (nseg < 0) return PURLIN_ERR_UNSUPPORTED;
 
     SnacKernel kernel = kernel_for(rq.coll, rq.dtype, rq.order);
