@@ -297,16 +297,28 @@ def bench_reference(args):
     print(json.dumps(line), flush=True)
 
 
-def traffic_from_profiles(kernel_key):
-    """Per-launch DRAM bytes of a kernel from the committed ncu summary, if it
-    was taken on the current kernel sources (else None)."""
+# Source files whose content determines each kernel family's code.
+KERNEL_SOURCES = {
+    "zs": ["atom.cuh", "plan.h", "zs_kernels.cu"],
+    "snac": ["atom.cuh", "plan.h", "snac.h", "snac_kernels.cu"],
+}
+
+
+def sources_digest(family):
     import hashlib
     src = os.path.join(ROOT, "reduce_datapath_gb300", "csrc")
     h = hashlib.sha256()
-    for f in sorted(os.listdir(src)):
+    for f in KERNEL_SOURCES[family]:
         with open(os.path.join(src, f), "rb") as fh:
             h.update(fh.read())
-    digest = h.hexdigest()[:16]
+    return h.hexdigest()[:16]
+
+
+def traffic_from_profiles(kernel_key):
+    """Per-launch DRAM bytes of a kernel from the committed ncu summary, if it
+    was taken on the current sources of that kernel family (else None)."""
+    family = "snac" if kernel_key.startswith("snac") else "zs"
+    digest = sources_digest(family)
     pdir = os.path.join(ROOT, "profiles")
     if not os.path.isdir(pdir):
         return None, digest
@@ -417,6 +429,12 @@ def bench_purlin(args):
     # ---- AllReduce latency at 4 KiB per rank (R=8 bf16, 2048 elements)
     lat = allreduce_latency(rd, torch, dev, stream, variant)
 
+    # ---- the same step through the staged (SNAC) path, default policy
+    staged = staged_step(rd, torch, h, rs, ag, stream, rs_b + ag_b, peak)
+
+    # ---- AllReduce size sweep: zero staging vs SNAC (default policy)
+    sweep = allreduce_sweep(rd, torch, dev, stream, peak)
+
     # ---- end to end: inputs from pinned host memory, outputs back to it
     e2e = bench_e2e(args, rd, torch, h, x, y, z, counts, stream)
 
@@ -449,6 +467,8 @@ def bench_purlin(args):
         "roofline": roofline,
         "per_collective": per,
         "allreduce_4KiB": lat,
+        "staged_step": staged,
+        "allreduce_sweep": sweep,
         "e2e": e2e,
         "cpu_baseline": cpu,
         "parity_vs_oracle": parity,
@@ -460,6 +480,100 @@ def bench_purlin(args):
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def _graph_us(torch, stream, fn, per_graph=50, replays=4):
+    """Device time per launch: `per_graph` launches captured in one CUDA graph,
+    replayed; None if the launch cannot be captured."""
+    try:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(per_graph):
+                fn()
+    except Exception:
+        torch.cuda.synchronize()
+        return None
+    with torch.cuda.stream(stream):
+        g.replay()
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(replays):
+            g.replay()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) * 1e3 / (per_graph * replays)
+
+
+def _events_us(torch, stream, fn, iters):
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(iters):
+        fn()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) * 1e3 / iters
+
+
+def staged_step(rd, torch, h, rs, ag, stream, step_b, peak):
+    """The benchmark step (RS then AG) through SNAC staging (default policy)."""
+    rd.purlin_set_policy(h, 0, 0, 0, rd.VARIANT_STAGED)
+    try:
+        for _ in range(3):
+            rs()
+            ag()
+        torch.cuda.synchronize()
+        rs_us = _events_us(torch, stream, rs, 20)
+        ag_us = _events_us(torch, stream, ag, 20)
+        info = rd.purlin_last_launch(h)
+        if rd.purlin_query_status(h) != rd.OK:
+            raise RuntimeError("staged step: device status not ok")
+    finally:
+        rd.purlin_set_policy(h, 0, 0, 0, rd.VARIANT_ZS)
+    us = rs_us + ag_us
+    return {"us": us, "gbs": step_b / (us / 1e6) / 1e9, "frac_of_peak": step_b / (us / 1e6) / 1e9 / peak,
+            "reduce_scatter_us": rs_us, "all_gather_us": ag_us, "chunk_bytes": info["chunk_bytes"],
+            "depth": info["depth"], "grid": info["grid"]}
+
+
+def allreduce_sweep(rd, torch, dev, stream, peak):
+    """AllReduce R=8 bf16 at 4 KiB..256 MiB per rank: zero staging and SNAC."""
+    import workloads
+    h = rd.purlin_create(R, 0, dev.index)
+    out = []
+    try:
+        for nbytes in workloads.SWEEP_BYTES:
+            n = nbytes // 2
+            x = [torch.randn(n, device=dev).to(torch.bfloat16) for _ in range(R)]
+            o = [torch.empty_like(t) for t in x]
+            row = {"bytes_per_rank": nbytes}
+            for name, variant in (("zs", rd.VARIANT_ZS), ("snac", rd.VARIANT_STAGED)):
+                rd.purlin_set_policy(h, 0, 0, 0, variant)
+                fn = lambda: rd.purlin_all_reduce(h, x, o, n, "bf16", stream=stream)
+                with torch.cuda.stream(stream):
+                    for _ in range(3):
+                        fn()
+                torch.cuda.synchronize()
+                host_us = _events_us(torch, stream, fn, 20 if nbytes >= (1 << 20) else 200)
+                # below 16 MiB a Python caller's launch rate hides the device
+                # time: take it from a CUDA graph of 50 launches instead
+                graph_us = _graph_us(torch, stream, fn) if nbytes < (16 << 20) else None
+                us = graph_us if graph_us is not None else host_us
+                gbs = 2 * R * nbytes / (us / 1e6) / 1e9
+                row[name] = {"us": round(us, 2), "gbs": round(gbs, 1),
+                             "frac_of_peak": round(gbs / peak, 3),
+                             "timing": "cuda graph" if graph_us is not None else "events",
+                             "us_host_launched": round(host_us, 2)}
+            out.append(row)
+            del x, o
+        if rd.purlin_query_status(h) != rd.OK:
+            raise RuntimeError("allreduce sweep: device status not ok")
+    finally:
+        rd.purlin_destroy(h)
+        torch.cuda.empty_cache()
+    return out
 
 
 def allreduce_latency(rd, torch, dev, stream, variant):
@@ -516,38 +630,68 @@ def allreduce_latency(rd, torch, dev, stream, variant):
 
 
 def bench_e2e(args, rd, torch, h, x, y, z, counts, stream):
+    """End to end through host buffers: every step copies its inputs from pinned
+    host memory, runs ReduceScatter then AllGather, and copies the gathered
+    outputs back to pinned host memory.  Steps are pipelined over three streams
+    (upload, compute, download) with double-buffered device inputs and outputs,
+    so step i+1's upload overlaps step i's download (the host link is full
+    duplex)."""
+    dev = x[0].device
     xh = [torch.empty_like(t, device="cpu").pin_memory() for t in x]
     zh = [torch.empty_like(t, device="cpu").pin_memory() for t in z]
     for a, b in zip(xh, x):
         a.copy_(b)
+    xs = [x, [torch.empty_like(t) for t in x]]
+    zs = [z, [torch.empty_like(t) for t in z]]
+    up = torch.cuda.Stream(device=dev)
+    down = torch.cuda.Stream(device=dev)
     torch.cuda.synchronize()
 
-    def step():
-        for a, b in zip(x, xh):
-            a.copy_(b, non_blocking=True)
-        rd.purlin_reduce_scatter(h, x, y, counts, None, "bf16", stream=stream)
-        rd.purlin_all_gather(h, y, z, counts, None, "bf16", stream=stream)
-        for a, b in zip(zh, z):
-            a.copy_(b, non_blocking=True)
-
-    with torch.cuda.stream(stream):
-        for _ in range(2):
-            step()
+    def run(K):
+        rs_done = [None, None]
+        d2h_done = [None, None]
+        start = torch.cuda.Event(enable_timing=True)
+        start.record(up)
+        for i in range(K):
+            b = i % 2
+            with torch.cuda.stream(up):
+                if rs_done[b] is not None:
+                    up.wait_event(rs_done[b])       # step i-2 no longer reads xs[b]
+                for a, src in zip(xs[b], xh):
+                    a.copy_(src, non_blocking=True)
+                h2d = torch.cuda.Event()
+                h2d.record(up)
+            stream.wait_event(h2d)
+            if d2h_done[b] is not None:
+                stream.wait_event(d2h_done[b])      # step i-2's outputs are downloaded
+            rd.purlin_reduce_scatter(h, xs[b], y, counts, None, "bf16", stream=stream)
+            rs_done[b] = torch.cuda.Event()
+            rs_done[b].record(stream)
+            rd.purlin_all_gather(h, y, zs[b], counts, None, "bf16", stream=stream)
+            ag = torch.cuda.Event()
+            ag.record(stream)
+            with torch.cuda.stream(down):
+                down.wait_event(ag)
+                for dst, a in zip(zh, zs[b]):
+                    dst.copy_(a, non_blocking=True)
+                d2h_done[b] = torch.cuda.Event()
+                d2h_done[b].record(down)
+        end = torch.cuda.Event(enable_timing=True)
+        up.wait_stream(down)
+        up.wait_stream(stream)
+        end.record(up)
         torch.cuda.synchronize()
-        K = max(1, args.e2e_steps)
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for _ in range(K):
-            step()
-        b.record(stream)
-    torch.cuda.synchronize()
-    ms = a.elapsed_time(b) / K
+        return start.elapsed_time(end)
+
+    run(2)
+    K = max(1, args.e2e_steps)
+    ms = run(K) / K
     rs_b, ag_b = step_bytes()
     return {"value": (rs_b + ag_b) / (ms / 1e3) / 1e9, "unit": UNIT,
             "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in xh),
             "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in zh),
-            "ms_per_step": ms, "steps": K}
+            "ms_per_step": ms, "steps": K,
+            "note": "pinned host buffers; upload, compute and download pipelined across steps"}
 
 
 def bench_only(args):
