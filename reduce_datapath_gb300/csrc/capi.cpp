@@ -44,6 +44,7 @@ struct purlin_handle {
     int max_unit_log2 = 0;   // 0: per collective (AllReduce 4 = 16 B, else 5 = 32 B)
     int l2_load = -1;        // -1: per collective; else kL2Normal/EvictFirst/EvictLast
     int l2_store = -1;
+    bool pdl = true;         // programmatic dependent launch of zero-staging kernels
     int inject = 0;  // purlin_debug_inject, one staged call
     purlin_launch_info_t last{};
 };
@@ -144,6 +145,7 @@ struct ZsKnobs {
     int max_unit_log2;
     uint32_t l2_load;
     uint32_t l2_store;
+    bool pdl;
 };
 
 // Measured on GB300 (64 MiB per rank, R = 8, bf16):
@@ -164,6 +166,7 @@ ZsKnobs zs_knobs(const purlin_handle* h, Coll coll)
     k.l2_store = h->l2_store >= 0 ? (uint32_t)h->l2_store
                                   : ((coll == Coll::AllReduce || coll == Coll::AllToAllV)
                                          ? kL2EvictFirst : kL2Normal);
+    k.pdl = h->pdl;
     return k;
 }
 
@@ -176,6 +179,7 @@ purlin_status_t make_params(ZsParams<MAXSEG>& p, const Piece* pieces, int npiece
     std::memset(&p, 0, sizeof(p));
     p.l2_load = k.l2_load;
     p.l2_store = k.l2_store;
+    p.pdl = k.pdl ? 1u : 0u;
     for (int r = 0; r < R; ++r) {
         p.in[r] = reinterpret_cast<const char*>(in[r]);
         p.out[r] = reinterpret_cast<char*>(out[r]);
@@ -392,6 +396,7 @@ purlin_status_t purlin_create(purlin_handle_t* out, int R, size_t staging_bytes,
         return PURLIN_ERR_CUDA;
     }
     // Tuning knobs for measurements only; the defaults are the measured best.
+    if (const char* u = std::getenv("PURLIN_PDL")) h->pdl = std::atoi(u) != 0;
     if (const char* u = std::getenv("PURLIN_L2_LOAD")) h->l2_load = std::atoi(u) % 3;
     if (const char* u = std::getenv("PURLIN_L2_STORE")) h->l2_store = std::atoi(u) % 3;
     if (const char* u = std::getenv("PURLIN_MAX_UNIT")) {

@@ -56,6 +56,7 @@ struct ZsParams {
     char* out[kMaxRanks];
     uint32_t l2_load;   // eviction priority of source loads (kL2*)
     uint32_t l2_store;  // ... and of destination stores
+    uint32_t pdl;       // launched with programmatic stream serialization
     uint32_t R;
     uint32_t nseg;
     uint32_t ntiles;

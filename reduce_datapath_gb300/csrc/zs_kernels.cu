@@ -33,6 +33,17 @@ __device__ __forceinline__ const Segment& segment_of(const ZsParams<MAXSEG>& p, 
     return p.seg[lo];
 }
 
+// Programmatic dependent launch: the grid may have been scheduled before the
+// previous kernel on the stream finished; griddepcontrol.wait blocks until that
+// kernel has completed and its writes are visible (it returns at once when the
+// launch had no programmatic dependency).  Triggering dependents right after
+// lets the next collective's CTAs be scheduled while this one runs.
+__device__ __forceinline__ void pdl_enter()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ reduce
 
 template <typename T, int ORDER, bool FAN_ALL, int BYTES>
@@ -77,6 +88,7 @@ template <typename T, int ORDER, bool FAN_ALL>
 __global__ void __launch_bounds__(kThreads, 2)
 zs_reduce_kernel(const __grid_constant__ ZsParams<kSegsSmall> p)
 {
+    pdl_enter();
     const int R = (int)p.R;
     const uint64_t lpol = atom::l2_policy(p.l2_load);
     const uint64_t spol = atom::l2_policy(p.l2_store);
@@ -145,6 +157,7 @@ template <bool FAN_ALL, int MAXSEG>
 __global__ void __launch_bounds__(kThreads, 2)
 zs_copy_kernel(const __grid_constant__ ZsParams<MAXSEG> p)
 {
+    pdl_enter();
     const uint64_t lpol = atom::l2_policy(p.l2_load);
     const uint64_t spol = atom::l2_policy(p.l2_store);
     for (uint32_t t = blockIdx.x; t < p.ntiles; t += gridDim.x) {
@@ -167,13 +180,16 @@ zs_copy_kernel(const __grid_constant__ ZsParams<MAXSEG> p)
 template <typename P>
 cudaError_t launch(void (*kernel)(P), const P& params, int grid, cudaStream_t stream)
 {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = params.pdl ? 1 : 0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
-    cfg.attrs = nullptr;
-    cfg.numAttrs = 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kernel, params);
 }
 
