@@ -432,6 +432,9 @@ def bench_purlin(args):
     # ---- the same step through the staged (SNAC) path, default policy
     staged = staged_step(rd, torch, h, rs, ag, stream, rs_b + ag_b, peak)
 
+    # ---- bandwidth vs CTAs launched, per Atom, and the copy-engine AllGather
+    frugal = cta_study(rd, torch, h, rs, ag, stream, rs_b, peak)
+
     # ---- AllReduce size sweep: zero staging vs SNAC (default policy)
     sweep = allreduce_sweep(rd, torch, dev, stream, peak)
 
@@ -468,6 +471,7 @@ def bench_purlin(args):
         "per_collective": per,
         "allreduce_4KiB": lat,
         "staged_step": staged,
+        "cta_study": frugal,
         "allreduce_sweep": sweep,
         "e2e": e2e,
         "cpu_baseline": cpu,
@@ -536,6 +540,46 @@ def staged_step(rd, torch, h, rs, ag, stream, step_b, peak):
     return {"us": us, "gbs": step_b / (us / 1e6) / 1e9, "frac_of_peak": step_b / (us / 1e6) / 1e9 / peak,
             "reduce_scatter_us": rs_us, "all_gather_us": ag_us, "chunk_bytes": info["chunk_bytes"],
             "depth": info["depth"], "grid": info["grid"]}
+
+
+def cta_study(rd, torch, h, rs, ag, stream, coll_b, peak):
+    """Bandwidth of the AllGather (copy) and ReduceScatter (sum) of the step as
+    a function of the CTAs launched, for the vector and TMA-bulk Atoms, plus the
+    AllGather on the copy engines (no kernel).  Concurrent SM use is bounded by
+    min(CTAs launched, SMs)."""
+    rows = []
+    try:
+        for atom_name, atom, ctas_list in (("vector", rd.ATOM_VECTOR, (8, 16, 38, 76, 152, 304)),
+                                           ("bulk", rd.ATOM_BULK, (8, 16, 38, 76, 152))):
+            rd.purlin_set_atom(h, atom)
+            for ctas in ctas_list:
+                rd.purlin_set_policy(h, 0, 0, ctas, rd.VARIANT_ZS)
+                ag()
+                us = _events_us(torch, stream, ag, 10)
+                rows.append({"collective": "all_gather", "atom": atom_name, "ctas": ctas,
+                             "us": round(us, 1), "gbs": round(coll_b / (us / 1e6) / 1e9, 1),
+                             "frac_of_peak": round(coll_b / (us / 1e6) / 1e9 / peak, 3)})
+        rd.purlin_set_atom(h, rd.ATOM_VECTOR)
+        for ctas in (8, 16, 38, 76, 152, 304):
+            rd.purlin_set_policy(h, 0, 0, ctas, rd.VARIANT_ZS)
+            rs()
+            us = _events_us(torch, stream, rs, 10)
+            rows.append({"collective": "reduce_scatter", "atom": "vector", "ctas": ctas,
+                         "us": round(us, 1), "gbs": round(coll_b / (us / 1e6) / 1e9, 1),
+                         "frac_of_peak": round(coll_b / (us / 1e6) / 1e9 / peak, 3)})
+        rd.purlin_set_policy(h, 0, 0, 0, rd.VARIANT_ZS)
+        rd.purlin_set_atom(h, rd.ATOM_COPY_ENGINE)
+        ag()
+        us = _events_us(torch, stream, ag, 10)
+        rows.append({"collective": "all_gather", "atom": "copy_engine", "ctas": 0,
+                     "us": round(us, 1), "gbs": round(coll_b / (us / 1e6) / 1e9, 1),
+                     "frac_of_peak": round(coll_b / (us / 1e6) / 1e9 / peak, 3)})
+        if rd.purlin_query_status(h) != rd.OK:
+            raise RuntimeError("cta study: device status not ok")
+    finally:
+        rd.purlin_set_atom(h, rd.ATOM_AUTO)
+        rd.purlin_set_policy(h, 0, 0, 0, rd.VARIANT_ZS)
+    return rows
 
 
 def allreduce_sweep(rd, torch, dev, stream, peak):

@@ -95,6 +95,19 @@ typedef enum {
                                 an odd last value carried up unchanged          */
 } purlin_order_t;
 
+/* Which mechanism moves the bytes of copy collectives (AllGather(V),
+ * AllToAll(V)) on the zero-staging path.  The pages' Atom has one
+ * specialization per GPU generation (Table 4) and note that one AllGather
+ * baseline "uses the copy engine and launches no kernel" (Figure 10). */
+typedef enum {
+    PURLIN_ATOM_AUTO = 0,         /* library's choice (measured best: VECTOR)        */
+    PURLIN_ATOM_VECTOR = 1,       /* every thread moves 16/32-byte vectors           */
+    PURLIN_ATOM_BULK = 2,         /* one thread per CTA drives TMA bulk copies
+                                     (cp.async.bulk) through a shared-memory ring   */
+    PURLIN_ATOM_COPY_ENGINE = 3   /* no kernel: one cudaMemcpyAsync per block and
+                                     destination, on the copy engines               */
+} purlin_atom_t;
+
 typedef struct purlin_handle* purlin_handle_t;
 
 /* What the last collective on a handle launched (for SM accounting, Figure 10:
@@ -239,6 +252,10 @@ PURLIN_API purlin_status_t purlin_all_reduce_noalloc(const void* const in[], voi
  * SNAC channels.  variant: a purlin_variant_t. */
 PURLIN_API purlin_status_t purlin_set_policy(purlin_handle_t h, size_t chunk_bytes, int depth,
                                   int ctas, int variant);
+
+/* Mechanism of copy collectives on the zero-staging path: a purlin_atom_t.
+ * Sums always run on the vector Atom; the staged path ignores this setting. */
+PURLIN_API purlin_status_t purlin_set_atom(purlin_handle_t h, int atom);
 
 /* Rank order of sums: PURLIN_ORDER_FIXED (default) or PURLIN_ORDER_TREE. */
 PURLIN_API purlin_status_t purlin_set_reduce_order(purlin_handle_t h, int order);

@@ -45,6 +45,7 @@ struct purlin_handle {
     int l2_load = -1;        // -1: per collective; else kL2Normal/EvictFirst/EvictLast
     int l2_store = -1;
     bool pdl = true;         // programmatic dependent launch of zero-staging kernels
+    int atom = PURLIN_ATOM_AUTO;
     int inject = 0;  // purlin_debug_inject, one staged call
     purlin_launch_info_t last{};
 };
@@ -142,6 +143,7 @@ purlin_status_t check_buffers(Coll coll, int R, const uint64_t* in, const uint64
 
 // Launch-wide knobs of the zero-staging kernels.
 struct ZsKnobs {
+    int unroll;
     int max_unit_log2;
     uint32_t l2_load;
     uint32_t l2_store;
@@ -160,6 +162,8 @@ struct ZsKnobs {
 ZsKnobs zs_knobs(const purlin_handle* h, Coll coll)
 {
     ZsKnobs k;
+    const bool reduce = coll == Coll::ReduceScatter || coll == Coll::AllReduce;
+    k.unroll = reduce ? kUnrollReduce : (h->atom == PURLIN_ATOM_BULK ? kUnrollBulk : kUnrollCopy);
     k.max_unit_log2 = h->max_unit_log2 ? h->max_unit_log2 : (coll == Coll::AllReduce ? 4 : 5);
     k.l2_load = h->l2_load >= 0 ? (uint32_t)h->l2_load
                                 : (coll == Coll::AllGather ? kL2Normal : kL2EvictFirst);
@@ -173,22 +177,23 @@ ZsKnobs zs_knobs(const purlin_handle* h, Coll coll)
 template <int MAXSEG>
 purlin_status_t make_params(ZsParams<MAXSEG>& p, const Piece* pieces, int npieces, int R,
                             const uint64_t* in, const uint64_t* out, size_t esz, bool reduce,
-                            const ZsKnobs& k)
+                            const ZsKnobs& k, int* status)
 {
     const int max_unit_log2 = k.max_unit_log2;
     std::memset(&p, 0, sizeof(p));
     p.l2_load = k.l2_load;
     p.l2_store = k.l2_store;
     p.pdl = k.pdl ? 1u : 0u;
+    p.status = status;
     for (int r = 0; r < R; ++r) {
         p.in[r] = reinterpret_cast<const char*>(in[r]);
         p.out[r] = reinterpret_cast<char*>(out[r]);
     }
     p.R = (uint32_t)R;
-    p.unroll = reduce ? kUnrollReduce : kUnrollCopy;
+    p.unroll = (uint32_t)k.unroll;
     uint32_t ntiles = 0;
-    int n = layout_segments(pieces, npieces, R, in, out, esz, reduce, max_unit_log2, p.seg,
-                            MAXSEG, &ntiles);
+    int n = layout_segments(pieces, npieces, R, in, out, esz, reduce, (int)p.unroll,
+                            max_unit_log2, p.seg, MAXSEG, &ntiles);
     if (n < 0) return PURLIN_ERR_UNSUPPORTED;
     p.nseg = (uint32_t)n;
     p.ntiles = ntiles;
@@ -307,30 +312,62 @@ purlin_status_t run(purlin_handle_t h, Coll coll, const void* const in_[], void*
     info.variant = PURLIN_VARIANT_ZS;
     cudaError_t ce = cudaSuccess;
     const ZsKnobs knobs = zs_knobs(h, coll);
-    if (coll == Coll::AllToAllV) {
+    const bool bulk = !reduce && h->atom == PURLIN_ATOM_BULK;
+    if (!reduce && h->atom == PURLIN_ATOM_COPY_ENGINE) {
+        // No kernel: every block goes to every destination through the copy
+        // engines, one asynchronous copy each, in stream order.
+        int copies = 0;
+        for (int i = 0; i < np && ce == cudaSuccess; ++i) {
+            const Piece& pc = pieces[i];
+            const char* src = reinterpret_cast<const char*>(in[pc.src]) + pc.src_off;
+            for (int j = 0; j < R; ++j) {
+                if (pc.dst != kEveryRank && pc.dst != j) continue;
+                char* dst = reinterpret_cast<char*>(out[j]) + pc.dst_off;
+                if (dst == src) continue;  // in-place AllGather block
+                ce = cudaMemcpyAsync(dst, src, pc.bytes, cudaMemcpyDeviceToDevice, s);
+                if (ce != cudaSuccess) break;
+                ++copies;
+            }
+        }
+        info.kernels = 0;
+        info.grid = 0;
+        info.block = 0;
+        info.chunk_bytes = 0;
+        (void)copies;
+    } else if (coll == Coll::AllToAllV) {
         static thread_local ZsParams<kSegsLarge> p;
-        st = make_params(p, pieces, np, R, in, out, esz, false, knobs);
+        st = make_params(p, pieces, np, R, in, out, esz, false, knobs, h->status);
         if (st != PURLIN_OK) return st;
-        int grid = zs_grid(h, p.ntiles, zs_copy_resident_ctas(true, false));
-        if (grid > 0) ce = zs_copy_launch(p, false, grid, s);
+        int grid;
+        if (bulk) {
+            grid = zs_grid(h, p.ntiles, zs_copy_bulk_resident_ctas(true, false));
+            if (grid > 0) ce = zs_copy_bulk_launch(p, false, grid, s);
+            info.block = kBulkThreads;
+        } else {
+            grid = zs_grid(h, p.ntiles, zs_copy_resident_ctas(true, false));
+            if (grid > 0) ce = zs_copy_launch(p, false, grid, s);
+        }
         info.grid = grid;
         info.kernels = grid > 0;
-        info.chunk_bytes = tile_bytes(knobs.max_unit_log2, kUnrollCopy);
+        info.chunk_bytes = tile_bytes(knobs.max_unit_log2, knobs.unroll);
     } else {
         static thread_local ZsParams<kSegsSmall> p;
-        st = make_params(p, pieces, np, R, in, out, esz, reduce, knobs);
+        st = make_params(p, pieces, np, R, in, out, esz, reduce, knobs, h->status);
         if (st != PURLIN_OK) return st;
         bool fan_all = coll == Coll::AllGather || coll == Coll::AllReduce;
         int grid;
         if (reduce) {
             grid = zs_grid(h, p.ntiles, zs_reduce_resident_ctas(dtype, h->order, fan_all));
             if (grid > 0) ce = zs_reduce_launch(p, dtype, h->order, fan_all, grid, s);
-            info.chunk_bytes = tile_bytes(knobs.max_unit_log2, kUnrollReduce);
+        } else if (bulk) {
+            grid = zs_grid(h, p.ntiles, zs_copy_bulk_resident_ctas(false, fan_all));
+            if (grid > 0) ce = zs_copy_bulk_launch(p, fan_all, grid, s);
+            info.block = kBulkThreads;
         } else {
             grid = zs_grid(h, p.ntiles, zs_copy_resident_ctas(false, fan_all));
             if (grid > 0) ce = zs_copy_launch(p, fan_all, grid, s);
-            info.chunk_bytes = tile_bytes(knobs.max_unit_log2, kUnrollCopy);
         }
+        info.chunk_bytes = tile_bytes(knobs.max_unit_log2, knobs.unroll);
         info.grid = grid;
         info.kernels = grid > 0;
     }
@@ -482,6 +519,14 @@ purlin_status_t purlin_set_policy(purlin_handle_t h, size_t chunk_bytes, int dep
     return PURLIN_OK;
 }
 
+purlin_status_t purlin_set_atom(purlin_handle_t h, int atom)
+{
+    if (!h || atom < PURLIN_ATOM_AUTO || atom > PURLIN_ATOM_COPY_ENGINE)
+        return PURLIN_ERR_INVALID_ARG;
+    h->atom = atom;
+    return PURLIN_OK;
+}
+
 purlin_status_t purlin_set_reduce_order(purlin_handle_t h, int order)
 {
     if (!h || (order != PURLIN_ORDER_FIXED && order != PURLIN_ORDER_TREE))
@@ -551,8 +596,9 @@ purlin_status_t purlin_plan_segments(purlin_collective_t coll, int R, const uint
     if (np < 0) return PURLIN_ERR_INVALID_ARG;
     Segment tmp[kSegsLarge];
     uint32_t nt = 0;
-    int n = layout_segments(pieces, np, R, in_addr, out_addr, esz, reduce, max_unit == 32 ? 5 : 4,
-                            tmp, kSegsLarge, &nt);
+    int n = layout_segments(pieces, np, R, in_addr, out_addr, esz, reduce,
+                            reduce ? kUnrollReduce : kUnrollCopy, max_unit == 32 ? 5 : 4, tmp,
+                            kSegsLarge, &nt);
     if (n < 0 || n > max_segs) return PURLIN_ERR_UNSUPPORTED;
     for (int i = 0; i < n; ++i) {
         segs[i].src_off = tmp[i].src_off;

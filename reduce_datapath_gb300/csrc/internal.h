@@ -27,4 +27,11 @@ cudaError_t zs_copy_launch(const ZsParams<kSegsLarge>& p, bool fan_all, int grid
                            cudaStream_t stream);
 int zs_copy_resident_ctas(bool large, bool fan_all);
 
+// Copy through TMA bulk transfers (plan built with kUnrollBulk tiles).
+cudaError_t zs_copy_bulk_launch(const ZsParams<kSegsSmall>& p, bool fan_all, int grid,
+                                cudaStream_t stream);
+cudaError_t zs_copy_bulk_launch(const ZsParams<kSegsLarge>& p, bool fan_all, int grid,
+                                cudaStream_t stream);
+int zs_copy_bulk_resident_ctas(bool large, bool fan_all);
+
 }  // namespace purlin

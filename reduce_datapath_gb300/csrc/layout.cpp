@@ -150,12 +150,11 @@ void layout_extents(Coll coll, int R, const size_t* counts, const size_t* da, co
 }
 
 int layout_segments(const Piece* pieces, int npieces, int R, const uint64_t* in_addr,
-                    const uint64_t* out_addr, size_t esz, bool reduce, int max_unit_log2,
-                    Segment* segs, int max_segs, uint32_t* ntiles)
+                    const uint64_t* out_addr, size_t esz, bool reduce, int unroll,
+                    int max_unit_log2, Segment* segs, int max_segs, uint32_t* ntiles)
 {
     int n = 0;
     uint64_t tiles = 0;
-    const int unroll = reduce ? kUnrollReduce : kUnrollCopy;
     const int elem_log2 = log2_exact(esz);
     auto push = [&](uint64_t so, uint64_t dof, uint64_t bytes, const Piece& p, int ulog2) {
         if (bytes == 0) return true;

@@ -57,6 +57,7 @@ struct ZsParams {
     uint32_t l2_load;   // eviction priority of source loads (kL2*)
     uint32_t l2_store;  // ... and of destination stores
     uint32_t pdl;       // launched with programmatic stream serialization
+    int* status;        // device status word (bounded waits of the bulk kernel)
     uint32_t R;
     uint32_t nseg;
     uint32_t ntiles;
@@ -69,6 +70,10 @@ PURLIN_HD inline uint64_t tile_bytes(int unit_log2, int unroll)
 {
     return (uint64_t)kThreads * ((uint64_t)1 << unit_log2) * (uint64_t)unroll;
 }
+
+constexpr int kUnrollBulk = 2;          // bulk-copy tiles: 256 x unit x 2 bytes (<= 16 KiB)
+constexpr int kBulkThreads = 32;        // one warp per bulk-copy CTA
+constexpr uint32_t kBulkStageBytes = 16 * 1024;
 
 enum class Coll : int { ReduceScatter = 0, AllGather = 1, AllReduce = 2, AllToAllV = 3 };
 
@@ -99,12 +104,12 @@ void layout_extents(Coll coll, int R, const size_t* counts, const size_t* da,
                     uint64_t in_extent[kMaxRanks], uint64_t out_extent[kMaxRanks]);
 
 // Split pieces into head / body / tail segments by the alignment of the actual
-// addresses, then number the tiles.  `reduce` selects element-wise heads and
+// addresses, then number the tiles (kThreads x unit x unroll bytes each).  `reduce` selects element-wise heads and
 // tails (sums) or byte-wise ones (copies).  max_unit_log2 caps the vector width
 // (4 = 16 B, 5 = 32 B).  Returns the segment count or -1 if max_segs is too
 // small; *ntiles receives the tile count.
 int layout_segments(const Piece* pieces, int npieces, int R, const uint64_t* in_addr,
-                    const uint64_t* out_addr, size_t elem_bytes, bool reduce,
+                    const uint64_t* out_addr, size_t elem_bytes, bool reduce, int unroll,
                     int max_unit_log2, Segment* segs, int max_segs, uint32_t* ntiles);
 
 }  // namespace purlin

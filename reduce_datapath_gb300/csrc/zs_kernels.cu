@@ -13,6 +13,7 @@
 // tiles, which sit in the kernel's constant parameter bank.
 #include "atom.cuh"
 #include "internal.h"
+#include "purlin.h"
 
 #include <mutex>
 #include <unordered_map>
@@ -175,6 +176,205 @@ zs_copy_kernel(const __grid_constant__ ZsParams<MAXSEG> p)
     }
 }
 
+// ------------------------------------------------------------ bulk copy
+// Atom::copy through the Tensor Memory Accelerator: lane 0 of a one-warp CTA
+// keeps a shared-memory ring of STAGES tiles busy -- cp.async.bulk
+// global->shared loads that complete on an mbarrier, then one cp.async.bulk
+// shared->global store per destination -- so a tile is read from HBM once and
+// written R times without per-thread store instructions.  Half of the ring
+// holds loads in flight ahead of the tile being stored, the other half tiles
+// whose stores are still reading shared memory.  Tiles whose streams are not
+// 16-byte aligned (unit < 16 B) are copied by the warp with ordinary accesses.
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p)
+{
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+                 ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Bounded wait for an mbarrier phase: at most ~2 s and 2^24 polls.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity)
+{
+    uint64_t start = 0;
+    for (uint32_t it = 0; it < (1u << 24); ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 255) == 255) {
+            const uint64_t t = global_ns();
+            if (start == 0) start = t;
+            else if (t - start > 2000000000ull) return false;
+        }
+    }
+    return false;
+}
+
+__device__ __forceinline__ void bulk_load(void* smem, const char* gmem, uint32_t bytes,
+                                          uint64_t* bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes"
+                 " [%0], [%1], %2, [%3];"
+                 ::"r"(smem_u32(smem)), "l"(gmem), "r"(bytes), "r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void bulk_store(char* gmem, const void* smem, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+                 ::"l"(gmem), "r"(smem_u32(smem)), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit()
+{
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void bulk_wait_read_all_but()
+{
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ void bulk_wait_all()
+{
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+template <int B, bool FAN_ALL, int MAXSEG>
+__device__ __forceinline__ void warp_copy_tile(const ZsParams<MAXSEG>& p, const Segment& s,
+                                               uint64_t base, uint64_t len)
+{
+    const char* src = p.in[s.src] + s.src_off + base;
+    for (uint64_t o = (uint64_t)threadIdx.x * B; o < len; o += (uint64_t)kBulkThreads * B) {
+        Unit<B> u;
+        load_unit<B>(u, src + o);
+        if (FAN_ALL) {
+            for (int r = 0; r < (int)p.R; ++r) {
+                char* dst = p.out[r] + s.dst_off + base + o;
+                if (dst != src + o) store_unit<B>(dst, u);
+            }
+        } else {
+            store_unit<B>(p.out[s.dst] + s.dst_off + base + o, u);
+        }
+    }
+}
+
+template <bool FAN_ALL, int MAXSEG, int STAGES>
+__global__ void __launch_bounds__(kBulkThreads)
+zs_copy_bulk_kernel(const __grid_constant__ ZsParams<MAXSEG> p)
+{
+    extern __shared__ __align__(128) char ring[];   // STAGES x kBulkStageBytes
+    __shared__ __align__(8) uint64_t bar[STAGES];
+    const uint32_t G = gridDim.x;
+    pdl_enter();
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) mbar_init(&bar[s]);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+
+        auto next_bulk = [&](uint32_t t) {
+            while (t < p.ntiles && segment_of(p, t).unit_log2 < 4) t += G;
+            return t;
+        };
+        auto tile_len = [&](uint32_t t, const Segment& s, uint64_t& base) {
+            const uint64_t tb = tile_bytes(s.unit_log2, kUnrollBulk);
+            base = (uint64_t)(t - s.tile0) * tb;
+            return (uint32_t)min(tb, s.bytes - base);
+        };
+        auto issue_load = [&](uint32_t t, uint32_t n) {
+            const Segment& s = segment_of(p, t);
+            uint64_t base;
+            const uint32_t len = tile_len(t, s, base);
+            const int st = (int)(n % STAGES);
+            mbar_expect_tx(&bar[st], len);
+            bulk_load(ring + (size_t)st * kBulkStageBytes, p.in[s.src] + s.src_off + base, len,
+                      &bar[st]);
+        };
+
+        constexpr int AHEAD = STAGES / 2;
+        uint32_t lt = next_bulk(blockIdx.x), stt = lt;
+        uint32_t nl = 0, ns = 0;
+        bool failed = false;
+        while (nl < AHEAD && lt < p.ntiles) {
+            issue_load(lt, nl++);
+            lt = next_bulk(lt + G);
+        }
+        while (stt < p.ntiles) {
+            const int st = (int)(ns % STAGES);
+            if (!mbar_wait(&bar[st], (ns / STAGES) & 1u)) { failed = true; break; }
+            const Segment& s = segment_of(p, stt);
+            uint64_t base;
+            const uint32_t len = tile_len(stt, s, base);
+            const char* stage = ring + (size_t)st * kBulkStageBytes;
+            if (FAN_ALL) {
+                const char* src = p.in[s.src] + s.src_off + base;
+                for (int r = 0; r < (int)p.R; ++r) {
+                    char* dst = p.out[r] + s.dst_off + base;
+                    if (dst != src) bulk_store(dst, stage, len);  // in-place block: skip
+                }
+            } else {
+                bulk_store(p.out[s.dst] + s.dst_off + base, stage, len);
+            }
+            bulk_commit();
+            ++ns;
+            stt = next_bulk(stt + G);
+            if (lt < p.ntiles) {
+                // the slot being refilled was last read by the stores of tile
+                // nl - STAGES: every store group but the newest STAGES - AHEAD
+                // must have finished reading shared memory
+                bulk_wait_read_all_but<STAGES - AHEAD>();
+                issue_load(lt, nl++);
+                lt = next_bulk(lt + G);
+            }
+        }
+        if (failed) {
+            atomicCAS(p.status, 0, (int)PURLIN_ERR_TIMEOUT);
+            // every load already issued must land before shared memory is released
+            for (uint32_t n = ns; n < nl; ++n) mbar_wait(&bar[n % STAGES], (n / STAGES) & 1u);
+        }
+        bulk_wait_all();
+    }
+    __syncwarp();
+
+    for (uint32_t t = blockIdx.x; t < p.ntiles; t += G) {
+        const Segment& s = segment_of(p, t);
+        if (s.unit_log2 >= 4) continue;
+        const uint64_t tb = tile_bytes(s.unit_log2, kUnrollBulk);
+        const uint64_t base = (uint64_t)(t - s.tile0) * tb;
+        const uint64_t len = min(tb, s.bytes - base);
+        switch (s.unit_log2) {
+        case 3: warp_copy_tile<8, FAN_ALL>(p, s, base, len); break;
+        case 2: warp_copy_tile<4, FAN_ALL>(p, s, base, len); break;
+        case 1: warp_copy_tile<2, FAN_ALL>(p, s, base, len); break;
+        default: warp_copy_tile<1, FAN_ALL>(p, s, base, len); break;
+        }
+    }
+}
+
 // ------------------------------------------------------------- dispatch
 
 template <typename P>
@@ -252,6 +452,81 @@ cudaError_t zs_copy_launch(const ZsParams<kSegsLarge>& p, bool fan_all, int grid
 {
     return launch(fan_all ? zs_copy_kernel<true, kSegsLarge> : zs_copy_kernel<false, kSegsLarge>,
                   p, grid, stream);
+}
+
+namespace {
+
+constexpr int kBulkStages = 8;
+
+template <bool FAN_ALL, int MAXSEG>
+cudaError_t bulk_launch_t(const ZsParams<MAXSEG>& p, int grid, cudaStream_t stream,
+                          int* resident_out)
+{
+    auto kernel = zs_copy_bulk_kernel<FAN_ALL, MAXSEG, kBulkStages>;
+    const size_t smem = (size_t)kBulkStages * kBulkStageBytes;
+    static std::mutex mu;
+    static bool ready[64] = {};
+    static int resident[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (!ready[dev]) {
+            cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 (int)smem);
+            if (e != cudaSuccess) return e;
+            int n = 0;
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, kBulkThreads, smem);
+            if (e != cudaSuccess) return e;
+            resident[dev] = n > 0 ? n : 1;
+            ready[dev] = true;
+        }
+    }
+    if (resident_out) {
+        *resident_out = resident[dev];
+        return cudaSuccess;
+    }
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = p.pdl ? 1 : 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kBulkThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, p);
+}
+
+}  // namespace
+
+cudaError_t zs_copy_bulk_launch(const ZsParams<kSegsSmall>& p, bool fan_all, int grid,
+                                cudaStream_t stream)
+{
+    return fan_all ? bulk_launch_t<true>(p, grid, stream, nullptr)
+                   : bulk_launch_t<false>(p, grid, stream, nullptr);
+}
+
+cudaError_t zs_copy_bulk_launch(const ZsParams<kSegsLarge>& p, bool fan_all, int grid,
+                                cudaStream_t stream)
+{
+    return fan_all ? bulk_launch_t<true>(p, grid, stream, nullptr)
+                   : bulk_launch_t<false>(p, grid, stream, nullptr);
+}
+
+int zs_copy_bulk_resident_ctas(bool large, bool fan_all)
+{
+    int n = 1;
+    cudaError_t e;
+    if (large) {
+        static const ZsParams<kSegsLarge> none{};
+        e = fan_all ? bulk_launch_t<true>(none, 0, nullptr, &n) : bulk_launch_t<false>(none, 0, nullptr, &n);
+    } else {
+        static const ZsParams<kSegsSmall> none{};
+        e = fan_all ? bulk_launch_t<true>(none, 0, nullptr, &n) : bulk_launch_t<false>(none, 0, nullptr, &n);
+    }
+    return e == cudaSuccess ? n : 1;
 }
 
 int zs_copy_resident_ctas(bool large, bool fan_all)

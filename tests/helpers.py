@@ -69,8 +69,9 @@ def handle(R):
     return _handles[R]
 
 
-def set_variant(h, variant, chunk=0, depth=0, ctas=0):
+def set_variant(h, variant, chunk=0, depth=0, ctas=0, atom=0):
     rd.purlin_set_policy(h, chunk, depth, ctas, variant)
+    rd.purlin_set_atom(h, atom)
 
 
 def close_handles():

@@ -160,8 +160,12 @@ def test_allreduce_sweep_r8(sweep_handle, nbytes, variant, chunk):
 
 # ---------------------------------------------------------------- moe_a2av_r8
 
-@pytest.mark.parametrize("variant", [rd.VARIANT_ZS, rd.VARIANT_STAGED])
-def test_moe_a2av_r8_dispatch_and_inverse(variant):
+ATOMS = [(rd.VARIANT_ZS, rd.ATOM_VECTOR), (rd.VARIANT_ZS, rd.ATOM_BULK),
+         (rd.VARIANT_ZS, rd.ATOM_COPY_ENGINE), (rd.VARIANT_STAGED, rd.ATOM_AUTO)]
+
+
+@pytest.mark.parametrize("variant,atom", ATOMS)
+def test_moe_a2av_r8_dispatch_and_inverse(variant, atom):
     R, T, H = 8, 4096, workloads.HIDDEN
     C = workloads.zipf_pair_counts(R, T, workloads.ZIPF_S, workloads.seed_for("moe_a2av_r8", 9))
     assert (C.sum(axis=1) == T).all()
@@ -172,6 +176,7 @@ def test_moe_a2av_r8_dispatch_and_inverse(variant):
     h = rd.purlin_create(R)
     try:
         rd.purlin_set_policy(h, 0, 0, 0, variant)
+        rd.purlin_set_atom(h, atom)
         rd.purlin_all_to_all_v(h, x, recv, C * H, None, None, "bf16")
         rd.purlin_all_to_all_v(h, recv, back, C.T * H, None, None, "bf16")
         _ok(h)
@@ -216,8 +221,8 @@ def test_dp_attention_agv_rsv(variant):
         assert _bits_equal(host_bits(rs_out[k]), want[k])
 
 
-@pytest.mark.parametrize("variant", [rd.VARIANT_ZS, rd.VARIANT_STAGED])
-def test_allgather_1GiB_out_per_rank(variant):
+@pytest.mark.parametrize("variant,atom", ATOMS)
+def test_allgather_1GiB_out_per_rank(variant, atom):
     R = 8
     c = 128 * MiB // 2
     x = workloads.rank_buffers("dp_attn_agv_rsv_r8", R, c, "bf16", role=3, device="cuda")
@@ -225,6 +230,7 @@ def test_allgather_1GiB_out_per_rank(variant):
     h = rd.purlin_create(R)
     try:
         rd.purlin_set_policy(h, 0, 0, 0, variant)
+        rd.purlin_set_atom(h, atom)
         rd.purlin_all_gather(h, x, out, [c] * R, None, "bf16")
         _ok(h)
     finally:

@@ -21,6 +21,9 @@ pytestmark = pytest.mark.gpu
 POLICIES = {
     "zs": (rd.VARIANT_ZS, 0, 0, 0),
     "zs_3ctas": (rd.VARIANT_ZS, 0, 0, 3),
+    "zs_bulk": (rd.VARIANT_ZS, 0, 0, 0, rd.ATOM_BULK),
+    "zs_bulk_3ctas": (rd.VARIANT_ZS, 0, 0, 3, rd.ATOM_BULK),
+    "zs_copy_engine": (rd.VARIANT_ZS, 0, 0, 0, rd.ATOM_COPY_ENGINE),
     "snac_tiny_chunks": (rd.VARIANT_STAGED, 256, 2, 3),
     "snac_default": (rd.VARIANT_STAGED, 0, 0, 0),
     "snac_deep": (rd.VARIANT_STAGED, 4096, 8, 5),
@@ -184,7 +187,7 @@ def test_all_gather_v(policy, dtype, R, explicit):
         assert outs[j].guards_intact()
 
 
-@pytest.mark.parametrize("policy", ["zs", "snac_tiny_chunks"])
+@pytest.mark.parametrize("policy", ["zs", "zs_bulk", "zs_copy_engine", "snac_tiny_chunks"])
 def test_all_gather_in_place(policy):
     R, c, dtype = 8, 999, "bf16"
     h = handle(R)
@@ -198,7 +201,7 @@ def test_all_gather_in_place(policy):
         assert same_bits(host_bits(outs[j]), want[j])
 
 
-@pytest.mark.parametrize("policy", ["zs", "snac_tiny_chunks"])
+@pytest.mark.parametrize("policy", ["zs", "zs_bulk", "zs_copy_engine", "snac_tiny_chunks"])
 def test_all_gather_bytes_at_odd_offsets(policy):
     """u8 payloads at odd byte offsets use narrow copy units."""
     R = 3
@@ -250,7 +253,7 @@ def test_all_to_all_v(policy, dtype, R, explicit):
         assert outs[j].guards_intact()
 
 
-@pytest.mark.parametrize("policy", ["zs", "snac_tiny_chunks"])
+@pytest.mark.parametrize("policy", ["zs", "zs_bulk", "zs_copy_engine", "snac_tiny_chunks"])
 def test_all_to_all_fixed_twice_is_identity(policy):
     R, c, dtype = 8, 3001, "bf16"
     h = handle(R)
