@@ -435,6 +435,9 @@ def bench_purlin(args):
     # ---- bandwidth vs CTAs launched, per Atom, and the copy-engine AllGather
     frugal = cta_study(rd, torch, h, rs, ag, stream, rs_b, peak)
 
+    # ---- the other workload configurations, zero staging (default policy)
+    configs = other_configs(rd, torch, dev, stream, peak)
+
     # ---- AllReduce size sweep: zero staging vs SNAC (default policy)
     sweep = allreduce_sweep(rd, torch, dev, stream, peak)
 
@@ -472,6 +475,7 @@ def bench_purlin(args):
         "allreduce_4KiB": lat,
         "staged_step": staged,
         "cta_study": frugal,
+        "configs": configs,
         "allreduce_sweep": sweep,
         "e2e": e2e,
         "cpu_baseline": cpu,
@@ -580,6 +584,103 @@ def cta_study(rd, torch, h, rs, ag, stream, coll_b, peak):
         rd.purlin_set_atom(h, rd.ATOM_AUTO)
         rd.purlin_set_policy(h, 0, 0, 0, rd.VARIANT_ZS)
     return rows
+
+
+def other_configs(rd, torch, dev, stream, peak):
+    """The remaining workload configurations, each timed with CUDA events:
+    AllReduce R=2 fp32 4096 elements (latency); MoE AllToAllV dispatch and its
+    inverse (R=8, 4096 tokens x 7168 bf16 per source, Zipf(1.2)); data-parallel
+    attention AllGatherV + ReduceScatterV (token counts uniform in [1, 2048]);
+    AllGather with 1 GiB out per rank; AllReduce with 1 GiB per rank."""
+    import workloads
+    H = workloads.HIDDEN
+    out = {}
+
+    def entry(us, nbytes):
+        gbs = nbytes / (us / 1e6) / 1e9
+        return {"us": round(us, 2), "gbs": round(gbs, 1), "frac_of_peak": round(gbs / peak, 3),
+                "algorithmic_bytes": nbytes}
+
+    # AllReduce R=2 fp32 4096 integers: a latency point
+    h2 = rd.purlin_create(2, 0, dev.index)
+    try:
+        x = workloads.rank_buffers("allreduce_r2_f32", 2, 4096, "f32", device=dev, values="int")
+        o = [torch.empty_like(t) for t in x]
+        fn = lambda: rd.purlin_all_reduce(h2, x, o, 4096, "f32", stream=stream)
+        fn()
+        us = _graph_us(torch, stream, fn) or _events_us(torch, stream, fn, 200)
+        out["allreduce_r2_f32_4096"] = entry(us, 2 * 2 * 4096 * 4) | {"timing": "cuda graph"}
+    finally:
+        rd.purlin_destroy(h2)
+
+    h = rd.purlin_create(R, 0, dev.index)
+    try:
+        # MoE dispatch and inverse
+        T = 4096
+        C = workloads.zipf_pair_counts(R, T, workloads.ZIPF_S, workloads.seed_for("moe_a2av_r8", 9))
+        x = workloads.rank_buffers("moe_a2av_r8", R, T * H, "bf16", device=dev)
+        recv = [torch.empty(int(C[:, j].sum()) * H, dtype=torch.bfloat16, device=dev)
+                for j in range(R)]
+        back = [torch.empty_like(t) for t in x]
+        fwd = lambda: rd.purlin_all_to_all_v(h, x, recv, C * H, None, None, "bf16", stream=stream)
+        inv = lambda: rd.purlin_all_to_all_v(h, recv, back, C.T * H, None, None, "bf16",
+                                             stream=stream)
+        for _ in range(3):
+            fwd()
+            inv()
+        nb = 2 * int(C.sum()) * H * 2
+        out["moe_a2av_dispatch"] = entry(_events_us(torch, stream, fwd, 20), nb)
+        out["moe_a2av_combine"] = entry(_events_us(torch, stream, inv, 20), nb)
+        out["moe_a2av_received_tokens"] = [int(v) for v in C.sum(axis=0)]
+        del x, recv, back
+
+        # data-parallel attention: AllGatherV + ReduceScatterV
+        tok = workloads.uniform_token_counts(R, 1, 2048, workloads.seed_for("dp_attn_agv_rsv_r8", 9))
+        counts = [int(t) * H for t in tok]
+        Tt = sum(counts)
+        ag_in = [torch.randn(c, device=dev).to(torch.bfloat16) for c in counts]
+        ag_out = [torch.empty(Tt, dtype=torch.bfloat16, device=dev) for _ in range(R)]
+        rs_in = [torch.randn(Tt, device=dev).to(torch.bfloat16) for _ in range(R)]
+        rs_out = [torch.empty(c, dtype=torch.bfloat16, device=dev) for c in counts]
+        agv = lambda: rd.purlin_all_gather(h, ag_in, ag_out, counts, None, "bf16", stream=stream)
+        rsv = lambda: rd.purlin_reduce_scatter(h, rs_in, rs_out, counts, None, "bf16",
+                                               stream=stream)
+        for _ in range(3):
+            agv()
+            rsv()
+        nb = (R + 1) * Tt * 2
+        out["dp_attn_allgatherv"] = entry(_events_us(torch, stream, agv, 20), nb)
+        out["dp_attn_reducescatterv"] = entry(_events_us(torch, stream, rsv, 20), nb)
+        out["dp_attn_tokens"] = [int(t) for t in tok]
+        del ag_in, ag_out, rs_in, rs_out
+        torch.cuda.empty_cache()
+
+        # AllGather, 1 GiB out per rank (128 MiB in per rank)
+        c = (128 << 20) // 2
+        ag_in = [torch.randn(c, device=dev).to(torch.bfloat16) for _ in range(R)]
+        ag_out = [torch.empty(R * c, dtype=torch.bfloat16, device=dev) for _ in range(R)]
+        ag1 = lambda: rd.purlin_all_gather(h, ag_in, ag_out, [c] * R, None, "bf16", stream=stream)
+        for _ in range(3):
+            ag1()
+        out["allgather_1GiB_out"] = entry(_events_us(torch, stream, ag1, 10), (R + 1) * R * c * 2)
+        del ag_in, ag_out
+        torch.cuda.empty_cache()
+
+        # AllReduce, 1 GiB per rank
+        n = (1 << 30) // 2
+        ar_in = [torch.empty(n, dtype=torch.bfloat16, device=dev).normal_() for _ in range(R)]
+        ar_out = [torch.empty_like(t) for t in ar_in]
+        ar1 = lambda: rd.purlin_all_reduce(h, ar_in, ar_out, n, "bf16", stream=stream)
+        for _ in range(3):
+            ar1()
+        out["allreduce_1GiB"] = entry(_events_us(torch, stream, ar1, 10), 2 * R * n * 2)
+        del ar_in, ar_out
+        if rd.purlin_query_status(h) != rd.OK:
+            raise RuntimeError("configs: device status not ok")
+    finally:
+        rd.purlin_destroy(h)
+        torch.cuda.empty_cache()
+    return out
 
 
 def allreduce_sweep(rd, torch, dev, stream, peak):
