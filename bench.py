@@ -362,11 +362,9 @@ def bench_purlin(args):
     counts = [PART] * R
     torch.cuda.synchronize()
 
-    def rs():
-        rd.purlin_reduce_scatter(h, x, y, counts, None, "bf16", stream=stream)
-
-    def ag():
-        rd.purlin_all_gather(h, y, z, counts, None, "bf16", stream=stream)
+    # marshalled once: each repeat is one C call
+    rs = rd.prepare(rd.purlin_reduce_scatter, h, x, y, counts, None, "bf16", stream=stream)
+    ag = rd.prepare(rd.purlin_all_gather, h, y, z, counts, None, "bf16", stream=stream)
 
     with torch.cuda.stream(stream):
         for _ in range(max(3, args.warmup)):
@@ -741,12 +739,13 @@ def allreduce_latency(rd, torch, dev, stream, variant):
         b.record(stream)
         b.synchronize()
         single.append(a.elapsed_time(b) * 1e3)
-    # 1000 launches back to back from the host
+    # 1000 launches back to back from the host (prepared call: one C call each)
+    call = rd.prepare(rd.purlin_all_reduce, h, x, o, n, "bf16", stream=stream)
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
     a.record(stream)
     for _ in range(1000):
-        rd.purlin_all_reduce(h, x, o, n, "bf16", stream=stream)
+        call()
     b.record(stream)
     torch.cuda.synchronize()
     b2b = a.elapsed_time(b) * 1e3 / 1000

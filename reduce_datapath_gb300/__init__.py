@@ -218,34 +218,85 @@ def purlin_destroy(h) -> None:
     _check(lib().purlin_destroy(h), "purlin_destroy")
 
 
+# Marshalling of each collective's arguments into the C call's ctypes values.
+def _m_reduce_scatter(h, ins, outs, recv_counts, in_displs=None, dtype="bf16", op="sum",
+                      stream=None):
+    return (h, _ptrs(ins), _ptrs(outs), _sizes(recv_counts), _sizes(in_displs), _dtype(dtype),
+            _op(op), _stream(stream))
+
+
+def _m_all_gather(h, ins, outs, counts, out_displs=None, dtype="bf16", stream=None):
+    return (h, _ptrs(ins), _ptrs(outs), _sizes(counts), _sizes(out_displs), _dtype(dtype),
+            _stream(stream))
+
+
+def _m_all_reduce(h, ins, outs, count, dtype="bf16", op="sum", stream=None):
+    return (h, _ptrs(ins), _ptrs(outs), int(count), _dtype(dtype), _op(op), _stream(stream))
+
+
+def _m_all_to_all(h, ins, outs, count_per_pair, dtype="bf16", stream=None):
+    return (h, _ptrs(ins), _ptrs(outs), int(count_per_pair), _dtype(dtype), _stream(stream))
+
+
+def _m_all_to_all_v(h, ins, outs, send_counts, send_displs=None, recv_displs=None,
+                    dtype="bf16", stream=None):
+    return (h, _ptrs(ins), _ptrs(outs), _sizes(send_counts), _sizes(send_displs),
+            _sizes(recv_displs), _dtype(dtype), _stream(stream))
+
+
+def _call(name, cargs):
+    _check(getattr(lib(), name)(*cargs), name)
+
+
 def purlin_reduce_scatter(h, ins, outs, recv_counts, in_displs=None, dtype="bf16", op="sum",
                           stream=None) -> None:
-    _check(lib().purlin_reduce_scatter(h, _ptrs(ins), _ptrs(outs), _sizes(recv_counts),
-                                       _sizes(in_displs), _dtype(dtype), _op(op),
-                                       _stream(stream)), "purlin_reduce_scatter")
+    _call("purlin_reduce_scatter",
+          _m_reduce_scatter(h, ins, outs, recv_counts, in_displs, dtype, op, stream))
 
 
 def purlin_all_gather(h, ins, outs, counts, out_displs=None, dtype="bf16", stream=None) -> None:
-    _check(lib().purlin_all_gather(h, _ptrs(ins), _ptrs(outs), _sizes(counts),
-                                   _sizes(out_displs), _dtype(dtype), _stream(stream)),
-           "purlin_all_gather")
+    _call("purlin_all_gather", _m_all_gather(h, ins, outs, counts, out_displs, dtype, stream))
 
 
 def purlin_all_reduce(h, ins, outs, count, dtype="bf16", op="sum", stream=None) -> None:
-    _check(lib().purlin_all_reduce(h, _ptrs(ins), _ptrs(outs), int(count), _dtype(dtype),
-                                   _op(op), _stream(stream)), "purlin_all_reduce")
+    _call("purlin_all_reduce", _m_all_reduce(h, ins, outs, count, dtype, op, stream))
 
 
 def purlin_all_to_all(h, ins, outs, count_per_pair, dtype="bf16", stream=None) -> None:
-    _check(lib().purlin_all_to_all(h, _ptrs(ins), _ptrs(outs), int(count_per_pair),
-                                   _dtype(dtype), _stream(stream)), "purlin_all_to_all")
+    _call("purlin_all_to_all", _m_all_to_all(h, ins, outs, count_per_pair, dtype, stream))
 
 
 def purlin_all_to_all_v(h, ins, outs, send_counts, send_displs=None, recv_displs=None,
                         dtype="bf16", stream=None) -> None:
-    _check(lib().purlin_all_to_all_v(h, _ptrs(ins), _ptrs(outs), _sizes(send_counts),
-                                     _sizes(send_displs), _sizes(recv_displs), _dtype(dtype),
-                                     _stream(stream)), "purlin_all_to_all_v")
+    _call("purlin_all_to_all_v",
+          _m_all_to_all_v(h, ins, outs, send_counts, send_displs, recv_displs, dtype, stream))
+
+
+_MARSHAL = {
+    "purlin_reduce_scatter": _m_reduce_scatter,
+    "purlin_all_gather": _m_all_gather,
+    "purlin_all_reduce": _m_all_reduce,
+    "purlin_all_to_all": _m_all_to_all,
+    "purlin_all_to_all_v": _m_all_to_all_v,
+}
+
+
+def prepare(fn, *args, **kwargs):
+    """Marshal the arguments of one collective call once and return a callable
+    that repeats exactly that C call (same handle, buffers, counts, dtype and
+    stream).  For loops that re-issue a collective on the same buffers: each
+    repeat costs only the C call.  The buffers must outlive the callable."""
+    name = fn if isinstance(fn, str) else fn.__name__
+    cargs = _MARSHAL[name](*args, **kwargs)
+    cfn = getattr(lib(), name)
+
+    def call() -> None:
+        st = cfn(*cargs)
+        if st != OK:
+            raise PurlinError(st, name)
+
+    call.c_args = cargs   # keeps the ctypes arrays alive with the callable
+    return call
 
 
 def purlin_set_policy(h, chunk_bytes=0, depth=0, ctas=0, variant=VARIANT_AUTO) -> None:

@@ -363,3 +363,24 @@ def test_last_launch_reports_the_call():
     info = rd.purlin_last_launch(h)
     assert info["variant"] == rd.VARIANT_STAGED and info["grid"] % 3 == 0
     run_ok(h)
+
+
+def test_prepared_call_repeats_the_same_collective():
+    """rd.prepare marshals once; every repeat must give the same bits as a
+    fresh call, and see policy changes made on the handle in between."""
+    R, n = 4, 50001
+    h = handle(R)
+    set_variant(h, rd.VARIANT_ZS)
+    x = inputs(R, n, "bf16", seed=61)
+    out = [torch.empty_like(t) for t in x]
+    want = oracle.all_reduce(oracle_in(x), dtype="bf16")
+    call = rd.prepare(rd.purlin_all_reduce, h, x, out, n, "bf16")
+    for variant in (rd.VARIANT_ZS, rd.VARIANT_STAGED, rd.VARIANT_ZS):
+        for o in out:
+            o.zero_()
+        rd.purlin_set_policy(h, 0, 0, 0, variant)
+        call()
+        run_ok(h)
+        for j in range(R):
+            assert same_bits(host_bits(out[j]), want[j])
+    set_variant(h, rd.VARIANT_ZS)
