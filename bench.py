@@ -439,8 +439,13 @@ def bench_purlin(args):
     # ---- AllReduce size sweep: zero staging vs SNAC (default policy)
     sweep = allreduce_sweep(rd, torch, dev, stream, peak)
 
-    # ---- end to end: inputs from pinned host memory, outputs back to it
+    # ---- end to end: inputs from pinned host memory, outputs back to it; with
+    # several ranks the job's figure is all ranks' bytes over the slowest rank
+    barrier(world, dev)
     e2e = bench_e2e(args, rd, torch, h, x, y, z, counts, stream)
+    e2e["value"], e2e_ms = whole_job_value(world, e2e["steps"], rs_b + ag_b,
+                                           e2e["ms_per_step"] * e2e["steps"], dev)
+    e2e["ms_per_step"] = e2e_ms / e2e["steps"]
 
     # ---- CPU oracle baseline and a bit-exact check of this run's result
     cpu = None

@@ -324,7 +324,7 @@ purlin_status_t run(purlin_handle_t h, Coll coll, const void* const in_[], void*
                 if (pc.dst != kEveryRank && pc.dst != j) continue;
                 char* dst = reinterpret_cast<char*>(out[j]) + pc.dst_off;
                 if (dst == src) continue;  // in-place AllGather block
-                ce = cudaMemcpyAsync(dst, src, pc.bytes, cudaMemcpyDeviceToDevice, s);
+                ce = cudaMemcpyAsync(dst, src, pc.bytes, cudaMemcpyDefault, s);
                 if (ce != cudaSuccess) break;
                 ++copies;
             }
