@@ -230,3 +230,23 @@ def test_plan_rejects_bad_arguments(lib):
     with pytest.raises(rd.PurlinError) as e:   # byte count overflows 64 bits
         rd.purlin_plan_segments(rd.COLL_ALL_GATHER, 2, a, a, [2 ** 63, 1], dtype="f32")
     assert e.value.status == rd.ERR_INVALID_ARG
+
+
+def test_plan_at_maximum_sizes(lib):
+    """Huge messages plan without overflow, and a tile count beyond 32 bits is
+    refused rather than wrapped."""
+    a = [1 << 44, 2 << 44, 3 << 44, 4 << 44, 5 << 44, 6 << 44, 7 << 44, 8 << 44]
+    b = [x + (1 << 43) for x in a]
+    # 64 GiB of bf16 per rank: 2^23 tiles of 8 KiB at 32-byte units
+    segs, nt = rd.purlin_plan_segments(rd.COLL_ALL_REDUCE, 8, a, b, count=1 << 35, dtype="bf16")
+    assert len(segs) == 1 and segs[0]["bytes"] == 1 << 36 and nt == (1 << 36) // 8192
+    # 2^45 bytes at 32-byte copy units -> 2^32 tiles of 32 KiB: refused
+    with pytest.raises(rd.PurlinError) as e:
+        rd.purlin_plan_segments(rd.COLL_ALL_GATHER, 1, a[:1], b[:1], [1 << 47], dtype="u8")
+    assert e.value.status == rd.ERR_UNSUPPORTED
+    # R * R pieces with 3 segments each fit the largest plan
+    R = 8
+    odd = [x + 1 for x in a]
+    C = np.full(R * R, 1001)
+    segs, _ = rd.purlin_plan_segments(rd.COLL_ALL_TO_ALL_V, R, odd, b, C, dtype="u8")
+    assert len(segs) <= 3 * R * R
