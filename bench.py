@@ -433,6 +433,9 @@ def bench_purlin(args):
     # ---- bandwidth vs CTAs launched, per Atom, and the copy-engine AllGather
     frugal = cta_study(rd, torch, h, rs, ag, stream, rs_b, peak)
 
+    # ---- the pairwise rank order, reported beside the fixed order
+    tree = tree_order_report(rd, torch, h, x, y, counts, stream, rs_b, peak)
+
     # ---- the other workload configurations, zero staging (default policy)
     configs = other_configs(rd, torch, dev, stream, peak)
 
@@ -479,6 +482,7 @@ def bench_purlin(args):
         "staged_step": staged,
         "cta_study": frugal,
         "configs": configs,
+        "tree_order": tree,
         "allreduce_sweep": sweep,
         "e2e": e2e,
         "cpu_baseline": cpu,
@@ -587,6 +591,39 @@ def cta_study(rd, torch, h, rs, ag, stream, coll_b, peak):
         rd.purlin_set_atom(h, rd.ATOM_AUTO)
         rd.purlin_set_policy(h, 0, 0, 0, rd.VARIANT_ZS)
     return rows
+
+
+def tree_order_report(rd, torch, h, x, y_fixed, counts, stream, coll_b, peak):
+    """The step's ReduceScatter with the pairwise rank order: its bandwidth and
+    how far it lands from the fixed order (y_fixed holds the fixed-order result
+    of the last timed step)."""
+    y = [torch.empty_like(t) for t in y_fixed]
+    rs_tree = rd.prepare(rd.purlin_reduce_scatter, h, x, y, counts, None, "bf16", stream=stream)
+    rd.purlin_set_reduce_order(h, rd.ORDER_TREE)
+    try:
+        for _ in range(3):
+            rs_tree()
+        us = _events_us(torch, stream, rs_tree, 20)
+    finally:
+        rd.purlin_set_reduce_order(h, rd.ORDER_FIXED)
+    c = y_fixed[0].numel()
+    differing, max_ulp, max_scaled = 0, 0, 0.0
+    for k in range(R):
+        a = y[k].view(torch.int16).int()
+        b = y_fixed[k].view(torch.int16).int()
+        differing += int((a != b).sum())
+        same_sign = (a < 0) == (b < 0)
+        if bool(same_sign.any()):
+            max_ulp = max(max_ulp, int((a - b).abs()[same_sign].max()))
+        mag = sum(t[k * c:(k + 1) * c].float().abs() for t in x)
+        err = (y[k].float() - y_fixed[k].float()).abs() / mag.clamp_min(1e-30)
+        max_scaled = max(max_scaled, float(err.max()))
+    gbs = coll_b / (us / 1e6) / 1e9
+    return {"collective": "reduce_scatter", "us": round(us, 2), "gbs": round(gbs, 1),
+            "frac_of_peak": round(gbs / peak, 3),
+            "elements_differing_from_fixed_order": round(differing / (R * c), 4),
+            "max_bf16_ulp_vs_fixed_order": max_ulp,
+            "max_abs_diff_over_sum_abs": max_scaled}
 
 
 def other_configs(rd, torch, dev, stream, peak):

@@ -99,7 +99,7 @@ __device__ __forceinline__ int ld_status(const int* s)
     return v;
 }
 
-// Bounded wait of one CTA for *flag >= want.  Thread 0 spins; the verdict is
+// Bounded wait of one CTA for *flag >= want.  Thread 0 spins; the outcome is
 // shared through shared memory.  Returns false if the CTA must leave (this
 // wait timed out, or another CTA recorded an error).
 __device__ bool cta_wait(const SnacParams& p, const uint64_t* flag, uint64_t want)

@@ -384,3 +384,22 @@ def test_prepared_call_repeats_the_same_collective():
         for j in range(R):
             assert same_bits(host_bits(out[j]), want[j])
     set_variant(h, rd.VARIANT_ZS)
+
+
+@pytest.mark.parametrize("fp8", ["float8_e4m3fn", "float8_e5m2"])
+def test_fp8_payloads_move_as_bytes(fp8):
+    """fp8 (or packed fp4) token payloads of an AllToAllV dispatch are 1-byte
+    copies: the binding maps torch's fp8 dtypes to the byte type."""
+    if not hasattr(torch, fp8):
+        pytest.skip("torch has no " + fp8)
+    R = 8
+    h = handle(R)
+    set_variant(h, rd.VARIANT_ZS)
+    C = np.random.default_rng(5).integers(0, 300, size=(R, R)) * 64
+    x = [torch.randn(int(C[s].sum()), device="cuda").to(getattr(torch, fp8)) for s in range(R)]
+    out = [torch.empty(int(C[:, j].sum()), dtype=x[0].dtype, device="cuda") for j in range(R)]
+    rd.purlin_all_to_all_v(h, x, out, C, None, None, x[0].dtype)
+    run_ok(h)
+    want = oracle.all_to_all_v([t.view(torch.uint8).cpu().numpy() for t in x], C)
+    for j in range(R):
+        assert same_bits(out[j].view(torch.uint8).cpu().numpy(), want[j])
