@@ -12,6 +12,7 @@
 #include "purlin_debug.h"
 
 #include <algorithm>
+#include <cstdio>
 #include <cstdlib>
 #include <cstring>
 #include <new>
@@ -44,6 +45,8 @@ struct purlin_handle {
     int max_unit_log2 = 0;   // 0: per collective (AllReduce 4 = 16 B, else 5 = 32 B)
     int l2_load = -1;        // -1: per collective; else kL2Normal/EvictFirst/EvictLast
     int l2_store = -1;
+    int l2_coll_load[4] = {-1, -1, -1, -1};   // per-collective overrides (by Coll)
+    int l2_coll_store[4] = {-1, -1, -1, -1};
     bool pdl = true;         // programmatic dependent launch of zero-staging kernels
     int atom = PURLIN_ATOM_AUTO;
     int inject = 0;  // purlin_debug_inject, one staged call
@@ -154,22 +157,24 @@ struct ZsKnobs {
 //  - the fused AllReduce (R loads and R stores per unit) runs best with 16-byte
 //    units (170 vs 174 us), everything else with 32-byte units (ReduceScatter
 //    91 vs 96 us);
-//  - sources that are read exactly once (sums, AllToAll) are loaded
-//    evict-first: in a ReduceScatter -> AllGather step this keeps the reduced
-//    partitions and the previous call's dirty lines in L2 (ReduceScatter
-//    108.8 -> 98.5 us inside the step); AllReduce and AllToAll outputs are
-//    written evict-first.
+//  - every source is read exactly once, so loads are evict-first; outputs are
+//    written evict-first except the ReduceScatter's, which a following
+//    collective (the AllGather of a ReduceScatter -> AllGather pair) reads
+//    next.  In that pair the AllGather's reads then hit L2 and DRAM sees
+//    almost only its writes: AllGather 104.3 -> 90.2 us, ReduceScatter
+//    108.8 -> 98.5 us, the pair 5599 -> 6332 GB/s.
 ZsKnobs zs_knobs(const purlin_handle* h, Coll coll)
 {
     ZsKnobs k;
     const bool reduce = coll == Coll::ReduceScatter || coll == Coll::AllReduce;
     k.unroll = reduce ? kUnrollReduce : (h->atom == PURLIN_ATOM_BULK ? kUnrollBulk : kUnrollCopy);
     k.max_unit_log2 = h->max_unit_log2 ? h->max_unit_log2 : (coll == Coll::AllReduce ? 4 : 5);
-    k.l2_load = h->l2_load >= 0 ? (uint32_t)h->l2_load
-                                : (coll == Coll::AllGather ? kL2Normal : kL2EvictFirst);
+    k.l2_load = h->l2_load >= 0 ? (uint32_t)h->l2_load : kL2EvictFirst;
     k.l2_store = h->l2_store >= 0 ? (uint32_t)h->l2_store
-                                  : ((coll == Coll::AllReduce || coll == Coll::AllToAllV)
-                                         ? kL2EvictFirst : kL2Normal);
+                                  : (coll == Coll::ReduceScatter ? kL2Normal : kL2EvictFirst);
+    const int ci = (int)coll;
+    if (h->l2_coll_load[ci] >= 0) k.l2_load = (uint32_t)h->l2_coll_load[ci];
+    if (h->l2_coll_store[ci] >= 0) k.l2_store = (uint32_t)h->l2_coll_store[ci];
     k.pdl = h->pdl;
     return k;
 }
@@ -435,6 +440,16 @@ purlin_status_t purlin_create(purlin_handle_t* out, int R, size_t staging_bytes,
     // Tuning knobs for measurements only; the defaults are the measured best.
     if (const char* u = std::getenv("PURLIN_PDL")) h->pdl = std::atoi(u) != 0;
     if (const char* u = std::getenv("PURLIN_L2_LOAD")) h->l2_load = std::atoi(u) % 3;
+    {
+        const char* names[4] = {"RS", "AG", "AR", "A2A"};
+        char var[40];
+        for (int i = 0; i < 4; ++i) {
+            std::snprintf(var, sizeof var, "PURLIN_L2_%s_LOAD", names[i]);
+            if (const char* u = std::getenv(var)) h->l2_coll_load[i] = std::atoi(u) % 3;
+            std::snprintf(var, sizeof var, "PURLIN_L2_%s_STORE", names[i]);
+            if (const char* u = std::getenv(var)) h->l2_coll_store[i] = std::atoi(u) % 3;
+        }
+    }
     if (const char* u = std::getenv("PURLIN_L2_STORE")) h->l2_store = std::atoi(u) % 3;
     if (const char* u = std::getenv("PURLIN_MAX_UNIT")) {
         int v = std::atoi(u);
