@@ -34,7 +34,6 @@ struct purlin_handle {
     uint64_t* flags = nullptr;
     size_t flag_words = 0;
     int* status = nullptr;
-    uint64_t call_seq = 0;  // SNAC epoch: grows by one per staged call
     // policy (0 = automatic)
     size_t chunk_bytes = 0;
     int depth = 0;
@@ -293,7 +292,6 @@ purlin_status_t run(purlin_handle_t h, Coll coll, const void* const in_[], void*
         cfg.flags = h->flags;
         cfg.flag_words = h->flag_words;
         cfg.status = h->status;
-        cfg.epoch = ++h->call_seq;
         cfg.chunk_bytes = h->chunk_bytes;
         cfg.depth = h->depth;
         cfg.channels = h->ctas;

@@ -16,7 +16,6 @@
 // per device (with that device current) and passed to the kernel.
 #include "purlin.h"
 
-#include <atomic>
 #include <cstdint>
 #include <mutex>
 
@@ -48,7 +47,6 @@ struct DeviceScratch {
     cudaError_t setup_error = cudaSuccess;
     char* base = nullptr;   // device address of g_noalloc_scratch on this device
     int sms = 0;
-    std::atomic<uint64_t> epoch{0};
 };
 
 DeviceScratch g_devices[kMaxDevices];
@@ -131,7 +129,6 @@ extern "C" PURLIN_API purlin_status_t purlin_all_reduce_noalloc(
     cfg.flags = reinterpret_cast<uint64_t*>(d.base + kFlagsOffset);
     cfg.flag_words = kFlagWords;
     cfg.status = status;
-    cfg.epoch = d.epoch.fetch_add(1) + 1;
     cfg.chunk_bytes = chunk;
     cfg.depth = dep;
     cfg.channels = 0;

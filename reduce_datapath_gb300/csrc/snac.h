@@ -40,10 +40,10 @@ struct SnacRequest {
 struct SnacConfig {
     char* staging;          // device ring memory (owned by the caller)
     size_t staging_bytes;
-    uint64_t* flags;        // device flag words, zeroed once at creation
+    uint64_t* flags;        // device flag words, zeroed once at creation; the last
+                            // two hold the device epoch and a completion counter
     size_t flag_words;
     int* status;            // device status word (0 = ok)
-    uint64_t epoch;         // > every epoch used before with these flags
     size_t chunk_bytes;     // 0 = automatic
     int depth;              // 0 = automatic
     int channels;           // 0 = automatic

@@ -24,8 +24,11 @@
 // Steps are the layout's segments cut into chunks of `chunk` bytes per rank;
 // step i belongs to channel i % channels and is that channel's n-th step,
 // n = i / channels, held in slot n % depth.  A flag holds the tag
-// (epoch << 32) | (n + 1); epochs grow by one per call, so flags never need
-// resetting.  Every wait is bounded (time and iteration count) and watches the
+// (epoch << 32) | (n + 1).  The epoch lives in device memory (the last flag
+// word): every CTA reads it when the kernel starts, and the last CTA to finish
+// advances it (a completion counter in the word before it), so each call --
+// also each replay of a captured CUDA graph -- runs with a fresh epoch and the
+// flags never need resetting.  Every wait is bounded (time and iteration count) and watches the
 // status word: on a timeout the waiter records PURLIN_ERR_TIMEOUT and every CTA
 // leaves at its next wait.
 #include "atom.cuh"
@@ -65,7 +68,8 @@ struct SnacParams {
     char* staging;
     uint64_t* flags;
     int* status;
-    uint64_t epoch;
+    uint64_t* epoch_word;    // device epoch of the last completed call
+    uint32_t* done_word;     // CTAs of the running call that have finished
     uint64_t timeout_ns;
     uint64_t max_spins;
     uint64_t chunk;        // bytes per rank per step (multiple of 256)
@@ -80,9 +84,9 @@ struct SnacParams {
     Segment seg[kSegsLarge];  // tile0 = first step of the segment
 };
 
-__device__ __forceinline__ uint64_t tag_of(const SnacParams& p, uint32_t n)
+__device__ __forceinline__ uint64_t tag_of(uint64_t epoch, uint32_t n)
 {
-    return (p.epoch << 32) | (uint64_t)(n + 1);
+    return (epoch << 32) | (uint64_t)(n + 1);
 }
 
 __device__ __forceinline__ uint64_t now_ns()
@@ -312,7 +316,7 @@ __device__ void cta_reduce(const SnacParams& p, int unit_log2, char* dst, const 
 // ------------------------------------------------------------------ roles
 
 template <int KIND>
-__device__ void producer(const SnacParams& p, uint32_t ch)
+__device__ void producer(const SnacParams& p, uint32_t ch, uint64_t epoch)
 {
     const bool reduce = KIND == kRS || KIND == kAR;
     // Sources are read exactly once: their lines go first, the ring stays.
@@ -322,7 +326,7 @@ __device__ void producer(const SnacParams& p, uint32_t ch)
     for (uint32_t i = ch; i < p.nsteps; i += p.nch, ++n) {
         const uint32_t slot = n % p.depth;
         uint64_t* f = slot_flags(p, ch, slot);
-        if (n >= p.depth && !cta_wait(p, f + kFree, tag_of(p, n - p.depth))) return;
+        if (n >= p.depth && !cta_wait(p, f + kFree, tag_of(epoch, n - p.depth))) return;
         const Segment& s = step_segment(p, i);
         const uint64_t off = (uint64_t)(i - s.tile0) * p.chunk;
         const uint64_t len = min(p.chunk, s.bytes - off);
@@ -334,12 +338,12 @@ __device__ void producer(const SnacParams& p, uint32_t ch)
                                        len, 0, lpol, spol);
         }
         if (p.inject && ch == 0 && n == 0) continue;  // testing: this notify never happens
-        cta_notify(f + kReady, tag_of(p, n));
+        cta_notify(f + kReady, tag_of(epoch, n));
     }
 }
 
 template <typename T, int ORDER, int KIND>
-__device__ void consumer(const SnacParams& p, uint32_t ch)
+__device__ void consumer(const SnacParams& p, uint32_t ch, uint64_t epoch)
 {
     // AllToAll outputs are written once and not read again here: evict-first.
     const uint64_t lpol = atom::l2_policy(kL2Normal);
@@ -348,7 +352,7 @@ __device__ void consumer(const SnacParams& p, uint32_t ch)
     for (uint32_t i = ch; i < p.nsteps; i += p.nch, ++n) {
         const uint32_t slot = n % p.depth;
         uint64_t* f = slot_flags(p, ch, slot);
-        if (!cta_wait(p, f + kReady, tag_of(p, n))) return;
+        if (!cta_wait(p, f + kReady, tag_of(epoch, n))) return;
         const Segment& s = step_segment(p, i);
         const uint64_t off = (uint64_t)(i - s.tile0) * p.chunk;
         const uint64_t len = min(p.chunk, s.bytes - off);
@@ -356,7 +360,7 @@ __device__ void consumer(const SnacParams& p, uint32_t ch)
         if (KIND == kRS) {
             cta_reduce<T, ORDER>(p, s.unit_log2, p.out[s.dst] + s.dst_off + off, staged, len, spol);
         } else if (KIND == kAR) {
-            if (n >= p.depth && !cta_wait(p, f + kYFree, tag_of(p, n - p.depth))) return;
+            if (n >= p.depth && !cta_wait(p, f + kYFree, tag_of(epoch, n - p.depth))) return;
             cta_reduce<T, ORDER>(p, s.unit_log2, staged + (uint64_t)p.R * p.chunk, staged, len,
                                  spol);
         } else if (KIND == kAG) {
@@ -366,12 +370,12 @@ __device__ void consumer(const SnacParams& p, uint32_t ch)
             cta_copy_any<true, false>(p, s.unit_log2, p.out[s.dst] + s.dst_off + off, 0, staged,
                                       len, 0, lpol, spol);
         }
-        cta_notify(f + kFree, tag_of(p, n));
-        if (KIND == kAR && threadIdx.x == 0) st_release(f + kYReady, tag_of(p, n));
+        cta_notify(f + kFree, tag_of(epoch, n));
+        if (KIND == kAR && threadIdx.x == 0) st_release(f + kYReady, tag_of(epoch, n));
     }
 }
 
-__device__ void gatherer(const SnacParams& p, uint32_t ch)
+__device__ void gatherer(const SnacParams& p, uint32_t ch, uint64_t epoch)
 {
     // The R outputs are written once: evict-first keeps the ring in L2.
     const uint64_t lpol = atom::l2_policy(kL2Normal);
@@ -380,7 +384,7 @@ __device__ void gatherer(const SnacParams& p, uint32_t ch)
     for (uint32_t i = ch; i < p.nsteps; i += p.nch, ++n) {
         const uint32_t slot = n % p.depth;
         uint64_t* f = slot_flags(p, ch, slot);
-        if (!cta_wait(p, f + kYReady, tag_of(p, n))) return;
+        if (!cta_wait(p, f + kYReady, tag_of(epoch, n))) return;
         const Segment& s = step_segment(p, i);
         const uint64_t off = (uint64_t)(i - s.tile0) * p.chunk;
         const uint64_t len = min(p.chunk, s.bytes - off);
@@ -388,18 +392,39 @@ __device__ void gatherer(const SnacParams& p, uint32_t ch)
         // In-place AllReduce writes out[r] == in[r]; this step's input range
         // was staged before the y tag was published, so the writes are safe.
         cta_copy_any<true, true>(p, s.unit_log2, nullptr, s.dst_off + off, y, len, 0, lpol, spol);
-        cta_notify(f + kYFree, tag_of(p, n));
+        cta_notify(f + kYFree, tag_of(epoch, n));
     }
 }
 
 template <typename T, int ORDER, int KIND>
 __global__ void __launch_bounds__(kThreads, 2) snac_kernel(const __grid_constant__ SnacParams p)
 {
+    __shared__ uint64_t epoch_s;
+    if (threadIdx.x == 0) {
+        uint64_t prev;
+        asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(prev) : "l"(p.epoch_word) : "memory");
+        epoch_s = prev + 1;
+    }
+    __syncthreads();
+    const uint64_t epoch = epoch_s;
     const uint32_t role = blockIdx.x / p.nch;
     const uint32_t ch = blockIdx.x % p.nch;
-    if (role == 0) producer<KIND>(p, ch);
-    else if (role == 1) consumer<T, ORDER, KIND>(p, ch);
-    else if (KIND == kAR) gatherer(p, ch);
+    if (role == 0) producer<KIND>(p, ch, epoch);
+    else if (role == 1) consumer<T, ORDER, KIND>(p, ch, epoch);
+    else if (KIND == kAR) gatherer(p, ch, epoch);
+    // Whatever path a role left by (done, or an error seen), the last CTA to
+    // get here publishes the epoch for the next call and resets the counter.
+    // No CTA reads the epoch word after its start, and every CTA has started
+    // before the last one arrives, so all of them used the same epoch.
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        if (atomicAdd(p.done_word, 1u) == gridDim.x - 1) {
+            atomicExch(p.done_word, 0u);
+            __threadfence();
+            st_release(p.epoch_word, epoch);
+        }
+    }
 }
 
 using SnacKernel = void (*)(SnacParams);
@@ -458,7 +483,8 @@ purlin_status_t snac_geometry(int R, Coll coll, const SnacConfig& cfg, int resid
     const size_t slot = (size_t)sub_slots(coll, R) * chunk;
     const size_t ring = (size_t)depth * slot;
     const long by_ring = ring ? (long)(cfg.staging_bytes / ring) : 0;
-    const long by_flags = (long)(cfg.flag_words / ((size_t)depth * kFlagsPerSlot));
+    // the last two flag words hold the epoch and the completion counter
+    const long by_flags = (long)((cfg.flag_words - 2) / ((size_t)depth * kFlagsPerSlot));
     const long by_residency = (long)resident_per_sm * cfg.sms / roles_of(coll);
     long nch = cfg.channels ? cfg.channels : kMaxChannels;
     nch = std::min({nch, by_ring, by_flags, by_residency});
@@ -512,7 +538,8 @@ purlin_status_t run_with(SnacParams& p, const SnacRequest& rq, const SnacConfig&
     p.staging = cfg.staging;
     p.flags = cfg.flags;
     p.status = cfg.status;
-    p.epoch = cfg.epoch;
+    p.epoch_word = cfg.flags + cfg.flag_words - 1;
+    p.done_word = reinterpret_cast<uint32_t*>(cfg.flags + cfg.flag_words - 2);
     p.timeout_ns = cfg.timeout_ns;
     p.max_spins = cfg.timeout_ns / 64 + 65536;
     p.chunk = chunk;
