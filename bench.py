@@ -578,6 +578,17 @@ def cta_study(rd, torch, h, rs, ag, stream, coll_b, peak):
             rows.append({"collective": "reduce_scatter", "atom": "vector", "ctas": ctas,
                          "us": round(us, 1), "gbs": round(coll_b / (us / 1e6) / 1e9, 1),
                          "frac_of_peak": round(coll_b / (us / 1e6) / 1e9 / peak, 3)})
+        rd.purlin_set_atom(h, rd.ATOM_VECTOR)
+        rd.purlin_set_direction(h, rd.DIRECTION_PULL)
+        for ctas in (152, 304):
+            rd.purlin_set_policy(h, 0, 0, ctas, rd.VARIANT_ZS)
+            ag()
+            us = _events_us(torch, stream, ag, 10)
+            rows.append({"collective": "all_gather", "atom": "vector", "direction": "pull",
+                         "ctas": ctas, "us": round(us, 1),
+                         "gbs": round(coll_b / (us / 1e6) / 1e9, 1),
+                         "frac_of_peak": round(coll_b / (us / 1e6) / 1e9 / peak, 3)})
+        rd.purlin_set_direction(h, rd.DIRECTION_AUTO)
         rd.purlin_set_policy(h, 0, 0, 0, rd.VARIANT_ZS)
         rd.purlin_set_atom(h, rd.ATOM_COPY_ENGINE)
         ag()
@@ -589,6 +600,7 @@ def cta_study(rd, torch, h, rs, ag, stream, coll_b, peak):
             raise RuntimeError("cta study: device status not ok")
     finally:
         rd.purlin_set_atom(h, rd.ATOM_AUTO)
+        rd.purlin_set_direction(h, rd.DIRECTION_AUTO)
         rd.purlin_set_policy(h, 0, 0, 0, rd.VARIANT_ZS)
     return rows
 

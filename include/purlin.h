@@ -108,6 +108,16 @@ typedef enum {
                                      destination, on the copy engines               */
 } purlin_atom_t;
 
+/* How an AllGather's copies are organized (push vs pull, Figures 7 and 11).
+ * PUSH: work is split by source tile; a tile is read once and written to all R
+ * destinations.  PULL: work is split by destination; each destination pulls
+ * every source's block (R reads of each source, from L2 after the first). */
+typedef enum {
+    PURLIN_DIRECTION_AUTO = 0,  /* library's choice (measured best: PUSH)        */
+    PURLIN_DIRECTION_PUSH = 1,
+    PURLIN_DIRECTION_PULL = 2
+} purlin_direction_t;
+
 typedef struct purlin_handle* purlin_handle_t;
 
 /* What the last collective on a handle launched (for SM accounting, Figure 10:
@@ -256,6 +266,10 @@ PURLIN_API purlin_status_t purlin_set_policy(purlin_handle_t h, size_t chunk_byt
 /* Mechanism of copy collectives on the zero-staging path: a purlin_atom_t.
  * Sums always run on the vector Atom; the staged path ignores this setting. */
 PURLIN_API purlin_status_t purlin_set_atom(purlin_handle_t h, int atom);
+
+/* Push or pull organization of AllGather(V) copies on the zero-staging path
+ * (a purlin_direction_t).  Other collectives ignore it. */
+PURLIN_API purlin_status_t purlin_set_direction(purlin_handle_t h, int direction);
 
 /* Rank order of sums: PURLIN_ORDER_FIXED (default) or PURLIN_ORDER_TREE. */
 PURLIN_API purlin_status_t purlin_set_reduce_order(purlin_handle_t h, int order);

@@ -48,6 +48,7 @@ struct purlin_handle {
     int l2_coll_store[4] = {-1, -1, -1, -1};
     bool pdl = true;         // programmatic dependent launch of zero-staging kernels
     int atom = PURLIN_ATOM_AUTO;
+    int direction = PURLIN_DIRECTION_AUTO;
     int inject = 0;  // purlin_debug_inject, one staged call
     purlin_launch_info_t last{};
 };
@@ -314,7 +315,7 @@ purlin_status_t run(purlin_handle_t h, Coll coll, const void* const in_[], void*
 
     info.variant = PURLIN_VARIANT_ZS;
     cudaError_t ce = cudaSuccess;
-    const ZsKnobs knobs = zs_knobs(h, coll);
+    ZsKnobs knobs = zs_knobs(h, coll);
     const bool bulk = !reduce && h->atom == PURLIN_ATOM_BULK;
     if (!reduce && h->atom == PURLIN_ATOM_COPY_ENGINE) {
         // No kernel: every block goes to every destination through the copy
@@ -337,9 +338,28 @@ purlin_status_t run(purlin_handle_t h, Coll coll, const void* const in_[], void*
         info.block = 0;
         info.chunk_bytes = 0;
         (void)copies;
-    } else if (coll == Coll::AllToAllV) {
+    } else if (coll == Coll::AllToAllV ||
+               (coll == Coll::AllGather && h->direction == PURLIN_DIRECTION_PULL)) {
         static thread_local ZsParams<kSegsLarge> p;
-        st = make_params(p, pieces, np, R, in, out, esz, false, knobs, h->status);
+        const Piece* plan = pieces;
+        int nplan = np;
+        Piece pulled[kMaxRanks * kMaxRanks];
+        if (coll == Coll::AllGather) {
+            // pull: one piece per (destination, source), destination by
+            // destination; every source is read R times (from L2 after the
+            // first read, hence normal priority for the loads)
+            nplan = 0;
+            for (int j = 0; j < R; ++j)
+                for (int i = 0; i < np; ++i) {
+                    Piece e = pieces[i];
+                    e.dst = (uint8_t)j;
+                    if (in[e.src] + e.src_off == out[j] + e.dst_off) continue;  // in place
+                    pulled[nplan++] = e;
+                }
+            plan = pulled;
+            if (h->l2_load < 0 && h->l2_coll_load[(int)coll] < 0) knobs.l2_load = kL2Normal;
+        }
+        st = make_params(p, plan, nplan, R, in, out, esz, false, knobs, h->status);
         if (st != PURLIN_OK) return st;
         int grid;
         if (bulk) {
@@ -537,6 +557,14 @@ purlin_status_t purlin_set_atom(purlin_handle_t h, int atom)
     if (!h || atom < PURLIN_ATOM_AUTO || atom > PURLIN_ATOM_COPY_ENGINE)
         return PURLIN_ERR_INVALID_ARG;
     h->atom = atom;
+    return PURLIN_OK;
+}
+
+purlin_status_t purlin_set_direction(purlin_handle_t h, int direction)
+{
+    if (!h || direction < PURLIN_DIRECTION_AUTO || direction > PURLIN_DIRECTION_PULL)
+        return PURLIN_ERR_INVALID_ARG;
+    h->direction = direction;
     return PURLIN_OK;
 }
 

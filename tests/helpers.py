@@ -69,9 +69,10 @@ def handle(R):
     return _handles[R]
 
 
-def set_variant(h, variant, chunk=0, depth=0, ctas=0, atom=0):
+def set_variant(h, variant, chunk=0, depth=0, ctas=0, atom=0, direction=0):
     rd.purlin_set_policy(h, chunk, depth, ctas, variant)
     rd.purlin_set_atom(h, atom)
+    rd.purlin_set_direction(h, direction)
 
 
 def close_handles():

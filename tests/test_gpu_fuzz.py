@@ -44,6 +44,7 @@ def _policy(rng, h, copy):
         rd.purlin_set_policy(h, 0, 0, int(rng.choice([0, 1, 3, 17])), rd.VARIANT_ZS)
         rd.purlin_set_atom(h, int(rng.choice([rd.ATOM_VECTOR, rd.ATOM_BULK, rd.ATOM_COPY_ENGINE]))
                            if copy else rd.ATOM_AUTO)
+        rd.purlin_set_direction(h, int(rng.choice([rd.DIRECTION_PUSH, rd.DIRECTION_PULL])))
     else:
         chunk = int(rng.choice([256, 512, 4096, 16384, 65536]))
         rd.purlin_set_policy(h, chunk, int(rng.integers(1, 9)), int(rng.choice([0, 1, 2, 5])),
@@ -115,4 +116,5 @@ def test_random_layout(seed):
     finally:
         rd.purlin_set_reduce_order(h, rd.ORDER_FIXED)
         rd.purlin_set_atom(h, rd.ATOM_AUTO)
+        rd.purlin_set_direction(h, rd.DIRECTION_AUTO)
         rd.purlin_set_policy(h, 0, 0, 0, rd.VARIANT_AUTO)

@@ -24,6 +24,8 @@ POLICIES = {
     "zs_bulk": (rd.VARIANT_ZS, 0, 0, 0, rd.ATOM_BULK),
     "zs_bulk_3ctas": (rd.VARIANT_ZS, 0, 0, 3, rd.ATOM_BULK),
     "zs_copy_engine": (rd.VARIANT_ZS, 0, 0, 0, rd.ATOM_COPY_ENGINE),
+    "zs_pull": (rd.VARIANT_ZS, 0, 0, 0, rd.ATOM_VECTOR, rd.DIRECTION_PULL),
+    "zs_pull_bulk_3ctas": (rd.VARIANT_ZS, 0, 0, 3, rd.ATOM_BULK, rd.DIRECTION_PULL),
     "snac_tiny_chunks": (rd.VARIANT_STAGED, 256, 2, 3),
     "snac_default": (rd.VARIANT_STAGED, 0, 0, 0),
     "snac_deep": (rd.VARIANT_STAGED, 4096, 8, 5),
@@ -187,7 +189,7 @@ def test_all_gather_v(policy, dtype, R, explicit):
         assert outs[j].guards_intact()
 
 
-@pytest.mark.parametrize("policy", ["zs", "zs_bulk", "zs_copy_engine", "snac_tiny_chunks"])
+@pytest.mark.parametrize("policy", ["zs", "zs_bulk", "zs_copy_engine", "zs_pull", "snac_tiny_chunks"])
 def test_all_gather_in_place(policy):
     R, c, dtype = 8, 999, "bf16"
     h = handle(R)
@@ -201,7 +203,7 @@ def test_all_gather_in_place(policy):
         assert same_bits(host_bits(outs[j]), want[j])
 
 
-@pytest.mark.parametrize("policy", ["zs", "zs_bulk", "zs_copy_engine", "snac_tiny_chunks"])
+@pytest.mark.parametrize("policy", ["zs", "zs_bulk", "zs_copy_engine", "zs_pull", "snac_tiny_chunks"])
 def test_all_gather_bytes_at_odd_offsets(policy):
     """u8 payloads at odd byte offsets use narrow copy units."""
     R = 3
