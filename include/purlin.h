@@ -271,6 +271,16 @@ PURLIN_API purlin_status_t purlin_set_atom(purlin_handle_t h, int atom);
  * (a purlin_direction_t).  Other collectives ignore it. */
 PURLIN_API purlin_status_t purlin_set_direction(purlin_handle_t h, int direction);
 
+/* Launch shape of zero-staging kernels by message size.  A call whose
+ * large-message plan has fewer than `tiles` tiles runs one-warp CTAs with one
+ * access unit per thread instead of 256-thread CTAs, so that a message of a few
+ * KiB is spread over many SMs rather than queued in the load/store path of one
+ * (a tile: 256 threads x one 16/32-byte unit for sums, x four units for
+ * copies; the TMA bulk Atom always runs its own shape).  tiles = 0: never;
+ * tiles = -1: the library default (152, measured on GB300).  Other negative
+ * values: PURLIN_ERR_INVALID_ARG. */
+PURLIN_API purlin_status_t purlin_set_small_tiles(purlin_handle_t h, int tiles);
+
 /* Rank order of sums: PURLIN_ORDER_FIXED (default) or PURLIN_ORDER_TREE. */
 PURLIN_API purlin_status_t purlin_set_reduce_order(purlin_handle_t h, int order);
 

@@ -39,6 +39,8 @@ ORDER_FIXED, ORDER_TREE = 0, 1
 ATOM_AUTO, ATOM_VECTOR, ATOM_BULK, ATOM_COPY_ENGINE = 0, 1, 2, 3
 # purlin_direction_t
 DIRECTION_AUTO, DIRECTION_PUSH, DIRECTION_PULL = 0, 1, 2
+# purlin_set_small_tiles: library default / never
+SMALL_TILES_DEFAULT, SMALL_TILES_NEVER = -1, 0
 # purlin_collective_t
 COLL_REDUCE_SCATTER, COLL_ALL_GATHER, COLL_ALL_REDUCE, COLL_ALL_TO_ALL_V = range(4)
 MAX_RANKS = 8
@@ -47,7 +49,8 @@ MAX_RANKS = 8
 EXPORTED = (
     "purlin_create", "purlin_destroy", "purlin_reduce_scatter", "purlin_all_gather",
     "purlin_all_reduce", "purlin_all_to_all", "purlin_all_to_all_v", "purlin_set_policy",
-    "purlin_set_reduce_order", "purlin_set_atom", "purlin_set_direction", "purlin_set_timeout", "purlin_query_status",
+    "purlin_set_reduce_order", "purlin_set_atom", "purlin_set_direction", "purlin_set_small_tiles",
+    "purlin_set_timeout", "purlin_query_status",
     "purlin_last_launch", "purlin_status_string", "purlin_version", "purlin_plan_segments",
     "purlin_debug_inject", "purlin_all_reduce_noalloc",
 )
@@ -118,6 +121,7 @@ def lib():
             "purlin_set_reduce_order": [vp, i32],
             "purlin_set_atom": [vp, i32],
             "purlin_set_direction": [vp, i32],
+            "purlin_set_small_tiles": [vp, i32],
             "purlin_set_timeout": [vp, u64],
             "purlin_query_status": [vp],
             "purlin_last_launch": [vp, ctypes.POINTER(LaunchInfo)],
@@ -317,6 +321,10 @@ def purlin_set_atom(h, atom) -> None:
 
 def purlin_set_direction(h, direction) -> None:
     _check(lib().purlin_set_direction(h, int(direction)), "purlin_set_direction")
+
+
+def purlin_set_small_tiles(h, tiles) -> None:
+    _check(lib().purlin_set_small_tiles(h, int(tiles)), "purlin_set_small_tiles")
 
 
 def purlin_set_timeout(h, timeout_ns) -> None:

@@ -23,6 +23,10 @@
 
 using namespace purlin;
 
+// A zero-staging call whose large-message plan has fewer tiles than this runs
+// one-warp CTAs (measured on GB300 with an AllReduce of R = 8, bf16).
+constexpr long kSmallTilesDefault = 152;
+
 struct purlin_handle {
     int R = 0;
     int device = 0;
@@ -47,6 +51,7 @@ struct purlin_handle {
     int l2_coll_load[4] = {-1, -1, -1, -1};   // per-collective overrides (by Coll)
     int l2_coll_store[4] = {-1, -1, -1, -1};
     bool pdl = true;         // programmatic dependent launch of zero-staging kernels
+    long small_tiles = kSmallTilesDefault;  // below this many large tiles: one-warp CTAs
     int atom = PURLIN_ATOM_AUTO;
     int direction = PURLIN_DIRECTION_AUTO;
     int inject = 0;  // purlin_debug_inject, one staged call
@@ -146,7 +151,7 @@ purlin_status_t check_buffers(Coll coll, int R, const uint64_t* in, const uint64
 
 // Launch-wide knobs of the zero-staging kernels.
 struct ZsKnobs {
-    int unroll;
+    int tile_units;
     int max_unit_log2;
     uint32_t l2_load;
     uint32_t l2_store;
@@ -167,7 +172,8 @@ ZsKnobs zs_knobs(const purlin_handle* h, Coll coll)
 {
     ZsKnobs k;
     const bool reduce = coll == Coll::ReduceScatter || coll == Coll::AllReduce;
-    k.unroll = reduce ? kUnrollReduce : (h->atom == PURLIN_ATOM_BULK ? kUnrollBulk : kUnrollCopy);
+    k.tile_units = reduce ? kTileUnitsReduce
+                          : (h->atom == PURLIN_ATOM_BULK ? kTileUnitsBulk : kTileUnitsCopy);
     k.max_unit_log2 = h->max_unit_log2 ? h->max_unit_log2 : (coll == Coll::AllReduce ? 4 : 5);
     k.l2_load = h->l2_load >= 0 ? (uint32_t)h->l2_load : kL2EvictFirst;
     k.l2_store = h->l2_store >= 0 ? (uint32_t)h->l2_store
@@ -195,14 +201,36 @@ purlin_status_t make_params(ZsParams<MAXSEG>& p, const Piece* pieces, int npiece
         p.out[r] = reinterpret_cast<char*>(out[r]);
     }
     p.R = (uint32_t)R;
-    p.unroll = (uint32_t)k.unroll;
+    p.tile_units = (uint32_t)k.tile_units;
     uint32_t ntiles = 0;
-    int n = layout_segments(pieces, npieces, R, in, out, esz, reduce, (int)p.unroll,
+    int n = layout_segments(pieces, npieces, R, in, out, esz, reduce, k.tile_units,
                             max_unit_log2, p.seg, MAXSEG, &ntiles);
     if (n < 0) return PURLIN_ERR_UNSUPPORTED;
     p.nseg = (uint32_t)n;
     p.ntiles = ntiles;
     return PURLIN_OK;
+}
+
+// Small messages: when the large-message plan has fewer than h->small_tiles
+// tiles, the call runs one-warp CTAs over one-warp tiles instead, so that its
+// few KiB spread over many SMs rather than queue in the load/store path of a
+// few.  Returns true (and the re-planned params) if so.
+template <int MAXSEG>
+bool replan_small(const purlin_handle* h, ZsParams<MAXSEG>& p, const Piece* pieces, int npieces,
+                  int R, const uint64_t* in, const uint64_t* out, size_t esz, bool reduce,
+                  ZsKnobs& k)
+{
+    if ((long)p.ntiles >= h->small_tiles) return false;
+    ZsKnobs ks = k;
+    ks.tile_units = kTileUnitsSmall;
+    if (make_params(p, pieces, npieces, R, in, out, esz, reduce, ks, p.status) != PURLIN_OK) {
+        // cannot happen (same segments, more tiles of a smaller size fit in
+        // 32 bits only if the large plan did); keep the large plan
+        make_params(p, pieces, npieces, R, in, out, esz, reduce, k, p.status);
+        return false;
+    }
+    k = ks;
+    return true;
 }
 
 size_t algorithmic_bytes(Coll coll, int R, const size_t* counts, size_t count, size_t esz)
@@ -367,30 +395,36 @@ purlin_status_t run(purlin_handle_t h, Coll coll, const void* const in_[], void*
             if (grid > 0) ce = zs_copy_bulk_launch(p, false, grid, s);
             info.block = kBulkThreads;
         } else {
-            grid = zs_grid(h, p.ntiles, zs_copy_resident_ctas(true, false));
-            if (grid > 0) ce = zs_copy_launch(p, false, grid, s);
+            const bool small = replan_small(h, p, plan, nplan, R, in, out, esz, false, knobs);
+            grid = zs_grid(h, p.ntiles, zs_copy_resident_ctas(true, false, small));
+            if (grid > 0) ce = zs_copy_launch(p, false, small, grid, s);
+            if (small) info.block = kSmallThreads;
         }
         info.grid = grid;
         info.kernels = grid > 0;
-        info.chunk_bytes = tile_bytes(knobs.max_unit_log2, knobs.unroll);
+        info.chunk_bytes = tile_bytes(knobs.max_unit_log2, knobs.tile_units);
     } else {
         static thread_local ZsParams<kSegsSmall> p;
         st = make_params(p, pieces, np, R, in, out, esz, reduce, knobs, h->status);
         if (st != PURLIN_OK) return st;
         bool fan_all = coll == Coll::AllGather || coll == Coll::AllReduce;
         int grid;
-        if (reduce) {
-            grid = zs_grid(h, p.ntiles, zs_reduce_resident_ctas(dtype, h->order, fan_all));
-            if (grid > 0) ce = zs_reduce_launch(p, dtype, h->order, fan_all, grid, s);
-        } else if (bulk) {
+        if (bulk) {
             grid = zs_grid(h, p.ntiles, zs_copy_bulk_resident_ctas(false, fan_all));
             if (grid > 0) ce = zs_copy_bulk_launch(p, fan_all, grid, s);
             info.block = kBulkThreads;
         } else {
-            grid = zs_grid(h, p.ntiles, zs_copy_resident_ctas(false, fan_all));
-            if (grid > 0) ce = zs_copy_launch(p, fan_all, grid, s);
+            const bool small = replan_small(h, p, pieces, np, R, in, out, esz, reduce, knobs);
+            if (reduce) {
+                grid = zs_grid(h, p.ntiles, zs_reduce_resident_ctas(dtype, h->order, fan_all, small));
+                if (grid > 0) ce = zs_reduce_launch(p, dtype, h->order, fan_all, small, grid, s);
+            } else {
+                grid = zs_grid(h, p.ntiles, zs_copy_resident_ctas(false, fan_all, small));
+                if (grid > 0) ce = zs_copy_launch(p, fan_all, small, grid, s);
+            }
+            if (small) info.block = kSmallThreads;
         }
-        info.chunk_bytes = tile_bytes(knobs.max_unit_log2, knobs.unroll);
+        info.chunk_bytes = tile_bytes(knobs.max_unit_log2, knobs.tile_units);
         info.grid = grid;
         info.kernels = grid > 0;
     }
@@ -469,10 +503,11 @@ purlin_status_t purlin_create(purlin_handle_t* out, int R, size_t staging_bytes,
         }
     }
     if (const char* u = std::getenv("PURLIN_L2_STORE")) h->l2_store = std::atoi(u) % 3;
+    if (const char* u = std::getenv("PURLIN_SMALL_TILES")) h->small_tiles = std::atol(u);
     if (const char* u = std::getenv("PURLIN_MAX_UNIT")) {
-        int v = std::atoi(u);
-        if (v == 16) h->max_unit_log2 = 4;
-        if (v == 32) h->max_unit_log2 = 5;
+        const int v = std::atoi(u);
+        for (int l = 1; l <= 5; ++l)
+            if (v == (1 << l)) h->max_unit_log2 = l;
     }
     *out = h;
     return PURLIN_OK;
@@ -583,6 +618,13 @@ purlin_status_t purlin_set_timeout(purlin_handle_t h, uint64_t timeout_ns)
     return PURLIN_OK;
 }
 
+purlin_status_t purlin_set_small_tiles(purlin_handle_t h, int tiles)
+{
+    if (!h || tiles < -1) return PURLIN_ERR_INVALID_ARG;
+    h->small_tiles = tiles == -1 ? kSmallTilesDefault : tiles;
+    return PURLIN_OK;
+}
+
 purlin_status_t purlin_debug_inject(purlin_handle_t h, int what)
 {
     if (!h || what < 0 || what > 1) return PURLIN_ERR_INVALID_ARG;
@@ -638,7 +680,7 @@ purlin_status_t purlin_plan_segments(purlin_collective_t coll, int R, const uint
     Segment tmp[kSegsLarge];
     uint32_t nt = 0;
     int n = layout_segments(pieces, np, R, in_addr, out_addr, esz, reduce,
-                            reduce ? kUnrollReduce : kUnrollCopy, max_unit == 32 ? 5 : 4, tmp,
+                            reduce ? kTileUnitsReduce : kTileUnitsCopy, max_unit == 32 ? 5 : 4, tmp,
                             kSegsLarge, &nt);
     if (n < 0 || n > max_segs) return PURLIN_ERR_UNSUPPORTED;
     for (int i = 0; i < n; ++i) {

@@ -150,7 +150,7 @@ void layout_extents(Coll coll, int R, const size_t* counts, const size_t* da, co
 }
 
 int layout_segments(const Piece* pieces, int npieces, int R, const uint64_t* in_addr,
-                    const uint64_t* out_addr, size_t esz, bool reduce, int unroll,
+                    const uint64_t* out_addr, size_t esz, bool reduce, int tile_units,
                     int max_unit_log2, Segment* segs, int max_segs, uint32_t* ntiles)
 {
     int n = 0;
@@ -167,7 +167,7 @@ int layout_segments(const Piece* pieces, int npieces, int R, const uint64_t* in_
         s.dst = p.dst;
         s.unit_log2 = (uint8_t)ulog2;
         s.tile0 = (uint32_t)tiles;
-        uint64_t tb = tile_bytes(ulog2, unroll);
+        uint64_t tb = tile_bytes(ulog2, tile_units);
         tiles += (bytes + tb - 1) / tb;
         if (tiles > 0xffffffffull) return false;
         segs[n++] = s;

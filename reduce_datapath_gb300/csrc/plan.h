@@ -10,8 +10,8 @@
 // the same offset of every destination buffer.  Each segment is executed with
 // one access width ("unit"): a 16- or 32-byte vector for aligned bodies, or the
 // element / byte for unaligned heads and tails.  The launch's work is a flat
-// space of TILES (one tile = kThreads threads x unit x unroll); a segment owns
-// the tiles [tile0, tile0 + its tile count).
+// space of TILES (one tile = tile_units units: the threads of a CTA x units per
+// thread); a segment owns the tiles [tile0, tile0 + its tile count).
 #pragma once
 
 #include <cstddef>
@@ -32,6 +32,13 @@ constexpr int kSegsSmall = 24;         // RS / AG / AR: <= 3 segments per rank
 constexpr int kSegsLarge = 3 * kMaxRanks * kMaxRanks;  // A2AV: <= 3 per pair
 constexpr int kUnrollReduce = 1;       // units per thread per tile, sums
 constexpr int kUnrollCopy = 4;         // units per thread per tile, copies
+// Units per tile of the large-message launches (kThreads threads per CTA).
+constexpr int kTileUnitsReduce = kThreads * kUnrollReduce;
+constexpr int kTileUnitsCopy = kThreads * kUnrollCopy;
+// Small messages run one-warp CTAs with one unit per thread, so that a few KiB
+// spread over many SMs instead of queueing in one.
+constexpr int kSmallThreads = 32;
+constexpr int kTileUnitsSmall = kSmallThreads;
 
 struct Segment {
     uint64_t src_off;   // byte offset in the source buffer(s)
@@ -61,17 +68,18 @@ struct ZsParams {
     uint32_t R;
     uint32_t nseg;
     uint32_t ntiles;
-    uint32_t unroll;
+    uint32_t tile_units;  // units per tile
     Segment seg[MAXSEG];
 };
 
 // Tile length in bytes of a segment with this unit.
-PURLIN_HD inline uint64_t tile_bytes(int unit_log2, int unroll)
+PURLIN_HD inline uint64_t tile_bytes(int unit_log2, int tile_units)
 {
-    return (uint64_t)kThreads * ((uint64_t)1 << unit_log2) * (uint64_t)unroll;
+    return (uint64_t)tile_units << unit_log2;
 }
 
 constexpr int kUnrollBulk = 2;          // bulk-copy tiles: 256 x unit x 2 bytes (<= 16 KiB)
+constexpr int kTileUnitsBulk = kThreads * kUnrollBulk;
 constexpr int kBulkThreads = 32;        // one warp per bulk-copy CTA
 constexpr uint32_t kBulkStageBytes = 16 * 1024;
 
@@ -104,12 +112,12 @@ void layout_extents(Coll coll, int R, const size_t* counts, const size_t* da,
                     uint64_t in_extent[kMaxRanks], uint64_t out_extent[kMaxRanks]);
 
 // Split pieces into head / body / tail segments by the alignment of the actual
-// addresses, then number the tiles (kThreads x unit x unroll bytes each).  `reduce` selects element-wise heads and
-// tails (sums) or byte-wise ones (copies).  max_unit_log2 caps the vector width
+// addresses, then number the tiles (tile_units x unit bytes each).  `reduce`
+// selects element-wise heads and tails (sums) or byte-wise ones (copies).  max_unit_log2 caps the vector width
 // (4 = 16 B, 5 = 32 B).  Returns the segment count or -1 if max_segs is too
 // small; *ntiles receives the tile count.
 int layout_segments(const Piece* pieces, int npieces, int R, const uint64_t* in_addr,
-                    const uint64_t* out_addr, size_t elem_bytes, bool reduce, int unroll,
+                    const uint64_t* out_addr, size_t elem_bytes, bool reduce, int tile_units,
                     int max_unit_log2, Segment* segs, int max_segs, uint32_t* ntiles);
 
 }  // namespace purlin

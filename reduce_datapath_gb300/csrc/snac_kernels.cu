@@ -504,7 +504,7 @@ purlin_status_t run_with(SnacParams& p, const SnacRequest& rq, const SnacConfig&
     const bool reduce = rq.coll == Coll::ReduceScatter || rq.coll == Coll::AllReduce;
     uint32_t ntiles = 0;
     int nseg = layout_segments(rq.pieces, rq.npieces, rq.R, rq.in, rq.out, rq.esz, reduce,
-                               reduce ? kUnrollReduce : kUnrollCopy, snac_unit_log2(), p.seg,
+                               reduce ? kTileUnitsReduce : kTileUnitsCopy, snac_unit_log2(), p.seg,
                                kSegsLarge, &ntiles);
     if (nseg < 0) return PURLIN_ERR_UNSUPPORTED;
 

@@ -85,8 +85,10 @@ __device__ __forceinline__ void reduce_element(const ZsParams<kSegsSmall>& p, co
     }
 }
 
-template <typename T, int ORDER, bool FAN_ALL>
-__global__ void __launch_bounds__(kThreads, 2)
+// THREADS threads per CTA, one unit per thread per tile: kThreads for large
+// messages, one warp (kSmallThreads) for small ones.
+template <typename T, int ORDER, bool FAN_ALL, int THREADS>
+__global__ void __launch_bounds__(THREADS, THREADS == kThreads ? 2 : 16)
 zs_reduce_kernel(const __grid_constant__ ZsParams<kSegsSmall> p)
 {
     pdl_enter();
@@ -96,7 +98,7 @@ zs_reduce_kernel(const __grid_constant__ ZsParams<kSegsSmall> p)
     for (uint32_t t = blockIdx.x; t < p.ntiles; t += gridDim.x) {
         const Segment& s = segment_of(p, t);
         const int ul = s.unit_log2;
-        const uint64_t off = (uint64_t)(t - s.tile0) * tile_bytes(ul, kUnrollReduce) +
+        const uint64_t off = (uint64_t)(t - s.tile0) * tile_bytes(ul, THREADS) +
                              ((uint64_t)threadIdx.x << ul);
         if (off >= s.bytes) continue;
         if (ul == 5) reduce_vector<T, ORDER, FAN_ALL, 32>(p, s, off, R, lpol, spol);
@@ -125,23 +127,23 @@ __device__ __forceinline__ void store_hinted(char* p, const Unit<BYTES>& u, uint
     else store_unit<BYTES>(p, u);
 }
 
-// Atom::copy of one tile: kUnrollCopy units per thread, each warp access
+// Atom::copy of one tile: UNROLL units per thread, each warp access
 // contiguous; every unit loaded once and stored to one or all R outputs.
-template <int BYTES, bool FAN_ALL, int MAXSEG>
+template <int BYTES, bool FAN_ALL, int THREADS, int UNROLL, int MAXSEG>
 __device__ __forceinline__ void copy_tile(const ZsParams<MAXSEG>& p, const Segment& s,
                                           uint64_t base, uint64_t lpol, uint64_t spol)
 {
     const uint64_t rem = s.bytes - base;
     const char* src = p.in[s.src] + s.src_off + base;
-    Unit<BYTES> u[kUnrollCopy];
+    Unit<BYTES> u[UNROLL];
 #pragma unroll
-    for (int k = 0; k < kUnrollCopy; ++k) {
-        const uint64_t o = (uint64_t)(k * kThreads + threadIdx.x) * BYTES;
+    for (int k = 0; k < UNROLL; ++k) {
+        const uint64_t o = (uint64_t)(k * THREADS + threadIdx.x) * BYTES;
         if (o < rem) load_hinted<BYTES>(u[k], src + o, lpol);
     }
 #pragma unroll
-    for (int k = 0; k < kUnrollCopy; ++k) {
-        const uint64_t o = (uint64_t)(k * kThreads + threadIdx.x) * BYTES;
+    for (int k = 0; k < UNROLL; ++k) {
+        const uint64_t o = (uint64_t)(k * THREADS + threadIdx.x) * BYTES;
         if (o >= rem) continue;
         if (FAN_ALL) {
             for (int r = 0; r < (int)p.R; ++r) {
@@ -154,8 +156,10 @@ __device__ __forceinline__ void copy_tile(const ZsParams<MAXSEG>& p, const Segme
     }
 }
 
-template <bool FAN_ALL, int MAXSEG>
-__global__ void __launch_bounds__(kThreads, 2)
+// THREADS x UNROLL units per tile: kThreads x kUnrollCopy for large messages,
+// one warp with one unit per thread for small ones.
+template <bool FAN_ALL, int MAXSEG, int THREADS, int UNROLL>
+__global__ void __launch_bounds__(THREADS, THREADS == kThreads ? 2 : 16)
 zs_copy_kernel(const __grid_constant__ ZsParams<MAXSEG> p)
 {
     pdl_enter();
@@ -164,14 +168,14 @@ zs_copy_kernel(const __grid_constant__ ZsParams<MAXSEG> p)
     for (uint32_t t = blockIdx.x; t < p.ntiles; t += gridDim.x) {
         const Segment& s = segment_of(p, t);
         const int ul = s.unit_log2;
-        const uint64_t base = (uint64_t)(t - s.tile0) * tile_bytes(ul, kUnrollCopy);
+        const uint64_t base = (uint64_t)(t - s.tile0) * tile_bytes(ul, THREADS * UNROLL);
         switch (ul) {
-        case 5: copy_tile<32, FAN_ALL>(p, s, base, lpol, spol); break;
-        case 4: copy_tile<16, FAN_ALL>(p, s, base, lpol, spol); break;
-        case 3: copy_tile<8, FAN_ALL>(p, s, base, lpol, spol); break;
-        case 2: copy_tile<4, FAN_ALL>(p, s, base, lpol, spol); break;
-        case 1: copy_tile<2, FAN_ALL>(p, s, base, lpol, spol); break;
-        default: copy_tile<1, FAN_ALL>(p, s, base, lpol, spol); break;
+        case 5: copy_tile<32, FAN_ALL, THREADS, UNROLL>(p, s, base, lpol, spol); break;
+        case 4: copy_tile<16, FAN_ALL, THREADS, UNROLL>(p, s, base, lpol, spol); break;
+        case 3: copy_tile<8, FAN_ALL, THREADS, UNROLL>(p, s, base, lpol, spol); break;
+        case 2: copy_tile<4, FAN_ALL, THREADS, UNROLL>(p, s, base, lpol, spol); break;
+        case 1: copy_tile<2, FAN_ALL, THREADS, UNROLL>(p, s, base, lpol, spol); break;
+        default: copy_tile<1, FAN_ALL, THREADS, UNROLL>(p, s, base, lpol, spol); break;
         }
     }
 }
@@ -301,7 +305,7 @@ zs_copy_bulk_kernel(const __grid_constant__ ZsParams<MAXSEG> p)
             return t;
         };
         auto tile_len = [&](uint32_t t, const Segment& s, uint64_t& base) {
-            const uint64_t tb = tile_bytes(s.unit_log2, kUnrollBulk);
+            const uint64_t tb = tile_bytes(s.unit_log2, kTileUnitsBulk);
             base = (uint64_t)(t - s.tile0) * tb;
             return (uint32_t)min(tb, s.bytes - base);
         };
@@ -363,7 +367,7 @@ zs_copy_bulk_kernel(const __grid_constant__ ZsParams<MAXSEG> p)
     for (uint32_t t = blockIdx.x; t < p.ntiles; t += G) {
         const Segment& s = segment_of(p, t);
         if (s.unit_log2 >= 4) continue;
-        const uint64_t tb = tile_bytes(s.unit_log2, kUnrollBulk);
+        const uint64_t tb = tile_bytes(s.unit_log2, kTileUnitsBulk);
         const uint64_t base = (uint64_t)(t - s.tile0) * tb;
         const uint64_t len = min(tb, s.bytes - base);
         switch (s.unit_log2) {
@@ -378,14 +382,14 @@ zs_copy_bulk_kernel(const __grid_constant__ ZsParams<MAXSEG> p)
 // ------------------------------------------------------------- dispatch
 
 template <typename P>
-cudaError_t launch(void (*kernel)(P), const P& params, int grid, cudaStream_t stream)
+cudaError_t launch(void (*kernel)(P), const P& params, int grid, int threads, cudaStream_t stream)
 {
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = params.pdl ? 1 : 0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3((unsigned)threads);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
     cfg.attrs = attr;
@@ -395,22 +399,40 @@ cudaError_t launch(void (*kernel)(P), const P& params, int grid, cudaStream_t st
 
 using ReduceKernel = void (*)(ZsParams<kSegsSmall>);
 
-template <typename T>
+template <typename T, int THREADS>
 ReduceKernel pick_reduce(int order, bool fan_all)
 {
-    if (order == 0) return fan_all ? zs_reduce_kernel<T, 0, true> : zs_reduce_kernel<T, 0, false>;
-    return fan_all ? zs_reduce_kernel<T, 1, true> : zs_reduce_kernel<T, 1, false>;
+    if (order == 0)
+        return fan_all ? zs_reduce_kernel<T, 0, true, THREADS> : zs_reduce_kernel<T, 0, false, THREADS>;
+    return fan_all ? zs_reduce_kernel<T, 1, true, THREADS> : zs_reduce_kernel<T, 1, false, THREADS>;
 }
 
-ReduceKernel reduce_kernel_for(int dtype, int order, bool fan_all)
+template <int THREADS>
+ReduceKernel reduce_kernel_t(int dtype, int order, bool fan_all)
 {
-    if (dtype == kF32) return pick_reduce<atom::F32>(order, fan_all);
-    if (dtype == kBF16) return pick_reduce<atom::BF16>(order, fan_all);
-    return pick_reduce<atom::F16>(order, fan_all);
+    if (dtype == kF32) return pick_reduce<atom::F32, THREADS>(order, fan_all);
+    if (dtype == kBF16) return pick_reduce<atom::BF16, THREADS>(order, fan_all);
+    return pick_reduce<atom::F16, THREADS>(order, fan_all);
 }
 
-// Resident CTAs per SM of a kernel at kThreads threads (cached per device).
-int resident_ctas(const void* kernel)
+ReduceKernel reduce_kernel_for(int dtype, int order, bool fan_all, bool small)
+{
+    return small ? reduce_kernel_t<kSmallThreads>(dtype, order, fan_all)
+                 : reduce_kernel_t<kThreads>(dtype, order, fan_all);
+}
+
+template <int MAXSEG>
+void (*copy_kernel_for(bool fan_all, bool small))(ZsParams<MAXSEG>)
+{
+    if (small)
+        return fan_all ? zs_copy_kernel<true, MAXSEG, kSmallThreads, 1>
+                       : zs_copy_kernel<false, MAXSEG, kSmallThreads, 1>;
+    return fan_all ? zs_copy_kernel<true, MAXSEG, kThreads, kUnrollCopy>
+                   : zs_copy_kernel<false, MAXSEG, kThreads, kUnrollCopy>;
+}
+
+// Resident CTAs per SM of a kernel at `threads` threads (cached per device).
+int resident_ctas(const void* kernel, int threads)
 {
     static std::mutex mu;
     static std::unordered_map<uint64_t, int> cache;
@@ -421,7 +443,7 @@ int resident_ctas(const void* kernel)
     auto it = cache.find(key);
     if (it != cache.end()) return it->second;
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, kThreads, 0) != cudaSuccess || n < 1)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, 0) != cudaSuccess || n < 1)
         n = 1;
     cache[key] = n;
     return n;
@@ -430,28 +452,30 @@ int resident_ctas(const void* kernel)
 }  // namespace
 
 cudaError_t zs_reduce_launch(const ZsParams<kSegsSmall>& p, int dtype, int order, bool fan_all,
-                             int grid, cudaStream_t stream)
+                             bool small, int grid, cudaStream_t stream)
 {
-    return launch(reduce_kernel_for(dtype, order, fan_all), p, grid, stream);
+    return launch(reduce_kernel_for(dtype, order, fan_all, small), p, grid,
+                  small ? kSmallThreads : kThreads, stream);
 }
 
-int zs_reduce_resident_ctas(int dtype, int order, bool fan_all)
+int zs_reduce_resident_ctas(int dtype, int order, bool fan_all, bool small)
 {
-    return resident_ctas(reinterpret_cast<const void*>(reduce_kernel_for(dtype, order, fan_all)));
+    return resident_ctas(reinterpret_cast<const void*>(reduce_kernel_for(dtype, order, fan_all, small)),
+                         small ? kSmallThreads : kThreads);
 }
 
-cudaError_t zs_copy_launch(const ZsParams<kSegsSmall>& p, bool fan_all, int grid,
+cudaError_t zs_copy_launch(const ZsParams<kSegsSmall>& p, bool fan_all, bool small, int grid,
                            cudaStream_t stream)
 {
-    return launch(fan_all ? zs_copy_kernel<true, kSegsSmall> : zs_copy_kernel<false, kSegsSmall>,
-                  p, grid, stream);
+    return launch(copy_kernel_for<kSegsSmall>(fan_all, small), p, grid,
+                  small ? kSmallThreads : kThreads, stream);
 }
 
-cudaError_t zs_copy_launch(const ZsParams<kSegsLarge>& p, bool fan_all, int grid,
+cudaError_t zs_copy_launch(const ZsParams<kSegsLarge>& p, bool fan_all, bool small, int grid,
                            cudaStream_t stream)
 {
-    return launch(fan_all ? zs_copy_kernel<true, kSegsLarge> : zs_copy_kernel<false, kSegsLarge>,
-                  p, grid, stream);
+    return launch(copy_kernel_for<kSegsLarge>(fan_all, small), p, grid,
+                  small ? kSmallThreads : kThreads, stream);
 }
 
 namespace {
@@ -529,16 +553,11 @@ int zs_copy_bulk_resident_ctas(bool large, bool fan_all)
     return e == cudaSuccess ? n : 1;
 }
 
-int zs_copy_resident_ctas(bool large, bool fan_all)
+int zs_copy_resident_ctas(bool large, bool fan_all, bool small)
 {
-    const void* k;
-    if (large)
-        k = reinterpret_cast<const void*>(fan_all ? zs_copy_kernel<true, kSegsLarge>
-                                                  : zs_copy_kernel<false, kSegsLarge>);
-    else
-        k = reinterpret_cast<const void*>(fan_all ? zs_copy_kernel<true, kSegsSmall>
-                                                  : zs_copy_kernel<false, kSegsSmall>);
-    return resident_ctas(k);
+    const void* k = large ? reinterpret_cast<const void*>(copy_kernel_for<kSegsLarge>(fan_all, small))
+                          : reinterpret_cast<const void*>(copy_kernel_for<kSegsSmall>(fan_all, small));
+    return resident_ctas(k, small ? kSmallThreads : kThreads);
 }
 
 }  // namespace purlin

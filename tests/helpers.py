@@ -69,10 +69,12 @@ def handle(R):
     return _handles[R]
 
 
-def set_variant(h, variant, chunk=0, depth=0, ctas=0, atom=0, direction=0):
+def set_variant(h, variant, chunk=0, depth=0, ctas=0, atom=0, direction=0,
+                small_tiles=rd.SMALL_TILES_DEFAULT):
     rd.purlin_set_policy(h, chunk, depth, ctas, variant)
     rd.purlin_set_atom(h, atom)
     rd.purlin_set_direction(h, direction)
+    rd.purlin_set_small_tiles(h, small_tiles)
 
 
 def close_handles():

@@ -3,7 +3,8 @@
 Each case draws a collective, R, a dtype, per-rank counts (zeros included), an
 element offset for every buffer (unaligned heads and tails), optional explicit
 displacements, a datapath (zero staging with one of three copy Atoms, or SNAC
-with a random chunk, depth and channel count) and, for sums, the rank order.
+with a random chunk, depth and channel count), the launch shape (one-warp or
+256-thread CTAs) and, for sums, the rank order.
 The outputs must equal the oracle's bit for bit and the canary guards around
 every output must survive.
 """
@@ -45,6 +46,8 @@ def _policy(rng, h, copy):
         rd.purlin_set_atom(h, int(rng.choice([rd.ATOM_VECTOR, rd.ATOM_BULK, rd.ATOM_COPY_ENGINE]))
                            if copy else rd.ATOM_AUTO)
         rd.purlin_set_direction(h, int(rng.choice([rd.DIRECTION_PUSH, rd.DIRECTION_PULL])))
+        rd.purlin_set_small_tiles(h, int(rng.choice([rd.SMALL_TILES_NEVER, rd.SMALL_TILES_DEFAULT,
+                                                     1 << 30])))
     else:
         chunk = int(rng.choice([256, 512, 4096, 16384, 65536]))
         rd.purlin_set_policy(h, chunk, int(rng.integers(1, 9)), int(rng.choice([0, 1, 2, 5])),
@@ -117,4 +120,5 @@ def test_random_layout(seed):
         rd.purlin_set_reduce_order(h, rd.ORDER_FIXED)
         rd.purlin_set_atom(h, rd.ATOM_AUTO)
         rd.purlin_set_direction(h, rd.DIRECTION_AUTO)
+        rd.purlin_set_small_tiles(h, rd.SMALL_TILES_DEFAULT)
         rd.purlin_set_policy(h, 0, 0, 0, rd.VARIANT_AUTO)

@@ -21,6 +21,12 @@ pytestmark = pytest.mark.gpu
 POLICIES = {
     "zs": (rd.VARIANT_ZS, 0, 0, 0),
     "zs_3ctas": (rd.VARIANT_ZS, 0, 0, 3),
+    # 256-thread CTAs at every size (small messages otherwise run one-warp CTAs)
+    "zs_large": (rd.VARIANT_ZS, 0, 0, 0, rd.ATOM_AUTO, rd.DIRECTION_AUTO, rd.SMALL_TILES_NEVER),
+    "zs_large_3ctas": (rd.VARIANT_ZS, 0, 0, 3, rd.ATOM_AUTO, rd.DIRECTION_AUTO,
+                       rd.SMALL_TILES_NEVER),
+    # one-warp CTAs at every size
+    "zs_small": (rd.VARIANT_ZS, 0, 0, 0, rd.ATOM_AUTO, rd.DIRECTION_AUTO, 1 << 30),
     "zs_bulk": (rd.VARIANT_ZS, 0, 0, 0, rd.ATOM_BULK),
     "zs_bulk_3ctas": (rd.VARIANT_ZS, 0, 0, 3, rd.ATOM_BULK),
     "zs_copy_engine": (rd.VARIANT_ZS, 0, 0, 0, rd.ATOM_COPY_ENGINE),
@@ -69,7 +75,7 @@ def test_all_reduce(policy, dtype, R, n):
         assert outs[j].guards_intact()
 
 
-@pytest.mark.parametrize("policy", ["zs", "snac_tiny_chunks"])
+@pytest.mark.parametrize("policy", ["zs", "zs_large", "snac_tiny_chunks"])
 @pytest.mark.parametrize("offset", [1, 3, 8])
 def test_all_reduce_unaligned_streams(policy, offset):
     """Streams starting at different offsets force element-wise segments."""
@@ -86,7 +92,7 @@ def test_all_reduce_unaligned_streams(policy, offset):
         assert outs[j].guards_intact()
 
 
-@pytest.mark.parametrize("policy", ["zs", "snac_tiny_chunks"])
+@pytest.mark.parametrize("policy", ["zs", "zs_large", "snac_tiny_chunks"])
 def test_all_reduce_in_place(policy):
     R, n, dtype = 8, 12345, "f32"
     h = handle(R)
@@ -133,7 +139,7 @@ def test_reduce_scatter_v(policy, dtype, R, explicit):
         assert outs[k].guards_intact()
 
 
-@pytest.mark.parametrize("policy", ["zs", "snac_tiny_chunks"])
+@pytest.mark.parametrize("policy", ["zs", "zs_large", "snac_tiny_chunks"])
 def test_reduce_scatter_in_place(policy):
     R, c, dtype = 8, 1001, "bf16"
     h = handle(R)
@@ -147,7 +153,7 @@ def test_reduce_scatter_in_place(policy):
         assert same_bits(host_bits(outs[k]), want[k])
 
 
-@pytest.mark.parametrize("policy", ["zs", "snac_tiny_chunks"])
+@pytest.mark.parametrize("policy", ["zs", "zs_large", "snac_tiny_chunks"])
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_reduce_scatter_unaligned_partitions(policy, dtype):
     """Partitions at odd element offsets: heads and tails are element-wise."""
@@ -189,7 +195,7 @@ def test_all_gather_v(policy, dtype, R, explicit):
         assert outs[j].guards_intact()
 
 
-@pytest.mark.parametrize("policy", ["zs", "zs_bulk", "zs_copy_engine", "zs_pull", "snac_tiny_chunks"])
+@pytest.mark.parametrize("policy", ["zs", "zs_large", "zs_bulk", "zs_copy_engine", "zs_pull", "snac_tiny_chunks"])
 def test_all_gather_in_place(policy):
     R, c, dtype = 8, 999, "bf16"
     h = handle(R)
@@ -203,7 +209,7 @@ def test_all_gather_in_place(policy):
         assert same_bits(host_bits(outs[j]), want[j])
 
 
-@pytest.mark.parametrize("policy", ["zs", "zs_bulk", "zs_copy_engine", "zs_pull", "snac_tiny_chunks"])
+@pytest.mark.parametrize("policy", ["zs", "zs_large", "zs_bulk", "zs_copy_engine", "zs_pull", "snac_tiny_chunks"])
 def test_all_gather_bytes_at_odd_offsets(policy):
     """u8 payloads at odd byte offsets use narrow copy units."""
     R = 3
@@ -255,7 +261,7 @@ def test_all_to_all_v(policy, dtype, R, explicit):
         assert outs[j].guards_intact()
 
 
-@pytest.mark.parametrize("policy", ["zs", "zs_bulk", "zs_copy_engine", "snac_tiny_chunks"])
+@pytest.mark.parametrize("policy", ["zs", "zs_large", "zs_bulk", "zs_copy_engine", "snac_tiny_chunks"])
 def test_all_to_all_fixed_twice_is_identity(policy):
     R, c, dtype = 8, 3001, "bf16"
     h = handle(R)
@@ -280,7 +286,7 @@ def _as_f64(bits, dtype):
     return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).double().numpy()
 
 
-@pytest.mark.parametrize("policy", ["zs", "snac_tiny_chunks"])
+@pytest.mark.parametrize("policy", ["zs", "zs_large", "snac_tiny_chunks"])
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 @pytest.mark.parametrize("R", [3, 8])
 def test_tree_order(policy, dtype, R):
