@@ -739,13 +739,16 @@ def allreduce_sweep(rd, torch, dev, stream, peak):
     """AllReduce R=8 bf16 at 4 KiB..256 MiB per rank: zero staging and SNAC."""
     import workloads
     h = rd.purlin_create(R, 0, dev.index)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     out = []
     try:
         for nbytes in workloads.SWEEP_BYTES:
             n = nbytes // 2
             x = [torch.randn(n, device=dev).to(torch.bfloat16) for _ in range(R)]
             o = [torch.empty_like(t) for t in x]
-            row = {"bytes_per_rank": nbytes}
+            # inputs + outputs that fit in L2 stay there across repeated launches,
+            # so their GB/s is not an HBM figure (it can exceed the HBM peak)
+            row = {"bytes_per_rank": nbytes, "fits_in_l2": 2 * R * nbytes <= l2}
             for name, variant in (("zs", rd.VARIANT_ZS), ("snac", rd.VARIANT_STAGED)):
                 rd.purlin_set_policy(h, 0, 0, 0, variant)
                 fn = lambda: rd.purlin_all_reduce(h, x, o, n, "bf16", stream=stream)
