@@ -557,45 +557,37 @@ def cta_study(rd, torch, h, rs, ag, stream, coll_b, peak):
     """Bandwidth of the AllGather (copy) and ReduceScatter (sum) of the step as
     a function of the CTAs launched, for the vector and TMA-bulk Atoms, plus the
     AllGather on the copy engines (no kernel).  Concurrent SM use is bounded by
-    min(CTAs launched, SMs)."""
+    min(CTAs launched, SMs); beyond the resident CTAs (2 per SM for the vector
+    kernels, 1 for the bulk one) extra CTAs queue and are handed to SMs as they
+    drain.  ctas 0 = the library's default grid (reported in `grid`)."""
     rows = []
+
+    def row(coll, fn, atom_name, ctas, **extra):
+        rd.purlin_set_policy(h, 0, 0, ctas, rd.VARIANT_ZS)
+        fn()
+        us = _events_us(torch, stream, fn, 10)
+        rows.append({"collective": coll, "atom": atom_name, **extra, "ctas": ctas,
+                     "grid": rd.purlin_last_launch(h)["grid"], "us": round(us, 1),
+                     "gbs": round(coll_b / (us / 1e6) / 1e9, 1),
+                     "frac_of_peak": round(coll_b / (us / 1e6) / 1e9 / peak, 3)})
+
     try:
-        for atom_name, atom, ctas_list in (("vector", rd.ATOM_VECTOR, (8, 16, 38, 76, 152, 304)),
-                                           ("bulk", rd.ATOM_BULK, (8, 16, 38, 76, 152))):
+        for atom_name, atom, ctas_list in (
+                ("vector", rd.ATOM_VECTOR, (8, 16, 38, 76, 152, 304, 608, 1216, 0)),
+                ("bulk", rd.ATOM_BULK, (8, 16, 38, 76, 152, 608, 0))):
             rd.purlin_set_atom(h, atom)
             for ctas in ctas_list:
-                rd.purlin_set_policy(h, 0, 0, ctas, rd.VARIANT_ZS)
-                ag()
-                us = _events_us(torch, stream, ag, 10)
-                rows.append({"collective": "all_gather", "atom": atom_name, "ctas": ctas,
-                             "us": round(us, 1), "gbs": round(coll_b / (us / 1e6) / 1e9, 1),
-                             "frac_of_peak": round(coll_b / (us / 1e6) / 1e9 / peak, 3)})
+                row("all_gather", ag, atom_name, ctas)
         rd.purlin_set_atom(h, rd.ATOM_VECTOR)
-        for ctas in (8, 16, 38, 76, 152, 304):
-            rd.purlin_set_policy(h, 0, 0, ctas, rd.VARIANT_ZS)
-            rs()
-            us = _events_us(torch, stream, rs, 10)
-            rows.append({"collective": "reduce_scatter", "atom": "vector", "ctas": ctas,
-                         "us": round(us, 1), "gbs": round(coll_b / (us / 1e6) / 1e9, 1),
-                         "frac_of_peak": round(coll_b / (us / 1e6) / 1e9 / peak, 3)})
+        for ctas in (8, 16, 38, 76, 152, 304, 1216, 0):
+            row("reduce_scatter", rs, "vector", ctas)
         rd.purlin_set_atom(h, rd.ATOM_VECTOR)
         rd.purlin_set_direction(h, rd.DIRECTION_PULL)
-        for ctas in (152, 304):
-            rd.purlin_set_policy(h, 0, 0, ctas, rd.VARIANT_ZS)
-            ag()
-            us = _events_us(torch, stream, ag, 10)
-            rows.append({"collective": "all_gather", "atom": "vector", "direction": "pull",
-                         "ctas": ctas, "us": round(us, 1),
-                         "gbs": round(coll_b / (us / 1e6) / 1e9, 1),
-                         "frac_of_peak": round(coll_b / (us / 1e6) / 1e9 / peak, 3)})
+        for ctas in (152, 304, 0):
+            row("all_gather", ag, "vector", ctas, direction="pull")
         rd.purlin_set_direction(h, rd.DIRECTION_AUTO)
-        rd.purlin_set_policy(h, 0, 0, 0, rd.VARIANT_ZS)
         rd.purlin_set_atom(h, rd.ATOM_COPY_ENGINE)
-        ag()
-        us = _events_us(torch, stream, ag, 10)
-        rows.append({"collective": "all_gather", "atom": "copy_engine", "ctas": 0,
-                     "us": round(us, 1), "gbs": round(coll_b / (us / 1e6) / 1e9, 1),
-                     "frac_of_peak": round(coll_b / (us / 1e6) / 1e9 / peak, 3)})
+        row("all_gather", ag, "copy_engine", 0)
         if rd.purlin_query_status(h) != rd.OK:
             raise RuntimeError("cta study: device status not ok")
     finally:

@@ -258,7 +258,8 @@ PURLIN_API purlin_status_t purlin_all_reduce_noalloc(const void* const in[], voi
 /* Codesign policy (Figure 1; chunk sizing after Table 3's bandwidth-delay
  * products; depth after Figure 11).  0 for any argument keeps the automatic
  * choice.  chunk_bytes: SNAC chunk, 16..(staging ring / (R * depth)), a multiple
- * of 16.  depth: ring slots per channel, 1..8.  ctas: CTAs per launch (ZS) or
+ * of 16.  depth: ring slots per channel, 1..8.  ctas: CTAs per launch (ZS;
+ * automatic: 16 per resident CTA slot of the device, at most one per tile) or
  * SNAC channels.  variant: a purlin_variant_t. */
 PURLIN_API purlin_status_t purlin_set_policy(purlin_handle_t h, size_t chunk_bytes, int depth,
                                   int ctas, int variant);
