@@ -61,6 +61,8 @@ def parse_args():
                     help="time one collective alone (profiling runs); prints a short line")
     ap.add_argument("--bytes-per-rank", type=int, default=BYTES_PER_RANK,
                     help="with --only: input bytes per rank")
+    ap.add_argument("--atom", choices=["auto", "vector", "bulk", "copy_engine"], default="auto",
+                    help="with --only: copy Atom of the zero-staging path")
     return ap.parse_args()
 
 
@@ -902,6 +904,8 @@ def bench_only(args):
     h = rd.purlin_create(R, args.staging, 0)
     variant = rd.VARIANT_ZS if args.variant == "zs" else rd.VARIANT_STAGED
     rd.purlin_set_policy(h, args.chunk, args.depth, args.ctas, variant)
+    rd.purlin_set_atom(h, {"auto": rd.ATOM_AUTO, "vector": rd.ATOM_VECTOR, "bulk": rd.ATOM_BULK,
+                           "copy_engine": rd.ATOM_COPY_ENGINE}[args.atom])
     stream = torch.cuda.Stream(device=dev)
     if args.only == "rs":
         x = workloads.rank_buffers(WORKLOAD, R, n, "bf16", device=dev)
