@@ -278,8 +278,9 @@ PURLIN_API purlin_status_t purlin_set_direction(purlin_handle_t h, int direction
  * KiB is spread over many SMs rather than queued in the load/store path of one
  * (a tile: 256 threads x one 16/32-byte unit for sums, x four units for
  * copies; the TMA bulk Atom always runs its own shape).  tiles = 0: never;
- * tiles = -1: the library default (152, measured on GB300).  Other negative
- * values: PURLIN_ERR_INVALID_ARG. */
+ * tiles = -1: the library default, per collective (measured on GB300: 256 for
+ * AllReduce, 64 for the others).  Other negative values:
+ * PURLIN_ERR_INVALID_ARG. */
 PURLIN_API purlin_status_t purlin_set_small_tiles(purlin_handle_t h, int tiles);
 
 /* Rank order of sums: PURLIN_ORDER_FIXED (default) or PURLIN_ORDER_TREE. */

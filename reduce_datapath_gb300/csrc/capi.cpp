@@ -24,8 +24,12 @@
 using namespace purlin;
 
 // A zero-staging call whose large-message plan has fewer tiles than this runs
-// one-warp CTAs (measured on GB300 with an AllReduce of R = 8, bf16).
-constexpr long kSmallTilesDefault = 152;
+// one-warp CTAs.  Measured on GB300, R = 8, bf16, per launch in a CUDA graph
+// (256-thread vs one-warp CTAs): AllReduce 1 MiB per rank (128 large tiles)
+// 3.28 vs 3.02 us, 4 MiB (512) 8.05 vs 8.81 us; ReduceScatter 256 KiB (32)
+// 1.93 vs 1.64 us, 1 MiB (128) 2.09 vs 2.32 us; AllGather 1 MiB out per rank
+// (32) 5.42 vs 3.17 us, 4 MiB (128) 6.26 vs 6.37 us.
+static long small_tiles_default(Coll coll) { return coll == Coll::AllReduce ? 256 : 64; }
 
 struct purlin_handle {
     int R = 0;
@@ -45,13 +49,13 @@ struct purlin_handle {
     int variant = PURLIN_VARIANT_AUTO;
     int order = PURLIN_ORDER_FIXED;
     uint64_t timeout_ns = 1000000000ull;
-    int max_unit_log2 = 0;   // 0: per collective (AllReduce 4 = 16 B, else 5 = 32 B)
+    int max_unit_log2 = 0;   // 0: automatic (32 B; 16 B for small sums)
     int l2_load = -1;        // -1: per collective; else kL2Normal/EvictFirst/EvictLast
     int l2_store = -1;
     int l2_coll_load[4] = {-1, -1, -1, -1};   // per-collective overrides (by Coll)
     int l2_coll_store[4] = {-1, -1, -1, -1};
     bool pdl = true;         // programmatic dependent launch of zero-staging kernels
-    long small_tiles = kSmallTilesDefault;  // below this many large tiles: one-warp CTAs
+    long small_tiles = -1;   // below this many large tiles: one-warp CTAs (-1: per collective)
     int atom = PURLIN_ATOM_AUTO;
     int direction = PURLIN_DIRECTION_AUTO;
     int inject = 0;  // purlin_debug_inject, one staged call
@@ -159,9 +163,9 @@ struct ZsKnobs {
 };
 
 // Measured on GB300 (64 MiB per rank, R = 8, bf16):
-//  - the fused AllReduce (R loads and R stores per unit) runs best with 16-byte
-//    units (170 vs 174 us), everything else with 32-byte units (ReduceScatter
-//    91 vs 96 us);
+//  - with the 16-wave grid every collective runs best with 32-byte units
+//    (AllReduce 154.8 vs 157.1 us, ReduceScatter 90.1 vs 97.4 us); small sums
+//    use 16-byte units (replan_small), which doubles their CTAs;
 //  - every source is read exactly once, so loads are evict-first; outputs are
 //    written evict-first except the ReduceScatter's, which a following
 //    collective (the AllGather of a ReduceScatter -> AllGather pair) reads
@@ -174,7 +178,7 @@ ZsKnobs zs_knobs(const purlin_handle* h, Coll coll)
     const bool reduce = coll == Coll::ReduceScatter || coll == Coll::AllReduce;
     k.tile_units = reduce ? kTileUnitsReduce
                           : (h->atom == PURLIN_ATOM_BULK ? kTileUnitsBulk : kTileUnitsCopy);
-    k.max_unit_log2 = h->max_unit_log2 ? h->max_unit_log2 : (coll == Coll::AllReduce ? 4 : 5);
+    k.max_unit_log2 = h->max_unit_log2 ? h->max_unit_log2 : 5;
     k.l2_load = h->l2_load >= 0 ? (uint32_t)h->l2_load : kL2EvictFirst;
     k.l2_store = h->l2_store >= 0 ? (uint32_t)h->l2_store
                                   : (coll == Coll::ReduceScatter ? kL2Normal : kL2EvictFirst);
@@ -216,13 +220,15 @@ purlin_status_t make_params(ZsParams<MAXSEG>& p, const Piece* pieces, int npiece
 // few KiB spread over many SMs rather than queue in the load/store path of a
 // few.  Returns true (and the re-planned params) if so.
 template <int MAXSEG>
-bool replan_small(const purlin_handle* h, ZsParams<MAXSEG>& p, const Piece* pieces, int npieces,
-                  int R, const uint64_t* in, const uint64_t* out, size_t esz, bool reduce,
-                  ZsKnobs& k)
+bool replan_small(const purlin_handle* h, Coll coll, ZsParams<MAXSEG>& p, const Piece* pieces,
+                  int npieces, int R, const uint64_t* in, const uint64_t* out, size_t esz,
+                  bool reduce, ZsKnobs& k)
 {
-    if ((long)p.ntiles >= h->small_tiles) return false;
+    const long threshold = h->small_tiles >= 0 ? h->small_tiles : small_tiles_default(coll);
+    if ((long)p.ntiles >= threshold) return false;
     ZsKnobs ks = k;
     ks.tile_units = kTileUnitsSmall;
+    if (reduce && !h->max_unit_log2) ks.max_unit_log2 = std::min(ks.max_unit_log2, 4);
     if (make_params(p, pieces, npieces, R, in, out, esz, reduce, ks, p.status) != PURLIN_OK) {
         // cannot happen (same segments, more tiles of a smaller size fit in
         // 32 bits only if the large plan did); keep the large plan
@@ -406,7 +412,7 @@ purlin_status_t run(purlin_handle_t h, Coll coll, const void* const in_[], void*
             if (grid > 0) ce = zs_copy_bulk_launch(p, false, grid, s);
             info.block = kBulkThreads;
         } else {
-            const bool small = replan_small(h, p, plan, nplan, R, in, out, esz, false, knobs);
+            const bool small = replan_small(h, coll, p, plan, nplan, R, in, out, esz, false, knobs);
             grid = zs_grid(h, p.ntiles, zs_copy_resident_ctas(true, false, small));
             if (grid > 0) ce = zs_copy_launch(p, false, small, grid, s);
             if (small) info.block = kSmallThreads;
@@ -425,7 +431,7 @@ purlin_status_t run(purlin_handle_t h, Coll coll, const void* const in_[], void*
             if (grid > 0) ce = zs_copy_bulk_launch(p, fan_all, grid, s);
             info.block = kBulkThreads;
         } else {
-            const bool small = replan_small(h, p, pieces, np, R, in, out, esz, reduce, knobs);
+            const bool small = replan_small(h, coll, p, pieces, np, R, in, out, esz, reduce, knobs);
             if (reduce) {
                 grid = zs_grid(h, p.ntiles, zs_reduce_resident_ctas(dtype, h->order, fan_all, small));
                 if (grid > 0) ce = zs_reduce_launch(p, dtype, h->order, fan_all, small, grid, s);
@@ -632,7 +638,7 @@ purlin_status_t purlin_set_timeout(purlin_handle_t h, uint64_t timeout_ns)
 purlin_status_t purlin_set_small_tiles(purlin_handle_t h, int tiles)
 {
     if (!h || tiles < -1) return PURLIN_ERR_INVALID_ARG;
-    h->small_tiles = tiles == -1 ? kSmallTilesDefault : tiles;
+    h->small_tiles = tiles;
     return PURLIN_OK;
 }
 
