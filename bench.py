@@ -260,6 +260,45 @@ def run_cpu_oracle(xh, budget_s, max_reps=20):
             "seconds": el}, y, z
 
 
+def run_cpu_oracle_threads(xh, budget_s, max_reps=20):
+    """The same oracle calls split by output partition over the host's cores:
+    thread k sums partition k (ReduceScatter restricted to one partition), then
+    thread j builds output j (the AllGather's block placement for one
+    destination, through the oracle's AllToAllV with only column j non-zero).
+    Each element's rank order is unchanged, so the results are bit-identical to
+    the single-threaded step; the oracle's own code is not changed.  ctypes
+    releases the interpreter lock during each C call."""
+    import numpy as np
+    from concurrent.futures import ThreadPoolExecutor
+    import oracle
+    threads = min(R, os.cpu_count() or 1)
+
+    def rs_part(k):
+        counts = [0] * R
+        counts[k] = PART
+        return oracle.reduce_scatter(xh, counts, [k * PART] * R, dtype="bf16")[k]
+
+    def ag_dest(j, y):
+        C = np.zeros((R, R), dtype=np.uint64)
+        C[:, j] = PART
+        return oracle.all_to_all_v(y, C)[j]
+
+    reps, t0 = 0, time.perf_counter()
+    with ThreadPoolExecutor(max_workers=threads) as pool:
+        while True:
+            y = list(pool.map(rs_part, range(R)))
+            z = list(pool.map(lambda j: ag_dest(j, y), range(R)))
+            reps += 1
+            el = time.perf_counter() - t0
+            if el >= budget_s or reps >= max_reps:
+                break
+    rs, ag = step_bytes()
+    return {"value": reps * (rs + ag) / el / 1e9, "unit": UNIT, "cores": threads,
+            "kind": "oracle, split by output partition",
+            "sample": f"{reps} full step(s) of the workload in {el:.1f} s, {threads} threads, "
+                      f"{cpu_model()}"}, y, z
+
+
 def bench_reference(args):
     """The reference arm: the CPU oracle timed on the host cores."""
     world, rank, local = dist_setup(args)
@@ -454,6 +493,7 @@ def bench_purlin(args):
 
     # ---- CPU oracle baseline and a bit-exact check of this run's result
     cpu = None
+    cpu_threads = None
     parity = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         xh = [host_bits(t) for t in x]
@@ -464,6 +504,10 @@ def bench_purlin(args):
         torch.cuda.synchronize()
         parity = all(np.array_equal(host_bits(y[k]), want_y[k]) for k in range(R)) and \
             all(np.array_equal(host_bits(z[k]), want_z[k]) for k in range(R))
+        cpu_threads, ty, tz = run_cpu_oracle_threads(xh, args.cpu_seconds / 2)
+        cpu_threads["bit_identical_to_single_thread"] = bool(
+            all(np.array_equal(ty[k], want_y[k]) for k in range(R)) and
+            all(np.array_equal(tz[k], want_z[k]) for k in range(R)))
 
     rd.purlin_destroy(h)
     if rank != 0:
@@ -488,6 +532,7 @@ def bench_purlin(args):
         "allreduce_sweep": sweep,
         "e2e": e2e,
         "cpu_baseline": cpu,
+        "cpu_baseline_threads": cpu_threads,
         "parity_vs_oracle": parity,
         "gpu_launches": launches,
         "clocks": clocks.summary(),
@@ -521,6 +566,23 @@ def _graph_us(torch, stream, fn, per_graph=50, replays=4):
         b.record(stream)
     torch.cuda.synchronize()
     return a.elapsed_time(b) * 1e3 / (per_graph * replays)
+
+
+def _cold_l2_us(torch, stream, fn, flush, reps=20):
+    """Median device time of one call right after a write of twice the L2
+    size, so that its buffers come from HBM."""
+    ts = []
+    with torch.cuda.stream(stream):
+        for _ in range(reps):
+            flush.fill_(1.0)
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            b.synchronize()
+            ts.append(a.elapsed_time(b) * 1e3)
+    return statistics.median(ts)
 
 
 def _events_us(torch, stream, fn, iters):
@@ -734,6 +796,7 @@ def allreduce_sweep(rd, torch, dev, stream, peak):
     import workloads
     h = rd.purlin_create(R, 0, dev.index)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2 // 4 + 1, dtype=torch.float32, device=dev)
     out = []
     try:
         for nbytes in workloads.SWEEP_BYTES:
@@ -760,6 +823,14 @@ def allreduce_sweep(rd, torch, dev, stream, peak):
                              "frac_of_peak": round(gbs / peak, 3),
                              "timing": "cuda graph" if graph_us is not None else "events",
                              "us_host_launched": round(host_us, 2)}
+            if row["fits_in_l2"]:
+                # after both warm timings: the flush leaves L2 full of dirty lines
+                for name, variant in (("zs", rd.VARIANT_ZS), ("snac", rd.VARIANT_STAGED)):
+                    rd.purlin_set_policy(h, 0, 0, 0, variant)
+                    fn = lambda: rd.purlin_all_reduce(h, x, o, n, "bf16", stream=stream)
+                    cold = _cold_l2_us(torch, stream, fn, flush)
+                    row[name]["us_cold_l2"] = round(cold, 2)
+                    row[name]["gbs_cold_l2"] = round(2 * R * nbytes / (cold / 1e6) / 1e9, 1)
             out.append(row)
             del x, o
         if rd.purlin_query_status(h) != rd.OK:

@@ -3,7 +3,8 @@
 With N ranks every rank runs an independent replica; the job's value is all
 ranks' bytes over the slowest rank's time.  Two CPU processes (world size 2,
 gloo, 127.0.0.1) check the max-over-ranks reduction and the whole-job value,
-and the reference arm does no work on ranks other than 0.
+and the reference arm does no work on ranks other than 0.  The CPU baseline's
+partition-split timing must give the single-threaded oracle's bits.
 """
 import io
 import os
@@ -72,3 +73,19 @@ def _args(bench):
         return bench.parse_args()
     finally:
         sys.argv = argv
+
+
+def test_threaded_oracle_baseline_is_bit_identical(monkeypatch):
+    """The partition-split CPU baseline must produce exactly the single-threaded
+    oracle's step (same per-element rank order)."""
+    import numpy as np
+    import bench
+    monkeypatch.setattr(bench, "PART", 777)
+    rng = np.random.default_rng(5)
+    xh = [rng.integers(0, 1 << 16, size=bench.R * 777, dtype=np.uint16) & 0xBFFF
+          for _ in range(bench.R)]
+    _, y1, z1 = bench.run_cpu_oracle(xh, 0.0, max_reps=1)
+    c2, y2, z2 = bench.run_cpu_oracle_threads(xh, 0.0, max_reps=1)
+    assert c2["cores"] >= 1 and c2["kind"].startswith("oracle")
+    assert all(np.array_equal(a, b) for a, b in zip(y1, y2))
+    assert all(np.array_equal(a, b) for a, b in zip(z1, z2))
