@@ -791,10 +791,14 @@ def other_configs(rd, torch, dev, stream, peak):
     return out
 
 
+SWEEP_RING = 96 << 20   # SNAC ring of the sweep: two 2 MiB-chunk channels, inside L2
+
+
 def allreduce_sweep(rd, torch, dev, stream, peak):
-    """AllReduce R=8 bf16 at 4 KiB..256 MiB per rank: zero staging and SNAC."""
+    """AllReduce R=8 bf16 at 4 KiB..256 MiB per rank: zero staging, SNAC with
+    its default chunk, and SNAC at every chunk of 64 KiB..2 MiB per rank."""
     import workloads
-    h = rd.purlin_create(R, 0, dev.index)
+    h = rd.purlin_create(R, SWEEP_RING, dev.index)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.empty(2 * l2 // 4 + 1, dtype=torch.float32, device=dev)
     out = []
@@ -806,8 +810,10 @@ def allreduce_sweep(rd, torch, dev, stream, peak):
             # inputs + outputs that fit in L2 stay there across repeated launches,
             # so their GB/s is not an HBM figure (it can exceed the HBM peak)
             row = {"bytes_per_rank": nbytes, "fits_in_l2": 2 * R * nbytes <= l2}
-            for name, variant in (("zs", rd.VARIANT_ZS), ("snac", rd.VARIANT_STAGED)):
-                rd.purlin_set_policy(h, 0, 0, 0, variant)
+            runs = [("zs", rd.VARIANT_ZS, 0), ("snac", rd.VARIANT_STAGED, 0)] + \
+                [(f"snac_chunk_{c >> 10}KiB", rd.VARIANT_STAGED, c) for c in workloads.SWEEP_CHUNKS]
+            for name, variant, chunk in runs:
+                rd.purlin_set_policy(h, chunk, 0, 0, variant)
                 fn = lambda: rd.purlin_all_reduce(h, x, o, n, "bf16", stream=stream)
                 with torch.cuda.stream(stream):
                     for _ in range(3):
@@ -823,6 +829,10 @@ def allreduce_sweep(rd, torch, dev, stream, peak):
                              "frac_of_peak": round(gbs / peak, 3),
                              "timing": "cuda graph" if graph_us is not None else "events",
                              "us_host_launched": round(host_us, 2)}
+                if variant == rd.VARIANT_STAGED:
+                    info = rd.purlin_last_launch(h)
+                    row[name]["chunk_bytes"] = info["chunk_bytes"]
+                    row[name]["channels"] = info["grid"] // 3
             if row["fits_in_l2"]:
                 # after both warm timings: the flush leaves L2 full of dirty lines
                 for name, variant in (("zs", rd.VARIANT_ZS), ("snac", rd.VARIANT_STAGED)):
@@ -831,6 +841,8 @@ def allreduce_sweep(rd, torch, dev, stream, peak):
                     cold = _cold_l2_us(torch, stream, fn, flush)
                     row[name]["us_cold_l2"] = round(cold, 2)
                     row[name]["gbs_cold_l2"] = round(2 * R * nbytes / (cold / 1e6) / 1e9, 1)
+            chunked = {k: v for k, v in row.items() if k.startswith("snac_chunk_")}
+            row["snac_best_chunk"] = min(chunked, key=lambda k: chunked[k]["us"])
             out.append(row)
             del x, o
         if rd.purlin_query_status(h) != rd.OK:

@@ -8,9 +8,10 @@
 //     AllReduce of Figure 6 (each summed unit written to all R outputs);
 //   - zs_copy:   AllGather(V) (each unit written to all R outputs) and
 //     AllToAll(V) (one destination per segment).
-// Work is a flat space of tiles (plan.h) walked grid-stride by a resident grid;
-// each CTA finds a tile's segment by binary search over the segments' first
-// tiles, which sit in the kernel's constant parameter bank.
+// Work is a flat space of tiles (plan.h) walked grid-stride; the host sizes the
+// grid (capi.cpp: several waves of CTAs, at most one per tile).  Each CTA finds
+// a tile's segment by binary search over the segments' first tiles, which sit
+// in the kernel's constant parameter bank.
 #include "atom.cuh"
 #include "internal.h"
 #include "purlin.h"

@@ -39,11 +39,14 @@ ZIPF_S = 1.2
 
 # Per-rank AllReduce message sizes of the sweep: 4 KiB * 4**i, i = 0..8.
 SWEEP_BYTES = [4 * KiB * 4 ** i for i in range(9)]
+# SNAC chunk sizes of the sweep (bytes per rank per step): 64 KiB .. 2 MiB.
+SWEEP_CHUNKS = [64 * KiB * 2 ** i for i in range(6)]
 
 WORKLOADS = {
     "allreduce_r2_f32": dict(R=2, dtype="f32", count=4096, values="int[-8,8]"),
     "rs_ag_r8_bf16": dict(R=8, dtype="bf16", count=64 * MiB // 2, values="N(0,1)"),
-    "allreduce_sweep_r8": dict(R=8, dtype="bf16", bytes=SWEEP_BYTES, values="N(0,1)"),
+    "allreduce_sweep_r8": dict(R=8, dtype="bf16", bytes=SWEEP_BYTES, chunks=SWEEP_CHUNKS,
+                               values="N(0,1)"),
     "moe_a2av_r8": dict(R=8, dtype="bf16", tokens=4096, hidden=HIDDEN, zipf_s=ZIPF_S,
                         values="N(0,1)"),
     "dp_attn_agv_rsv_r8": dict(R=8, dtype="bf16", tokens=(1, 2048), hidden=HIDDEN,
