@@ -229,6 +229,12 @@ bool replan_small(const purlin_handle* h, Coll coll, ZsParams<MAXSEG>& p, const 
     ZsKnobs ks = k;
     ks.tile_units = kTileUnitsSmall;
     if (reduce && !h->max_unit_log2) ks.max_unit_log2 = std::min(ks.max_unit_log2, 4);
+    // A small message cannot crowd other data out of L2, and a caller that
+    // repeats it (or has just written its inputs) finds it there: no
+    // evict-first marking, which would let any other resident data outlast it.
+    const int ci = (int)coll;
+    if (h->l2_load < 0 && h->l2_coll_load[ci] < 0) ks.l2_load = kL2Normal;
+    if (h->l2_store < 0 && h->l2_coll_store[ci] < 0) ks.l2_store = kL2Normal;
     if (make_params(p, pieces, npieces, R, in, out, esz, reduce, ks, p.status) != PURLIN_OK) {
         // cannot happen (same segments, more tiles of a smaller size fit in
         // 32 bits only if the large plan did); keep the large plan
