@@ -273,12 +273,15 @@ size_t algorithmic_bytes(Coll coll, int R, const size_t* counts, size_t count, s
 // AllReduce 171.3 -> 157.8 us, AllToAllV 173.7 -> 155.5 us; AllGather with
 // 1 GiB out per rank 1634 -> 1460 us.  One CTA per tile is slower again
 // (AllReduce 161.5 us): a CTA's launch costs about as much as a tile.
+// The TMA bulk Atom (one resident CTA per SM, each setting up a shared-memory
+// ring) is best at 4 waves: AllGather 96.2 us at 608 CTAs vs 100.3 at 2432.
 constexpr long kGridWaves = 16;
+constexpr long kGridWavesBulk = 4;
 
-int zs_grid(const purlin_handle* h, uint32_t ntiles, int resident)
+int zs_grid(const purlin_handle* h, uint32_t ntiles, int resident, long waves = kGridWaves)
 {
     if (ntiles == 0) return 0;
-    long g = h->ctas > 0 ? h->ctas : (long)h->sms * resident * kGridWaves;
+    long g = h->ctas > 0 ? h->ctas : (long)h->sms * resident * waves;
     return (int)std::max<long>(1, std::min<long>(g, (long)ntiles));
 }
 
@@ -414,7 +417,7 @@ purlin_status_t run(purlin_handle_t h, Coll coll, const void* const in_[], void*
         if (st != PURLIN_OK) return st;
         int grid;
         if (bulk) {
-            grid = zs_grid(h, p.ntiles, zs_copy_bulk_resident_ctas(true, false));
+            grid = zs_grid(h, p.ntiles, zs_copy_bulk_resident_ctas(true, false), kGridWavesBulk);
             if (grid > 0) ce = zs_copy_bulk_launch(p, false, grid, s);
             info.block = kBulkThreads;
         } else {
@@ -433,7 +436,7 @@ purlin_status_t run(purlin_handle_t h, Coll coll, const void* const in_[], void*
         bool fan_all = coll == Coll::AllGather || coll == Coll::AllReduce;
         int grid;
         if (bulk) {
-            grid = zs_grid(h, p.ntiles, zs_copy_bulk_resident_ctas(false, fan_all));
+            grid = zs_grid(h, p.ntiles, zs_copy_bulk_resident_ctas(false, fan_all), kGridWavesBulk);
             if (grid > 0) ce = zs_copy_bulk_launch(p, fan_all, grid, s);
             info.block = kBulkThreads;
         } else {
