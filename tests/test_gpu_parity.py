@@ -411,3 +411,30 @@ def test_fp8_payloads_move_as_bytes(fp8):
     want = oracle.all_to_all_v([t.view(torch.uint8).cpu().numpy() for t in x], C)
     for j in range(R):
         assert same_bits(out[j].view(torch.uint8).cpu().numpy(), want[j])
+
+
+@pytest.mark.parametrize("policy", ["zs", "zs_large", "snac_default"])
+def test_nvfp4_dispatch_and_combine(policy):
+    """An NVFP4 MoE dispatch: each token is 7168 e2m1 values packed two per byte
+    (3584 payload bytes) plus one e4m3 scale per 16 values (448 bytes).  Both
+    streams move as byte AllToAllV copies with per-token byte counts; the
+    inverse AllToAllV must give every source its tokens back."""
+    R, T, H = 8, 512, workloads.HIDDEN
+    h = handle(R)
+    set_variant(h, *POLICIES[policy])
+    C = workloads.zipf_pair_counts(R, T, workloads.ZIPF_S, workloads.seed_for("moe_a2av_r8", 21))
+    g = torch.Generator().manual_seed(77)
+    for per_token in (H // 2, H // 16):          # payload, then block scales
+        x = [torch.randint(0, 256, (T * per_token,), generator=g, dtype=torch.uint8).cuda()
+             for _ in range(R)]
+        recv = [torch.empty(int(C[:, j].sum()) * per_token, dtype=torch.uint8, device="cuda")
+                for j in range(R)]
+        rd.purlin_all_to_all_v(h, x, recv, C * per_token, None, None, "u8")
+        back = [torch.empty_like(t) for t in x]
+        rd.purlin_all_to_all_v(h, recv, back, C.T * per_token, None, None, "u8")
+        run_ok(h)
+        want = oracle.all_to_all_v([host_bits(t) for t in x], C * per_token)
+        for j in range(R):
+            assert same_bits(host_bits(recv[j]), want[j]), (per_token, j)
+        for s in range(R):
+            assert same_bits(host_bits(back[s]), host_bits(x[s])), (per_token, s)
