@@ -257,10 +257,18 @@ PURLIN_API purlin_status_t purlin_all_reduce_noalloc(const void* const in[], voi
 
 /* Codesign policy (Figure 1; chunk sizing after Table 3's bandwidth-delay
  * products; depth after Figure 11).  0 for any argument keeps the automatic
- * choice.  chunk_bytes: SNAC chunk, 16..(staging ring / (R * depth)), a multiple
- * of 16.  depth: ring slots per channel, 1..8.  ctas: CTAs per launch (ZS;
- * automatic: 16 per resident CTA slot of the device, at most one per tile) or
- * SNAC channels.  variant: a purlin_variant_t. */
+ * choice.
+ *   chunk_bytes  SNAC bytes per rank per pipeline step, a multiple of 16 (the
+ *                staged kernels round it up to a multiple of 256).  A staged call
+ *                whose ring cannot hold one channel -- depth x chunk x (R + 1 for
+ *                AllReduce, R for ReduceScatter, 1 for copies) above the
+ *                handle's staging bytes -- returns PURLIN_ERR_UNSUPPORTED.
+ *   depth        SNAC ring slots per channel, 1..8.
+ *   ctas         0..65535: CTAs per zero-staging launch (automatic: 16 per
+ *                resident CTA slot of the device, 4 for the TMA bulk Atom, at
+ *                most one per tile), or SNAC channels (CTAs per role).
+ *   variant      a purlin_variant_t.
+ * Out-of-range values: PURLIN_ERR_INVALID_ARG. */
 PURLIN_API purlin_status_t purlin_set_policy(purlin_handle_t h, size_t chunk_bytes, int depth,
                                   int ctas, int variant);
 
