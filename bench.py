@@ -55,6 +55,9 @@ def parse_args():
     ap.add_argument("--staging", type=int, default=0,
                     help="SNAC staging ring bytes of the handle (0 = library default)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--quick", action="store_true",
+                    help="only the timed step, its split and the end-to-end figure "
+                         "(no side studies, no CPU baseline)")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--only", choices=["rs", "ag", "ar", "a2av"], default=None,
@@ -419,24 +422,39 @@ def bench_purlin(args):
     ag_info = rd.purlin_last_launch(h)
     torch.cuda.synchronize()
 
+    # The timed region: K steps back to back, events only at its two ends, so
+    # that nothing sits between the kernels (an event between two launches
+    # stops the second one's programmatic early launch).
     K = max(1, args.steps)
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(dev)
     barrier(world, dev)
     torch.cuda.synchronize()
     clocks.start()
+    t0.record(stream)
     for i in range(K):
+        rs()
+        ag()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clocks.stop()
+    barrier(world, dev)
+    total_ms = t0.elapsed_time(t1)
+    # The split between the two collectives, from a second run of the same
+    # steps with an event around each launch.
+    Kb = min(K, 100)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(Kb)]
+    for i in range(Kb):
         ev[i][0].record(stream)
         rs()
         ev[i][1].record(stream)
         ag()
         ev[i][2].record(stream)
     torch.cuda.synchronize()
-    clocks.stop()
-    barrier(world, dev)
-    total_ms = ev[0][0].elapsed_time(ev[K - 1][2])
-    rs_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
-    ag_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
+    rs_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(Kb)]
+    ag_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(Kb)]
+    split_ms = sum(rs_ms) + sum(ag_ms)
     status = rd.purlin_query_status(h)
     if status != rd.OK:
         raise RuntimeError("device status: " + rd.purlin_status_string(status))
@@ -444,8 +462,8 @@ def bench_purlin(args):
     rs_b, ag_b = step_bytes()
     value, max_ms = whole_job_value(world, K, rs_b + ag_b, total_ms, dev)
 
-    rs_avg = sum(rs_ms) / K
-    ag_avg = sum(ag_ms) / K
+    rs_avg = sum(rs_ms) / Kb
+    ag_avg = sum(ag_ms) / Kb
     per = {
         "reduce_scatter": {"us": rs_avg * 1e3, "gbs": rs_b / (rs_avg / 1e3) / 1e9,
                            "bytes": rs_b, "grid": rs_info["grid"]},
@@ -465,23 +483,27 @@ def bench_purlin(args):
                 if peak_kind == "measured" else "fallback 6.8 TB/s",
                 "algorithmic_bytes_per_launch": per[dom]["bytes"]}
 
-    # ---- AllReduce latency at 4 KiB per rank (R=8 bf16, 2048 elements)
-    lat = allreduce_latency(rd, torch, dev, stream, variant)
+    per["split_run_step_us"] = split_ms / Kb * 1e3
 
-    # ---- the same step through the staged (SNAC) path, default policy
-    staged = staged_step(rd, torch, h, rs, ag, stream, rs_b + ag_b, peak)
+    lat = staged = frugal = tree = configs = sweep = None
+    if not args.quick:
+        # ---- AllReduce latency at 4 KiB per rank (R=8 bf16, 2048 elements)
+        lat = allreduce_latency(rd, torch, dev, stream, variant)
 
-    # ---- bandwidth vs CTAs launched, per Atom, and the copy-engine AllGather
-    frugal = cta_study(rd, torch, h, rs, ag, stream, rs_b, peak)
+        # ---- the same step through the staged (SNAC) path, default policy
+        staged = staged_step(rd, torch, h, rs, ag, stream, rs_b + ag_b, peak)
 
-    # ---- the pairwise rank order, reported beside the fixed order
-    tree = tree_order_report(rd, torch, h, x, y, counts, stream, rs_b, peak)
+        # ---- bandwidth vs CTAs launched, per Atom, and the copy-engine AllGather
+        frugal = cta_study(rd, torch, h, rs, ag, stream, rs_b, peak)
 
-    # ---- the other workload configurations, zero staging (default policy)
-    configs = other_configs(rd, torch, dev, stream, peak)
+        # ---- the pairwise rank order, reported beside the fixed order
+        tree = tree_order_report(rd, torch, h, x, y, counts, stream, rs_b, peak)
 
-    # ---- AllReduce size sweep: zero staging vs SNAC (default policy)
-    sweep = allreduce_sweep(rd, torch, dev, stream, peak)
+        # ---- the other workload configurations, zero staging (default policy)
+        configs = other_configs(rd, torch, dev, stream, peak)
+
+        # ---- AllReduce size sweep: zero staging vs SNAC (default policy)
+        sweep = allreduce_sweep(rd, torch, dev, stream, peak)
 
     # ---- end to end: inputs from pinned host memory, outputs back to it; with
     # several ranks the job's figure is all ranks' bytes over the slowest rank
@@ -495,7 +517,7 @@ def bench_purlin(args):
     cpu = None
     cpu_threads = None
     parity = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.quick:
         xh = [host_bits(t) for t in x]
         cpu, want_y, want_z = run_cpu_oracle(xh, args.cpu_seconds)
         cpu.pop("seconds", None)
