@@ -345,9 +345,13 @@ __device__ void producer(const SnacParams& p, uint32_t ch, uint64_t epoch)
 template <typename T, int ORDER, int KIND>
 __device__ void consumer(const SnacParams& p, uint32_t ch, uint64_t epoch)
 {
-    // AllToAll outputs are written once and not read again here: evict-first.
+    // AllGather and AllToAll outputs are written once and not read again here:
+    // evict-first, so that they do not push the ring out of L2.  A
+    // ReduceScatter's outputs stay at normal priority (a following AllGather
+    // reads them), and an AllReduce's consumer writes into the ring's y part.
     const uint64_t lpol = atom::l2_policy(kL2Normal);
-    const uint64_t spol = atom::l2_policy(KIND == kA2A ? kL2EvictFirst : kL2Normal);
+    const uint64_t spol =
+        atom::l2_policy((KIND == kA2A || KIND == kAG) ? kL2EvictFirst : kL2Normal);
     uint32_t n = 0;
     for (uint32_t i = ch; i < p.nsteps; i += p.nch, ++n) {
         const uint32_t slot = n % p.depth;
