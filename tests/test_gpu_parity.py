@@ -14,7 +14,8 @@ import torch
 import oracle
 import reduce_datapath_gb300 as rd
 import workloads
-from helpers import Guarded, handle, host_bits, inputs, same_bits, set_variant, close_handles
+from helpers import (TORCH, Guarded, close_handles, handle, host_bits, inputs, same_bits,
+                     set_variant)
 
 pytestmark = pytest.mark.gpu
 
@@ -438,3 +439,55 @@ def test_nvfp4_dispatch_and_combine(policy):
             assert same_bits(host_bits(recv[j]), want[j]), (per_token, j)
         for s in range(R):
             assert same_bits(host_bits(back[s]), host_bits(x[s])), (per_token, s)
+
+
+# Special values of each type as raw bits: signed zeros, the smallest and largest
+# subnormals, the smallest normal, the largest finite value, infinities, a quiet
+# NaN, and ordinary values near 1 (ties in the final rounding).
+SPECIAL_BITS = {
+    "f32": [0x00000000, 0x80000000, 0x00000001, 0x807FFFFF, 0x00800000, 0x7F7FFFFF,
+            0xFF7FFFFF, 0x7F800000, 0xFF800000, 0x7FC00000, 0x3F800000, 0x3F800001,
+            0x33800000, 0xBF800000],
+    "bf16": [0x0000, 0x8000, 0x0001, 0x807F, 0x0080, 0x7F7F, 0xFF7F, 0x7F80, 0xFF80, 0x7FC0,
+             0x3F80, 0x3F81, 0x3B80, 0xBF80],
+    "f16": [0x0000, 0x8000, 0x0001, 0x83FF, 0x0400, 0x7BFF, 0xFBFF, 0x7C00, 0xFC00, 0x7E00,
+            0x3C00, 0x3C01, 0x1400, 0xBC00],
+}
+
+
+def _is_nan(bits, dtype):
+    if dtype == "f32":
+        return np.isnan(bits.view(np.float32))
+    exp_mask, man_mask = (0x7F80, 0x007F) if dtype == "bf16" else (0x7C00, 0x03FF)
+    b = bits.view(np.uint16)
+    return ((b & exp_mask) == exp_mask) & ((b & man_mask) != 0)
+
+
+@pytest.mark.parametrize("policy", ["zs", "zs_large", "snac_default"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+@pytest.mark.parametrize("R", [2, 3, 8])
+def test_special_values_sum(policy, dtype, R):
+    """Sums over signed zeros, subnormals, overflow to infinity, inf - inf and
+    NaN: every non-NaN output bit-exact to the oracle (fold from rank 0's value,
+    subnormals kept, one round to nearest even), and NaN exactly where the
+    oracle has NaN (payloads are not compared)."""
+    n = 3000
+    rng = np.random.default_rng(R * 7 + len(dtype))
+    pool = np.array(SPECIAL_BITS[dtype], dtype=np.uint32 if dtype == "f32" else np.uint16)
+    host = [pool[rng.integers(0, len(pool), size=n)] for _ in range(R)]
+    h = handle(R)
+    set_variant(h, *POLICIES[policy])
+    x = [torch.from_numpy(b.view(np.int32 if dtype == "f32" else np.int16).copy()).cuda()
+         .view(TORCH[dtype]) for b in host]
+    ar = [Guarded(n, dtype) for _ in range(R)]
+    rd.purlin_all_reduce(h, x, [o.view for o in ar], n, dtype)
+    run_ok(h)
+    want = oracle.all_reduce([host_bits(t) for t in x], dtype=dtype)
+    for j in range(R):
+        got = host_bits(ar[j].view)
+        gi = got.view(np.uint32 if dtype == "f32" else np.uint16)
+        wi = want[j].view(np.uint32 if dtype == "f32" else np.uint16)
+        nan_w = _is_nan(wi, dtype)
+        assert np.array_equal(_is_nan(gi, dtype), nan_w), j
+        assert np.array_equal(gi[~nan_w], wi[~nan_w]), j
+        assert ar[j].guards_intact()
