@@ -341,9 +341,9 @@ def bench_reference(args):
     print(json.dumps(line), flush=True)
 
 
-# Source files whose content determines each kernel family's code.
+# Source files whose content determines each kernel family's device code.
 KERNEL_SOURCES = {
-    "zs": ["atom.cuh", "plan.h", "zs_kernels.cu"],
+    "zs": ["atom.cuh", "plan.h", "zs_kernels.cuh"],
     "snac": ["atom.cuh", "plan.h", "snac.h", "snac_kernels.cu"],
 }
 
@@ -406,9 +406,13 @@ def bench_purlin(args):
     counts = [PART] * R
     torch.cuda.synchronize()
 
-    # marshalled once: each repeat is one C call
+    # marshalled once: each repeat is one C call that plans and launches (the
+    # side studies change the handle's policy between calls)
     rs = rd.prepare(rd.purlin_reduce_scatter, h, x, y, counts, None, "bf16", stream=stream)
     ag = rd.prepare(rd.purlin_all_gather, h, y, z, counts, None, "bf16", stream=stream)
+    # planned once: each timed repeat is one launch of the kept plan
+    rs_plan = rd.plan(rd.purlin_reduce_scatter, h, x, y, counts, None, "bf16", stream=stream)
+    ag_plan = rd.plan(rd.purlin_all_gather, h, y, z, counts, None, "bf16", stream=stream)
 
     with torch.cuda.stream(stream):
         for _ in range(max(3, args.warmup)):
@@ -434,8 +438,8 @@ def bench_purlin(args):
     clocks.start()
     t0.record(stream)
     for i in range(K):
-        rs()
-        ag()
+        rs_plan()
+        ag_plan()
     t1.record(stream)
     torch.cuda.synchronize()
     clocks.stop()
@@ -447,9 +451,9 @@ def bench_purlin(args):
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(Kb)]
     for i in range(Kb):
         ev[i][0].record(stream)
-        rs()
+        rs_plan()
         ev[i][1].record(stream)
-        ag()
+        ag_plan()
         ev[i][2].record(stream)
     torch.cuda.synchronize()
     rs_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(Kb)]
@@ -895,16 +899,25 @@ def allreduce_latency(rd, torch, dev, stream, variant):
         b.record(stream)
         b.synchronize()
         single.append(a.elapsed_time(b) * 1e3)
-    # 1000 launches back to back from the host (prepared call: one C call each)
-    call = rd.prepare(rd.purlin_all_reduce, h, x, o, n, "bf16", stream=stream)
-    a = torch.cuda.Event(enable_timing=True)
-    b = torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(1000):
-        call()
-    b.record(stream)
-    torch.cuda.synchronize()
-    b2b = a.elapsed_time(b) * 1e3 / 1000
+    # 1000 launches back to back from the host: a prepared call (one C call
+    # that plans and launches) and a plan (one launch of the kept plan)
+    b2b = {}
+    for name, call in (("prepared", rd.prepare(rd.purlin_all_reduce, h, x, o, n, "bf16",
+                                                 stream=stream)),
+                       ("plan", rd.plan(rd.purlin_all_reduce, h, x, o, n, "bf16", stream=stream))):
+        for _ in range(20):
+            call()
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        t_host = time.perf_counter()
+        a.record(stream)
+        for _ in range(1000):
+            call()
+        b.record(stream)
+        host_us = (time.perf_counter() - t_host) * 1e6 / 1000
+        torch.cuda.synchronize()
+        b2b[name] = (a.elapsed_time(b) * 1e3 / 1000, host_us)
     # CUDA graph of 100 launches, replayed 10 times
     graph_us = None
     try:
@@ -925,7 +938,9 @@ def allreduce_latency(rd, torch, dev, stream, variant):
         graph_us = f"capture failed: {e}"
     torch.cuda.synchronize()
     rd.purlin_destroy(h)
-    return {"us_graph_per_launch": graph_us, "us_back_to_back": b2b,
+    return {"us_graph_per_launch": graph_us, "us_back_to_back": b2b["plan"][0],
+            "us_back_to_back_prepared_call": b2b["prepared"][0],
+            "host_us_per_call": {"plan": b2b["plan"][1], "prepared_call": b2b["prepared"][1]},
             "us_single_event_median": statistics.median(single), "R": R, "bytes_per_rank": 4096}
 
 

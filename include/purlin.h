@@ -119,6 +119,7 @@ typedef enum {
 } purlin_direction_t;
 
 typedef struct purlin_handle* purlin_handle_t;
+typedef struct purlin_plan* purlin_plan_t;
 
 /* What the last collective on a handle launched (for SM accounting, Figure 10:
  * concurrent SM use is bounded by min(CTAs launched, SMs)). */
@@ -250,6 +251,35 @@ PURLIN_API purlin_status_t purlin_all_reduce_noalloc(const void* const in[], voi
                                                      int R, size_t count, purlin_dtype_t dtype,
                                                      size_t chunk_bytes, int depth,
                                                      int* device_status, purlin_stream_t stream);
+
+/* ------------------------------------------------------------------------- */
+/* Plans: check and lay out a collective once, launch it many times           */
+/* ------------------------------------------------------------------------- */
+
+/* The layout module turns a collective's naming into a plan (Figure 1:
+ * collectives are "a naming of an input and output layout"); these calls keep
+ * that plan so that a call repeated on the same buffers costs one launch.
+ *
+ * purlin_plan_begin(h): the NEXT collective call on h (any entry point above
+ * that takes h) is checked and planned exactly as usual, with h's policy at that
+ * moment, but enqueues nothing.  A second collective call before
+ * purlin_plan_end returns PURLIN_ERR_INVALID_ARG.  Errors of the recorded call
+ * are returned by that call, as usual.
+ * purlin_plan_end(h, &plan): *plan receives the recorded call (NULL and
+ * PURLIN_ERR_INVALID_ARG if none was recorded).  Recording stops either way.
+ * purlin_plan_launch(plan, stream): enqueue the planned call on `stream`; same
+ * kernels, same parameters, same result bit for bit as the direct call.  The
+ * buffers, counts and displacements are those of the recorded call: the caller
+ * keeps the buffers alive and the plan sees whatever they hold at launch time.
+ * The plan uses h's staging ring, flags and status word (staged calls), so h
+ * must outlive it, and launches of plans and calls of one handle must not
+ * overlap on the GPU (as for any call on h).  Safe to capture in a CUDA graph.
+ * purlin_plan_destroy(plan): free the plan (host memory only); NULL is
+ * ignored. */
+PURLIN_API purlin_status_t purlin_plan_begin(purlin_handle_t h);
+PURLIN_API purlin_status_t purlin_plan_end(purlin_handle_t h, purlin_plan_t* plan);
+PURLIN_API purlin_status_t purlin_plan_launch(purlin_plan_t plan, purlin_stream_t stream);
+PURLIN_API purlin_status_t purlin_plan_destroy(purlin_plan_t plan);
 
 /* ------------------------------------------------------------------------- */
 /* Policy, status, introspection                                              */

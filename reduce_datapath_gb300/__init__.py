@@ -50,7 +50,8 @@ EXPORTED = (
     "purlin_create", "purlin_destroy", "purlin_reduce_scatter", "purlin_all_gather",
     "purlin_all_reduce", "purlin_all_to_all", "purlin_all_to_all_v", "purlin_set_policy",
     "purlin_set_reduce_order", "purlin_set_atom", "purlin_set_direction", "purlin_set_small_tiles",
-    "purlin_set_timeout", "purlin_query_status",
+    "purlin_set_timeout", "purlin_query_status", "purlin_plan_begin", "purlin_plan_end",
+    "purlin_plan_launch", "purlin_plan_destroy",
     "purlin_last_launch", "purlin_status_string", "purlin_version", "purlin_plan_segments",
     "purlin_debug_inject", "purlin_all_reduce_noalloc",
 )
@@ -122,6 +123,10 @@ def lib():
             "purlin_set_atom": [vp, i32],
             "purlin_set_direction": [vp, i32],
             "purlin_set_small_tiles": [vp, i32],
+            "purlin_plan_begin": [vp],
+            "purlin_plan_end": [vp, ctypes.POINTER(vp)],
+            "purlin_plan_launch": [vp, vp],
+            "purlin_plan_destroy": [vp],
             "purlin_set_timeout": [vp, u64],
             "purlin_query_status": [vp],
             "purlin_last_launch": [vp, ctypes.POINTER(LaunchInfo)],
@@ -304,6 +309,67 @@ def prepare(fn, *args, **kwargs):
 
     call.c_args = cargs   # keeps the ctypes arrays alive with the callable
     return call
+
+
+def purlin_plan_begin(h) -> None:
+    _check(lib().purlin_plan_begin(h), "purlin_plan_begin")
+
+
+def purlin_plan_end(h):
+    plan = ctypes.c_void_p()
+    _check(lib().purlin_plan_end(h, ctypes.byref(plan)), "purlin_plan_end")
+    return plan.value
+
+
+def purlin_plan_launch(plan, stream=None) -> None:
+    _check(lib().purlin_plan_launch(plan, _stream(stream)), "purlin_plan_launch")
+
+
+def purlin_plan_destroy(plan) -> None:
+    _check(lib().purlin_plan_destroy(plan), "purlin_plan_destroy")
+
+
+class Plan:
+    """One collective call planned once (purlin_plan_begin / _end): calling the
+    object launches that call again on the stream it was planned with (or on
+    `stream`).  The buffers must outlive the plan; the handle's policy is the
+    one in force when the plan was made."""
+
+    def __init__(self, fn, h, *args, **kwargs):
+        name = fn if isinstance(fn, str) else fn.__name__
+        self._stream = _stream(kwargs.get("stream"))
+        self._lib = lib()
+        purlin_plan_begin(h)
+        try:
+            _call(name, _MARSHAL[name](h, *args, **kwargs))
+        finally:
+            plan = ctypes.c_void_p()
+            st = self._lib.purlin_plan_end(h, ctypes.byref(plan))
+        _check(st, "purlin_plan_end")
+        self.handle = plan.value
+        self._launch = self._lib.purlin_plan_launch
+
+    def __call__(self, stream=None) -> None:
+        st = self._launch(self.handle, self._stream if stream is None else _stream(stream))
+        if st != OK:
+            raise PurlinError(st, "purlin_plan_launch")
+
+    def destroy(self) -> None:
+        if self.handle:
+            self._lib.purlin_plan_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.destroy()
+        except Exception:
+            pass
+
+
+def plan(fn, h, *args, **kwargs) -> Plan:
+    """Plan one collective call (same arguments as the call itself) for repeated
+    launches: each launch is one C call of two arguments."""
+    return Plan(fn, h, *args, **kwargs)
 
 
 def purlin_set_policy(h, chunk_bytes=0, depth=0, ctas=0, variant=VARIANT_AUTO) -> None:

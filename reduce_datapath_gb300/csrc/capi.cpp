@@ -16,6 +16,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <new>
+#include <vector>
 
 #include "internal.h"
 #include "plan.h"
@@ -60,6 +61,27 @@ struct purlin_handle {
     int direction = PURLIN_DIRECTION_AUTO;
     int inject = 0;  // purlin_debug_inject, one staged call
     purlin_launch_info_t last{};
+    // purlin_plan_begin .. purlin_plan_end: the call is planned, not launched
+    bool recording = false;
+    purlin_plan* recorded = nullptr;
+};
+
+// One planned collective call: a kernel launch with its parameter block, or the
+// copy-engine copies of a kernel-less AllGather / AllToAll, or nothing (an
+// empty call).
+struct CopyOp {
+    void* dst;
+    const void* src;
+    size_t bytes;
+};
+
+struct purlin_plan {
+    purlin_handle_t h = nullptr;
+    int device = 0;
+    int kind = 0;  // 0 nothing, 1 kernel, 2 copies
+    purlin::KernelLaunch k;
+    std::vector<CopyOp> copies;
+    purlin_launch_info_t info{};
 };
 
 namespace {
@@ -331,6 +353,16 @@ purlin_status_t run(purlin_handle_t h, Coll coll, const void* const in_[], void*
     info.block = kThreads;
     info.bytes_moved = algorithmic_bytes(coll, R, counts, count, esz);
 
+    // The call's launch is built in thread-local storage (no copy of the
+    // parameter block on the way to the launch), then made at once or, while
+    // a plan is being recorded, kept.
+    static thread_local KernelLaunch tl_k;
+    static thread_local std::vector<CopyOp> tl_copies;
+    KernelLaunch& k = tl_k;
+    k.grid = 0;
+    tl_copies.clear();
+    int kind = 0;
+
     if (wants_staged(h) && np > 0) {
         SnacRequest rq{};
         rq.coll = coll;
@@ -353,106 +385,139 @@ purlin_status_t run(purlin_handle_t h, Coll coll, const void* const in_[], void*
         cfg.sms = h->sms;
         cfg.timeout_ns = h->timeout_ns;
         cfg.inject_skip_notify = h->inject;
-        h->inject = 0;
         SnacLaunch sl{};
-        purlin_status_t ss = snac_run(rq, cfg, s, &sl);
+        purlin_status_t ss = snac_plan(rq, cfg, k, &sl);
         if (ss != PURLIN_OK) return ss;
+        h->inject = 0;
+        kind = k.grid > 0 ? 1 : 0;
         info.variant = PURLIN_VARIANT_STAGED;
         info.kernels = sl.kernels;
         info.grid = sl.grid;
         info.block = sl.block;
         info.depth = sl.depth;
         info.chunk_bytes = sl.chunk_bytes;
-        h->last = info;
-        return PURLIN_OK;
+    } else {
+        info.variant = PURLIN_VARIANT_ZS;
+        ZsKnobs knobs = zs_knobs(h, coll);
+        const bool bulk = !reduce && h->atom == PURLIN_ATOM_BULK;
+        if (!reduce && h->atom == PURLIN_ATOM_COPY_ENGINE) {
+            // No kernel: every block goes to every destination through the
+            // copy engines, one asynchronous copy each, in stream order.
+            for (int i = 0; i < np; ++i) {
+                const Piece& pc = pieces[i];
+                const char* src = reinterpret_cast<const char*>(in[pc.src]) + pc.src_off;
+                for (int j = 0; j < R; ++j) {
+                    if (pc.dst != kEveryRank && pc.dst != j) continue;
+                    char* dst = reinterpret_cast<char*>(out[j]) + pc.dst_off;
+                    if (dst == src) continue;  // in-place AllGather block
+                    tl_copies.push_back(CopyOp{dst, src, (size_t)pc.bytes});
+                }
+            }
+            kind = tl_copies.empty() ? 0 : 2;
+            info.kernels = 0;
+            info.grid = 0;
+            info.block = 0;
+            info.chunk_bytes = 0;
+        } else if (coll == Coll::AllToAllV ||
+                   (coll == Coll::AllGather && h->direction == PURLIN_DIRECTION_PULL)) {
+            ZsParams<kSegsLarge>& p = *reinterpret_cast<ZsParams<kSegsLarge>*>(k.params);
+            const Piece* plan = pieces;
+            int nplan = np;
+            Piece pulled[kMaxRanks * kMaxRanks];
+            if (coll == Coll::AllGather) {
+                // pull: one piece per (destination, source), destination by
+                // destination; every source is read R times (from L2 after
+                // the first read, hence normal priority for the loads)
+                nplan = 0;
+                for (int j = 0; j < R; ++j)
+                    for (int i = 0; i < np; ++i) {
+                        Piece e = pieces[i];
+                        e.dst = (uint8_t)j;
+                        if (in[e.src] + e.src_off == out[j] + e.dst_off) continue;  // in place
+                        pulled[nplan++] = e;
+                    }
+                plan = pulled;
+                if (h->l2_load < 0 && h->l2_coll_load[(int)coll] < 0) knobs.l2_load = kL2Normal;
+            }
+            st = make_params(p, plan, nplan, R, in, out, esz, false, knobs, h->status);
+            if (st != PURLIN_OK) return st;
+            int grid;
+            if (bulk) {
+                grid = zs_grid(h, p.ntiles, zs_copy_bulk_resident_ctas(true, false), kGridWavesBulk);
+                if (zs_copy_bulk_select(k, true, false) != cudaSuccess) return PURLIN_ERR_CUDA;
+                info.block = kBulkThreads;
+            } else {
+                const bool small = replan_small(h, coll, p, plan, nplan, R, in, out, esz, false, knobs);
+                grid = zs_grid(h, p.ntiles, zs_copy_resident_ctas(true, false, small));
+                zs_copy_select(k, true, false, small);
+                if (small) info.block = kSmallThreads;
+            }
+            k.grid = (unsigned)grid;
+            k.pdl = p.pdl != 0;
+            kind = grid > 0 ? 1 : 0;
+            info.grid = grid;
+            info.kernels = grid > 0;
+            info.chunk_bytes = tile_bytes(knobs.max_unit_log2, knobs.tile_units);
+        } else {
+            ZsParams<kSegsSmall>& p = *reinterpret_cast<ZsParams<kSegsSmall>*>(k.params);
+            st = make_params(p, pieces, np, R, in, out, esz, reduce, knobs, h->status);
+            if (st != PURLIN_OK) return st;
+            bool fan_all = coll == Coll::AllGather || coll == Coll::AllReduce;
+            int grid;
+            if (bulk) {
+                grid = zs_grid(h, p.ntiles, zs_copy_bulk_resident_ctas(false, fan_all), kGridWavesBulk);
+                if (zs_copy_bulk_select(k, false, fan_all) != cudaSuccess) return PURLIN_ERR_CUDA;
+                info.block = kBulkThreads;
+            } else {
+                const bool small = replan_small(h, coll, p, pieces, np, R, in, out, esz, reduce, knobs);
+                if (reduce) {
+                    grid = zs_grid(h, p.ntiles, zs_reduce_resident_ctas(dtype, h->order, fan_all, small));
+                    zs_reduce_select(k, dtype, h->order, fan_all, small);
+                } else {
+                    grid = zs_grid(h, p.ntiles, zs_copy_resident_ctas(false, fan_all, small));
+                    zs_copy_select(k, false, fan_all, small);
+                }
+                if (small) info.block = kSmallThreads;
+            }
+            k.grid = (unsigned)grid;
+            k.pdl = p.pdl != 0;
+            kind = grid > 0 ? 1 : 0;
+            info.chunk_bytes = tile_bytes(knobs.max_unit_log2, knobs.tile_units);
+            info.grid = grid;
+            info.kernels = grid > 0;
+        }
     }
 
-    info.variant = PURLIN_VARIANT_ZS;
+    if (h->recording) {
+        if (h->recorded) return PURLIN_ERR_INVALID_ARG;  // one call per plan
+        purlin_plan* plan = new (std::nothrow) purlin_plan;
+        if (!plan) return PURLIN_ERR_OOM;
+        plan->h = h;
+        plan->device = h->device;
+        plan->kind = kind;
+        if (kind == 1) {
+            plan->k.func = k.func;
+            plan->k.grid = k.grid;
+            plan->k.block = k.block;
+            plan->k.smem = k.smem;
+            plan->k.pdl = k.pdl;
+            plan->k.cooperative = k.cooperative;
+            plan->k.params_bytes = k.params_bytes;
+            std::memcpy(plan->k.params, k.params, k.params_bytes);
+        }
+        plan->copies = tl_copies;
+        plan->info = info;
+        h->recorded = plan;
+        return PURLIN_OK;
+    }
     cudaError_t ce = cudaSuccess;
-    ZsKnobs knobs = zs_knobs(h, coll);
-    const bool bulk = !reduce && h->atom == PURLIN_ATOM_BULK;
-    if (!reduce && h->atom == PURLIN_ATOM_COPY_ENGINE) {
-        // No kernel: every block goes to every destination through the copy
-        // engines, one asynchronous copy each, in stream order.
-        int copies = 0;
-        for (int i = 0; i < np && ce == cudaSuccess; ++i) {
-            const Piece& pc = pieces[i];
-            const char* src = reinterpret_cast<const char*>(in[pc.src]) + pc.src_off;
-            for (int j = 0; j < R; ++j) {
-                if (pc.dst != kEveryRank && pc.dst != j) continue;
-                char* dst = reinterpret_cast<char*>(out[j]) + pc.dst_off;
-                if (dst == src) continue;  // in-place AllGather block
-                ce = cudaMemcpyAsync(dst, src, pc.bytes, cudaMemcpyDefault, s);
-                if (ce != cudaSuccess) break;
-                ++copies;
-            }
+    if (kind == 1) {
+        ce = launch_kernel(k, s);
+    } else if (kind == 2) {
+        for (const CopyOp& c : tl_copies) {
+            ce = cudaMemcpyAsync(c.dst, c.src, c.bytes, cudaMemcpyDefault, s);
+            if (ce != cudaSuccess) break;
         }
-        info.kernels = 0;
-        info.grid = 0;
-        info.block = 0;
-        info.chunk_bytes = 0;
-        (void)copies;
-    } else if (coll == Coll::AllToAllV ||
-               (coll == Coll::AllGather && h->direction == PURLIN_DIRECTION_PULL)) {
-        static thread_local ZsParams<kSegsLarge> p;
-        const Piece* plan = pieces;
-        int nplan = np;
-        Piece pulled[kMaxRanks * kMaxRanks];
-        if (coll == Coll::AllGather) {
-            // pull: one piece per (destination, source), destination by
-            // destination; every source is read R times (from L2 after the
-            // first read, hence normal priority for the loads)
-            nplan = 0;
-            for (int j = 0; j < R; ++j)
-                for (int i = 0; i < np; ++i) {
-                    Piece e = pieces[i];
-                    e.dst = (uint8_t)j;
-                    if (in[e.src] + e.src_off == out[j] + e.dst_off) continue;  // in place
-                    pulled[nplan++] = e;
-                }
-            plan = pulled;
-            if (h->l2_load < 0 && h->l2_coll_load[(int)coll] < 0) knobs.l2_load = kL2Normal;
-        }
-        st = make_params(p, plan, nplan, R, in, out, esz, false, knobs, h->status);
-        if (st != PURLIN_OK) return st;
-        int grid;
-        if (bulk) {
-            grid = zs_grid(h, p.ntiles, zs_copy_bulk_resident_ctas(true, false), kGridWavesBulk);
-            if (grid > 0) ce = zs_copy_bulk_launch(p, false, grid, s);
-            info.block = kBulkThreads;
-        } else {
-            const bool small = replan_small(h, coll, p, plan, nplan, R, in, out, esz, false, knobs);
-            grid = zs_grid(h, p.ntiles, zs_copy_resident_ctas(true, false, small));
-            if (grid > 0) ce = zs_copy_launch(p, false, small, grid, s);
-            if (small) info.block = kSmallThreads;
-        }
-        info.grid = grid;
-        info.kernels = grid > 0;
-        info.chunk_bytes = tile_bytes(knobs.max_unit_log2, knobs.tile_units);
-    } else {
-        static thread_local ZsParams<kSegsSmall> p;
-        st = make_params(p, pieces, np, R, in, out, esz, reduce, knobs, h->status);
-        if (st != PURLIN_OK) return st;
-        bool fan_all = coll == Coll::AllGather || coll == Coll::AllReduce;
-        int grid;
-        if (bulk) {
-            grid = zs_grid(h, p.ntiles, zs_copy_bulk_resident_ctas(false, fan_all), kGridWavesBulk);
-            if (grid > 0) ce = zs_copy_bulk_launch(p, fan_all, grid, s);
-            info.block = kBulkThreads;
-        } else {
-            const bool small = replan_small(h, coll, p, pieces, np, R, in, out, esz, reduce, knobs);
-            if (reduce) {
-                grid = zs_grid(h, p.ntiles, zs_reduce_resident_ctas(dtype, h->order, fan_all, small));
-                if (grid > 0) ce = zs_reduce_launch(p, dtype, h->order, fan_all, small, grid, s);
-            } else {
-                grid = zs_grid(h, p.ntiles, zs_copy_resident_ctas(false, fan_all, small));
-                if (grid > 0) ce = zs_copy_launch(p, fan_all, small, grid, s);
-            }
-            if (small) info.block = kSmallThreads;
-        }
-        info.chunk_bytes = tile_bytes(knobs.max_unit_log2, knobs.tile_units);
-        info.grid = grid;
-        info.kernels = grid > 0;
     }
     if (ce != cudaSuccess) return PURLIN_ERR_CUDA;
     h->last = info;
@@ -542,6 +607,7 @@ purlin_status_t purlin_create(purlin_handle_t* out, int R, size_t staging_bytes,
 purlin_status_t purlin_destroy(purlin_handle_t h)
 {
     if (!h) return PURLIN_OK;
+    delete h->recorded;  // a plan begun and never ended
     purlin_status_t st = PURLIN_OK;
     {
         DeviceGuard guard(h->device);
@@ -641,6 +707,55 @@ purlin_status_t purlin_set_timeout(purlin_handle_t h, uint64_t timeout_ns)
 {
     if (!h || timeout_ns == 0) return PURLIN_ERR_INVALID_ARG;
     h->timeout_ns = timeout_ns;
+    return PURLIN_OK;
+}
+
+purlin_status_t purlin_plan_begin(purlin_handle_t h)
+{
+    if (!h || h->recording) return PURLIN_ERR_INVALID_ARG;
+    h->recording = true;
+    h->recorded = nullptr;
+    return PURLIN_OK;
+}
+
+purlin_status_t purlin_plan_end(purlin_handle_t h, purlin_plan_t* plan)
+{
+    if (plan) *plan = nullptr;
+    if (!h || !h->recording) return PURLIN_ERR_INVALID_ARG;
+    h->recording = false;
+    purlin_plan* rec = h->recorded;
+    h->recorded = nullptr;
+    if (!plan || !rec) {
+        delete rec;
+        return PURLIN_ERR_INVALID_ARG;
+    }
+    *plan = rec;
+    return PURLIN_OK;
+}
+
+purlin_status_t purlin_plan_launch(purlin_plan_t plan, purlin_stream_t stream)
+{
+    if (!plan) return PURLIN_ERR_INVALID_ARG;
+    DeviceGuard guard(plan->device);
+    if (!guard.ok) return PURLIN_ERR_CUDA;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t ce = cudaSuccess;
+    if (plan->kind == 1) {
+        ce = launch_kernel(plan->k, s);
+    } else if (plan->kind == 2) {
+        for (const CopyOp& c : plan->copies) {
+            ce = cudaMemcpyAsync(c.dst, c.src, c.bytes, cudaMemcpyDefault, s);
+            if (ce != cudaSuccess) break;
+        }
+    }
+    if (ce != cudaSuccess) return PURLIN_ERR_CUDA;
+    plan->h->last = plan->info;
+    return PURLIN_OK;
+}
+
+purlin_status_t purlin_plan_destroy(purlin_plan_t plan)
+{
+    delete plan;
     return PURLIN_OK;
 }
 

@@ -11,29 +11,54 @@ namespace purlin {
 // Element type codes (the values of purlin_dtype_t).
 enum : int { kF32 = 0, kBF16 = 1, kF16 = 2, kU8 = 3 };
 
+// ---- one kernel launch, fully planned --------------------------------------
+// The C-ABI layer builds a call's kernel parameters directly in `params`, the
+// kernel translation units fill in the function and its launch shape, and the
+// launch is then either made at once or kept in a plan and made many times.
+
+constexpr size_t kMaxLaunchParams = 8192;
+
+struct KernelLaunch {
+    const void* func = nullptr;
+    unsigned grid = 0;
+    unsigned block = 0;
+    size_t smem = 0;
+    bool pdl = false;          // programmatic stream serialization
+    bool cooperative = false;  // every CTA resident at once
+    size_t params_bytes = 0;
+    alignas(16) unsigned char params[kMaxLaunchParams];
+};
+
+// Launch k on `stream` (its parameter block passed by value).
+cudaError_t launch_kernel(const KernelLaunch& k, cudaStream_t stream);
+
+// Resident CTAs per SM of `kernel` at `threads` threads and no dynamic shared
+// memory, on the current device (occupancy API, cached without allocating; 1
+// if the query fails).
+int resident_ctas_of(const void* kernel, int threads);
+
 // ---- zero-staging Atom kernels (zs_kernels.cu) -----------------------------
+
+// Each *_select call fills k's function, block, dynamic shared memory and
+// parameter size for a parameter block already built in k.params; the caller
+// sets the grid and pdl.
 
 // Sum over ranks.  fan_all: write each result to every output (AllReduce),
 // else to the segment's destination (ReduceScatter).  small: one-warp CTAs, plan
 // built with kTileUnitsSmall; else kThreads-thread CTAs, kTileUnitsReduce.
-cudaError_t zs_reduce_launch(const ZsParams<kSegsSmall>& p, int dtype, int order, bool fan_all,
-                             bool small, int grid, cudaStream_t stream);
+void zs_reduce_select(KernelLaunch& k, int dtype, int order, bool fan_all, bool small);
 int zs_reduce_resident_ctas(int dtype, int order, bool fan_all, bool small);
 
 // Copy.  fan_all: every segment goes to every output (AllGather), else to the
-// segment's destination (AllToAll(V)).  small: one-warp CTAs, plan built with
-// kTileUnitsSmall; else kThreads-thread CTAs, kTileUnitsCopy.
-cudaError_t zs_copy_launch(const ZsParams<kSegsSmall>& p, bool fan_all, bool small, int grid,
-                           cudaStream_t stream);
-cudaError_t zs_copy_launch(const ZsParams<kSegsLarge>& p, bool fan_all, bool small, int grid,
-                           cudaStream_t stream);
+// segment's destination (AllToAll(V)).  large: ZsParams<kSegsLarge> (else
+// kSegsSmall).  small: one-warp CTAs, plan built with kTileUnitsSmall; else
+// kThreads-thread CTAs, kTileUnitsCopy.
+void zs_copy_select(KernelLaunch& k, bool large, bool fan_all, bool small);
 int zs_copy_resident_ctas(bool large, bool fan_all, bool small);
 
 // Copy through TMA bulk transfers (plan built with kTileUnitsBulk tiles).
-cudaError_t zs_copy_bulk_launch(const ZsParams<kSegsSmall>& p, bool fan_all, int grid,
-                                cudaStream_t stream);
-cudaError_t zs_copy_bulk_launch(const ZsParams<kSegsLarge>& p, bool fan_all, int grid,
-                                cudaStream_t stream);
+// Returns the CUDA error of the one-time shared-memory opt-in, if any.
+cudaError_t zs_copy_bulk_select(KernelLaunch& k, bool large, bool fan_all);
 int zs_copy_bulk_resident_ctas(bool large, bool fan_all);
 
 }  // namespace purlin

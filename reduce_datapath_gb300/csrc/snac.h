@@ -20,6 +20,7 @@
 
 #include <cuda_runtime.h>
 
+#include "internal.h"
 #include "plan.h"
 #include "purlin.h"
 
@@ -61,15 +62,18 @@ struct SnacLaunch {
     size_t chunk_bytes;
 };
 
-purlin_status_t snac_run(const SnacRequest& rq, const SnacConfig& cfg, cudaStream_t stream,
-                         SnacLaunch* launch);
+// Plan one staged call: the cooperative kernel, its launch shape and its
+// parameter block in k (k.grid = 0: nothing to launch).  Launch with
+// launch_kernel (internal.h), once or many times.
+purlin_status_t snac_plan(const SnacRequest& rq, const SnacConfig& cfg, KernelLaunch& k,
+                          SnacLaunch* launch);
 
-// Same as snac_run, with the kernel's parameter block on the caller's stack
-// instead of in thread-local storage (no memory is allocated).
+// Plan and launch at once, with the parameter block on the caller's stack (no
+// memory is allocated).
 purlin_status_t snac_run_on_stack(const SnacRequest& rq, const SnacConfig& cfg,
                                   cudaStream_t stream, SnacLaunch* launch);
 
-// Channels, chunk and depth that snac_run would use (for introspection/tests).
+// Channels, chunk and depth that snac_plan would choose.
 purlin_status_t snac_geometry(int R, Coll coll, const SnacConfig& cfg, int resident_per_sm,
                               size_t* chunk, int* depth, int* channels);
 

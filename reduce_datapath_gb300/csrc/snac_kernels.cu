@@ -501,10 +501,16 @@ purlin_status_t snac_geometry(int R, Coll coll, const SnacConfig& cfg, int resid
 
 namespace {
 
-purlin_status_t run_with(SnacParams& p, const SnacRequest& rq, const SnacConfig& cfg,
-                         cudaStream_t stream, SnacLaunch* launch)
+static_assert(sizeof(SnacParams) <= kMaxLaunchParams, "launch parameter block");
+
+// Plan one staged call into k: the kernel, its launch shape and its parameter
+// block (k.grid = 0: nothing to launch).
+purlin_status_t plan_into(KernelLaunch& k, const SnacRequest& rq, const SnacConfig& cfg,
+                          SnacLaunch* launch)
 {
+    SnacParams& p = *reinterpret_cast<SnacParams*>(k.params);
     std::memset(&p, 0, sizeof(p));
+    k.grid = 0;
     const bool reduce = rq.coll == Coll::ReduceScatter || rq.coll == Coll::AllReduce;
     uint32_t ntiles = 0;
     int nseg = layout_segments(rq.pieces, rq.npieces, rq.R, rq.in, rq.out, rq.esz, reduce,
@@ -513,10 +519,8 @@ purlin_status_t run_with(SnacParams& p, const SnacRequest& rq, const SnacConfig&
     if (nseg < 0) return PURLIN_ERR_UNSUPPORTED;
 
     SnacKernel kernel = kernel_for(rq.coll, rq.dtype, rq.order);
-    int resident = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&resident, kernel, kThreads, 0) !=
-            cudaSuccess || resident < 1)
-        return PURLIN_ERR_CUDA;
+    const int resident = resident_ctas_of(reinterpret_cast<const void*>(kernel), kThreads);
+    if (resident < 1) return PURLIN_ERR_CUDA;
     size_t chunk = 0;
     int depth = 0, nch = 0;
     purlin_status_t st = snac_geometry(rq.R, rq.coll, cfg, resident, &chunk, &depth, &nch);
@@ -557,36 +561,32 @@ purlin_status_t run_with(SnacParams& p, const SnacRequest& rq, const SnacConfig&
     p.inject = (uint32_t)cfg.inject_skip_notify;
 
     const int grid = nch * roles_of(rq.coll);
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
-    cudaLaunchConfig_t lc = {};
-    lc.gridDim = dim3((unsigned)grid);
-    lc.blockDim = dim3(kThreads);
-    lc.dynamicSmemBytes = 0;
-    lc.stream = stream;
-    lc.attrs = attr;
-    lc.numAttrs = 1;
-    cudaError_t ce = cudaLaunchKernelEx(&lc, kernel, p);
-    if (ce != cudaSuccess) return PURLIN_ERR_CUDA;
+    k.func = reinterpret_cast<const void*>(kernel);
+    k.grid = (unsigned)grid;
+    k.block = kThreads;
+    k.smem = 0;
+    k.pdl = false;
+    k.cooperative = true;  // every waiter's partner must be resident
+    k.params_bytes = sizeof(SnacParams);
     *launch = SnacLaunch{1, grid, kThreads, depth, nch, chunk};
     return PURLIN_OK;
 }
 
 }  // namespace
 
-purlin_status_t snac_run(const SnacRequest& rq, const SnacConfig& cfg, cudaStream_t stream,
-                         SnacLaunch* launch)
+purlin_status_t snac_plan(const SnacRequest& rq, const SnacConfig& cfg, KernelLaunch& k,
+                          SnacLaunch* launch)
 {
-    static thread_local SnacParams p;
-    return run_with(p, rq, cfg, stream, launch);
+    return plan_into(k, rq, cfg, launch);
 }
 
 purlin_status_t snac_run_on_stack(const SnacRequest& rq, const SnacConfig& cfg,
                                   cudaStream_t stream, SnacLaunch* launch)
 {
-    SnacParams p;
-    return run_with(p, rq, cfg, stream, launch);
+    KernelLaunch k;
+    purlin_status_t st = plan_into(k, rq, cfg, launch);
+    if (st != PURLIN_OK || k.grid == 0) return st;
+    return launch_kernel(k, stream) == cudaSuccess ? PURLIN_OK : PURLIN_ERR_CUDA;
 }
 
 }  // namespace purlin

@@ -1,402 +1,15 @@
-// zs_kernels.cu -- zero-staging ("ZS") Atom kernels for sm_103a.
-//
-// Page "Purlin: Separating Orchestration from the Datapath of Collectives",
-// Figure 10: "Purlin-ZS omits staging" when buffers are directly accessible.  On
-// one GPU every virtual rank's buffer is directly accessible, so the ZS kernels
-// read the sources and write the destinations in one pass:
-//   - zs_reduce: ReduceScatter(V) (one destination per segment) and the fused
-//     AllReduce of Figure 6 (each summed unit written to all R outputs);
-//   - zs_copy:   AllGather(V) (each unit written to all R outputs) and
-//     AllToAll(V) (one destination per segment).
-// Work is a flat space of tiles (plan.h) walked grid-stride; the host sizes the
-// grid (capi.cpp: several waves of CTAs, at most one per tile).  Each CTA finds
-// a tile's segment by binary search over the segments' first tiles, which sit
-// in the kernel's constant parameter bank.
-#include "atom.cuh"
-#include "internal.h"
-#include "purlin.h"
+// zs_kernels.cu -- host-side selection and launch of the zero-staging Atom
+// kernels (zs_kernels.cuh): which instantiation serves a call, its launch
+// shape, its residency, and the one launch routine every planned call goes
+// through (capi.cpp builds the parameter blocks).
+#include "zs_kernels.cuh"
 
 #include <mutex>
-#include <unordered_map>
 
 namespace purlin {
-
 namespace {
 
-template <int MAXSEG>
-__device__ __forceinline__ const Segment& segment_of(const ZsParams<MAXSEG>& p, uint32_t t)
-{
-    int lo = 0, hi = (int)p.nseg - 1;
-    while (lo < hi) {
-        int mid = (lo + hi + 1) >> 1;
-        if (p.seg[mid].tile0 <= t) lo = mid;
-        else hi = mid - 1;
-    }
-    return p.seg[lo];
-}
-
-// Programmatic dependent launch: the grid may have been scheduled before the
-// previous kernel on the stream finished; griddepcontrol.wait blocks until that
-// kernel has completed and its writes are visible (it returns at once when the
-// launch had no programmatic dependency).  Triggering dependents right after
-// lets the next collective's CTAs be scheduled while this one runs.
-__device__ __forceinline__ void pdl_enter()
-{
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
-// ------------------------------------------------------------------ reduce
-
-template <typename T, int ORDER, bool FAN_ALL, int BYTES>
-__device__ __forceinline__ void reduce_vector(const ZsParams<kSegsSmall>& p, const Segment& s,
-                                              uint64_t off, int R, uint64_t lpol, uint64_t spol)
-{
-    atom::Vec<BYTES> v[kMaxRanks];
-    // All R loads are issued before the first add: R independent requests in
-    // flight per thread.
-#pragma unroll
-    for (int r = 0; r < kMaxRanks; ++r)
-        if (r < R) atom::load(v[r], p.in[r] + s.src_off + off, lpol);
-    atom::Vec<BYTES> o;
-    atom::reduce_unit<T, ORDER, BYTES>(v, R, o);
-    if (FAN_ALL) {
-#pragma unroll
-        for (int r = 0; r < kMaxRanks; ++r)
-            if (r < R) atom::store(p.out[r] + s.dst_off + off, o, spol);
-    } else {
-        atom::store(p.out[s.dst] + s.dst_off + off, o, spol);
-    }
-}
-
-template <typename T, int ORDER, bool FAN_ALL>
-__device__ __forceinline__ void reduce_element(const ZsParams<kSegsSmall>& p, const Segment& s,
-                                               uint64_t off, int R)
-{
-    float v[kMaxRanks];
-#pragma unroll
-    for (int r = 0; r < kMaxRanks; ++r) v[r] = (r < R) ? T::load1(p.in[r] + s.src_off + off) : 0.0f;
-    float acc = atom::fold<ORDER>(v, R);
-    if (FAN_ALL) {
-#pragma unroll
-        for (int r = 0; r < kMaxRanks; ++r)
-            if (r < R) T::store1(p.out[r] + s.dst_off + off, acc);
-    } else {
-        T::store1(p.out[s.dst] + s.dst_off + off, acc);
-    }
-}
-
-// THREADS threads per CTA, one unit per thread per tile: kThreads for large
-// messages, one warp (kSmallThreads) for small ones.
-template <typename T, int ORDER, bool FAN_ALL, int THREADS>
-__global__ void __launch_bounds__(THREADS, THREADS == kThreads ? 2 : 16)
-zs_reduce_kernel(const __grid_constant__ ZsParams<kSegsSmall> p)
-{
-    pdl_enter();
-    const int R = (int)p.R;
-    const uint64_t lpol = atom::l2_policy(p.l2_load);
-    const uint64_t spol = atom::l2_policy(p.l2_store);
-    for (uint32_t t = blockIdx.x; t < p.ntiles; t += gridDim.x) {
-        const Segment& s = segment_of(p, t);
-        const int ul = s.unit_log2;
-        const uint64_t off = (uint64_t)(t - s.tile0) * tile_bytes(ul, THREADS) +
-                             ((uint64_t)threadIdx.x << ul);
-        if (off >= s.bytes) continue;
-        if (ul == 5) reduce_vector<T, ORDER, FAN_ALL, 32>(p, s, off, R, lpol, spol);
-        else if (ul == 4) reduce_vector<T, ORDER, FAN_ALL, 16>(p, s, off, R, lpol, spol);
-        else reduce_element<T, ORDER, FAN_ALL>(p, s, off, R);
-    }
-}
-
-// -------------------------------------------------------------------- copy
-
-using atom::Unit;
-using atom::load_unit;
-using atom::store_unit;
-
-template <int BYTES>
-__device__ __forceinline__ void load_hinted(Unit<BYTES>& u, const char* p, uint64_t pol)
-{
-    if constexpr (BYTES >= 16) atom::load(u.v, p, pol);
-    else load_unit<BYTES>(u, p);
-}
-
-template <int BYTES>
-__device__ __forceinline__ void store_hinted(char* p, const Unit<BYTES>& u, uint64_t pol)
-{
-    if constexpr (BYTES >= 16) atom::store(p, u.v, pol);
-    else store_unit<BYTES>(p, u);
-}
-
-// Atom::copy of one tile: UNROLL units per thread, each warp access
-// contiguous; every unit loaded once and stored to one or all R outputs.
-template <int BYTES, bool FAN_ALL, int THREADS, int UNROLL, int MAXSEG>
-__device__ __forceinline__ void copy_tile(const ZsParams<MAXSEG>& p, const Segment& s,
-                                          uint64_t base, uint64_t lpol, uint64_t spol)
-{
-    const uint64_t rem = s.bytes - base;
-    const char* src = p.in[s.src] + s.src_off + base;
-    Unit<BYTES> u[UNROLL];
-#pragma unroll
-    for (int k = 0; k < UNROLL; ++k) {
-        const uint64_t o = (uint64_t)(k * THREADS + threadIdx.x) * BYTES;
-        if (o < rem) load_hinted<BYTES>(u[k], src + o, lpol);
-    }
-#pragma unroll
-    for (int k = 0; k < UNROLL; ++k) {
-        const uint64_t o = (uint64_t)(k * THREADS + threadIdx.x) * BYTES;
-        if (o >= rem) continue;
-        if (FAN_ALL) {
-            for (int r = 0; r < (int)p.R; ++r) {
-                char* dst = p.out[r] + s.dst_off + base + o;
-                if (dst != src + o) store_hinted<BYTES>(dst, u[k], spol);  // in-place: skip
-            }
-        } else {
-            store_hinted<BYTES>(p.out[s.dst] + s.dst_off + base + o, u[k], spol);
-        }
-    }
-}
-
-// THREADS x UNROLL units per tile: kThreads x kUnrollCopy for large messages,
-// one warp with one unit per thread for small ones.
-template <bool FAN_ALL, int MAXSEG, int THREADS, int UNROLL>
-__global__ void __launch_bounds__(THREADS, THREADS == kThreads ? 2 : 16)
-zs_copy_kernel(const __grid_constant__ ZsParams<MAXSEG> p)
-{
-    pdl_enter();
-    const uint64_t lpol = atom::l2_policy(p.l2_load);
-    const uint64_t spol = atom::l2_policy(p.l2_store);
-    for (uint32_t t = blockIdx.x; t < p.ntiles; t += gridDim.x) {
-        const Segment& s = segment_of(p, t);
-        const int ul = s.unit_log2;
-        const uint64_t base = (uint64_t)(t - s.tile0) * tile_bytes(ul, THREADS * UNROLL);
-        switch (ul) {
-        case 5: copy_tile<32, FAN_ALL, THREADS, UNROLL>(p, s, base, lpol, spol); break;
-        case 4: copy_tile<16, FAN_ALL, THREADS, UNROLL>(p, s, base, lpol, spol); break;
-        case 3: copy_tile<8, FAN_ALL, THREADS, UNROLL>(p, s, base, lpol, spol); break;
-        case 2: copy_tile<4, FAN_ALL, THREADS, UNROLL>(p, s, base, lpol, spol); break;
-        case 1: copy_tile<2, FAN_ALL, THREADS, UNROLL>(p, s, base, lpol, spol); break;
-        default: copy_tile<1, FAN_ALL, THREADS, UNROLL>(p, s, base, lpol, spol); break;
-        }
-    }
-}
-
-// ------------------------------------------------------------ bulk copy
-// Atom::copy through the Tensor Memory Accelerator: lane 0 of a one-warp CTA
-// keeps a shared-memory ring of STAGES tiles busy -- cp.async.bulk
-// global->shared loads that complete on an mbarrier, then one cp.async.bulk
-// shared->global store per destination -- so a tile is read from HBM once and
-// written R times without per-thread store instructions.  Half of the ring
-// holds loads in flight ahead of the tile being stored, the other half tiles
-// whose stores are still reading shared memory.  Tiles whose streams are not
-// 16-byte aligned (unit < 16 B) are copied by the warp with ordinary accesses.
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p)
-{
-    return (uint32_t)__cvta_generic_to_shared(p);
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t* bar)
-{
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(bar)) : "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes)
-{
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
-                 ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile("{\n\t.reg .pred p;\n\t"
-                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-                 "selp.u32 %0, 1, 0, p;\n\t}"
-                 : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
-    return ok != 0;
-}
-
-__device__ __forceinline__ uint64_t global_ns()
-{
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-// Bounded wait for an mbarrier phase: at most ~2 s and 2^24 polls.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity)
-{
-    uint64_t start = 0;
-    for (uint32_t it = 0; it < (1u << 24); ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 255) == 255) {
-            const uint64_t t = global_ns();
-            if (start == 0) start = t;
-            else if (t - start > 2000000000ull) return false;
-        }
-    }
-    return false;
-}
-
-__device__ __forceinline__ void bulk_load(void* smem, const char* gmem, uint32_t bytes,
-                                          uint64_t* bar)
-{
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes"
-                 " [%0], [%1], %2, [%3];"
-                 ::"r"(smem_u32(smem)), "l"(gmem), "r"(bytes), "r"(smem_u32(bar)) : "memory");
-}
-
-__device__ __forceinline__ void bulk_store(char* gmem, const void* smem, uint32_t bytes)
-{
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
-                 ::"l"(gmem), "r"(smem_u32(smem)), "r"(bytes) : "memory");
-}
-
-__device__ __forceinline__ void bulk_commit()
-{
-    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-
-template <int N>
-__device__ __forceinline__ void bulk_wait_read_all_but()
-{
-    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
-}
-
-__device__ __forceinline__ void bulk_wait_all()
-{
-    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-}
-
-template <int B, bool FAN_ALL, int MAXSEG>
-__device__ __forceinline__ void warp_copy_tile(const ZsParams<MAXSEG>& p, const Segment& s,
-                                               uint64_t base, uint64_t len)
-{
-    const char* src = p.in[s.src] + s.src_off + base;
-    for (uint64_t o = (uint64_t)threadIdx.x * B; o < len; o += (uint64_t)kBulkThreads * B) {
-        Unit<B> u;
-        load_unit<B>(u, src + o);
-        if (FAN_ALL) {
-            for (int r = 0; r < (int)p.R; ++r) {
-                char* dst = p.out[r] + s.dst_off + base + o;
-                if (dst != src + o) store_unit<B>(dst, u);
-            }
-        } else {
-            store_unit<B>(p.out[s.dst] + s.dst_off + base + o, u);
-        }
-    }
-}
-
-template <bool FAN_ALL, int MAXSEG, int STAGES>
-__global__ void __launch_bounds__(kBulkThreads)
-zs_copy_bulk_kernel(const __grid_constant__ ZsParams<MAXSEG> p)
-{
-    extern __shared__ __align__(128) char ring[];   // STAGES x kBulkStageBytes
-    __shared__ __align__(8) uint64_t bar[STAGES];
-    const uint32_t G = gridDim.x;
-    pdl_enter();
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) mbar_init(&bar[s]);
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-
-        auto next_bulk = [&](uint32_t t) {
-            while (t < p.ntiles && segment_of(p, t).unit_log2 < 4) t += G;
-            return t;
-        };
-        auto tile_len = [&](uint32_t t, const Segment& s, uint64_t& base) {
-            const uint64_t tb = tile_bytes(s.unit_log2, kTileUnitsBulk);
-            base = (uint64_t)(t - s.tile0) * tb;
-            return (uint32_t)min(tb, s.bytes - base);
-        };
-        auto issue_load = [&](uint32_t t, uint32_t n) {
-            const Segment& s = segment_of(p, t);
-            uint64_t base;
-            const uint32_t len = tile_len(t, s, base);
-            const int st = (int)(n % STAGES);
-            mbar_expect_tx(&bar[st], len);
-            bulk_load(ring + (size_t)st * kBulkStageBytes, p.in[s.src] + s.src_off + base, len,
-                      &bar[st]);
-        };
-
-        constexpr int AHEAD = STAGES / 2;
-        uint32_t lt = next_bulk(blockIdx.x), stt = lt;
-        uint32_t nl = 0, ns = 0;
-        bool failed = false;
-        while (nl < AHEAD && lt < p.ntiles) {
-            issue_load(lt, nl++);
-            lt = next_bulk(lt + G);
-        }
-        while (stt < p.ntiles) {
-            const int st = (int)(ns % STAGES);
-            if (!mbar_wait(&bar[st], (ns / STAGES) & 1u)) { failed = true; break; }
-            const Segment& s = segment_of(p, stt);
-            uint64_t base;
-            const uint32_t len = tile_len(stt, s, base);
-            const char* stage = ring + (size_t)st * kBulkStageBytes;
-            if (FAN_ALL) {
-                const char* src = p.in[s.src] + s.src_off + base;
-                for (int r = 0; r < (int)p.R; ++r) {
-                    char* dst = p.out[r] + s.dst_off + base;
-                    if (dst != src) bulk_store(dst, stage, len);  // in-place block: skip
-                }
-            } else {
-                bulk_store(p.out[s.dst] + s.dst_off + base, stage, len);
-            }
-            bulk_commit();
-            ++ns;
-            stt = next_bulk(stt + G);
-            if (lt < p.ntiles) {
-                // the slot being refilled was last read by the stores of tile
-                // nl - STAGES: every store group but the newest STAGES - AHEAD
-                // must have finished reading shared memory
-                bulk_wait_read_all_but<STAGES - AHEAD>();
-                issue_load(lt, nl++);
-                lt = next_bulk(lt + G);
-            }
-        }
-        if (failed) {
-            atomicCAS(p.status, 0, (int)PURLIN_ERR_TIMEOUT);
-            // every load already issued must land before shared memory is released
-            for (uint32_t n = ns; n < nl; ++n) mbar_wait(&bar[n % STAGES], (n / STAGES) & 1u);
-        }
-        bulk_wait_all();
-    }
-    __syncwarp();
-
-    for (uint32_t t = blockIdx.x; t < p.ntiles; t += G) {
-        const Segment& s = segment_of(p, t);
-        if (s.unit_log2 >= 4) continue;
-        const uint64_t tb = tile_bytes(s.unit_log2, kTileUnitsBulk);
-        const uint64_t base = (uint64_t)(t - s.tile0) * tb;
-        const uint64_t len = min(tb, s.bytes - base);
-        switch (s.unit_log2) {
-        case 3: warp_copy_tile<8, FAN_ALL>(p, s, base, len); break;
-        case 2: warp_copy_tile<4, FAN_ALL>(p, s, base, len); break;
-        case 1: warp_copy_tile<2, FAN_ALL>(p, s, base, len); break;
-        default: warp_copy_tile<1, FAN_ALL>(p, s, base, len); break;
-        }
-    }
-}
-
 // ------------------------------------------------------------- dispatch
-
-template <typename P>
-cudaError_t launch(void (*kernel)(P), const P& params, int grid, int threads, cudaStream_t stream)
-{
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = params.pdl ? 1 : 0;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)grid);
-    cfg.blockDim = dim3((unsigned)threads);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = stream;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kernel, params);
-}
 
 using ReduceKernel = void (*)(ZsParams<kSegsSmall>);
 
@@ -432,31 +45,109 @@ void (*copy_kernel_for(bool fan_all, bool small))(ZsParams<MAXSEG>)
                    : zs_copy_kernel<false, MAXSEG, kThreads, kUnrollCopy>;
 }
 
-// Resident CTAs per SM of a kernel at `threads` threads (cached per device).
+const void* copy_kernel_any(bool large, bool fan_all, bool small)
+{
+    return large ? reinterpret_cast<const void*>(copy_kernel_for<kSegsLarge>(fan_all, small))
+                 : reinterpret_cast<const void*>(copy_kernel_for<kSegsSmall>(fan_all, small));
+}
+
+// Resident CTAs per SM of a kernel at `threads` threads, cached per device in a
+// fixed table (no heap allocation: the allocation-free AllReduce plans through
+// this too).  At least 1.
 int resident_ctas(const void* kernel, int threads)
 {
+    struct Entry { const void* kernel; int device; int threads; int n; };
     static std::mutex mu;
-    static std::unordered_map<uint64_t, int> cache;
+    static Entry cache[512];
+    static int used = 0;
     int dev = 0;
     cudaGetDevice(&dev);
-    uint64_t key = reinterpret_cast<uint64_t>(kernel) ^ ((uint64_t)dev << 56);
     std::lock_guard<std::mutex> lock(mu);
-    auto it = cache.find(key);
-    if (it != cache.end()) return it->second;
+    for (int i = 0; i < used; ++i)
+        if (cache[i].kernel == kernel && cache[i].device == dev && cache[i].threads == threads)
+            return cache[i].n;
     int n = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, 0) != cudaSuccess || n < 1)
         n = 1;
-    cache[key] = n;
+    if (used < 512) cache[used++] = Entry{kernel, dev, threads, n};
     return n;
+}
+
+constexpr int kBulkStages = 8;
+constexpr size_t kBulkSmem = (size_t)kBulkStages * kBulkStageBytes;
+
+// The bulk kernel's one-time shared-memory opt-in and residency, per device.
+template <bool FAN_ALL, int MAXSEG>
+cudaError_t bulk_setup(const void** func, int* resident_out)
+{
+    auto kernel = zs_copy_bulk_kernel<FAN_ALL, MAXSEG, kBulkStages>;
+    static std::mutex mu;
+    static bool ready[64] = {};
+    static int resident[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!ready[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)kBulkSmem);
+        if (e != cudaSuccess) return e;
+        int n = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, kBulkThreads, kBulkSmem);
+        if (e != cudaSuccess) return e;
+        resident[dev] = n > 0 ? n : 1;
+        ready[dev] = true;
+    }
+    if (func) *func = reinterpret_cast<const void*>(kernel);
+    if (resident_out) *resident_out = resident[dev];
+    return cudaSuccess;
+}
+
+cudaError_t bulk_setup_any(bool large, bool fan_all, const void** func, int* resident)
+{
+    if (large)
+        return fan_all ? bulk_setup<true, kSegsLarge>(func, resident)
+                       : bulk_setup<false, kSegsLarge>(func, resident);
+    return fan_all ? bulk_setup<true, kSegsSmall>(func, resident)
+                   : bulk_setup<false, kSegsSmall>(func, resident);
 }
 
 }  // namespace
 
-cudaError_t zs_reduce_launch(const ZsParams<kSegsSmall>& p, int dtype, int order, bool fan_all,
-                             bool small, int grid, cudaStream_t stream)
+int resident_ctas_of(const void* kernel, int threads)
 {
-    return launch(reduce_kernel_for(dtype, order, fan_all, small), p, grid,
-                  small ? kSmallThreads : kThreads, stream);
+    return resident_ctas(kernel, threads);
+}
+
+cudaError_t launch_kernel(const KernelLaunch& k, cudaStream_t stream)
+{
+    cudaLaunchAttribute attr[2];
+    unsigned n = 0;
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = k.pdl ? 1 : 0;
+    ++n;
+    if (k.cooperative) {
+        attr[n].id = cudaLaunchAttributeCooperative;
+        attr[n].val.cooperative = 1;
+        ++n;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(k.grid);
+    cfg.blockDim = dim3(k.block);
+    cfg.dynamicSmemBytes = k.smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    void* args[1] = {const_cast<unsigned char*>(k.params)};
+    return cudaLaunchKernelExC(&cfg, k.func, args);
+}
+
+void zs_reduce_select(KernelLaunch& k, int dtype, int order, bool fan_all, bool small)
+{
+    k.func = reinterpret_cast<const void*>(reduce_kernel_for(dtype, order, fan_all, small));
+    k.block = small ? kSmallThreads : kThreads;
+    k.smem = 0;
+    k.cooperative = false;
+    k.params_bytes = sizeof(ZsParams<kSegsSmall>);
 }
 
 int zs_reduce_resident_ctas(int dtype, int order, bool fan_all, bool small)
@@ -465,100 +156,36 @@ int zs_reduce_resident_ctas(int dtype, int order, bool fan_all, bool small)
                          small ? kSmallThreads : kThreads);
 }
 
-cudaError_t zs_copy_launch(const ZsParams<kSegsSmall>& p, bool fan_all, bool small, int grid,
-                           cudaStream_t stream)
+void zs_copy_select(KernelLaunch& k, bool large, bool fan_all, bool small)
 {
-    return launch(copy_kernel_for<kSegsSmall>(fan_all, small), p, grid,
-                  small ? kSmallThreads : kThreads, stream);
+    k.func = copy_kernel_any(large, fan_all, small);
+    k.block = small ? kSmallThreads : kThreads;
+    k.smem = 0;
+    k.cooperative = false;
+    k.params_bytes = large ? sizeof(ZsParams<kSegsLarge>) : sizeof(ZsParams<kSegsSmall>);
 }
 
-cudaError_t zs_copy_launch(const ZsParams<kSegsLarge>& p, bool fan_all, bool small, int grid,
-                           cudaStream_t stream)
+int zs_copy_resident_ctas(bool large, bool fan_all, bool small)
 {
-    return launch(copy_kernel_for<kSegsLarge>(fan_all, small), p, grid,
-                  small ? kSmallThreads : kThreads, stream);
+    return resident_ctas(copy_kernel_any(large, fan_all, small), small ? kSmallThreads : kThreads);
 }
 
-namespace {
-
-constexpr int kBulkStages = 8;
-
-template <bool FAN_ALL, int MAXSEG>
-cudaError_t bulk_launch_t(const ZsParams<MAXSEG>& p, int grid, cudaStream_t stream,
-                          int* resident_out)
+cudaError_t zs_copy_bulk_select(KernelLaunch& k, bool large, bool fan_all)
 {
-    auto kernel = zs_copy_bulk_kernel<FAN_ALL, MAXSEG, kBulkStages>;
-    const size_t smem = (size_t)kBulkStages * kBulkStageBytes;
-    static std::mutex mu;
-    static bool ready[64] = {};
-    static int resident[64] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    {
-        std::lock_guard<std::mutex> lock(mu);
-        if (!ready[dev]) {
-            cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 (int)smem);
-            if (e != cudaSuccess) return e;
-            int n = 0;
-            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, kBulkThreads, smem);
-            if (e != cudaSuccess) return e;
-            resident[dev] = n > 0 ? n : 1;
-            ready[dev] = true;
-        }
-    }
-    if (resident_out) {
-        *resident_out = resident[dev];
-        return cudaSuccess;
-    }
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = p.pdl ? 1 : 0;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)grid);
-    cfg.blockDim = dim3(kBulkThreads);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kernel, p);
-}
-
-}  // namespace
-
-cudaError_t zs_copy_bulk_launch(const ZsParams<kSegsSmall>& p, bool fan_all, int grid,
-                                cudaStream_t stream)
-{
-    return fan_all ? bulk_launch_t<true>(p, grid, stream, nullptr)
-                   : bulk_launch_t<false>(p, grid, stream, nullptr);
-}
-
-cudaError_t zs_copy_bulk_launch(const ZsParams<kSegsLarge>& p, bool fan_all, int grid,
-                                cudaStream_t stream)
-{
-    return fan_all ? bulk_launch_t<true>(p, grid, stream, nullptr)
-                   : bulk_launch_t<false>(p, grid, stream, nullptr);
+    cudaError_t e = bulk_setup_any(large, fan_all, &k.func, nullptr);
+    k.block = kBulkThreads;
+    k.smem = kBulkSmem;
+    k.cooperative = false;
+    k.params_bytes = large ? sizeof(ZsParams<kSegsLarge>) : sizeof(ZsParams<kSegsSmall>);
+    return e;
 }
 
 int zs_copy_bulk_resident_ctas(bool large, bool fan_all)
 {
     int n = 1;
-    cudaError_t e;
-    if (large) {
-        static const ZsParams<kSegsLarge> none{};
-        e = fan_all ? bulk_launch_t<true>(none, 0, nullptr, &n) : bulk_launch_t<false>(none, 0, nullptr, &n);
-    } else {
-        static const ZsParams<kSegsSmall> none{};
-        e = fan_all ? bulk_launch_t<true>(none, 0, nullptr, &n) : bulk_launch_t<false>(none, 0, nullptr, &n);
-    }
-    return e == cudaSuccess ? n : 1;
+    return bulk_setup_any(large, fan_all, nullptr, &n) == cudaSuccess ? n : 1;
 }
 
-int zs_copy_resident_ctas(bool large, bool fan_all, bool small)
-{
-    const void* k = large ? reinterpret_cast<const void*>(copy_kernel_for<kSegsLarge>(fan_all, small))
-                          : reinterpret_cast<const void*>(copy_kernel_for<kSegsSmall>(fan_all, small));
-    return resident_ctas(k, small ? kSmallThreads : kThreads);
-}
+static_assert(sizeof(ZsParams<kSegsLarge>) <= kMaxLaunchParams, "launch parameter block");
 
 }  // namespace purlin
