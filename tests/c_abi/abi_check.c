@@ -5,7 +5,8 @@
  *                    check that the segments cover every output byte once.
  *   abi_check gpu    create a handle for 4 ranks, AllReduce fp32 integer values
  *                    (sums are exact in any order) and compare with the sums
- *                    computed here; then ReduceScatter + AllGather must equal it.
+ *                    computed here; then ReduceScatter + AllGather must equal it;
+ *                    then the AllReduce kept as a plan and launched twice.
  * Exit status 0 on success.
  */
 #include <stdint.h>
@@ -94,6 +95,29 @@ static int gpu_check(void)
         cudaMemcpy(got, dout[r], N * sizeof(float), cudaMemcpyDeviceToHost);
         if (memcmp(got, exact, N * sizeof(float)) != 0) return 19;
     }
+    /* the AllReduce kept as a plan: recording enqueues nothing, each launch
+       gives the exact sums again */
+    purlin_plan_t plan = NULL;
+    for (int r = 0; r < R; ++r) cudaMemset(dout[r], 0, N * sizeof(float));
+    if (purlin_plan_begin(h) != PURLIN_OK ||
+        purlin_all_reduce(h, (const void* const*)din, dout, N, PURLIN_F32, PURLIN_OP_SUM, NULL) !=
+            PURLIN_OK ||
+        purlin_plan_end(h, &plan) != PURLIN_OK || plan == NULL)
+        return 21;
+    if (cudaDeviceSynchronize() != cudaSuccess) return 22;
+    cudaMemcpy(got, dout[0], N * sizeof(float), cudaMemcpyDeviceToHost);
+    for (int i = 0; i < N; ++i)
+        if (got[i] != 0.0f) return 23;
+    for (int rep = 0; rep < 2; ++rep) {
+        if (purlin_plan_launch(plan, NULL) != PURLIN_OK) return 24;
+        if (cudaDeviceSynchronize() != cudaSuccess || purlin_query_status(h) != PURLIN_OK)
+            return 25;
+        for (int r = 0; r < R; ++r) {
+            cudaMemcpy(got, dout[r], N * sizeof(float), cudaMemcpyDeviceToHost);
+            if (memcmp(got, exact, N * sizeof(float)) != 0) return 26;
+        }
+    }
+    if (purlin_plan_destroy(plan) != PURLIN_OK) return 27;
     if (purlin_destroy(h) != PURLIN_OK) return 20;
     for (int r = 0; r < R; ++r) {
         cudaFree(din[r]);
