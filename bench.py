@@ -48,7 +48,7 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["purlin", "reference"], default="purlin")
-    ap.add_argument("--variant", choices=["zs", "staged"], default="zs")
+    ap.add_argument("--variant", choices=["zs", "staged", "staged_y"], default="zs")
     ap.add_argument("--chunk", type=int, default=0, help="SNAC chunk bytes (0 = auto)")
     ap.add_argument("--depth", type=int, default=0, help="SNAC ring depth (0 = auto)")
     ap.add_argument("--ctas", type=int, default=0, help="CTAs / channels (0 = auto)")
@@ -397,7 +397,8 @@ def bench_purlin(args):
     peak, peak_kind = measured_peaks()
     stream = torch.cuda.Stream(device=dev)
     h = rd.purlin_create(R, args.staging, local)
-    variant = rd.VARIANT_ZS if args.variant == "zs" else rd.VARIANT_STAGED
+    variant = {"zs": rd.VARIANT_ZS, "staged": rd.VARIANT_STAGED,
+               "staged_y": rd.VARIANT_STAGED_Y}[args.variant]
     rd.purlin_set_policy(h, args.chunk, args.depth, args.ctas, variant)
 
     x = workloads.rank_buffers(WORKLOAD, R, ELEMS_PER_RANK, "bf16", device=dev)
@@ -623,24 +624,34 @@ def _events_us(torch, stream, fn, iters):
 
 
 def staged_step(rd, torch, h, rs, ag, stream, step_b, peak):
-    """The benchmark step (RS then AG) through SNAC staging (default policy)."""
-    rd.purlin_set_policy(h, 0, 0, 0, rd.VARIANT_STAGED)
-    try:
-        for _ in range(3):
-            rs()
-            ag()
-        torch.cuda.synchronize()
-        rs_us = _events_us(torch, stream, rs, 20)
-        ag_us = _events_us(torch, stream, ag, 20)
-        info = rd.purlin_last_launch(h)
-        if rd.purlin_query_status(h) != rd.OK:
-            raise RuntimeError("staged step: device status not ok")
-    finally:
-        rd.purlin_set_policy(h, 0, 0, 0, rd.VARIANT_ZS)
-    us = rs_us + ag_us
-    return {"us": us, "gbs": step_b / (us / 1e6) / 1e9, "frac_of_peak": step_b / (us / 1e6) / 1e9 / peak,
-            "reduce_scatter_us": rs_us, "all_gather_us": ag_us, "chunk_bytes": info["chunk_bytes"],
-            "depth": info["depth"], "grid": info["grid"]}
+    """The benchmark step (RS then AG) through SNAC staging (default policy):
+    sums staging the R input chunks (the top-level figures) and, under
+    `staged_y`, sums staging the reduced chunk."""
+    def one(variant):
+        rd.purlin_set_policy(h, 0, 0, 0, variant)
+        try:
+            for _ in range(3):
+                rs()
+                ag()
+            torch.cuda.synchronize()
+            rs_us = _events_us(torch, stream, rs, 20)
+            rs_info = rd.purlin_last_launch(h)
+            ag_us = _events_us(torch, stream, ag, 20)
+            info = rd.purlin_last_launch(h)
+            if rd.purlin_query_status(h) != rd.OK:
+                raise RuntimeError("staged step: device status not ok")
+        finally:
+            rd.purlin_set_policy(h, 0, 0, 0, rd.VARIANT_ZS)
+        us = rs_us + ag_us
+        return {"us": us, "gbs": step_b / (us / 1e6) / 1e9,
+                "frac_of_peak": step_b / (us / 1e6) / 1e9 / peak,
+                "reduce_scatter_us": rs_us, "all_gather_us": ag_us,
+                "reduce_scatter_chunk_bytes": rs_info["chunk_bytes"],
+                "chunk_bytes": info["chunk_bytes"], "depth": info["depth"], "grid": info["grid"]}
+
+    out = one(rd.VARIANT_STAGED)
+    out["staged_y"] = one(rd.VARIANT_STAGED_Y)
+    return out
 
 
 def cta_study(rd, torch, h, rs, ag, stream, coll_b, peak):
@@ -836,8 +847,10 @@ def allreduce_sweep(rd, torch, dev, stream, peak):
             # inputs + outputs that fit in L2 stay there across repeated launches,
             # so their GB/s is not an HBM figure (it can exceed the HBM peak)
             row = {"bytes_per_rank": nbytes, "fits_in_l2": 2 * R * nbytes <= l2}
-            runs = [("zs", rd.VARIANT_ZS, 0), ("snac", rd.VARIANT_STAGED, 0)] + \
-                [(f"snac_chunk_{c >> 10}KiB", rd.VARIANT_STAGED, c) for c in workloads.SWEEP_CHUNKS]
+            runs = [("zs", rd.VARIANT_ZS, 0), ("snac", rd.VARIANT_STAGED, 0),
+                    ("snac_y", rd.VARIANT_STAGED_Y, 0)] + \
+                [(f"snac_chunk_{c >> 10}KiB", rd.VARIANT_STAGED, c) for c in workloads.SWEEP_CHUNKS] + \
+                [(f"snac_y_chunk_{c >> 10}KiB", rd.VARIANT_STAGED_Y, c) for c in workloads.SWEEP_CHUNKS]
             for name, variant, chunk in runs:
                 rd.purlin_set_policy(h, chunk, 0, 0, variant)
                 fn = lambda: rd.purlin_all_reduce(h, x, o, n, "bf16", stream=stream)
@@ -855,10 +868,10 @@ def allreduce_sweep(rd, torch, dev, stream, peak):
                              "frac_of_peak": round(gbs / peak, 3),
                              "timing": "cuda graph" if graph_us is not None else "events",
                              "us_host_launched": round(host_us, 2)}
-                if variant == rd.VARIANT_STAGED:
+                if variant != rd.VARIANT_ZS:
                     info = rd.purlin_last_launch(h)
                     row[name]["chunk_bytes"] = info["chunk_bytes"]
-                    row[name]["channels"] = info["grid"] // 3
+                    row[name]["channels"] = info["grid"] // (3 if variant == rd.VARIANT_STAGED else 2)
             if row["fits_in_l2"]:
                 # after both warm timings: the flush leaves L2 full of dirty lines
                 for name, variant in (("zs", rd.VARIANT_ZS), ("snac", rd.VARIANT_STAGED)):
@@ -867,8 +880,9 @@ def allreduce_sweep(rd, torch, dev, stream, peak):
                     cold = _cold_l2_us(torch, stream, fn, flush)
                     row[name]["us_cold_l2"] = round(cold, 2)
                     row[name]["gbs_cold_l2"] = round(2 * R * nbytes / (cold / 1e6) / 1e9, 1)
-            chunked = {k: v for k, v in row.items() if k.startswith("snac_chunk_")}
-            row["snac_best_chunk"] = min(chunked, key=lambda k: chunked[k]["us"])
+            for prefix in ("snac_chunk_", "snac_y_chunk_"):
+                chunked = {k: v for k, v in row.items() if k.startswith(prefix)}
+                row[prefix.replace("chunk_", "best_chunk")] = min(chunked, key=lambda k: chunked[k]["us"])
             out.append(row)
             del x, o
         if rd.purlin_query_status(h) != rd.OK:
@@ -1022,7 +1036,8 @@ def bench_only(args):
     n = args.bytes_per_rank // 2
     c = n // R
     h = rd.purlin_create(R, args.staging, 0)
-    variant = rd.VARIANT_ZS if args.variant == "zs" else rd.VARIANT_STAGED
+    variant = {"zs": rd.VARIANT_ZS, "staged": rd.VARIANT_STAGED,
+               "staged_y": rd.VARIANT_STAGED_Y}[args.variant]
     rd.purlin_set_policy(h, args.chunk, args.depth, args.ctas, variant)
     rd.purlin_set_atom(h, {"auto": rd.ATOM_AUTO, "vector": rd.ATOM_VECTOR, "bulk": rd.ATOM_BULK,
                            "copy_engine": rd.ATOM_COPY_ENGINE}[args.atom])

@@ -84,9 +84,15 @@ typedef enum {
     PURLIN_VARIANT_AUTO = 0,    /* library's choice                               */
     PURLIN_VARIANT_ZS = 1,      /* zero staging: kernels read the sources directly
                                    (Figure 10, "Purlin-ZS omits staging")          */
-    PURLIN_VARIANT_STAGED = 2   /* SNAC: producers stage chunks into the handle's
+    PURLIN_VARIANT_STAGED = 2,  /* SNAC: producers stage chunks into the handle's
                                    staging ring, notify through flags, consumers
-                                   consume (abstract; Figure 6)                   */
+                                   consume (abstract; Figure 6).  Sums stage the R
+                                   input chunks and the consumer reduces them      */
+    PURLIN_VARIANT_STAGED_Y = 3 /* SNAC as above, but for sums the producer reduces
+                                   the R input chunks and stages the reduced chunk
+                                   y, which the consumer copies to its destination
+                                   (ReduceScatter) or to all R outputs (AllReduce);
+                                   copies are staged as with PURLIN_VARIANT_STAGED */
 } purlin_variant_t;
 
 typedef enum {

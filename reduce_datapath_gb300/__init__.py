@@ -32,7 +32,7 @@ ELEM_BYTES = {F32: 4, BF16: 2, F16: 2, U8: 1}
 # purlin_op_t
 OP_COPY, OP_SUM = 0, 1
 # purlin_variant_t
-VARIANT_AUTO, VARIANT_ZS, VARIANT_STAGED = 0, 1, 2
+VARIANT_AUTO, VARIANT_ZS, VARIANT_STAGED, VARIANT_STAGED_Y = 0, 1, 2, 3
 # purlin_order_t
 ORDER_FIXED, ORDER_TREE = 0, 1
 # purlin_atom_t

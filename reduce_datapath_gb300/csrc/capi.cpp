@@ -309,7 +309,7 @@ int zs_grid(const purlin_handle* h, uint32_t ntiles, int resident, long waves = 
 
 bool wants_staged(const purlin_handle* h)
 {
-    return h->variant == PURLIN_VARIANT_STAGED;
+    return h->variant == PURLIN_VARIANT_STAGED || h->variant == PURLIN_VARIANT_STAGED_Y;
 }
 
 purlin_status_t run(purlin_handle_t h, Coll coll, const void* const in_[], void* const out_[],
@@ -372,6 +372,7 @@ purlin_status_t run(purlin_handle_t h, Coll coll, const void* const in_[], void*
         rq.esz = esz;
         rq.pieces = pieces;
         rq.npieces = np;
+        rq.stage_y = h->variant == PURLIN_VARIANT_STAGED_Y;
         for (int r = 0; r < R; ++r) { rq.in[r] = in[r]; rq.out[r] = out[r]; }
         SnacConfig cfg{};
         cfg.staging = h->staging;
@@ -390,7 +391,7 @@ purlin_status_t run(purlin_handle_t h, Coll coll, const void* const in_[], void*
         if (ss != PURLIN_OK) return ss;
         h->inject = 0;
         kind = k.grid > 0 ? 1 : 0;
-        info.variant = PURLIN_VARIANT_STAGED;
+        info.variant = h->variant;
         info.kernels = sl.kernels;
         info.grid = sl.grid;
         info.block = sl.block;
@@ -670,7 +671,7 @@ purlin_status_t purlin_set_policy(purlin_handle_t h, size_t chunk_bytes, int dep
 {
     if (!h) return PURLIN_ERR_INVALID_ARG;
     if (chunk_bytes % 16 || depth < 0 || depth > 8 || ctas < 0 || ctas > 65535 ||
-        variant < PURLIN_VARIANT_AUTO || variant > PURLIN_VARIANT_STAGED)
+        variant < PURLIN_VARIANT_AUTO || variant > PURLIN_VARIANT_STAGED_Y)
         return PURLIN_ERR_INVALID_ARG;
     h->chunk_bytes = chunk_bytes;
     h->depth = depth;

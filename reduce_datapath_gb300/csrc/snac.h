@@ -36,6 +36,7 @@ struct SnacRequest {
     int npieces;
     uint64_t in[kMaxRanks];
     uint64_t out[kMaxRanks];
+    bool stage_y;  // sums: the producer reduces and stages the reduced chunk
 };
 
 struct SnacConfig {
@@ -74,7 +75,8 @@ purlin_status_t snac_run_on_stack(const SnacRequest& rq, const SnacConfig& cfg,
                                   cudaStream_t stream, SnacLaunch* launch);
 
 // Channels, chunk and depth that snac_plan would choose.
-purlin_status_t snac_geometry(int R, Coll coll, const SnacConfig& cfg, int resident_per_sm,
-                              size_t* chunk, int* depth, int* channels);
+purlin_status_t snac_geometry(int R, Coll coll, bool stage_y, const SnacConfig& cfg,
+                              int resident_per_sm, uint64_t total_bytes, size_t* chunk,
+                              int* depth, int* channels);
 
 }  // namespace purlin

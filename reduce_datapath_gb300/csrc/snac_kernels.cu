@@ -43,7 +43,10 @@ namespace purlin {
 
 namespace {
 
-enum Kind : int { kRS = 0, kAG = 1, kAR = 2, kA2A = 3 };
+// kRS / kAR stage the R input chunks of a step and the consumer reduces them;
+// kRSY / kARY reduce in the producer and stage the reduced chunk y, which the
+// consumer copies to its destination (kRSY) or to all R outputs (kARY).
+enum Kind : int { kRS = 0, kAG = 1, kAR = 2, kA2A = 3, kRSY = 4, kARY = 5 };
 enum : int { kReady = 0, kFree = 1, kYReady = 2, kYFree = 3, kFlagsPerSlot = 4 };
 
 // Default chunk per rank per step, measured best on GB300 at 64 MiB per rank,
@@ -51,8 +54,12 @@ enum : int { kReady = 0, kFree = 1, kYReady = 2, kYFree = 3, kFlagsPerSlot = 4 }
 // channels of small chunks (AllReduce 3468 GB/s at 16 KiB vs 2102 at 64 KiB);
 // copies stage one part per slot and favour larger chunks (AllToAllV 4029 GB/s
 // at 128 KiB vs 1414 at 16 KiB; AllGather 3561 at 256 KiB vs 3125 at 16 KiB).
-size_t default_chunk(Coll coll)
+size_t default_chunk(Coll coll, bool stage_y)
 {
+    // one part per slot, as for copies; measured at 64 MiB per rank, R = 8,
+    // depth 2: AllReduce 211.7 us at 64 KiB (258.9 at 256 KiB), ReduceScatter
+    // 129.6 us at 128 KiB (171.0 at 16 KiB)
+    if (stage_y) return coll == Coll::ReduceScatter ? 128 * 1024 : 64 * 1024;
     switch (coll) {
     case Coll::AllGather: return 256 * 1024;
     case Coll::AllToAllV: return 128 * 1024;
@@ -60,7 +67,8 @@ size_t default_chunk(Coll coll)
     }
 }
 constexpr int kDefaultDepth = 2;
-constexpr int kMaxChannels = 128;
+constexpr int kMaxChannels = 256;
+constexpr size_t kMinAutoChunk = 1024;
 
 struct SnacParams {
     const char* in[kMaxRanks];
@@ -313,12 +321,54 @@ __device__ void cta_reduce(const SnacParams& p, int unit_log2, char* dst, const 
     else cta_reduce_elem<T, ORDER>(p, dst, staged, len);
 }
 
+// STAGE of a reduced chunk: Atom::reduce over the sources' chunk, written to
+// the slot (all R loads of a unit in flight before the fold).
+template <typename T, int ORDER, int B>
+__device__ __forceinline__ void cta_reduce_src_vec(const SnacParams& p, char* dst,
+                                                   uint64_t src_off, uint64_t len, uint64_t lpol,
+                                                   uint64_t spol)
+{
+    const int R = (int)p.R;
+    for (uint64_t o = (uint64_t)threadIdx.x * B; o < len; o += (uint64_t)kThreads * B) {
+        atom::Vec<B> v[kMaxRanks];
+#pragma unroll
+        for (int r = 0; r < kMaxRanks; ++r)
+            if (r < R) atom::load(v[r], p.in[r] + src_off + o, lpol);
+        atom::Vec<B> out;
+        atom::reduce_unit<T, ORDER, B>(v, R, out);
+        atom::store(dst + o, out, spol);
+    }
+}
+
+template <typename T, int ORDER>
+__device__ __forceinline__ void cta_reduce_src_elem(const SnacParams& p, char* dst,
+                                                    uint64_t src_off, uint64_t len)
+{
+    const int R = (int)p.R;
+    for (uint64_t o = (uint64_t)threadIdx.x * T::kBytes; o < len; o += (uint64_t)kThreads * T::kBytes) {
+        float v[kMaxRanks];
+#pragma unroll
+        for (int r = 0; r < kMaxRanks; ++r) v[r] = (r < R) ? T::load1(p.in[r] + src_off + o) : 0.0f;
+        T::store1(dst + o, atom::fold<ORDER>(v, R));
+    }
+}
+
+template <typename T, int ORDER>
+__device__ void cta_reduce_src(const SnacParams& p, int unit_log2, char* dst, uint64_t src_off,
+                               uint64_t len, uint64_t lpol, uint64_t spol)
+{
+    if (unit_log2 == 5) cta_reduce_src_vec<T, ORDER, 32>(p, dst, src_off, len, lpol, spol);
+    else if (unit_log2 == 4) cta_reduce_src_vec<T, ORDER, 16>(p, dst, src_off, len, lpol, spol);
+    else cta_reduce_src_elem<T, ORDER>(p, dst, src_off, len);
+}
+
 // ------------------------------------------------------------------ roles
 
-template <int KIND>
+template <typename T, int ORDER, int KIND>
 __device__ void producer(const SnacParams& p, uint32_t ch, uint64_t epoch)
 {
     const bool reduce = KIND == kRS || KIND == kAR;
+    const bool reduce_here = KIND == kRSY || KIND == kARY;
     // Sources are read exactly once: their lines go first, the ring stays.
     const uint64_t lpol = atom::l2_policy(kL2EvictFirst);
     const uint64_t spol = atom::l2_policy(kL2Normal);
@@ -333,6 +383,8 @@ __device__ void producer(const SnacParams& p, uint32_t ch, uint64_t epoch)
         char* staged = slot_data(p, ch, slot);
         if (reduce) {
             cta_stage_any(p, s.unit_log2, staged, s.src_off + off, len, lpol);
+        } else if (reduce_here) {
+            cta_reduce_src<T, ORDER>(p, s.unit_log2, staged, s.src_off + off, len, lpol, spol);
         } else {
             cta_copy_any<false, false>(p, s.unit_log2, staged, 0, p.in[s.src] + s.src_off + off,
                                        len, 0, lpol, spol);
@@ -350,8 +402,8 @@ __device__ void consumer(const SnacParams& p, uint32_t ch, uint64_t epoch)
     // ReduceScatter's outputs stay at normal priority (a following AllGather
     // reads them), and an AllReduce's consumer writes into the ring's y part.
     const uint64_t lpol = atom::l2_policy(kL2Normal);
-    const uint64_t spol =
-        atom::l2_policy((KIND == kA2A || KIND == kAG) ? kL2EvictFirst : kL2Normal);
+    const uint64_t spol = atom::l2_policy(
+        (KIND == kA2A || KIND == kAG || KIND == kARY) ? kL2EvictFirst : kL2Normal);
     uint32_t n = 0;
     for (uint32_t i = ch; i < p.nsteps; i += p.nch, ++n) {
         const uint32_t slot = n % p.depth;
@@ -370,6 +422,11 @@ __device__ void consumer(const SnacParams& p, uint32_t ch, uint64_t epoch)
         } else if (KIND == kAG) {
             cta_copy_any<true, true>(p, s.unit_log2, nullptr, s.dst_off + off, staged, len,
                                      (uintptr_t)(p.in[s.src] + s.src_off + off), lpol, spol);
+        } else if (KIND == kARY) {
+            // In-place AllReduce (out[r] == in[r]): this step's input range was
+            // read by the producer before the ready tag was published.
+            cta_copy_any<true, true>(p, s.unit_log2, nullptr, s.dst_off + off, staged, len, 0,
+                                     lpol, spol);
         } else {
             cta_copy_any<true, false>(p, s.unit_log2, p.out[s.dst] + s.dst_off + off, 0, staged,
                                       len, 0, lpol, spol);
@@ -413,7 +470,7 @@ __global__ void __launch_bounds__(kThreads, 2) snac_kernel(const __grid_constant
     const uint64_t epoch = epoch_s;
     const uint32_t role = blockIdx.x / p.nch;
     const uint32_t ch = blockIdx.x % p.nch;
-    if (role == 0) producer<KIND>(p, ch, epoch);
+    if (role == 0) producer<T, ORDER, KIND>(p, ch, epoch);
     else if (role == 1) consumer<T, ORDER, KIND>(p, ch, epoch);
     else if (KIND == kAR) gatherer(p, ch, epoch);
     // Whatever path a role left by (done, or an error seen), the last CTA to
@@ -447,17 +504,17 @@ SnacKernel pick_dtype(int dtype, int order)
     return pick_order<atom::F16, KIND>(order);
 }
 
-SnacKernel kernel_for(Coll coll, int dtype, int order)
+SnacKernel kernel_for(Coll coll, int dtype, int order, bool stage_y)
 {
     switch (coll) {
-    case Coll::ReduceScatter: return pick_dtype<kRS>(dtype, order);
-    case Coll::AllReduce: return pick_dtype<kAR>(dtype, order);
+    case Coll::ReduceScatter: return stage_y ? pick_dtype<kRSY>(dtype, order) : pick_dtype<kRS>(dtype, order);
+    case Coll::AllReduce: return stage_y ? pick_dtype<kARY>(dtype, order) : pick_dtype<kAR>(dtype, order);
     case Coll::AllGather: return snac_kernel<atom::F32, 0, kAG>;
     default: return snac_kernel<atom::F32, 0, kA2A>;
     }
 }
 
-int roles_of(Coll coll) { return coll == Coll::AllReduce ? 3 : 2; }
+int roles_of(Coll coll, bool stage_y) { return coll == Coll::AllReduce && !stage_y ? 3 : 2; }
 
 // Widest access of the staged kernels (tuning knob for measurements only).
 int snac_unit_log2()
@@ -469,8 +526,9 @@ int snac_unit_log2()
     return u;
 }
 
-int sub_slots(Coll coll, int R)
+int sub_slots(Coll coll, int R, bool stage_y)
 {
+    if (stage_y) return 1;
     if (coll == Coll::AllReduce) return R + 1;
     if (coll == Coll::ReduceScatter) return R;
     return 1;
@@ -478,18 +536,28 @@ int sub_slots(Coll coll, int R)
 
 }  // namespace
 
-purlin_status_t snac_geometry(int R, Coll coll, const SnacConfig& cfg, int resident_per_sm,
-                              size_t* chunk_out, int* depth_out, int* channels_out)
+purlin_status_t snac_geometry(int R, Coll coll, bool stage_y, const SnacConfig& cfg,
+                              int resident_per_sm, uint64_t total_bytes, size_t* chunk_out,
+                              int* depth_out, int* channels_out)
 {
-    size_t chunk = cfg.chunk_bytes ? cfg.chunk_bytes : default_chunk(coll);
+    const long resident_channels = (long)resident_per_sm * cfg.sms / roles_of(coll, stage_y);
+    size_t chunk = cfg.chunk_bytes;
+    if (!chunk) {
+        // the measured default, but small enough that a short message still
+        // spreads over every channel the GPU can hold (at least 1 KiB)
+        const long target = std::max<long>(1, std::min<long>(resident_channels, kMaxChannels));
+        const uint64_t spread = (total_bytes + (uint64_t)target - 1) / (uint64_t)target;
+        chunk = std::min<size_t>(default_chunk(coll, stage_y),
+                                 std::max<size_t>(kMinAutoChunk, (size_t)spread));
+    }
     chunk = std::max<size_t>(256, (chunk + 255) & ~(size_t)255);
     const int depth = cfg.depth ? cfg.depth : kDefaultDepth;
-    const size_t slot = (size_t)sub_slots(coll, R) * chunk;
+    const size_t slot = (size_t)sub_slots(coll, R, stage_y) * chunk;
     const size_t ring = (size_t)depth * slot;
     const long by_ring = ring ? (long)(cfg.staging_bytes / ring) : 0;
     // the last two flag words hold the epoch and the completion counter
     const long by_flags = (long)((cfg.flag_words - 2) / ((size_t)depth * kFlagsPerSlot));
-    const long by_residency = (long)resident_per_sm * cfg.sms / roles_of(coll);
+    const long by_residency = resident_channels;
     long nch = cfg.channels ? cfg.channels : kMaxChannels;
     nch = std::min({nch, by_ring, by_flags, by_residency});
     if (nch < 1) return PURLIN_ERR_UNSUPPORTED;  // ring too small for this chunk/depth
@@ -518,12 +586,15 @@ purlin_status_t plan_into(KernelLaunch& k, const SnacRequest& rq, const SnacConf
                                kSegsLarge, &ntiles);
     if (nseg < 0) return PURLIN_ERR_UNSUPPORTED;
 
-    SnacKernel kernel = kernel_for(rq.coll, rq.dtype, rq.order);
+    SnacKernel kernel = kernel_for(rq.coll, rq.dtype, rq.order, rq.stage_y);
     const int resident = resident_ctas_of(reinterpret_cast<const void*>(kernel), kThreads);
     if (resident < 1) return PURLIN_ERR_CUDA;
     size_t chunk = 0;
     int depth = 0, nch = 0;
-    purlin_status_t st = snac_geometry(rq.R, rq.coll, cfg, resident, &chunk, &depth, &nch);
+    uint64_t total_bytes = 0;
+    for (int i = 0; i < nseg; ++i) total_bytes += p.seg[i].bytes;
+    purlin_status_t st = snac_geometry(rq.R, rq.coll, rq.stage_y, cfg, resident, total_bytes,
+                                       &chunk, &depth, &nch);
     if (st != PURLIN_OK) return st;
 
     // Steps: every segment cut into chunks of `chunk` bytes.
@@ -551,7 +622,7 @@ purlin_status_t plan_into(KernelLaunch& k, const SnacRequest& rq, const SnacConf
     p.timeout_ns = cfg.timeout_ns;
     p.max_spins = cfg.timeout_ns / 64 + 65536;
     p.chunk = chunk;
-    p.slot_stride = (uint64_t)sub_slots(rq.coll, rq.R) * chunk;
+    p.slot_stride = (uint64_t)sub_slots(rq.coll, rq.R, rq.stage_y) * chunk;
     p.chan_stride = (uint64_t)depth * p.slot_stride;
     p.R = (uint32_t)rq.R;
     p.nch = (uint32_t)nch;
@@ -560,7 +631,7 @@ purlin_status_t plan_into(KernelLaunch& k, const SnacRequest& rq, const SnacConf
     p.nsteps = (uint32_t)steps;
     p.inject = (uint32_t)cfg.inject_skip_notify;
 
-    const int grid = nch * roles_of(rq.coll);
+    const int grid = nch * roles_of(rq.coll, rq.stage_y);
     k.func = reinterpret_cast<const void*>(kernel);
     k.grid = (unsigned)grid;
     k.block = kThreads;

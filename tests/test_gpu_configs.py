@@ -59,7 +59,7 @@ def _sample_idx(n, k, seed):
 
 # --------------------------------------------------------------- allreduce_r2_f32
 
-@pytest.mark.parametrize("variant", [rd.VARIANT_ZS, rd.VARIANT_STAGED])
+@pytest.mark.parametrize("variant", [rd.VARIANT_ZS, rd.VARIANT_STAGED, rd.VARIANT_STAGED_Y])
 def test_allreduce_r2_f32_integers(variant):
     R, n = 2, 4096
     x = workloads.rank_buffers("allreduce_r2_f32", R, n, "f32", device="cuda", values="int")
@@ -87,7 +87,7 @@ def test_allreduce_r2_f32_integers(variant):
 
 # -------------------------------------------------------------- rs_ag_r8_bf16
 
-@pytest.mark.parametrize("variant", [rd.VARIANT_ZS, rd.VARIANT_STAGED])
+@pytest.mark.parametrize("variant", [rd.VARIANT_ZS, rd.VARIANT_STAGED, rd.VARIANT_STAGED_Y])
 def test_rs_ag_r8_bf16_64MiB_full(variant):
     R, n = 8, 64 * MiB // 2
     c = n // R
@@ -131,7 +131,8 @@ def _check_allreduce(x, out, n, sampled, seed):
 
 SWEEP = [(b, v, ch) for b in workloads.SWEEP_BYTES for (v, ch) in
          [(rd.VARIANT_ZS, 0), (rd.VARIANT_STAGED, 64 * 1024), (rd.VARIANT_STAGED, 256 * 1024),
-          (rd.VARIANT_STAGED, 1 * MiB), (rd.VARIANT_STAGED, 2 * MiB)]]
+          (rd.VARIANT_STAGED, 1 * MiB), (rd.VARIANT_STAGED, 2 * MiB),
+          (rd.VARIANT_STAGED_Y, 64 * 1024), (rd.VARIANT_STAGED_Y, 2 * MiB)]]
 
 
 @pytest.fixture(scope="module")
@@ -144,7 +145,7 @@ def sweep_handle():
 
 
 @pytest.mark.parametrize("nbytes,variant,chunk", SWEEP,
-                         ids=[f"{b >> 10}KiB-{'zs' if v == 1 else 'snac'}-{c >> 10}K"
+                         ids=[f"{b >> 10}KiB-{ {1: 'zs', 2: 'snac', 3: 'snac_y'}[v] }-{c >> 10}K"
                               for b, v, c in SWEEP])
 def test_allreduce_sweep_r8(sweep_handle, nbytes, variant, chunk):
     R, n = 8, nbytes // 2
@@ -161,7 +162,8 @@ def test_allreduce_sweep_r8(sweep_handle, nbytes, variant, chunk):
 # ---------------------------------------------------------------- moe_a2av_r8
 
 ATOMS = [(rd.VARIANT_ZS, rd.ATOM_VECTOR), (rd.VARIANT_ZS, rd.ATOM_BULK),
-         (rd.VARIANT_ZS, rd.ATOM_COPY_ENGINE), (rd.VARIANT_STAGED, rd.ATOM_AUTO)]
+         (rd.VARIANT_ZS, rd.ATOM_COPY_ENGINE), (rd.VARIANT_STAGED, rd.ATOM_AUTO),
+         (rd.VARIANT_STAGED_Y, rd.ATOM_AUTO)]
 
 
 @pytest.mark.parametrize("variant,atom", ATOMS)
@@ -193,7 +195,7 @@ def test_moe_a2av_r8_dispatch_and_inverse(variant, atom):
 
 # ---------------------------------------------------------- dp_attn_agv_rsv_r8
 
-@pytest.mark.parametrize("variant", [rd.VARIANT_ZS, rd.VARIANT_STAGED])
+@pytest.mark.parametrize("variant", [rd.VARIANT_ZS, rd.VARIANT_STAGED, rd.VARIANT_STAGED_Y])
 def test_dp_attention_agv_rsv(variant):
     R, H = 8, workloads.HIDDEN
     tok = workloads.uniform_token_counts(R, 1, 2048, workloads.seed_for("dp_attn_agv_rsv_r8", 9))
@@ -249,7 +251,7 @@ def test_allgather_1GiB_out_per_rank(variant, atom):
     torch.cuda.empty_cache()
 
 
-@pytest.mark.parametrize("variant", [rd.VARIANT_ZS, rd.VARIANT_STAGED])
+@pytest.mark.parametrize("variant", [rd.VARIANT_ZS, rd.VARIANT_STAGED, rd.VARIANT_STAGED_Y])
 def test_allreduce_1GiB_per_rank(variant):
     R, n = 8, GiB // 2
     x = workloads.rank_buffers("dp_attn_agv_rsv_r8", R, n, "bf16", role=4, device="cuda")

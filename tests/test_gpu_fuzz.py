@@ -51,7 +51,7 @@ def _policy(rng, h, copy):
     else:
         chunk = int(rng.choice([256, 512, 4096, 16384, 65536]))
         rd.purlin_set_policy(h, chunk, int(rng.integers(1, 9)), int(rng.choice([0, 1, 2, 5])),
-                             rd.VARIANT_STAGED)
+                             int(rng.choice([rd.VARIANT_STAGED, rd.VARIANT_STAGED_Y])))
         rd.purlin_set_atom(h, rd.ATOM_AUTO)
 
 

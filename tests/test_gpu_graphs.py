@@ -18,7 +18,7 @@ from helpers import host_bits
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("variant", [rd.VARIANT_ZS, rd.VARIANT_STAGED])
+@pytest.mark.parametrize("variant", [rd.VARIANT_ZS, rd.VARIANT_STAGED, rd.VARIANT_STAGED_Y])
 def test_replayed_graph_matches_oracle_every_time(variant):
     rd.build()
     R, c = 8, 40000
@@ -29,7 +29,7 @@ def test_replayed_graph_matches_oracle_every_time(variant):
     a = [torch.empty(n, dtype=torch.bfloat16, device="cuda") for _ in range(R)]
     h = rd.purlin_create(R)
     try:
-        rd.purlin_set_policy(h, 4096 if variant == rd.VARIANT_STAGED else 0, 2, 3, variant)
+        rd.purlin_set_policy(h, 0 if variant == rd.VARIANT_ZS else 4096, 2, 3, variant)
         for t in x:
             t.zero_()
         stream = torch.cuda.Stream()

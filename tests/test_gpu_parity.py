@@ -36,6 +36,9 @@ POLICIES = {
     "snac_tiny_chunks": (rd.VARIANT_STAGED, 256, 2, 3),
     "snac_default": (rd.VARIANT_STAGED, 0, 0, 0),
     "snac_deep": (rd.VARIANT_STAGED, 4096, 8, 5),
+    # sums reduced by the producer, the reduced chunk staged
+    "snac_y_default": (rd.VARIANT_STAGED_Y, 0, 0, 0),
+    "snac_y_tiny_chunks": (rd.VARIANT_STAGED_Y, 256, 3, 3),
 }
 
 
@@ -76,7 +79,7 @@ def test_all_reduce(policy, dtype, R, n):
         assert outs[j].guards_intact()
 
 
-@pytest.mark.parametrize("policy", ["zs", "zs_large", "snac_tiny_chunks"])
+@pytest.mark.parametrize("policy", ["zs", "zs_large", "snac_tiny_chunks", "snac_y_tiny_chunks"])
 @pytest.mark.parametrize("offset", [1, 3, 8])
 def test_all_reduce_unaligned_streams(policy, offset):
     """Streams starting at different offsets force element-wise segments."""
@@ -93,7 +96,7 @@ def test_all_reduce_unaligned_streams(policy, offset):
         assert outs[j].guards_intact()
 
 
-@pytest.mark.parametrize("policy", ["zs", "zs_large", "snac_tiny_chunks"])
+@pytest.mark.parametrize("policy", ["zs", "zs_large", "snac_tiny_chunks", "snac_y_tiny_chunks"])
 def test_all_reduce_in_place(policy):
     R, n, dtype = 8, 12345, "f32"
     h = handle(R)
@@ -140,7 +143,7 @@ def test_reduce_scatter_v(policy, dtype, R, explicit):
         assert outs[k].guards_intact()
 
 
-@pytest.mark.parametrize("policy", ["zs", "zs_large", "snac_tiny_chunks"])
+@pytest.mark.parametrize("policy", ["zs", "zs_large", "snac_tiny_chunks", "snac_y_tiny_chunks"])
 def test_reduce_scatter_in_place(policy):
     R, c, dtype = 8, 1001, "bf16"
     h = handle(R)
@@ -154,7 +157,7 @@ def test_reduce_scatter_in_place(policy):
         assert same_bits(host_bits(outs[k]), want[k])
 
 
-@pytest.mark.parametrize("policy", ["zs", "zs_large", "snac_tiny_chunks"])
+@pytest.mark.parametrize("policy", ["zs", "zs_large", "snac_tiny_chunks", "snac_y_tiny_chunks"])
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_reduce_scatter_unaligned_partitions(policy, dtype):
     """Partitions at odd element offsets: heads and tails are element-wise."""
@@ -287,7 +290,7 @@ def _as_f64(bits, dtype):
     return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).double().numpy()
 
 
-@pytest.mark.parametrize("policy", ["zs", "zs_large", "snac_tiny_chunks"])
+@pytest.mark.parametrize("policy", ["zs", "zs_large", "snac_tiny_chunks", "snac_y_tiny_chunks"])
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 @pytest.mark.parametrize("R", [3, 8])
 def test_tree_order(policy, dtype, R):
@@ -463,7 +466,7 @@ def _is_nan(bits, dtype):
     return ((b & exp_mask) == exp_mask) & ((b & man_mask) != 0)
 
 
-@pytest.mark.parametrize("policy", ["zs", "zs_large", "snac_default"])
+@pytest.mark.parametrize("policy", ["zs", "zs_large", "snac_default", "snac_y_default"])
 @pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
 @pytest.mark.parametrize("R", [2, 3, 8])
 def test_special_values_sum(policy, dtype, R):

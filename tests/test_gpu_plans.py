@@ -24,6 +24,7 @@ POLICIES = {
     "zs_bulk": (rd.VARIANT_ZS, 0, 0, 0, rd.ATOM_BULK),
     "zs_copy_engine": (rd.VARIANT_ZS, 0, 0, 0, rd.ATOM_COPY_ENGINE),
     "snac": (rd.VARIANT_STAGED,),
+    "snac_y": (rd.VARIANT_STAGED_Y,),
 }
 
 

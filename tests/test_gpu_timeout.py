@@ -19,13 +19,14 @@ from helpers import host_bits, inputs
 pytestmark = pytest.mark.gpu
 
 
+@pytest.mark.parametrize("variant", [rd.VARIANT_STAGED, rd.VARIANT_STAGED_Y])
 @pytest.mark.parametrize("coll", ["all_reduce", "reduce_scatter", "all_gather"])
-def test_wait_that_runs_out_reports_timeout(coll):
+def test_wait_that_runs_out_reports_timeout(coll, variant):
     rd.build()
     R, c = 4, 1 << 14
     h = rd.purlin_create(R)
     try:
-        rd.purlin_set_policy(h, 4096, 2, 2, rd.VARIANT_STAGED)
+        rd.purlin_set_policy(h, 4096, 2, 2, variant)
         rd.purlin_set_timeout(h, 50_000_000)
         x = inputs(R, R * c, "bf16", seed=4)
         small = [t[:c] for t in x]
