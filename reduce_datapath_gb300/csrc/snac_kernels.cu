@@ -48,6 +48,13 @@ namespace {
 // consumer copies to its destination (kRSY) or to all R outputs (kARY).
 enum Kind : int { kRS = 0, kAG = 1, kAR = 2, kA2A = 3, kRSY = 4, kARY = 5 };
 enum : int { kReady = 0, kFree = 1, kYReady = 2, kYFree = 3, kFlagsPerSlot = 4 };
+// kRSY / kARY use no y part: the slot's kYReady word carries the step staged in
+// the slot (or kNoStep: the producer has no step left).  Every value written
+// there stays below 2^32, hence below every tag (epochs start at 1), so a later
+// call of another kind that waits on the same word for a tag is never released
+// by it.
+enum : int { kStepOf = kYReady };
+constexpr uint64_t kNoStep = 0xffffffffull;  // steps are < 2^32 - 1 (plan_into)
 
 // Default chunk per rank per step, measured best on GB300 at 64 MiB per rank,
 // R = 8, 32 MiB ring, depth 2: sums stage R + 1 parts per slot and favour many
@@ -57,9 +64,9 @@ enum : int { kReady = 0, kFree = 1, kYReady = 2, kYFree = 3, kFlagsPerSlot = 4 }
 size_t default_chunk(Coll coll, bool stage_y)
 {
     // one part per slot, as for copies; measured at 64 MiB per rank, R = 8,
-    // depth 2: AllReduce 211.7 us at 64 KiB (258.9 at 256 KiB), ReduceScatter
-    // 129.6 us at 128 KiB (171.0 at 16 KiB)
-    if (stage_y) return coll == Coll::ReduceScatter ? 128 * 1024 : 64 * 1024;
+    // depth 2, 32 MiB ring: AllReduce 198.4 us at 64 KiB (200.4 at 32 KiB,
+    // 218.6 at 128 KiB), ReduceScatter 122.5 us at 64 KiB (130.2 at 128 KiB)
+    if (stage_y) return 64 * 1024;
     switch (coll) {
     case Coll::AllGather: return 256 * 1024;
     case Coll::AllToAllV: return 128 * 1024;
@@ -78,6 +85,7 @@ struct SnacParams {
     int* status;
     uint64_t* epoch_word;    // device epoch of the last completed call
     uint32_t* done_word;     // CTAs of the running call that have finished
+    unsigned long long* step_word;  // next step to hand out (kRSY / kARY)
     uint64_t timeout_ns;
     uint64_t max_spins;
     uint64_t chunk;        // bytes per rank per step (multiple of 256)
@@ -364,6 +372,87 @@ __device__ void cta_reduce_src(const SnacParams& p, int unit_log2, char* dst, ui
 
 // ------------------------------------------------------------------ roles
 
+// Relaxed access to a flag-area word that a release / acquire pair orders.
+__device__ __forceinline__ uint64_t ld_relaxed(const uint64_t* w)
+{
+    uint64_t v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(w) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_relaxed(uint64_t* w, uint64_t v)
+{
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(w), "l"(v) : "memory");
+}
+
+// The reduced-chunk kinds hand out steps from a counter instead of dealing them
+// round-robin: a channel whose SM drains faster takes more steps, so the slowest
+// SMs do not set the time.  The producer records the step in the slot's step
+// word before notifying; the consumer reads it after the acquire.
+template <typename T, int ORDER, int KIND>
+__device__ void producer_dynamic(const SnacParams& p, uint32_t ch, uint64_t epoch)
+{
+    __shared__ uint64_t step_s;
+    const uint64_t lpol = atom::l2_policy(kL2EvictFirst);
+    const uint64_t spol = atom::l2_policy(kL2Normal);
+    for (uint32_t n = 0;; ++n) {
+        const uint32_t slot = n % p.depth;
+        uint64_t* f = slot_flags(p, ch, slot);
+        if (n >= p.depth && !cta_wait(p, f + kFree, tag_of(epoch, n - p.depth))) return;
+        if (threadIdx.x == 0) step_s = atomicAdd(p.step_word, 1ull);
+        __syncthreads();
+        const uint64_t i = step_s;
+        __syncthreads();  // step_s is rewritten next step
+        if (i >= p.nsteps) {
+            if (threadIdx.x == 0) st_relaxed(f + kStepOf, kNoStep);
+            cta_notify(f + kReady, tag_of(epoch, n));
+            return;
+        }
+        const Segment& s = step_segment(p, (uint32_t)i);
+        const uint64_t off = (uint64_t)((uint32_t)i - s.tile0) * p.chunk;
+        const uint64_t len = min(p.chunk, s.bytes - off);
+        cta_reduce_src<T, ORDER>(p, s.unit_log2, slot_data(p, ch, slot), s.src_off + off, len,
+                                 lpol, spol);
+        if (threadIdx.x == 0) st_relaxed(f + kStepOf, i);
+        if (p.inject && ch == 0 && n == 0) continue;  // testing: this notify never happens
+        cta_notify(f + kReady, tag_of(epoch, n));
+    }
+}
+
+template <typename T, int ORDER, int KIND>
+__device__ void consumer_dynamic(const SnacParams& p, uint32_t ch, uint64_t epoch)
+{
+    __shared__ uint64_t step_s;
+    // AllReduce outputs are written once: evict-first.  A ReduceScatter's stay
+    // at normal priority (a following AllGather reads them).
+    const uint64_t lpol = atom::l2_policy(kL2Normal);
+    const uint64_t spol = atom::l2_policy(KIND == kARY ? kL2EvictFirst : kL2Normal);
+    for (uint32_t n = 0;; ++n) {
+        const uint32_t slot = n % p.depth;
+        uint64_t* f = slot_flags(p, ch, slot);
+        if (!cta_wait(p, f + kReady, tag_of(epoch, n))) return;
+        if (threadIdx.x == 0) step_s = ld_relaxed(f + kStepOf);
+        __syncthreads();
+        const uint64_t i = step_s;
+        __syncthreads();
+        if (i >= p.nsteps) return;  // kNoStep: the producer is done
+        const Segment& s = step_segment(p, (uint32_t)i);
+        const uint64_t off = (uint64_t)((uint32_t)i - s.tile0) * p.chunk;
+        const uint64_t len = min(p.chunk, s.bytes - off);
+        const char* staged = slot_data(p, ch, slot);
+        if (KIND == kARY) {
+            // In-place AllReduce (out[r] == in[r]): this step's input range was
+            // read by the producer before the ready tag was published.
+            cta_copy_any<true, true>(p, s.unit_log2, nullptr, s.dst_off + off, staged, len, 0,
+                                     lpol, spol);
+        } else {
+            cta_copy_any<true, false>(p, s.unit_log2, p.out[s.dst] + s.dst_off + off, 0, staged,
+                                      len, 0, lpol, spol);
+        }
+        cta_notify(f + kFree, tag_of(epoch, n));
+    }
+}
+
 template <typename T, int ORDER, int KIND>
 __device__ void producer(const SnacParams& p, uint32_t ch, uint64_t epoch)
 {
@@ -470,9 +559,16 @@ __global__ void __launch_bounds__(kThreads, 2) snac_kernel(const __grid_constant
     const uint64_t epoch = epoch_s;
     const uint32_t role = blockIdx.x / p.nch;
     const uint32_t ch = blockIdx.x % p.nch;
-    if (role == 0) producer<T, ORDER, KIND>(p, ch, epoch);
-    else if (role == 1) consumer<T, ORDER, KIND>(p, ch, epoch);
-    else if (KIND == kAR) gatherer(p, ch, epoch);
+    if (KIND == kRSY || KIND == kARY) {
+        if (role == 0) producer_dynamic<T, ORDER, KIND>(p, ch, epoch);
+        else consumer_dynamic<T, ORDER, KIND>(p, ch, epoch);
+    } else if (role == 0) {
+        producer<T, ORDER, KIND>(p, ch, epoch);
+    } else if (role == 1) {
+        consumer<T, ORDER, KIND>(p, ch, epoch);
+    } else if (KIND == kAR) {
+        gatherer(p, ch, epoch);
+    }
     // Whatever path a role left by (done, or an error seen), the last CTA to
     // get here publishes the epoch for the next call and resets the counter.
     // No CTA reads the epoch word after its start, and every CTA has started
@@ -482,6 +578,7 @@ __global__ void __launch_bounds__(kThreads, 2) snac_kernel(const __grid_constant
         __threadfence();
         if (atomicAdd(p.done_word, 1u) == gridDim.x - 1) {
             atomicExch(p.done_word, 0u);
+            atomicExch(p.step_word, 0ull);
             __threadfence();
             st_release(p.epoch_word, epoch);
         }
@@ -555,8 +652,9 @@ purlin_status_t snac_geometry(int R, Coll coll, bool stage_y, const SnacConfig& 
     const size_t slot = (size_t)sub_slots(coll, R, stage_y) * chunk;
     const size_t ring = (size_t)depth * slot;
     const long by_ring = ring ? (long)(cfg.staging_bytes / ring) : 0;
-    // the last two flag words hold the epoch and the completion counter
-    const long by_flags = (long)((cfg.flag_words - 2) / ((size_t)depth * kFlagsPerSlot));
+    // the last three flag words hold the epoch, the completion counter and
+    // the step counter
+    const long by_flags = (long)((cfg.flag_words - 3) / ((size_t)depth * kFlagsPerSlot));
     const long by_residency = resident_channels;
     long nch = cfg.channels ? cfg.channels : kMaxChannels;
     nch = std::min({nch, by_ring, by_flags, by_residency});
@@ -619,6 +717,7 @@ purlin_status_t plan_into(KernelLaunch& k, const SnacRequest& rq, const SnacConf
     p.status = cfg.status;
     p.epoch_word = cfg.flags + cfg.flag_words - 1;
     p.done_word = reinterpret_cast<uint32_t*>(cfg.flags + cfg.flag_words - 2);
+    p.step_word = reinterpret_cast<unsigned long long*>(cfg.flags + cfg.flag_words - 3);
     p.timeout_ns = cfg.timeout_ns;
     p.max_spins = cfg.timeout_ns / 64 + 65536;
     p.chunk = chunk;

@@ -494,3 +494,31 @@ def test_special_values_sum(policy, dtype, R):
         assert np.array_equal(_is_nan(gi, dtype), nan_w), j
         assert np.array_equal(gi[~nan_w], wi[~nan_w]), j
         assert ar[j].guards_intact()
+
+
+def test_staged_kinds_share_a_handle():
+    """Calls of every staged kind alternate on one handle: each kind's flag words
+    (ready / free tags, the y part's tags, the reduced-chunk kinds' step words)
+    must never release a wait of another kind (every tag is above 2^32, every
+    step word below it)."""
+    R, n = 8, 300_000
+    h = handle(R)
+    x = inputs(R, n, "bf16", seed=61)
+    want_ar = oracle.all_reduce(oracle_in(x), dtype="bf16")
+    c = n // R
+    want_rs = oracle.reduce_scatter(oracle_in(x), [c] * R, dtype="bf16")
+    try:
+        for rep in range(3):
+            for variant, chunk in ((rd.VARIANT_STAGED_Y, 4096), (rd.VARIANT_STAGED, 4096),
+                                   (rd.VARIANT_STAGED_Y, 0), (rd.VARIANT_STAGED, 0)):
+                set_variant(h, variant, chunk, 2, 0)
+                out = [torch.empty_like(t) for t in x]
+                rd.purlin_all_reduce(h, x, out, n, "bf16")
+                ys = [torch.empty(c, dtype=torch.bfloat16, device="cuda") for _ in range(R)]
+                rd.purlin_reduce_scatter(h, x, ys, [c] * R, None, "bf16")
+                run_ok(h)
+                for j in range(R):
+                    assert same_bits(host_bits(out[j]), want_ar[j]), (rep, variant, chunk, j)
+                    assert same_bits(host_bits(ys[j]), want_rs[j]), (rep, variant, chunk, j)
+    finally:
+        set_variant(h, rd.VARIANT_AUTO)
