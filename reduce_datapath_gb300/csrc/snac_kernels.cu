@@ -13,24 +13,29 @@
 //
 // One cooperative launch holds every role, so each waiting CTA's partner is
 // resident.  Roles by blockIdx.x / channels:
-//   0 producer(ch): for each step dealt to ch, wait until its ring slot is free,
-//     STAGE the step's chunk of every source into the slot, NOTIFY (release).
-//   1 consumer(ch): wait for the step's tag (acquire), CONSUME: sum the R staged
-//     pieces (Atom::reduce) into the destination -- or, for AllReduce, into the
-//     slot's y part -- or copy the staged piece (Atom::copy) to its
-//     destination(s); then free the slot.
-//   2 gatherer(ch), AllReduce only: wait for the y tag, copy the reduced chunk to
-//     all R outputs, free the y part.
-// Steps are the layout's segments cut into chunks of `chunk` bytes per rank;
-// step i belongs to channel i % channels and is that channel's n-th step,
-// n = i / channels, held in slot n % depth.  A flag holds the tag
-// (epoch << 32) | (n + 1).  The epoch lives in device memory (the last flag
-// word): every CTA reads it when the kernel starts, and the last CTA to finish
-// advances it (a completion counter in the word before it), so each call --
-// also each replay of a captured CUDA graph -- runs with a fresh epoch and the
-// flags never need resetting.  Every wait is bounded (time and iteration count) and watches the
-// status word: on a timeout the waiter records PURLIN_ERR_TIMEOUT and every CTA
-// leaves at its next wait.
+//   0 producer(ch): for each of its steps, wait until its ring slot is free,
+//     STAGE the step into the slot, NOTIFY (release).  It stages the step's
+//     chunk of the source (copies), the R input chunks (sums, inputs staged),
+//     or the chunk of y it reduces from the R inputs itself (sums, reduced
+//     chunk staged).
+//   1 consumer(ch): wait for the step's tag (acquire), CONSUME the slot: sum
+//     the R staged chunks into the destination -- or, for AllReduce, into the
+//     slot's y part -- or copy the staged chunk to its destination(s); then
+//     free the slot.
+//   2 gatherer(ch), AllReduce with inputs staged only: wait for the y tag, copy
+//     the reduced chunk to all R outputs, free the y part.
+// Steps are the layout's segments cut into chunks of `chunk` bytes per rank.
+// With the inputs of a sum staged, step i belongs to channel i % channels; the
+// two-role kinds take steps from a device counter instead, and the producer
+// records in the slot which step it staged.  A channel's n-th step sits in slot
+// n % depth; a flag holds the tag (epoch << 32) | (n + 1).  The epoch lives in
+// device memory (the last flag word): every CTA reads it when the kernel
+// starts, and the last CTA to finish advances it (a completion counter in the
+// word before it) and resets the step counter (the word before that), so each
+// call -- also each replay of a captured CUDA graph -- runs with a fresh epoch
+// and the flags never need resetting.  Every wait is bounded (time and
+// iteration count) and watches the status word: on a timeout the waiter
+// records PURLIN_ERR_TIMEOUT and every CTA leaves at its next wait.
 #include "atom.cuh"
 #include "internal.h"
 #include "snac.h"
@@ -48,8 +53,9 @@ namespace {
 // consumer copies to its destination (kRSY) or to all R outputs (kARY).
 enum Kind : int { kRS = 0, kAG = 1, kAR = 2, kA2A = 3, kRSY = 4, kARY = 5 };
 enum : int { kReady = 0, kFree = 1, kYReady = 2, kYFree = 3, kFlagsPerSlot = 4 };
-// kRSY / kARY use no y part: the slot's kYReady word carries the step staged in
-// the slot (or kNoStep: the producer has no step left).  Every value written
+// The two-role kinds (kAG, kA2A, kRSY, kARY) use no y part: the slot's kYReady
+// word carries the step staged in the slot (or kNoStep: the producer has no
+// step left).  Every value written
 // there stays below 2^32, hence below every tag (epochs start at 1), so a later
 // call of another kind that waits on the same word for a tag is never released
 // by it.
@@ -57,22 +63,25 @@ enum : int { kStepOf = kYReady };
 constexpr uint64_t kNoStep = 0xffffffffull;  // steps are < 2^32 - 1 (plan_into)
 
 // Default chunk per rank per step, measured best on GB300 at 64 MiB per rank,
-// R = 8, 32 MiB ring, depth 2: sums stage R + 1 parts per slot and favour many
-// channels of small chunks (AllReduce 3468 GB/s at 16 KiB vs 2102 at 64 KiB);
-// copies stage one part per slot and favour larger chunks (AllToAllV 4029 GB/s
-// at 128 KiB vs 1414 at 16 KiB; AllGather 3561 at 256 KiB vs 3125 at 16 KiB).
+// R = 8, 32 MiB ring, depth 2:
+//   - sums with the inputs staged put R + 1 parts in a slot and favour many
+//     channels of small chunks (AllReduce 3468 GB/s at 16 KiB vs 2102 at 64 KiB);
+//   - sums with the reduced chunk staged put one part in a slot: AllReduce
+//     198.4 us at 64 KiB (200.4 at 32 KiB, 218.6 at 128 KiB), ReduceScatter
+//     122.5 us at 64 KiB (130.2 at 128 KiB);
+//   - copies put one part in a slot; with steps handed out from a counter the
+//     AllGather runs 115.0 us at 64 KiB (135.4 at 128 KiB, 169.1 at 256 KiB),
+//     the AllToAllV 270.3 us at 128 KiB (301.6 at 64 KiB, 343.7 at 256 KiB).
 size_t default_chunk(Coll coll, bool stage_y)
 {
-    // one part per slot, as for copies; measured at 64 MiB per rank, R = 8,
-    // depth 2, 32 MiB ring: AllReduce 198.4 us at 64 KiB (200.4 at 32 KiB,
-    // 218.6 at 128 KiB), ReduceScatter 122.5 us at 64 KiB (130.2 at 128 KiB)
-    if (stage_y) return 64 * 1024;
+    if (stage_y && (coll == Coll::ReduceScatter || coll == Coll::AllReduce)) return 64 * 1024;
     switch (coll) {
-    case Coll::AllGather: return 256 * 1024;
+    case Coll::AllGather: return 64 * 1024;
     case Coll::AllToAllV: return 128 * 1024;
     default: return 16 * 1024;
     }
 }
+
 constexpr int kDefaultDepth = 2;
 constexpr int kMaxChannels = 256;
 constexpr size_t kMinAutoChunk = 1024;
@@ -85,7 +94,7 @@ struct SnacParams {
     int* status;
     uint64_t* epoch_word;    // device epoch of the last completed call
     uint32_t* done_word;     // CTAs of the running call that have finished
-    unsigned long long* step_word;  // next step to hand out (kRSY / kARY)
+    unsigned long long* step_word;  // next step to hand out (two-role kinds)
     uint64_t timeout_ns;
     uint64_t max_spins;
     uint64_t chunk;        // bytes per rank per step (multiple of 256)
@@ -385,9 +394,9 @@ __device__ __forceinline__ void st_relaxed(uint64_t* w, uint64_t v)
     asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(w), "l"(v) : "memory");
 }
 
-// The reduced-chunk kinds hand out steps from a counter instead of dealing them
-// round-robin: a channel whose SM drains faster takes more steps, so the slowest
-// SMs do not set the time.  The producer records the step in the slot's step
+// The two-role kinds (copies, and sums staging the reduced chunk) hand out
+// steps from a counter instead of dealing them round-robin: a channel whose SM
+// drains faster takes more steps, so the slowest SMs do not set the time.  The producer records the step in the slot's step
 // word before notifying; the consumer reads it after the acquire.
 template <typename T, int ORDER, int KIND>
 __device__ void producer_dynamic(const SnacParams& p, uint32_t ch, uint64_t epoch)
@@ -411,8 +420,13 @@ __device__ void producer_dynamic(const SnacParams& p, uint32_t ch, uint64_t epoc
         const Segment& s = step_segment(p, (uint32_t)i);
         const uint64_t off = (uint64_t)((uint32_t)i - s.tile0) * p.chunk;
         const uint64_t len = min(p.chunk, s.bytes - off);
-        cta_reduce_src<T, ORDER>(p, s.unit_log2, slot_data(p, ch, slot), s.src_off + off, len,
-                                 lpol, spol);
+        if (KIND == kRSY || KIND == kARY) {
+            cta_reduce_src<T, ORDER>(p, s.unit_log2, slot_data(p, ch, slot), s.src_off + off, len,
+                                     lpol, spol);
+        } else {
+            cta_copy_any<false, false>(p, s.unit_log2, slot_data(p, ch, slot), 0,
+                                       p.in[s.src] + s.src_off + off, len, 0, lpol, spol);
+        }
         if (threadIdx.x == 0) st_relaxed(f + kStepOf, i);
         if (p.inject && ch == 0 && n == 0) continue;  // testing: this notify never happens
         cta_notify(f + kReady, tag_of(epoch, n));
@@ -423,10 +437,11 @@ template <typename T, int ORDER, int KIND>
 __device__ void consumer_dynamic(const SnacParams& p, uint32_t ch, uint64_t epoch)
 {
     __shared__ uint64_t step_s;
-    // AllReduce outputs are written once: evict-first.  A ReduceScatter's stay
-    // at normal priority (a following AllGather reads them).
+    // AllReduce, AllGather and AllToAll outputs are written once: evict-first.
+    // A ReduceScatter's stay at normal priority (a following AllGather reads
+    // them).
     const uint64_t lpol = atom::l2_policy(kL2Normal);
-    const uint64_t spol = atom::l2_policy(KIND == kARY ? kL2EvictFirst : kL2Normal);
+    const uint64_t spol = atom::l2_policy(KIND == kRSY ? kL2Normal : kL2EvictFirst);
     for (uint32_t n = 0;; ++n) {
         const uint32_t slot = n % p.depth;
         uint64_t* f = slot_flags(p, ch, slot);
@@ -445,6 +460,9 @@ __device__ void consumer_dynamic(const SnacParams& p, uint32_t ch, uint64_t epoc
             // read by the producer before the ready tag was published.
             cta_copy_any<true, true>(p, s.unit_log2, nullptr, s.dst_off + off, staged, len, 0,
                                      lpol, spol);
+        } else if (KIND == kAG) {
+            cta_copy_any<true, true>(p, s.unit_log2, nullptr, s.dst_off + off, staged, len,
+                                     (uintptr_t)(p.in[s.src] + s.src_off + off), lpol, spol);
         } else {
             cta_copy_any<true, false>(p, s.unit_log2, p.out[s.dst] + s.dst_off + off, 0, staged,
                                       len, 0, lpol, spol);
@@ -453,14 +471,13 @@ __device__ void consumer_dynamic(const SnacParams& p, uint32_t ch, uint64_t epoc
     }
 }
 
-template <typename T, int ORDER, int KIND>
+// The three-role and R-part kinds (kRS, kAR: the R input chunks staged) deal
+// steps round-robin: step i belongs to channel i % channels.
+template <int KIND>
 __device__ void producer(const SnacParams& p, uint32_t ch, uint64_t epoch)
 {
-    const bool reduce = KIND == kRS || KIND == kAR;
-    const bool reduce_here = KIND == kRSY || KIND == kARY;
     // Sources are read exactly once: their lines go first, the ring stays.
     const uint64_t lpol = atom::l2_policy(kL2EvictFirst);
-    const uint64_t spol = atom::l2_policy(kL2Normal);
     uint32_t n = 0;
     for (uint32_t i = ch; i < p.nsteps; i += p.nch, ++n) {
         const uint32_t slot = n % p.depth;
@@ -469,15 +486,7 @@ __device__ void producer(const SnacParams& p, uint32_t ch, uint64_t epoch)
         const Segment& s = step_segment(p, i);
         const uint64_t off = (uint64_t)(i - s.tile0) * p.chunk;
         const uint64_t len = min(p.chunk, s.bytes - off);
-        char* staged = slot_data(p, ch, slot);
-        if (reduce) {
-            cta_stage_any(p, s.unit_log2, staged, s.src_off + off, len, lpol);
-        } else if (reduce_here) {
-            cta_reduce_src<T, ORDER>(p, s.unit_log2, staged, s.src_off + off, len, lpol, spol);
-        } else {
-            cta_copy_any<false, false>(p, s.unit_log2, staged, 0, p.in[s.src] + s.src_off + off,
-                                       len, 0, lpol, spol);
-        }
+        cta_stage_any(p, s.unit_log2, slot_data(p, ch, slot), s.src_off + off, len, lpol);
         if (p.inject && ch == 0 && n == 0) continue;  // testing: this notify never happens
         cta_notify(f + kReady, tag_of(epoch, n));
     }
@@ -486,13 +495,9 @@ __device__ void producer(const SnacParams& p, uint32_t ch, uint64_t epoch)
 template <typename T, int ORDER, int KIND>
 __device__ void consumer(const SnacParams& p, uint32_t ch, uint64_t epoch)
 {
-    // AllGather and AllToAll outputs are written once and not read again here:
-    // evict-first, so that they do not push the ring out of L2.  A
-    // ReduceScatter's outputs stay at normal priority (a following AllGather
-    // reads them), and an AllReduce's consumer writes into the ring's y part.
-    const uint64_t lpol = atom::l2_policy(kL2Normal);
-    const uint64_t spol = atom::l2_policy(
-        (KIND == kA2A || KIND == kAG || KIND == kARY) ? kL2EvictFirst : kL2Normal);
+    // A ReduceScatter's outputs stay at normal priority (a following AllGather
+    // reads them); an AllReduce's consumer writes into the ring's y part.
+    const uint64_t spol = atom::l2_policy(kL2Normal);
     uint32_t n = 0;
     for (uint32_t i = ch; i < p.nsteps; i += p.nch, ++n) {
         const uint32_t slot = n % p.depth;
@@ -504,21 +509,10 @@ __device__ void consumer(const SnacParams& p, uint32_t ch, uint64_t epoch)
         char* staged = slot_data(p, ch, slot);
         if (KIND == kRS) {
             cta_reduce<T, ORDER>(p, s.unit_log2, p.out[s.dst] + s.dst_off + off, staged, len, spol);
-        } else if (KIND == kAR) {
+        } else {
             if (n >= p.depth && !cta_wait(p, f + kYFree, tag_of(epoch, n - p.depth))) return;
             cta_reduce<T, ORDER>(p, s.unit_log2, staged + (uint64_t)p.R * p.chunk, staged, len,
                                  spol);
-        } else if (KIND == kAG) {
-            cta_copy_any<true, true>(p, s.unit_log2, nullptr, s.dst_off + off, staged, len,
-                                     (uintptr_t)(p.in[s.src] + s.src_off + off), lpol, spol);
-        } else if (KIND == kARY) {
-            // In-place AllReduce (out[r] == in[r]): this step's input range was
-            // read by the producer before the ready tag was published.
-            cta_copy_any<true, true>(p, s.unit_log2, nullptr, s.dst_off + off, staged, len, 0,
-                                     lpol, spol);
-        } else {
-            cta_copy_any<true, false>(p, s.unit_log2, p.out[s.dst] + s.dst_off + off, 0, staged,
-                                      len, 0, lpol, spol);
         }
         cta_notify(f + kFree, tag_of(epoch, n));
         if (KIND == kAR && threadIdx.x == 0) st_release(f + kYReady, tag_of(epoch, n));
@@ -559,15 +553,13 @@ __global__ void __launch_bounds__(kThreads, 2) snac_kernel(const __grid_constant
     const uint64_t epoch = epoch_s;
     const uint32_t role = blockIdx.x / p.nch;
     const uint32_t ch = blockIdx.x % p.nch;
-    if (KIND == kRSY || KIND == kARY) {
+    if constexpr (KIND == kRS || KIND == kAR) {
+        if (role == 0) producer<KIND>(p, ch, epoch);
+        else if (role == 1) consumer<T, ORDER, KIND>(p, ch, epoch);
+        else if (KIND == kAR) gatherer(p, ch, epoch);
+    } else {
         if (role == 0) producer_dynamic<T, ORDER, KIND>(p, ch, epoch);
         else consumer_dynamic<T, ORDER, KIND>(p, ch, epoch);
-    } else if (role == 0) {
-        producer<T, ORDER, KIND>(p, ch, epoch);
-    } else if (role == 1) {
-        consumer<T, ORDER, KIND>(p, ch, epoch);
-    } else if (KIND == kAR) {
-        gatherer(p, ch, epoch);
     }
     // Whatever path a role left by (done, or an error seen), the last CTA to
     // get here publishes the epoch for the next call and resets the counter.
