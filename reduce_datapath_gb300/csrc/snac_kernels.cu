@@ -25,7 +25,7 @@
 //   2 gatherer(ch), AllReduce with inputs staged only: wait for the y tag, copy
 //     the reduced chunk to all R outputs, free the y part.
 // Steps are the layout's segments cut into chunks of `chunk` bytes per rank.
-// With the inputs of a sum staged, step i belongs to channel i % channels; the
+// In the three-role AllReduce step i belongs to channel i % channels; the
 // two-role kinds take steps from a device counter instead, and the producer
 // records in the slot which step it staged.  A channel's n-th step sits in slot
 // n % depth; a flag holds the tag (epoch << 32) | (n + 1).  The epoch lives in
@@ -53,9 +53,9 @@ namespace {
 // consumer copies to its destination (kRSY) or to all R outputs (kARY).
 enum Kind : int { kRS = 0, kAG = 1, kAR = 2, kA2A = 3, kRSY = 4, kARY = 5 };
 enum : int { kReady = 0, kFree = 1, kYReady = 2, kYFree = 3, kFlagsPerSlot = 4 };
-// The two-role kinds (kAG, kA2A, kRSY, kARY) use no y part: the slot's kYReady
-// word carries the step staged in the slot (or kNoStep: the producer has no
-// step left).  Every value written
+// The two-role kinds (kRS, kAG, kA2A, kRSY, kARY) use no y part: the slot's
+// kYReady word carries the step staged in the slot (or kNoStep: the producer
+// has no step left).  Every value written
 // there stays below 2^32, hence below every tag (epochs start at 1), so a later
 // call of another kind that waits on the same word for a tag is never released
 // by it.
@@ -394,9 +394,10 @@ __device__ __forceinline__ void st_relaxed(uint64_t* w, uint64_t v)
     asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(w), "l"(v) : "memory");
 }
 
-// The two-role kinds (copies, and sums staging the reduced chunk) hand out
-// steps from a counter instead of dealing them round-robin: a channel whose SM
-// drains faster takes more steps, so the slowest SMs do not set the time.  The producer records the step in the slot's step
+// The two-role kinds (copies, ReduceScatter, and sums staging the reduced
+// chunk) hand out steps from a counter instead of dealing them round-robin: a
+// channel whose SM drains faster takes more steps, so the slowest SMs do not
+// set the time.  The producer records the step in the slot's step
 // word before notifying; the consumer reads it after the acquire.
 template <typename T, int ORDER, int KIND>
 __device__ void producer_dynamic(const SnacParams& p, uint32_t ch, uint64_t epoch)
@@ -423,6 +424,8 @@ __device__ void producer_dynamic(const SnacParams& p, uint32_t ch, uint64_t epoc
         if (KIND == kRSY || KIND == kARY) {
             cta_reduce_src<T, ORDER>(p, s.unit_log2, slot_data(p, ch, slot), s.src_off + off, len,
                                      lpol, spol);
+        } else if (KIND == kRS) {
+            cta_stage_any(p, s.unit_log2, slot_data(p, ch, slot), s.src_off + off, len, lpol);
         } else {
             cta_copy_any<false, false>(p, s.unit_log2, slot_data(p, ch, slot), 0,
                                        p.in[s.src] + s.src_off + off, len, 0, lpol, spol);
@@ -441,7 +444,8 @@ __device__ void consumer_dynamic(const SnacParams& p, uint32_t ch, uint64_t epoc
     // A ReduceScatter's stay at normal priority (a following AllGather reads
     // them).
     const uint64_t lpol = atom::l2_policy(kL2Normal);
-    const uint64_t spol = atom::l2_policy(KIND == kRSY ? kL2Normal : kL2EvictFirst);
+    const uint64_t spol =
+        atom::l2_policy((KIND == kRSY || KIND == kRS) ? kL2Normal : kL2EvictFirst);
     for (uint32_t n = 0;; ++n) {
         const uint32_t slot = n % p.depth;
         uint64_t* f = slot_flags(p, ch, slot);
@@ -455,7 +459,10 @@ __device__ void consumer_dynamic(const SnacParams& p, uint32_t ch, uint64_t epoc
         const uint64_t off = (uint64_t)((uint32_t)i - s.tile0) * p.chunk;
         const uint64_t len = min(p.chunk, s.bytes - off);
         const char* staged = slot_data(p, ch, slot);
-        if (KIND == kARY) {
+        if (KIND == kRS) {
+            cta_reduce<T, ORDER>(p, s.unit_log2, p.out[s.dst] + s.dst_off + off, staged, len,
+                                 spol);
+        } else if (KIND == kARY) {
             // In-place AllReduce (out[r] == in[r]): this step's input range was
             // read by the producer before the ready tag was published.
             cta_copy_any<true, true>(p, s.unit_log2, nullptr, s.dst_off + off, staged, len, 0,
@@ -471,8 +478,9 @@ __device__ void consumer_dynamic(const SnacParams& p, uint32_t ch, uint64_t epoc
     }
 }
 
-// The three-role and R-part kinds (kRS, kAR: the R input chunks staged) deal
-// steps round-robin: step i belongs to channel i % channels.
+// The three-role kind (kAR: the R input chunks of an AllReduce staged, a
+// gatherer role copying y out) deals steps round-robin: step i belongs to
+// channel i % channels.
 template <int KIND>
 __device__ void producer(const SnacParams& p, uint32_t ch, uint64_t epoch)
 {
@@ -495,8 +503,7 @@ __device__ void producer(const SnacParams& p, uint32_t ch, uint64_t epoch)
 template <typename T, int ORDER, int KIND>
 __device__ void consumer(const SnacParams& p, uint32_t ch, uint64_t epoch)
 {
-    // A ReduceScatter's outputs stay at normal priority (a following AllGather
-    // reads them); an AllReduce's consumer writes into the ring's y part.
+    // The consumer writes into the ring's y part, which the gatherer reads.
     const uint64_t spol = atom::l2_policy(kL2Normal);
     uint32_t n = 0;
     for (uint32_t i = ch; i < p.nsteps; i += p.nch, ++n) {
@@ -507,15 +514,10 @@ __device__ void consumer(const SnacParams& p, uint32_t ch, uint64_t epoch)
         const uint64_t off = (uint64_t)(i - s.tile0) * p.chunk;
         const uint64_t len = min(p.chunk, s.bytes - off);
         char* staged = slot_data(p, ch, slot);
-        if (KIND == kRS) {
-            cta_reduce<T, ORDER>(p, s.unit_log2, p.out[s.dst] + s.dst_off + off, staged, len, spol);
-        } else {
-            if (n >= p.depth && !cta_wait(p, f + kYFree, tag_of(epoch, n - p.depth))) return;
-            cta_reduce<T, ORDER>(p, s.unit_log2, staged + (uint64_t)p.R * p.chunk, staged, len,
-                                 spol);
-        }
+        if (n >= p.depth && !cta_wait(p, f + kYFree, tag_of(epoch, n - p.depth))) return;
+        cta_reduce<T, ORDER>(p, s.unit_log2, staged + (uint64_t)p.R * p.chunk, staged, len, spol);
         cta_notify(f + kFree, tag_of(epoch, n));
-        if (KIND == kAR && threadIdx.x == 0) st_release(f + kYReady, tag_of(epoch, n));
+        if (threadIdx.x == 0) st_release(f + kYReady, tag_of(epoch, n));
     }
 }
 
@@ -553,7 +555,7 @@ __global__ void __launch_bounds__(kThreads, 2) snac_kernel(const __grid_constant
     const uint64_t epoch = epoch_s;
     const uint32_t role = blockIdx.x / p.nch;
     const uint32_t ch = blockIdx.x % p.nch;
-    if constexpr (KIND == kRS || KIND == kAR) {
+    if constexpr (KIND == kAR) {
         if (role == 0) producer<KIND>(p, ch, epoch);
         else if (role == 1) consumer<T, ORDER, KIND>(p, ch, epoch);
         else if (KIND == kAR) gatherer(p, ch, epoch);
