@@ -15,7 +15,8 @@
 //   gatherer CTAs  (AllReduce) acquire the y tag and copy the reduced chunk to
 //                  all R outputs (the AllGather half of Figure 6).
 // Each CHANNEL is one producer, one consumer (and one gatherer) with its own
-// ring of `depth` slots; steps (chunks) are dealt to channels round-robin.
+// ring of `depth` slots; steps (chunks) are handed to channels from a device
+// counter as their producers ask for them.
 #pragma once
 
 #include <cuda_runtime.h>

@@ -25,9 +25,8 @@
 //   2 gatherer(ch), AllReduce with inputs staged only: wait for the y tag, copy
 //     the reduced chunk to all R outputs, free the y part.
 // Steps are the layout's segments cut into chunks of `chunk` bytes per rank.
-// In the three-role AllReduce step i belongs to channel i % channels; the
-// two-role kinds take steps from a device counter instead, and the producer
-// records in the slot which step it staged.  A channel's n-th step sits in slot
+// Producers take steps from a device counter, and the producer records in the
+// slot which step it staged.  A channel's n-th step sits in slot
 // n % depth; a flag holds the tag (epoch << 32) | (n + 1).  The epoch lives in
 // device memory (the last flag word): every CTA reads it when the kernel
 // starts, and the last CTA to finish advances it (a completion counter in the
@@ -52,15 +51,15 @@ namespace {
 // kRSY / kARY reduce in the producer and stage the reduced chunk y, which the
 // consumer copies to its destination (kRSY) or to all R outputs (kARY).
 enum Kind : int { kRS = 0, kAG = 1, kAR = 2, kA2A = 3, kRSY = 4, kARY = 5 };
-enum : int { kReady = 0, kFree = 1, kYReady = 2, kYFree = 3, kFlagsPerSlot = 4 };
-// The two-role kinds (kRS, kAG, kA2A, kRSY, kARY) use no y part: the slot's
-// kYReady word carries the step staged in the slot (or kNoStep: the producer
-// has no step left).  Every value written
-// there stays below 2^32, hence below every tag (epochs start at 1), so a later
-// call of another kind that waits on the same word for a tag is never released
-// by it.
-enum : int { kStepOf = kYReady };
-constexpr uint64_t kNoStep = 0xffffffffull;  // steps are < 2^32 - 1 (plan_into)
+// Words per (channel, slot): the ready / free tags of the slot, the y-ready /
+// y-free tags of its y part (three-role AllReduce), the step staged in the slot
+// and the step whose reduced chunk sits in the y part.  Tags are
+// (epoch << 32) | (n + 1) with epoch >= 1, so always >= 2^32; step words are
+// always < 2^32; so a word one kind leaves behind can never release a wait of
+// another kind on the same handle.
+enum : int { kReady = 0, kFree = 1, kYReady = 2, kYFree = 3, kStepOf = 4, kYStepOf = 5,
+             kFlagsPerSlot = 6 };
+constexpr uint64_t kNoStep = 0xffffffffull;  // no step left; steps are < 2^32 - 1 (plan_into)
 
 // Default chunk per rank per step, measured best on GB300 at 64 MiB per rank,
 // R = 8, 32 MiB ring, depth 2:
@@ -94,7 +93,7 @@ struct SnacParams {
     int* status;
     uint64_t* epoch_word;    // device epoch of the last completed call
     uint32_t* done_word;     // CTAs of the running call that have finished
-    unsigned long long* step_word;  // next step to hand out (two-role kinds)
+    unsigned long long* step_word;  // next step to hand out
     uint64_t timeout_ns;
     uint64_t max_spins;
     uint64_t chunk;        // bytes per rank per step (multiple of 256)
@@ -394,10 +393,9 @@ __device__ __forceinline__ void st_relaxed(uint64_t* w, uint64_t v)
     asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(w), "l"(v) : "memory");
 }
 
-// The two-role kinds (copies, ReduceScatter, and sums staging the reduced
-// chunk) hand out steps from a counter instead of dealing them round-robin: a
-// channel whose SM drains faster takes more steps, so the slowest SMs do not
-// set the time.  The producer records the step in the slot's step
+// Every kind hands out steps from a counter instead of dealing them
+// round-robin: a channel whose SM drains faster takes more steps, so the
+// slowest SMs do not set the time.  The producer records the step in the slot's step
 // word before notifying; the consumer reads it after the acquire.
 template <typename T, int ORDER, int KIND>
 __device__ void producer_dynamic(const SnacParams& p, uint32_t ch, uint64_t epoch)
@@ -424,7 +422,7 @@ __device__ void producer_dynamic(const SnacParams& p, uint32_t ch, uint64_t epoc
         if (KIND == kRSY || KIND == kARY) {
             cta_reduce_src<T, ORDER>(p, s.unit_log2, slot_data(p, ch, slot), s.src_off + off, len,
                                      lpol, spol);
-        } else if (KIND == kRS) {
+        } else if (KIND == kRS || KIND == kAR) {
             cta_stage_any(p, s.unit_log2, slot_data(p, ch, slot), s.src_off + off, len, lpol);
         } else {
             cta_copy_any<false, false>(p, s.unit_log2, slot_data(p, ch, slot), 0,
@@ -478,61 +476,57 @@ __device__ void consumer_dynamic(const SnacParams& p, uint32_t ch, uint64_t epoc
     }
 }
 
-// The three-role kind (kAR: the R input chunks of an AllReduce staged, a
-// gatherer role copying y out) deals steps round-robin: step i belongs to
-// channel i % channels.
-template <int KIND>
-__device__ void producer(const SnacParams& p, uint32_t ch, uint64_t epoch)
+// The three-role AllReduce (the R input chunks staged): the consumer sums them
+// into the slot's y part and records the step there; the gatherer copies y to
+// all R outputs.
+template <typename T, int ORDER>
+__device__ void consumer_ar(const SnacParams& p, uint32_t ch, uint64_t epoch)
 {
-    // Sources are read exactly once: their lines go first, the ring stays.
-    const uint64_t lpol = atom::l2_policy(kL2EvictFirst);
-    uint32_t n = 0;
-    for (uint32_t i = ch; i < p.nsteps; i += p.nch, ++n) {
-        const uint32_t slot = n % p.depth;
-        uint64_t* f = slot_flags(p, ch, slot);
-        if (n >= p.depth && !cta_wait(p, f + kFree, tag_of(epoch, n - p.depth))) return;
-        const Segment& s = step_segment(p, i);
-        const uint64_t off = (uint64_t)(i - s.tile0) * p.chunk;
-        const uint64_t len = min(p.chunk, s.bytes - off);
-        cta_stage_any(p, s.unit_log2, slot_data(p, ch, slot), s.src_off + off, len, lpol);
-        if (p.inject && ch == 0 && n == 0) continue;  // testing: this notify never happens
-        cta_notify(f + kReady, tag_of(epoch, n));
-    }
-}
-
-template <typename T, int ORDER, int KIND>
-__device__ void consumer(const SnacParams& p, uint32_t ch, uint64_t epoch)
-{
+    __shared__ uint64_t step_s;
     // The consumer writes into the ring's y part, which the gatherer reads.
     const uint64_t spol = atom::l2_policy(kL2Normal);
-    uint32_t n = 0;
-    for (uint32_t i = ch; i < p.nsteps; i += p.nch, ++n) {
+    for (uint32_t n = 0;; ++n) {
         const uint32_t slot = n % p.depth;
         uint64_t* f = slot_flags(p, ch, slot);
         if (!cta_wait(p, f + kReady, tag_of(epoch, n))) return;
-        const Segment& s = step_segment(p, i);
-        const uint64_t off = (uint64_t)(i - s.tile0) * p.chunk;
-        const uint64_t len = min(p.chunk, s.bytes - off);
-        char* staged = slot_data(p, ch, slot);
+        if (threadIdx.x == 0) step_s = ld_relaxed(f + kStepOf);
+        __syncthreads();
+        const uint64_t i = step_s;
+        __syncthreads();
+        // the y part of this slot is free once the gatherer is done with step n - depth
         if (n >= p.depth && !cta_wait(p, f + kYFree, tag_of(epoch, n - p.depth))) return;
-        cta_reduce<T, ORDER>(p, s.unit_log2, staged + (uint64_t)p.R * p.chunk, staged, len, spol);
+        if (i < p.nsteps) {
+            const Segment& s = step_segment(p, (uint32_t)i);
+            const uint64_t off = (uint64_t)((uint32_t)i - s.tile0) * p.chunk;
+            const uint64_t len = min(p.chunk, s.bytes - off);
+            char* staged = slot_data(p, ch, slot);
+            cta_reduce<T, ORDER>(p, s.unit_log2, staged + (uint64_t)p.R * p.chunk, staged, len,
+                                 spol);
+        }
+        if (threadIdx.x == 0) st_relaxed(f + kYStepOf, i);  // kNoStep passes through
         cta_notify(f + kFree, tag_of(epoch, n));
         if (threadIdx.x == 0) st_release(f + kYReady, tag_of(epoch, n));
+        if (i >= p.nsteps) return;
     }
 }
 
 __device__ void gatherer(const SnacParams& p, uint32_t ch, uint64_t epoch)
 {
+    __shared__ uint64_t step_s;
     // The R outputs are written once: evict-first keeps the ring in L2.
     const uint64_t lpol = atom::l2_policy(kL2Normal);
     const uint64_t spol = atom::l2_policy(kL2EvictFirst);
-    uint32_t n = 0;
-    for (uint32_t i = ch; i < p.nsteps; i += p.nch, ++n) {
+    for (uint32_t n = 0;; ++n) {
         const uint32_t slot = n % p.depth;
         uint64_t* f = slot_flags(p, ch, slot);
         if (!cta_wait(p, f + kYReady, tag_of(epoch, n))) return;
-        const Segment& s = step_segment(p, i);
-        const uint64_t off = (uint64_t)(i - s.tile0) * p.chunk;
+        if (threadIdx.x == 0) step_s = ld_relaxed(f + kYStepOf);
+        __syncthreads();
+        const uint64_t i = step_s;
+        __syncthreads();
+        if (i >= p.nsteps) return;
+        const Segment& s = step_segment(p, (uint32_t)i);
+        const uint64_t off = (uint64_t)((uint32_t)i - s.tile0) * p.chunk;
         const uint64_t len = min(p.chunk, s.bytes - off);
         const char* y = slot_data(p, ch, slot) + (uint64_t)p.R * p.chunk;
         // In-place AllReduce writes out[r] == in[r]; this step's input range
@@ -555,13 +549,13 @@ __global__ void __launch_bounds__(kThreads, 2) snac_kernel(const __grid_constant
     const uint64_t epoch = epoch_s;
     const uint32_t role = blockIdx.x / p.nch;
     const uint32_t ch = blockIdx.x % p.nch;
-    if constexpr (KIND == kAR) {
-        if (role == 0) producer<KIND>(p, ch, epoch);
-        else if (role == 1) consumer<T, ORDER, KIND>(p, ch, epoch);
-        else if (KIND == kAR) gatherer(p, ch, epoch);
+    if (role == 0) {
+        producer_dynamic<T, ORDER, KIND>(p, ch, epoch);
+    } else if constexpr (KIND == kAR) {
+        if (role == 1) consumer_ar<T, ORDER>(p, ch, epoch);
+        else gatherer(p, ch, epoch);
     } else {
-        if (role == 0) producer_dynamic<T, ORDER, KIND>(p, ch, epoch);
-        else consumer_dynamic<T, ORDER, KIND>(p, ch, epoch);
+        consumer_dynamic<T, ORDER, KIND>(p, ch, epoch);
     }
     // Whatever path a role left by (done, or an error seen), the last CTA to
     // get here publishes the epoch for the next call and resets the counter.
