@@ -403,11 +403,16 @@ __device__ void producer_dynamic(const SnacParams& p, uint32_t ch, uint64_t epoc
     __shared__ uint64_t step_s;
     const uint64_t lpol = atom::l2_policy(kL2EvictFirst);
     const uint64_t spol = atom::l2_policy(kL2Normal);
+    // A channel's first step is its own index (steps >= channels); every later
+    // one comes from the counter when the channel is ready for it (taking it
+    // one step ahead, to hide the atomic's round trip, balanced worse:
+    // AllReduce 192.5 -> 201.2 us).
     for (uint32_t n = 0;; ++n) {
         const uint32_t slot = n % p.depth;
         uint64_t* f = slot_flags(p, ch, slot);
         if (n >= p.depth && !cta_wait(p, f + kFree, tag_of(epoch, n - p.depth))) return;
-        if (threadIdx.x == 0) step_s = atomicAdd(p.step_word, 1ull);
+        if (threadIdx.x == 0)
+            step_s = n == 0 ? (uint64_t)ch : (uint64_t)p.nch + atomicAdd(p.step_word, 1ull);
         __syncthreads();
         const uint64_t i = step_s;
         __syncthreads();  // step_s is rewritten next step
