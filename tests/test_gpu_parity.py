@@ -522,3 +522,37 @@ def test_staged_kinds_share_a_handle():
                     assert same_bits(host_bits(ys[j]), want_rs[j]), (rep, variant, chunk, j)
     finally:
         set_variant(h, rd.VARIANT_AUTO)
+
+
+@pytest.mark.parametrize("coll,nbytes,small", [
+    ("ar", 4096, True), ("ar", 1 << 20, True), ("ar", 4 << 20, False),
+    ("rs", 256 << 10, True), ("rs", 1 << 20, False),
+    ("ag", 1 << 20, True), ("ag", 16 << 20, False),
+])
+def test_launch_shape_follows_message_size(coll, nbytes, small):
+    """One-warp CTAs below the per-collective threshold (AllReduce: 256 tiles of
+    256 x 32 B; the others: 64 tiles), 256-thread CTAs above it; the result is
+    the oracle's either way."""
+    R = 8
+    n = nbytes // 2
+    c = n // R
+    h = handle(R)
+    set_variant(h, rd.VARIANT_ZS)
+    x = inputs(R, n if coll != "ag" else c, "bf16", seed=nbytes % 1000 + len(coll))
+    if coll == "ar":
+        out = [torch.empty(n, dtype=torch.bfloat16, device="cuda") for _ in range(R)]
+        rd.purlin_all_reduce(h, x, out, n, "bf16")
+        want = oracle.all_reduce(oracle_in(x), dtype="bf16")
+    elif coll == "rs":
+        out = [torch.empty(c, dtype=torch.bfloat16, device="cuda") for _ in range(R)]
+        rd.purlin_reduce_scatter(h, x, out, [c] * R, None, "bf16")
+        want = oracle.reduce_scatter(oracle_in(x), [c] * R, dtype="bf16")
+    else:
+        out = [torch.empty(R * c, dtype=torch.bfloat16, device="cuda") for _ in range(R)]
+        rd.purlin_all_gather(h, x, out, [c] * R, None, "bf16")
+        want = oracle.all_gather(oracle_in(x))
+    run_ok(h)
+    info = rd.purlin_last_launch(h)
+    assert info["block"] == (32 if small else 256), info
+    for j in range(R):
+        assert same_bits(host_bits(out[j]), want[j]), j
