@@ -52,7 +52,11 @@ typedef struct {
  *   in_addr, out_addr  R integer addresses standing for the buffers.
  *   max_unit   widest access in bytes (16 or 32).
  *   segs       caller array of max_segs entries; *nsegs receives the count and
- *              *ntiles the number of tiles.
+ *              *ntiles the number of tiles.  Tiles are those of the 256-thread
+ *              zero-staging launch (256 units for sums, 1024 for copies); a call
+ *              with fewer than the small-message threshold of them
+ *              (purlin_set_small_tiles) runs one-warp tiles of 32 units over the
+ *              same segments.
  * Returns PURLIN_OK, PURLIN_ERR_INVALID_ARG (bad R, dtype, NULL array, element
  * misalignment for a sum, byte overflow) or PURLIN_ERR_UNSUPPORTED (more
  * segments than max_segs).  Never calls CUDA. */
