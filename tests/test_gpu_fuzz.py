@@ -8,6 +8,8 @@ with a random chunk, depth and channel count), the launch shape (one-warp or
 The outputs must equal the oracle's bit for bit and the canary guards around
 every output must survive.
 """
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -18,7 +20,9 @@ from helpers import Guarded, close_handles, handle, host_bits, inputs, same_bits
 
 pytestmark = pytest.mark.gpu
 
-CASES = 240
+# PURLIN_FUZZ_CASES widens the sweep for a soak run (the default keeps the suite
+# to seconds).
+CASES = int(os.environ.get("PURLIN_FUZZ_CASES", "240"))
 
 
 @pytest.fixture(scope="module", autouse=True)
