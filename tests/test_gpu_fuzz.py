@@ -61,6 +61,19 @@ def _policy(rng, h, copy):
 
 @pytest.mark.parametrize("seed", range(CASES))
 def test_random_layout(seed):
+    _case(seed, 1)
+
+
+# Fewer, 100x larger cases: many SNAC steps per channel, many tiles per CTA.
+LARGE_CASES = int(os.environ.get("PURLIN_FUZZ_LARGE_CASES", "16"))
+
+
+@pytest.mark.parametrize("seed", range(LARGE_CASES))
+def test_random_layout_large(seed):
+    _case(50_000 + seed, 100)
+
+
+def _case(seed, scale):
     rng = np.random.default_rng(1000 + seed)
     coll = ["rs", "ag", "ar", "a2av"][seed % 4]
     R = int(rng.integers(1, 9))
@@ -73,7 +86,7 @@ def test_random_layout(seed):
     off = lambda: int(rng.integers(0, 18))
     try:
         if coll == "ar":
-            n = int(rng.integers(0, 20000))
+            n = int(rng.integers(0, 20000 * scale))
             x = [inputs(1, n, dtype, seed=seed * 10 + r, offset=off())[0] for r in range(R)]
             outs = [Guarded(n, dtype, offset=off()) for _ in range(R)]
             rd.purlin_all_reduce(h, x, [o.view for o in outs], n, dtype)
@@ -86,7 +99,7 @@ def test_random_layout(seed):
             else:
                 want = oracle.all_reduce(xs, dtype=dtype)
         elif coll == "rs":
-            counts = rng.integers(0, 3000, size=R)
+            counts = rng.integers(0, 3000 * scale, size=R)
             counts[rng.random(R) < 0.2] = 0
             explicit = rng.random() < 0.5
             displs, total = _layout(rng, counts, explicit) if explicit else (None, int(counts.sum()))
@@ -96,7 +109,7 @@ def test_random_layout(seed):
             want = oracle.reduce_scatter([host_bits(t) for t in x], counts, displs, dtype=dtype,
                                          order="tree" if order == rd.ORDER_TREE else "fixed")
         elif coll == "ag":
-            counts = rng.integers(0, 3000, size=R)
+            counts = rng.integers(0, 3000 * scale, size=R)
             counts[rng.random(R) < 0.2] = 0
             explicit = rng.random() < 0.5
             displs, total = _layout(rng, counts, explicit) if explicit else (None, int(counts.sum()))
@@ -108,7 +121,7 @@ def test_random_layout(seed):
             rd.purlin_all_gather(h, x, [o.view for o in outs], counts, displs, dtype)
             want = oracle.all_gather([host_bits(t) for t in x], counts, displs, out_count=total)
         else:
-            C = rng.integers(0, 600, size=(R, R))
+            C = rng.integers(0, 600 * scale, size=(R, R))
             C[rng.random((R, R)) < 0.25] = 0
             x = [inputs(1, int(C[s].sum()), dtype, seed=seed * 10 + s, offset=off())[0]
                  for s in range(R)]
