@@ -58,3 +58,37 @@ def test_replayed_graph_matches_oracle_every_time(variant):
     finally:
         torch.cuda.synchronize()
         rd.purlin_destroy(h)
+
+
+@pytest.mark.parametrize("atom", [rd.ATOM_COPY_ENGINE, rd.ATOM_BULK])
+def test_replayed_graph_with_other_copy_atoms(atom):
+    """The copy-engine Atom (memcpy nodes, no kernel) and the TMA bulk Atom inside
+    a captured graph: every replay copies the buffers' current contents."""
+    rd.build()
+    R, c = 8, 30001
+    y = [torch.empty(c, dtype=torch.bfloat16, device="cuda") for _ in range(R)]
+    z = [torch.empty(R * c, dtype=torch.bfloat16, device="cuda") for _ in range(R)]
+    h = rd.purlin_create(R)
+    try:
+        rd.purlin_set_policy(h, 0, 0, 0, rd.VARIANT_ZS)
+        rd.purlin_set_atom(h, atom)
+        stream = torch.cuda.Stream()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            rd.purlin_all_gather(h, y, z, [c] * R, None, "bf16")
+        for replay in range(3):
+            fresh = workloads.rank_buffers("rs_ag_r8_bf16", R, c, "bf16", role=20 + replay,
+                                           device="cuda")
+            for dst, src in zip(y, fresh):
+                dst.copy_(src)
+            torch.cuda.synchronize()
+            g.replay()
+            torch.cuda.synchronize()
+            assert rd.purlin_query_status(h) == rd.OK
+            want = np.concatenate([host_bits(t) for t in y])
+            for k in range(R):
+                assert np.array_equal(host_bits(z[k]), want), (replay, k)
+        del g
+    finally:
+        torch.cuda.synchronize()
+        rd.purlin_destroy(h)
