@@ -53,6 +53,16 @@ def test_null_handle_is_invalid(lib):
     assert lib.purlin_query_status(None) == rd.ERR_INVALID_ARG
     assert lib.purlin_destroy(None) == rd.OK
     assert lib.purlin_all_reduce(None, None, None, 4, rd.F32, rd.OP_SUM, None) == rd.ERR_INVALID_ARG
+    for setter in (lib.purlin_set_atom, lib.purlin_set_direction, lib.purlin_set_small_tiles,
+                   lib.purlin_set_reduce_order, lib.purlin_debug_inject):
+        assert setter(None, 0) == rd.ERR_INVALID_ARG
+    assert lib.purlin_set_timeout(None, 1) == rd.ERR_INVALID_ARG
+    assert lib.purlin_last_launch(None, None) == rd.ERR_INVALID_ARG
+    # plans: no handle, no plan
+    assert lib.purlin_plan_begin(None) == rd.ERR_INVALID_ARG
+    assert lib.purlin_plan_end(None, None) == rd.ERR_INVALID_ARG
+    assert lib.purlin_plan_launch(None, None) == rd.ERR_INVALID_ARG
+    assert lib.purlin_plan_destroy(None) == rd.OK
 
 
 # ----------------------------------------------------------------- plan tests
