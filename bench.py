@@ -506,6 +506,7 @@ def bench_purlin(args):
 
         # ---- the other workload configurations, zero staging (default policy)
         configs = other_configs(rd, torch, dev, stream, peak)
+        configs["zs_by_rank_count"] = rank_scaling(rd, torch, dev, stream, peak)
 
         # ---- AllReduce size sweep: zero staging vs SNAC (default policy)
         sweep = allreduce_sweep(rd, torch, dev, stream, peak)
@@ -729,6 +730,44 @@ def tree_order_report(rd, torch, h, x, y_fixed, counts, stream, coll_b, peak):
             "elements_differing_from_fixed_order": round(differing / (R * c), 4),
             "max_bf16_ulp_vs_fixed_order": max_ulp,
             "max_abs_diff_over_sum_abs": max_scaled}
+
+
+def rank_scaling(rd, torch, dev, stream, peak):
+    """Zero-staging bandwidth against the number of virtual ranks (64 MiB per
+    rank, bf16): the Atom's R-way loop at R = 2, 4, 8 and the fp32 sums."""
+    out = []
+    n = BYTES_PER_RANK // 2
+    for R_ in (2, 4, 8):
+        h = rd.purlin_create(R_, 0, dev.index)
+        try:
+            x = [torch.randn(n, device=dev).to(torch.bfloat16) for _ in range(R_)]
+            o = [torch.empty_like(t) for t in x]
+            c = n // R_
+            y = [torch.empty(c, dtype=torch.bfloat16, device=dev) for _ in range(R_)]
+            runs = (("all_reduce", lambda: rd.purlin_all_reduce(h, x, o, n, "bf16", stream=stream),
+                     2 * R_ * n * 2),
+                    ("reduce_scatter", lambda: rd.purlin_reduce_scatter(h, x, y, [c] * R_, None, "bf16",
+                                                                         stream=stream),
+                     (R_ + 1) * c * R_ * 2),
+                    ("all_gather", lambda: rd.purlin_all_gather(h, y, o, [c] * R_, None, "bf16",
+                                                                 stream=stream),
+                     (R_ + 1) * c * R_ * 2))
+            for name, fn, nbytes in runs:
+                with torch.cuda.stream(stream):
+                    for _ in range(3):
+                        fn()
+                torch.cuda.synchronize()
+                us = _events_us(torch, stream, fn, 20)
+                gbs = nbytes / (us / 1e6) / 1e9
+                out.append({"R": R_, "collective": name, "us": round(us, 1), "gbs": round(gbs, 1),
+                            "frac_of_peak": round(gbs / peak, 3)})
+            del x, o, y
+            if rd.purlin_query_status(h) != rd.OK:
+                raise RuntimeError("rank scaling: device status not ok")
+        finally:
+            rd.purlin_destroy(h)
+            torch.cuda.empty_cache()
+    return out
 
 
 def other_configs(rd, torch, dev, stream, peak):
