@@ -252,13 +252,14 @@ struct F16 {
 //          last value moves up a level unchanged.
 // __fadd_rn keeps every add a separately rounded IEEE binary32 add.
 
-template <int ORDER>
-__device__ __forceinline__ float fold(float (&v)[kMaxRanks], int R)
+template <int ORDER, int N>
+__device__ __forceinline__ float fold(float (&v)[N], int R)
 {
+    static_assert(N <= kMaxRanks, "at most kMaxRanks values");
     if (ORDER == 0) {
         float acc = v[0];
 #pragma unroll
-        for (int r = 1; r < kMaxRanks; ++r)
+        for (int r = 1; r < N; ++r)
             if (r < R) acc = __fadd_rn(acc, v[r]);
         return acc;
     } else {
@@ -266,7 +267,7 @@ __device__ __forceinline__ float fold(float (&v)[kMaxRanks], int R)
 #pragma unroll
         for (int level = 0; level < 3; ++level) {
 #pragma unroll
-            for (int p = 0; p < kMaxRanks / 2; ++p) {
+            for (int p = 0; p < N / 2; ++p) {
                 if (2 * p + 1 < live) v[p] = __fadd_rn(v[2 * p], v[2 * p + 1]);
                 else if (2 * p < live) v[p] = v[2 * p];
             }
@@ -276,9 +277,10 @@ __device__ __forceinline__ float fold(float (&v)[kMaxRanks], int R)
     }
 }
 
-// Atom::reduce of one vector unit: R source vectors -> one output vector.
-template <typename T, int ORDER, int BYTES>
-__device__ __forceinline__ void reduce_unit(const Vec<BYTES> (&src)[kMaxRanks], int R,
+// Atom::reduce of one vector unit: R source vectors (R <= NSRC) -> one output
+// vector.
+template <typename T, int ORDER, int BYTES, int NSRC>
+__device__ __forceinline__ void reduce_unit(const Vec<BYTES> (&src)[NSRC], int R,
                                             Vec<BYTES>& dst)
 {
     constexpr int W = BYTES / 4;
@@ -287,9 +289,9 @@ __device__ __forceinline__ void reduce_unit(const Vec<BYTES> (&src)[kMaxRanks], 
         float out[2];
 #pragma unroll
         for (int h = 0; h < T::kPerWord; ++h) {
-            float v[kMaxRanks];
+            float v[NSRC];
 #pragma unroll
-            for (int r = 0; r < kMaxRanks; ++r) v[r] = (r < R) ? T::widen(src[r].w[w], h) : 0.0f;
+            for (int r = 0; r < NSRC; ++r) v[r] = (r < R) ? T::widen(src[r].w[w], h) : 0.0f;
             out[h] = fold<ORDER>(v, R);
         }
         dst.w[w] = T::narrow(out);

@@ -198,7 +198,7 @@ ZsKnobs zs_knobs(const purlin_handle* h, Coll coll)
 {
     ZsKnobs k;
     const bool reduce = coll == Coll::ReduceScatter || coll == Coll::AllReduce;
-    k.tile_units = reduce ? kTileUnitsReduce
+    k.tile_units = reduce ? kThreads * reduce_unroll(h->R, h->order)
                           : (h->atom == PURLIN_ATOM_BULK ? kTileUnitsBulk : kTileUnitsCopy);
     k.max_unit_log2 = h->max_unit_log2 ? h->max_unit_log2 : 5;
     k.l2_load = h->l2_load >= 0 ? (uint32_t)h->l2_load : kL2EvictFirst;
@@ -472,8 +472,8 @@ purlin_status_t run(purlin_handle_t h, Coll coll, const void* const in_[], void*
             } else {
                 const bool small = replan_small(h, coll, p, pieces, np, R, in, out, esz, reduce, knobs);
                 if (reduce) {
-                    grid = zs_grid(h, p.ntiles, zs_reduce_resident_ctas(dtype, h->order, fan_all, small));
-                    zs_reduce_select(k, dtype, h->order, fan_all, small);
+                    grid = zs_grid(h, p.ntiles, zs_reduce_resident_ctas(dtype, h->order, fan_all, small, R));
+                    zs_reduce_select(k, dtype, h->order, fan_all, small, R);
                 } else {
                     grid = zs_grid(h, p.ntiles, zs_copy_resident_ctas(false, fan_all, small));
                     zs_copy_select(k, false, fan_all, small);

@@ -46,8 +46,12 @@ int resident_ctas_of(const void* kernel, int threads);
 // Sum over ranks.  fan_all: write each result to every output (AllReduce),
 // else to the segment's destination (ReduceScatter).  small: one-warp CTAs, plan
 // built with kTileUnitsSmall; else kThreads-thread CTAs, kTileUnitsReduce.
-void zs_reduce_select(KernelLaunch& k, int dtype, int order, bool fan_all, bool small);
-int zs_reduce_resident_ctas(int dtype, int order, bool fan_all, bool small);
+// Units per thread of the kThreads-thread sum kernel for R ranks and a rank
+// order (R x units <= kMaxRanks vectors in flight per thread); the plan's tiles
+// are kThreads x reduce_unroll(R, order) units.
+int reduce_unroll(int R, int order);
+void zs_reduce_select(KernelLaunch& k, int dtype, int order, bool fan_all, bool small, int R);
+int zs_reduce_resident_ctas(int dtype, int order, bool fan_all, bool small, int R);
 
 // Copy.  fan_all: every segment goes to every output (AllGather), else to the
 // segment's destination (AllToAll(V)).  large: ZsParams<kSegsLarge> (else

@@ -13,26 +13,33 @@ namespace {
 
 using ReduceKernel = void (*)(ZsParams<kSegsSmall>);
 
-template <typename T, int THREADS>
+// NR = kMaxRanks / units per thread.  The pairwise rank order keeps one unit
+// per thread (NR = kMaxRanks).
+template <typename T, int THREADS, int NR>
 ReduceKernel pick_reduce(int order, bool fan_all)
 {
     if (order == 0)
-        return fan_all ? zs_reduce_kernel<T, 0, true, THREADS> : zs_reduce_kernel<T, 0, false, THREADS>;
-    return fan_all ? zs_reduce_kernel<T, 1, true, THREADS> : zs_reduce_kernel<T, 1, false, THREADS>;
+        return fan_all ? zs_reduce_kernel<T, 0, true, THREADS, NR> : zs_reduce_kernel<T, 0, false, THREADS, NR>;
+    return fan_all ? zs_reduce_kernel<T, 1, true, THREADS, kMaxRanks>
+                   : zs_reduce_kernel<T, 1, false, THREADS, kMaxRanks>;
 }
 
-template <int THREADS>
+template <int THREADS, int NR>
 ReduceKernel reduce_kernel_t(int dtype, int order, bool fan_all)
 {
-    if (dtype == kF32) return pick_reduce<atom::F32, THREADS>(order, fan_all);
-    if (dtype == kBF16) return pick_reduce<atom::BF16, THREADS>(order, fan_all);
-    return pick_reduce<atom::F16, THREADS>(order, fan_all);
+    if (dtype == kF32) return pick_reduce<atom::F32, THREADS, NR>(order, fan_all);
+    if (dtype == kBF16) return pick_reduce<atom::BF16, THREADS, NR>(order, fan_all);
+    return pick_reduce<atom::F16, THREADS, NR>(order, fan_all);
 }
 
-ReduceKernel reduce_kernel_for(int dtype, int order, bool fan_all, bool small)
+ReduceKernel reduce_kernel_for(int dtype, int order, bool fan_all, bool small, int unroll)
 {
-    return small ? reduce_kernel_t<kSmallThreads>(dtype, order, fan_all)
-                 : reduce_kernel_t<kThreads>(dtype, order, fan_all);
+    if (small) return reduce_kernel_t<kSmallThreads, kMaxRanks>(dtype, order, fan_all);
+    switch (unroll) {
+    case 4: return reduce_kernel_t<kThreads, kMaxRanks / 4>(dtype, order, fan_all);
+    case 2: return reduce_kernel_t<kThreads, kMaxRanks / 2>(dtype, order, fan_all);
+    default: return reduce_kernel_t<kThreads, kMaxRanks>(dtype, order, fan_all);
+    }
 }
 
 template <int MAXSEG>
@@ -141,18 +148,26 @@ cudaError_t launch_kernel(const KernelLaunch& k, cudaStream_t stream)
     return cudaLaunchKernelExC(&cfg, k.func, args);
 }
 
-void zs_reduce_select(KernelLaunch& k, int dtype, int order, bool fan_all, bool small)
+int reduce_unroll(int R, int order)
 {
-    k.func = reinterpret_cast<const void*>(reduce_kernel_for(dtype, order, fan_all, small));
+    if (order != 0) return 1;
+    return R >= 5 ? 1 : R >= 3 ? 2 : 4;
+}
+
+void zs_reduce_select(KernelLaunch& k, int dtype, int order, bool fan_all, bool small, int R)
+{
+    k.func = reinterpret_cast<const void*>(
+        reduce_kernel_for(dtype, order, fan_all, small, reduce_unroll(R, order)));
     k.block = small ? kSmallThreads : kThreads;
     k.smem = 0;
     k.cooperative = false;
     k.params_bytes = sizeof(ZsParams<kSegsSmall>);
 }
 
-int zs_reduce_resident_ctas(int dtype, int order, bool fan_all, bool small)
+int zs_reduce_resident_ctas(int dtype, int order, bool fan_all, bool small, int R)
 {
-    return resident_ctas(reinterpret_cast<const void*>(reduce_kernel_for(dtype, order, fan_all, small)),
+    return resident_ctas(reinterpret_cast<const void*>(
+                             reduce_kernel_for(dtype, order, fan_all, small, reduce_unroll(R, order))),
                          small ? kSmallThreads : kThreads);
 }
 

@@ -48,24 +48,39 @@ __device__ __forceinline__ void pdl_enter()
 
 // ------------------------------------------------------------------ reduce
 
-template <typename T, int ORDER, bool FAN_ALL, int BYTES>
-__device__ __forceinline__ void reduce_vector(const ZsParams<kSegsSmall>& p, const Segment& s,
-                                              uint64_t off, int R, uint64_t lpol, uint64_t spol)
+// One tile of vector units: U = kMaxRanks / NR units per thread for at most NR
+// ranks (R <= NR), each warp access contiguous.  All R x U loads are issued
+// before the first add, so every rank count keeps up to kMaxRanks independent
+// requests in flight per thread.
+template <typename T, int ORDER, bool FAN_ALL, int BYTES, int NR, int THREADS>
+__device__ __forceinline__ void reduce_tile(const ZsParams<kSegsSmall>& p, const Segment& s,
+                                            uint64_t base, int R, uint64_t lpol, uint64_t spol)
 {
-    atom::Vec<BYTES> v[kMaxRanks];
-    // All R loads are issued before the first add: R independent requests in
-    // flight per thread.
+    constexpr int U = kMaxRanks / NR;
+    const uint64_t rem = s.bytes - base;
+    atom::Vec<BYTES> v[U][NR];
 #pragma unroll
-    for (int r = 0; r < kMaxRanks; ++r)
-        if (r < R) atom::load(v[r], p.in[r] + s.src_off + off, lpol);
-    atom::Vec<BYTES> o;
-    atom::reduce_unit<T, ORDER, BYTES>(v, R, o);
-    if (FAN_ALL) {
+    for (int k = 0; k < U; ++k) {
+        const uint64_t o = (uint64_t)(k * THREADS + threadIdx.x) * BYTES;
+        if (o < rem) {
 #pragma unroll
-        for (int r = 0; r < kMaxRanks; ++r)
-            if (r < R) atom::store(p.out[r] + s.dst_off + off, o, spol);
-    } else {
-        atom::store(p.out[s.dst] + s.dst_off + off, o, spol);
+            for (int r = 0; r < NR; ++r)
+                if (r < R) atom::load(v[k][r], p.in[r] + s.src_off + base + o, lpol);
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < U; ++k) {
+        const uint64_t o = (uint64_t)(k * THREADS + threadIdx.x) * BYTES;
+        if (o >= rem) continue;
+        atom::Vec<BYTES> out;
+        atom::reduce_unit<T, ORDER, BYTES, NR>(v[k], R, out);
+        if (FAN_ALL) {
+#pragma unroll
+            for (int r = 0; r < NR; ++r)
+                if (r < R) atom::store(p.out[r] + s.dst_off + base + o, out, spol);
+        } else {
+            atom::store(p.out[s.dst] + s.dst_off + base + o, out, spol);
+        }
     }
 }
 
@@ -86,12 +101,15 @@ __device__ __forceinline__ void reduce_element(const ZsParams<kSegsSmall>& p, co
     }
 }
 
-// THREADS threads per CTA, one unit per thread per tile: kThreads for large
-// messages, one warp (kSmallThreads) for small ones.
-template <typename T, int ORDER, bool FAN_ALL, int THREADS>
+// THREADS threads per CTA: kThreads for large messages, one warp
+// (kSmallThreads) for small ones.  NR bounds the rank count (R <= NR); a tile
+// holds THREADS x (kMaxRanks / NR) units, so sums of 2 or 4 ranks take 4 or 2
+// units per thread.
+template <typename T, int ORDER, bool FAN_ALL, int THREADS, int NR>
 __global__ void __launch_bounds__(THREADS, THREADS == kThreads ? 2 : 16)
 zs_reduce_kernel(const __grid_constant__ ZsParams<kSegsSmall> p)
 {
+    constexpr int U = kMaxRanks / NR;
     pdl_enter();
     const int R = (int)p.R;
     const uint64_t lpol = atom::l2_policy(p.l2_load);
@@ -99,12 +117,18 @@ zs_reduce_kernel(const __grid_constant__ ZsParams<kSegsSmall> p)
     for (uint32_t t = blockIdx.x; t < p.ntiles; t += gridDim.x) {
         const Segment& s = segment_of(p, t);
         const int ul = s.unit_log2;
-        const uint64_t off = (uint64_t)(t - s.tile0) * tile_bytes(ul, THREADS) +
-                             ((uint64_t)threadIdx.x << ul);
-        if (off >= s.bytes) continue;
-        if (ul == 5) reduce_vector<T, ORDER, FAN_ALL, 32>(p, s, off, R, lpol, spol);
-        else if (ul == 4) reduce_vector<T, ORDER, FAN_ALL, 16>(p, s, off, R, lpol, spol);
-        else reduce_element<T, ORDER, FAN_ALL>(p, s, off, R);
+        const uint64_t base = (uint64_t)(t - s.tile0) * tile_bytes(ul, THREADS * U);
+        if (ul == 5) {
+            reduce_tile<T, ORDER, FAN_ALL, 32, NR, THREADS>(p, s, base, R, lpol, spol);
+        } else if (ul == 4) {
+            reduce_tile<T, ORDER, FAN_ALL, 16, NR, THREADS>(p, s, base, R, lpol, spol);
+        } else {
+#pragma unroll
+            for (int k = 0; k < U; ++k) {
+                const uint64_t off = base + ((uint64_t)(k * THREADS + threadIdx.x) << ul);
+                if (off < s.bytes) reduce_element<T, ORDER, FAN_ALL>(p, s, off, R);
+            }
+        }
     }
 }
 

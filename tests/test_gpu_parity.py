@@ -64,7 +64,7 @@ def oracle_in(bufs):
 
 @pytest.mark.parametrize("policy", list(POLICIES))
 @pytest.mark.parametrize("dtype", ["bf16", "f32", "f16"])
-@pytest.mark.parametrize("R", [1, 2, 3, 8])
+@pytest.mark.parametrize("R", [1, 2, 3, 4, 8])
 @pytest.mark.parametrize("n", [0, 1, 7, 33, 4096, 70001])
 def test_all_reduce(policy, dtype, R, n):
     h = handle(R)
@@ -126,7 +126,7 @@ def _rs_case(R, seed, explicit):
 
 @pytest.mark.parametrize("policy", list(POLICIES))
 @pytest.mark.parametrize("dtype", ["bf16", "f32", "f16"])
-@pytest.mark.parametrize("R", [1, 3, 8])
+@pytest.mark.parametrize("R", [1, 2, 3, 4, 8])
 @pytest.mark.parametrize("explicit", [False, True])
 def test_reduce_scatter_v(policy, dtype, R, explicit):
     h = handle(R)
@@ -174,6 +174,36 @@ def test_reduce_scatter_unaligned_partitions(policy, dtype):
     for k in range(R):
         assert same_bits(host_bits(outs[k].view), want[k])
         assert outs[k].guards_intact()
+
+
+@pytest.mark.parametrize("coll", ["all_reduce", "reduce_scatter"])
+@pytest.mark.parametrize("dtype", ["bf16", "f32", "f16"])
+@pytest.mark.parametrize("R", [2, 3, 4, 5])
+@pytest.mark.parametrize("offset", [0, 1, 4, 8])
+def test_sums_of_few_ranks_over_many_tiles(coll, dtype, R, offset):
+    """Sums of 2 to 4 ranks take 2 or 4 units per thread: messages of several
+    such tiles (256 threads x 4 x 32 B = 32 KiB) with a ragged tail; streams
+    `offset` elements into their allocations leave 32-byte, 16-byte or
+    element-wise bodies."""
+    esize = 4 if dtype == "f32" else 2
+    n = (5 * 32768 + 4 * 777) // esize + 3
+    h = handle(R)
+    set_variant(h, *POLICIES["zs_large"])
+    x = [inputs(1, n, dtype, seed=900 + 10 * R + r, offset=offset)[0] for r in range(R)]
+    if coll == "all_reduce":
+        outs = [Guarded(n, dtype, offset=offset) for _ in range(R)]
+        rd.purlin_all_reduce(h, x, [o.view for o in outs], n, dtype)
+        want = oracle.all_reduce(oracle_in(x), dtype=dtype)
+    else:
+        counts = np.full(R, n // R)
+        counts[-1] += n - int(counts.sum())
+        outs = [Guarded(int(c), dtype, offset=offset) for c in counts]
+        rd.purlin_reduce_scatter(h, x, [o.view for o in outs], counts, None, dtype)
+        want = oracle.reduce_scatter(oracle_in(x), counts, None, dtype=dtype)
+    run_ok(h)
+    for j in range(R):
+        assert same_bits(host_bits(outs[j].view), want[j]), j
+        assert outs[j].guards_intact()
 
 
 # ------------------------------------------------------------------ AllGather
