@@ -320,8 +320,9 @@ PURLIN_API purlin_status_t purlin_set_direction(purlin_handle_t h, int direction
  * large-message plan has fewer than `tiles` tiles runs one-warp CTAs with one
  * access unit per thread instead of 256-thread CTAs, so that a message of a few
  * KiB is spread over many SMs rather than queued in the load/store path of one
- * (a tile: 256 threads x one 16/32-byte unit for sums, x four units for
- * copies; the TMA bulk Atom always runs its own shape).  tiles = 0: never;
+ * (a tile here: 256 threads x one 16/32-byte unit for sums, counted so also
+ * where sums of 2 to 4 ranks run larger tiles; x four units for copies; the TMA
+ * bulk Atom always runs its own shape).  tiles = 0: never;
  * tiles = -1: the library default, per collective (measured on GB300: 256 for
  * AllReduce, 64 for the others).  Other negative values:
  * PURLIN_ERR_INVALID_ARG. */

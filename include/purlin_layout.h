@@ -53,7 +53,9 @@ typedef struct {
  *   max_unit   widest access in bytes (16 or 32).
  *   segs       caller array of max_segs entries; *nsegs receives the count and
  *              *ntiles the number of tiles.  Tiles are those of the 256-thread
- *              zero-staging launch (256 units for sums, 1024 for copies); a call
+ *              zero-staging launch: 1024 units for copies; for sums in the fixed
+ *              rank order 256 x U units, U = 4 for R <= 2, 2 for R = 3..4 and 1
+ *              above (the pairwise order keeps U = 1, so its tiles differ); a call
  *              with fewer than the small-message threshold of them
  *              (purlin_set_small_tiles) runs one-warp tiles of 32 units over the
  *              same segments.

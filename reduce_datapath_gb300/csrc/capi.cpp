@@ -238,7 +238,7 @@ purlin_status_t make_params(ZsParams<MAXSEG>& p, const Piece* pieces, int npiece
 }
 
 // Small messages: when the large-message plan has fewer than h->small_tiles
-// tiles, the call runs one-warp CTAs over one-warp tiles instead, so that its
+// tiles (of kTileUnitsReduce units for sums, kTileUnitsCopy for copies), the call runs one-warp CTAs over one-warp tiles instead, so that its
 // few KiB spread over many SMs rather than queue in the load/store path of a
 // few.  Returns true (and the re-planned params) if so.
 template <int MAXSEG>
@@ -247,7 +247,10 @@ bool replan_small(const purlin_handle* h, Coll coll, ZsParams<MAXSEG>& p, const 
                   bool reduce, ZsKnobs& k)
 {
     const long threshold = h->small_tiles >= 0 ? h->small_tiles : small_tiles_default(coll);
-    if ((long)p.ntiles >= threshold) return false;
+    // counted in tiles of one unit per thread for sums, whatever reduce_unroll
+    // gave, so that the switch sits at the same message size for every R
+    const long scale = reduce ? std::max(1, (int)k.tile_units / kTileUnitsReduce) : 1;
+    if ((long)p.ntiles * scale >= threshold) return false;
     ZsKnobs ks = k;
     ks.tile_units = kTileUnitsSmall;
     if (reduce && !h->max_unit_log2) ks.max_unit_log2 = std::min(ks.max_unit_log2, 4);
@@ -822,7 +825,8 @@ purlin_status_t purlin_plan_segments(purlin_collective_t coll, int R, const uint
     Segment tmp[kSegsLarge];
     uint32_t nt = 0;
     int n = layout_segments(pieces, np, R, in_addr, out_addr, esz, reduce,
-                            reduce ? kTileUnitsReduce : kTileUnitsCopy, max_unit == 32 ? 5 : 4, tmp,
+                            reduce ? kThreads * reduce_unroll(R, 0) : kTileUnitsCopy,
+                            max_unit == 32 ? 5 : 4, tmp,
                             kSegsLarge, &nt);
     if (n < 0 || n > max_segs) return PURLIN_ERR_UNSUPPORTED;
     for (int i = 0; i < n; ++i) {

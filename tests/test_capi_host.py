@@ -133,8 +133,9 @@ def check_alignment(segs, R, in_addr, out_addr, reduce, esz):
             assert u in (esz, 16, 32)
 
 
-def check_tiles(segs, ntiles, reduce):
-    unroll = 1 if reduce else 4
+def check_tiles(segs, ntiles, reduce, R):
+    # sums in the fixed rank order: 4 units per thread for R <= 2, 2 for R <= 4
+    unroll = (4 if R <= 2 else 2 if R <= 4 else 1) if reduce else 4
     t = 0
     for s in segs:
         assert s["tile0"] == t
@@ -199,7 +200,7 @@ def test_plan_covers_every_output_byte_once(lib, coll, dtype, seed):
     segs, ntiles = rd.purlin_plan_segments(coll, R, in_addr, out_addr, counts, da, db, count,
                                            dtype)
     check_alignment(segs, R, in_addr, out_addr, reduce, esz)
-    check_tiles(segs, ntiles, reduce)
+    check_tiles(segs, ntiles, reduce, R)
     got = plan_map(segs, R)
     want = expected_map(coll, R, counts, da, db, count, esz)
     assert got == want

@@ -554,16 +554,18 @@ def test_staged_kinds_share_a_handle():
         set_variant(h, rd.VARIANT_AUTO)
 
 
-@pytest.mark.parametrize("coll,nbytes,small", [
-    ("ar", 4096, True), ("ar", 1 << 20, True), ("ar", 4 << 20, False),
-    ("rs", 256 << 10, True), ("rs", 1 << 20, False),
-    ("ag", 1 << 20, True), ("ag", 16 << 20, False),
+@pytest.mark.parametrize("coll,nbytes,small,R", [
+    ("ar", 4096, True, 8), ("ar", 1 << 20, True, 8), ("ar", 4 << 20, False, 8),
+    ("rs", 256 << 10, True, 8), ("rs", 1 << 20, False, 8),
+    ("ag", 1 << 20, True, 8), ("ag", 16 << 20, False, 8),
+    # sums of 2 ranks run 4 units per thread; the switch stays at the same size
+    ("ar", 1 << 20, True, 2), ("ar", 4 << 20, False, 2),
+    ("rs", 256 << 10, True, 2), ("rs", 1 << 20, False, 2),
 ])
-def test_launch_shape_follows_message_size(coll, nbytes, small):
+def test_launch_shape_follows_message_size(coll, nbytes, small, R):
     """One-warp CTAs below the per-collective threshold (AllReduce: 256 tiles of
     256 x 32 B; the others: 64 tiles), 256-thread CTAs above it; the result is
     the oracle's either way."""
-    R = 8
     n = nbytes // 2
     c = n // R
     h = handle(R)
