@@ -494,6 +494,7 @@ def bench_purlin(args):
     if not args.quick:
         # ---- AllReduce latency at 4 KiB per rank (R=8 bf16, 2048 elements)
         lat = allreduce_latency(rd, torch, dev, stream, variant)
+        lat["c_caller"] = c_caller_cost(rd)
 
         # ---- the same step through the staged (SNAC) path, default policy
         staged = staged_step(rd, torch, h, rs, ag, stream, rs_b + ag_b, peak)
@@ -995,6 +996,34 @@ def allreduce_latency(rd, torch, dev, stream, variant):
             "us_back_to_back_prepared_call": b2b["prepared"][0],
             "host_us_per_call": {"plan": b2b["plan"][1], "prepared_call": b2b["prepared"][1]},
             "us_single_event_median": statistics.median(single), "R": R, "bytes_per_rank": 4096}
+
+
+def c_caller_cost(rd):
+    """Host time per call of the same AllReduce from a plain C99 caller
+    (tests/c_abi/abi_check.c, built here against include/*.h and the library):
+    planning alone, recording a plan, a direct call, a plan launch."""
+    import shutil
+    import tempfile
+    from reduce_datapath_gb300 import _build
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        return "unavailable: no C compiler"
+    cuda = os.path.dirname(os.path.dirname(_build.nvcc()))
+    libdir = os.path.dirname(rd.LIB_PATH)
+    with tempfile.TemporaryDirectory() as tmp:
+        exe = os.path.join(tmp, "abi_check")
+        cmd = [gcc, "-std=c99", "-O1", "-o", exe,
+               os.path.join(ROOT, "tests", "c_abi", "abi_check.c"),
+               "-I", os.path.join(ROOT, "include"), "-I", os.path.join(cuda, "include"),
+               "-L", libdir, "-lpurlin", "-L", os.path.join(cuda, "lib64"), "-lcudart",
+               "-Wl,-rpath," + libdir, "-Wl,-rpath," + os.path.join(cuda, "lib64")]
+        b = subprocess.run(cmd, capture_output=True, text=True)
+        if b.returncode != 0:
+            return "unavailable: build failed: " + (b.stderr.strip().splitlines() or ["?"])[-1]
+        r = subprocess.run([exe, "cost"], capture_output=True, text=True, timeout=120)
+        if r.returncode != 0:
+            return f"failed: exit {r.returncode}"
+        return json.loads(r.stdout.strip().splitlines()[-1])
 
 
 def bench_e2e(args, rd, torch, h, x, y, z, counts, stream):

@@ -30,8 +30,7 @@ constexpr int kThreads = 256;          // threads per CTA of every Atom kernel
 constexpr uint8_t kEveryRank = 0xff;   // src: sum over all ranks; dst: all outputs
 constexpr int kSegsSmall = 24;         // RS / AG / AR: <= 3 segments per rank
 constexpr int kSegsLarge = 3 * kMaxRanks * kMaxRanks;  // A2AV: <= 3 per pair
-constexpr int kUnrollReduce = 1;       // units per thread per tile, sums of > 4 ranks
-                                       // (reduce_unroll: 2 for 3-4 ranks, 4 for 1-2)
+constexpr int kUnrollReduce = 1;       // units per thread per tile, sums
 constexpr int kUnrollCopy = 4;         // units per thread per tile, copies
 // Units per tile of the large-message launches (kThreads threads per CTA).
 constexpr int kTileUnitsReduce = kThreads * kUnrollReduce;

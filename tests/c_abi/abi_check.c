@@ -7,12 +7,20 @@
  *                    (sums are exact in any order) and compare with the sums
  *                    computed here; then ReduceScatter + AllGather must equal it;
  *                    then the AllReduce kept as a plan and launched twice.
+ *   abi_check cost   host time per call of an 8-rank bf16 AllReduce of 4 KiB per
+ *                    rank, printed as one JSON line: planning alone
+ *                    (purlin_plan_segments), recording a plan (begin, call, end,
+ *                    destroy: layout and kernel parameters, nothing enqueued),
+ *                    a direct call (planning + launch) and a recorded plan's
+ *                    launch.
  * Exit status 0 on success.
  */
+#define _POSIX_C_SOURCE 199309L
 #include <stdint.h>
 #include <stdio.h>
 #include <stdlib.h>
 #include <string.h>
+#include <time.h>
 
 #include <cuda_runtime_api.h>
 
@@ -130,8 +138,85 @@ static int gpu_check(void)
     return 0;
 }
 
+static double now_us(void)
+{
+    struct timespec t;
+    clock_gettime(CLOCK_MONOTONIC, &t);
+    return t.tv_sec * 1e6 + t.tv_nsec * 1e-3;
+}
+
+static int cost_check(void)
+{
+    enum { R = 8, N = 2048, ITERS = 20000 };   /* 2048 bf16 = 4 KiB per rank */
+    void* din[R];
+    void* dout[R];
+    uint64_t in_addr[R], out_addr[R];
+    for (int r = 0; r < R; ++r) {
+        if (cudaMalloc(&din[r], N * 2) != cudaSuccess || cudaMalloc(&dout[r], N * 2) != cudaSuccess)
+            return 30;
+        cudaMemset(din[r], 0, N * 2);
+        in_addr[r] = (uint64_t)(uintptr_t)din[r];
+        out_addr[r] = (uint64_t)(uintptr_t)dout[r];
+    }
+    purlin_segment_t segs[64];
+    int nseg = 0;
+    uint32_t tiles = 0;
+    double t0 = now_us();
+    for (int i = 0; i < ITERS; ++i)
+        if (purlin_plan_segments(PURLIN_COLL_ALL_REDUCE, R, in_addr, out_addr, NULL, NULL, NULL, N,
+                                 PURLIN_BF16, 32, segs, 64, &nseg, &tiles) != PURLIN_OK)
+            return 31;
+    const double plan_us = (now_us() - t0) / ITERS;
+
+    purlin_handle_t h = NULL;
+    if (purlin_create(&h, R, 0, 0) != PURLIN_OK) return 32;
+    purlin_plan_t plan = NULL;
+    for (int i = 0; i < 100; ++i)   /* warm-up: context, module, residency queries */
+        if (purlin_all_reduce(h, (const void* const*)din, dout, N, PURLIN_BF16, PURLIN_OP_SUM,
+                              NULL) != PURLIN_OK)
+            return 33;
+    if (cudaDeviceSynchronize() != cudaSuccess) return 34;
+    t0 = now_us();
+    for (int i = 0; i < ITERS; ++i) {
+        if (purlin_plan_begin(h) != PURLIN_OK ||
+            purlin_all_reduce(h, (const void* const*)din, dout, N, PURLIN_BF16, PURLIN_OP_SUM,
+                              NULL) != PURLIN_OK ||
+            purlin_plan_end(h, &plan) != PURLIN_OK || purlin_plan_destroy(plan) != PURLIN_OK)
+            return 35;
+    }
+    const double record_us = (now_us() - t0) / ITERS;
+    t0 = now_us();
+    for (int i = 0; i < ITERS; ++i)
+        if (purlin_all_reduce(h, (const void* const*)din, dout, N, PURLIN_BF16, PURLIN_OP_SUM,
+                              NULL) != PURLIN_OK)
+            return 36;
+    const double call_us = (now_us() - t0) / ITERS;
+    if (cudaDeviceSynchronize() != cudaSuccess) return 37;
+    if (purlin_plan_begin(h) != PURLIN_OK ||
+        purlin_all_reduce(h, (const void* const*)din, dout, N, PURLIN_BF16, PURLIN_OP_SUM, NULL) !=
+            PURLIN_OK ||
+        purlin_plan_end(h, &plan) != PURLIN_OK)
+        return 38;
+    t0 = now_us();
+    for (int i = 0; i < ITERS; ++i)
+        if (purlin_plan_launch(plan, NULL) != PURLIN_OK) return 39;
+    const double launch_us = (now_us() - t0) / ITERS;
+    if (cudaDeviceSynchronize() != cudaSuccess || purlin_query_status(h) != PURLIN_OK) return 40;
+    purlin_plan_destroy(plan);
+    purlin_destroy(h);
+    for (int r = 0; r < R; ++r) {
+        cudaFree(din[r]);
+        cudaFree(dout[r]);
+    }
+    printf("{\"R\": %d, \"bytes_per_rank\": %d, \"segments\": %d, \"plan_segments_us\": %.3f, "
+           "\"record_plan_us\": %.3f, \"call_us\": %.3f, \"plan_launch_us\": %.3f, \"iters\": %d}\n",
+           R, N * 2, nseg, plan_us, record_us, call_us, launch_us, ITERS);
+    return 0;
+}
+
 int main(int argc, char** argv)
 {
+    if (argc > 1 && strcmp(argv[1], "cost") == 0) return cost_check();
     if (argc > 1 && strcmp(argv[1], "gpu") == 0) {
         int rc = gpu_check();
         printf("gpu check: %d\n", rc);

@@ -3,8 +3,9 @@
 The program includes only include/*.h and links only libpurlin.so and the CUDA
 runtime.  On the CPU it plans an AllGather (host-only call); on the GPU it runs
 an AllReduce and a ReduceScatter + AllGather of fp32 integers and checks the
-exact sums it computes itself.
+exact sums it computes itself, and times the host side of small AllReduces.
 """
+import json
 import os
 import shutil
 import subprocess
@@ -48,3 +49,16 @@ def test_plan_from_c(program):
 def test_collectives_from_c(program):
     r = subprocess.run([program, "gpu"], capture_output=True, text=True, timeout=120)
     assert r.returncode == 0, r.stdout + r.stderr
+
+
+@pytest.mark.gpu
+def test_host_cost_from_c(program):
+    """Host time per call of a 4 KiB-per-rank AllReduce from C: one JSON line,
+    planning far below the launch (loose bounds: a shared host)."""
+    r = subprocess.run([program, "cost"], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stdout + r.stderr
+    cost = json.loads(r.stdout.strip().splitlines()[-1])
+    assert cost["segments"] == 1
+    assert 0 < cost["plan_segments_us"] < 20
+    assert 0 < cost["record_plan_us"] < 50
+    assert 0 < cost["plan_launch_us"] < 200 and 0 < cost["call_us"] < 200
