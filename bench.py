@@ -82,14 +82,28 @@ def measured_peaks():
 
 
 def cpu_model():
+    """The host CPU's model name (lscpu's on Arm, where /proc/cpuinfo gives
+    only a part number)."""
+    part = None
     try:
         with open("/proc/cpuinfo") as f:
             for line in f:
-                if line.lower().startswith(("model name", "cpu part")):
+                key = line.lower()
+                if key.startswith("model name"):
                     return line.split(":", 1)[1].strip()
+                if key.startswith("cpu part") and part is None:
+                    part = line.split(":", 1)[1].strip()
     except OSError:
         pass
-    return os.uname().machine
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name:"):
+                name = line.split(":", 1)[1].strip()
+                return f"{name} ({part})" if part else name
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return part or os.uname().machine
 
 
 class ClockSampler:
@@ -264,40 +278,47 @@ def run_cpu_oracle(xh, budget_s, max_reps=20):
 
 
 def run_cpu_oracle_threads(xh, budget_s, max_reps=20):
-    """The same oracle calls split by output partition over the host's cores:
-    thread k sums partition k (ReduceScatter restricted to one partition), then
-    thread j builds output j (the AllGather's block placement for one
-    destination, through the oracle's AllToAllV with only column j non-zero).
-    Each element's rank order is unchanged, so the results are bit-identical to
-    the single-threaded step; the oracle's own code is not changed.  ctypes
-    releases the interpreter lock during each C call."""
+    """The same oracle calls split over all the host's cores: the ReduceScatter
+    by output sub-range (partition k, elements [a, b): a ReduceScatter with only
+    that slice of partition k), the AllGather by (destination, source) block
+    (the oracle's AllToAllV with only that block non-zero).  Each element's rank
+    order is unchanged, so the results are bit-identical to the single-threaded
+    step; the oracle's own code is not changed.  ctypes releases the interpreter
+    lock during each C call."""
     import numpy as np
     from concurrent.futures import ThreadPoolExecutor
     import oracle
-    threads = min(R, os.cpu_count() or 1)
+    threads = max(1, os.cpu_count() or 1)
+    splits = max(1, -(-threads // R))            # sub-ranges per partition
+    bounds = [PART * i // splits for i in range(splits + 1)]
 
-    def rs_part(k):
+    def rs_slice(task):
+        k, i = divmod(task, splits)
+        a, b = bounds[i], bounds[i + 1]
         counts = [0] * R
-        counts[k] = PART
-        return oracle.reduce_scatter(xh, counts, [k * PART] * R, dtype="bf16")[k]
+        counts[k] = b - a
+        return oracle.reduce_scatter(xh, counts, [k * PART + a] * R, dtype="bf16")[k]
 
-    def ag_dest(j, y):
+    def ag_block(task, y):
+        j, src = divmod(task, R)
         C = np.zeros((R, R), dtype=np.uint64)
-        C[:, j] = PART
+        C[src, j] = PART
         return oracle.all_to_all_v(y, C)[j]
 
     reps, t0 = 0, time.perf_counter()
     with ThreadPoolExecutor(max_workers=threads) as pool:
         while True:
-            y = list(pool.map(rs_part, range(R)))
-            z = list(pool.map(lambda j: ag_dest(j, y), range(R)))
+            parts = list(pool.map(rs_slice, range(R * splits)))
+            y = [np.concatenate(parts[k * splits:(k + 1) * splits]) for k in range(R)]
+            blocks = list(pool.map(lambda t: ag_block(t, y), range(R * R)))
+            z = [np.concatenate(blocks[j * R:(j + 1) * R]) for j in range(R)]
             reps += 1
             el = time.perf_counter() - t0
             if el >= budget_s or reps >= max_reps:
                 break
     rs, ag = step_bytes()
     return {"value": reps * (rs + ag) / el / 1e9, "unit": UNIT, "cores": threads,
-            "kind": "oracle, split by output partition",
+            "kind": "oracle, split by output range",
             "sample": f"{reps} full step(s) of the workload in {el:.1f} s, {threads} threads, "
                       f"{cpu_model()}"}, y, z
 

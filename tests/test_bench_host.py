@@ -75,17 +75,19 @@ def _args(bench):
         sys.argv = argv
 
 
-def test_threaded_oracle_baseline_is_bit_identical(monkeypatch):
-    """The partition-split CPU baseline must produce exactly the single-threaded
-    oracle's step (same per-element rank order)."""
+@pytest.mark.parametrize("cores", [1, 8, 16, 20])
+def test_threaded_oracle_baseline_is_bit_identical(monkeypatch, cores):
+    """The range-split CPU baseline must produce exactly the single-threaded
+    oracle's step (same per-element rank order), whatever the core count."""
     import numpy as np
     import bench
     monkeypatch.setattr(bench, "PART", 777)
+    monkeypatch.setattr(bench.os, "cpu_count", lambda: cores)
     rng = np.random.default_rng(5)
     xh = [rng.integers(0, 1 << 16, size=bench.R * 777, dtype=np.uint16) & 0xBFFF
           for _ in range(bench.R)]
     _, y1, z1 = bench.run_cpu_oracle(xh, 0.0, max_reps=1)
     c2, y2, z2 = bench.run_cpu_oracle_threads(xh, 0.0, max_reps=1)
-    assert c2["cores"] >= 1 and c2["kind"].startswith("oracle")
+    assert c2["cores"] == cores and c2["kind"].startswith("oracle")
     assert all(np.array_equal(a, b) for a, b in zip(y1, y2))
     assert all(np.array_equal(a, b) for a, b in zip(z1, z2))
