@@ -48,6 +48,28 @@ MUTANTS = {
                                       "        for (uint64_t i = 0; i < recv_counts[k]; ++i)\n"
                                       "            store_elem("),
     "tree_drops_odd_carry": ("if (live & 1) v[next++] = v[live - 1];", ";"),
+    "tree_is_a_left_fold": ("            int live = R;\n",
+                            "            int live = R;\n"
+                            "            for (int r = 1; r < R; ++r) v[0] = v[0] + v[r];\n"
+                            "            live = 1;\n"),
+    "bf16_nan_becomes_infinity": ("return (uint16_t)((u >> 16) | 0x0040u);",
+                                  "return (uint16_t)((u >> 16) & 0xff80u);"),
+    "f16_overflow_saturates": ("if (enc > 0x7c00u) enc = 0x7c00u;",
+                               "if (enc > 0x7bffu) enc = 0x7bffu;"),
+    "f16_nan_becomes_infinity": ("if (a > 0x7f800000u) return (uint16_t)(sign | 0x7e00u);",
+                                 "if (a > 0x7f800000u) return (uint16_t)(sign | 0x7c00u);"),
+    "allreduce_skips_last_output": ("        for (int j = 0; j < R; ++j)\n"
+                                    "            store_elem(out[j], i, acc, dtype);",
+                                    "        for (int j = 0; j + 1 < R; ++j)\n"
+                                    "            store_elem(out[j], i, acc, dtype);"),
+    "allgather_ignores_out_displs": ("uint64_t D = start_of(counts, out_displs, k);",
+                                     "uint64_t D = start_of(counts, 0, k);"),
+    "alltoall_ignores_send_displs": ("send_displs ? send_displs + (size_t)s * R : 0, j);",
+                                     "0, j);"),
+    "alltoall_ignores_recv_displs": ("uint64_t rd = recv_displs ? recv_displs[(size_t)j * R + s] : packed_recv;",
+                                     "uint64_t rd = packed_recv;"),
+    "packed_partitions_skip_one": ("for (int m = 0; m < k; ++m) s += counts[m];",
+                                   "for (int m = 1; m < k; ++m) s += counts[m];"),
 }
 
 
