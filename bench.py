@@ -278,47 +278,43 @@ def run_cpu_oracle(xh, budget_s, max_reps=20):
 
 
 def run_cpu_oracle_threads(xh, budget_s, max_reps=20):
-    """The same oracle calls split over all the host's cores: the ReduceScatter
-    by output sub-range (partition k, elements [a, b): a ReduceScatter with only
-    that slice of partition k), the AllGather by (destination, source) block
-    (the oracle's AllToAllV with only that block non-zero).  Each element's rank
-    order is unchanged, so the results are bit-identical to the single-threaded
-    step; the oracle's own code is not changed.  ctypes releases the interpreter
-    lock during each C call."""
+    """The same oracle calls split by output partition over up to R host
+    threads: thread k sums partition k (ReduceScatter restricted to one
+    partition), then thread j builds output j (the AllGather's block placement
+    for one destination, through the oracle's AllToAllV with only column j
+    non-zero).  Each element's rank order is unchanged, so the results are
+    bit-identical to the single-threaded step; the oracle's own code is not
+    changed.  ctypes releases the interpreter lock during each C call.  A finer
+    split (sub-ranges of each partition over all 16 cores of a Grace host) needs
+    the oracle's separately returned pieces copied together, and that memory-
+    bound step then ran slower (10.6 GB/s against 12.3-13.4 GB/s)."""
     import numpy as np
     from concurrent.futures import ThreadPoolExecutor
     import oracle
-    threads = max(1, os.cpu_count() or 1)
-    splits = max(1, -(-threads // R))            # sub-ranges per partition
-    bounds = [PART * i // splits for i in range(splits + 1)]
+    threads = max(1, min(R, os.cpu_count() or 1))
 
-    def rs_slice(task):
-        k, i = divmod(task, splits)
-        a, b = bounds[i], bounds[i + 1]
+    def rs_part(k):
         counts = [0] * R
-        counts[k] = b - a
-        return oracle.reduce_scatter(xh, counts, [k * PART + a] * R, dtype="bf16")[k]
+        counts[k] = PART
+        return oracle.reduce_scatter(xh, counts, [k * PART] * R, dtype="bf16")[k]
 
-    def ag_block(task, y):
-        j, src = divmod(task, R)
+    def ag_dest(j, y):
         C = np.zeros((R, R), dtype=np.uint64)
-        C[src, j] = PART
+        C[:, j] = PART
         return oracle.all_to_all_v(y, C)[j]
 
     reps, t0 = 0, time.perf_counter()
     with ThreadPoolExecutor(max_workers=threads) as pool:
         while True:
-            parts = list(pool.map(rs_slice, range(R * splits)))
-            y = [np.concatenate(parts[k * splits:(k + 1) * splits]) for k in range(R)]
-            blocks = list(pool.map(lambda t: ag_block(t, y), range(R * R)))
-            z = [np.concatenate(blocks[j * R:(j + 1) * R]) for j in range(R)]
+            y = list(pool.map(rs_part, range(R)))
+            z = list(pool.map(lambda j: ag_dest(j, y), range(R)))
             reps += 1
             el = time.perf_counter() - t0
             if el >= budget_s or reps >= max_reps:
                 break
     rs, ag = step_bytes()
     return {"value": reps * (rs + ag) / el / 1e9, "unit": UNIT, "cores": threads,
-            "kind": "oracle, split by output range",
+            "kind": "oracle, split by output partition",
             "sample": f"{reps} full step(s) of the workload in {el:.1f} s, {threads} threads, "
                       f"{cpu_model()}"}, y, z
 
@@ -756,39 +752,43 @@ def tree_order_report(rd, torch, h, x, y_fixed, counts, stream, coll_b, peak):
 
 def rank_scaling(rd, torch, dev, stream, peak):
     """Zero-staging bandwidth against the number of virtual ranks (64 MiB per
-    rank, bf16): the Atom's R-way loop at R = 2, 4, 8 and the fp32 sums."""
+    rank): the Atom's R-way loop at R = 2, 4, 8 in bf16 (AllReduce,
+    ReduceScatter, AllGather), and the fp32 sums (AllReduce, ReduceScatter)."""
     out = []
-    n = BYTES_PER_RANK // 2
-    for R_ in (2, 4, 8):
-        h = rd.purlin_create(R_, 0, dev.index)
-        try:
-            x = [torch.randn(n, device=dev).to(torch.bfloat16) for _ in range(R_)]
-            o = [torch.empty_like(t) for t in x]
-            c = n // R_
-            y = [torch.empty(c, dtype=torch.bfloat16, device=dev) for _ in range(R_)]
-            runs = (("all_reduce", lambda: rd.purlin_all_reduce(h, x, o, n, "bf16", stream=stream),
-                     2 * R_ * n * 2),
-                    ("reduce_scatter", lambda: rd.purlin_reduce_scatter(h, x, y, [c] * R_, None, "bf16",
-                                                                         stream=stream),
-                     (R_ + 1) * c * R_ * 2),
-                    ("all_gather", lambda: rd.purlin_all_gather(h, y, o, [c] * R_, None, "bf16",
-                                                                 stream=stream),
-                     (R_ + 1) * c * R_ * 2))
-            for name, fn, nbytes in runs:
-                with torch.cuda.stream(stream):
-                    for _ in range(3):
-                        fn()
-                torch.cuda.synchronize()
-                us = _events_us(torch, stream, fn, 20)
-                gbs = nbytes / (us / 1e6) / 1e9
-                out.append({"R": R_, "collective": name, "us": round(us, 1), "gbs": round(gbs, 1),
-                            "frac_of_peak": round(gbs / peak, 3)})
-            del x, o, y
-            if rd.purlin_query_status(h) != rd.OK:
-                raise RuntimeError("rank scaling: device status not ok")
-        finally:
-            rd.purlin_destroy(h)
-            torch.cuda.empty_cache()
+    for dtype, colls in (("bf16", ("all_reduce", "reduce_scatter", "all_gather")),
+                         ("f32", ("all_reduce", "reduce_scatter"))):
+        tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+        esz = 2 if dtype == "bf16" else 4
+        n = BYTES_PER_RANK // esz
+        for R_ in (2, 4, 8):
+            h = rd.purlin_create(R_, 0, dev.index)
+            try:
+                x = [torch.randn(n, device=dev).to(tdt) for _ in range(R_)]
+                o = [torch.empty_like(t) for t in x]
+                c = n // R_
+                y = [torch.empty(c, dtype=tdt, device=dev) for _ in range(R_)]
+                runs = {"all_reduce": (lambda: rd.purlin_all_reduce(h, x, o, n, dtype, stream=stream),
+                                       2 * R_ * n * esz),
+                        "reduce_scatter": (lambda: rd.purlin_reduce_scatter(
+                            h, x, y, [c] * R_, None, dtype, stream=stream), (R_ + 1) * c * R_ * esz),
+                        "all_gather": (lambda: rd.purlin_all_gather(
+                            h, y, o, [c] * R_, None, dtype, stream=stream), (R_ + 1) * c * R_ * esz)}
+                for name in colls:
+                    fn, nbytes = runs[name]
+                    with torch.cuda.stream(stream):
+                        for _ in range(3):
+                            fn()
+                    torch.cuda.synchronize()
+                    us = _events_us(torch, stream, fn, 20)
+                    gbs = nbytes / (us / 1e6) / 1e9
+                    out.append({"R": R_, "dtype": dtype, "collective": name, "us": round(us, 1),
+                                "gbs": round(gbs, 1), "frac_of_peak": round(gbs / peak, 3)})
+                del x, o, y
+                if rd.purlin_query_status(h) != rd.OK:
+                    raise RuntimeError("rank scaling: device status not ok")
+            finally:
+                rd.purlin_destroy(h)
+                torch.cuda.empty_cache()
     return out
 
 
