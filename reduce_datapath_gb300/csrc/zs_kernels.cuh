@@ -48,10 +48,32 @@ __device__ __forceinline__ void pdl_enter()
 
 // ------------------------------------------------------------------ reduce
 
-// One tile of vector units: U = kMaxRanks / NR units per thread for at most NR
-// ranks (R <= NR), each warp access contiguous.  All R x U loads are issued
-// before the first add, so every rank count keeps up to kMaxRanks independent
-// requests in flight per thread.
+// One unit per thread (sums of more than 4 ranks, and the pairwise order).
+template <typename T, int ORDER, bool FAN_ALL, int BYTES>
+__device__ __forceinline__ void reduce_vector(const ZsParams<kSegsSmall>& p, const Segment& s,
+                                              uint64_t off, int R, uint64_t lpol, uint64_t spol)
+{
+    atom::Vec<BYTES> v[kMaxRanks];
+    // All R loads are issued before the first add: R independent requests in
+    // flight per thread.
+#pragma unroll
+    for (int r = 0; r < kMaxRanks; ++r)
+        if (r < R) atom::load(v[r], p.in[r] + s.src_off + off, lpol);
+    atom::Vec<BYTES> o;
+    atom::reduce_unit<T, ORDER, BYTES>(v, R, o);
+    if (FAN_ALL) {
+#pragma unroll
+        for (int r = 0; r < kMaxRanks; ++r)
+            if (r < R) atom::store(p.out[r] + s.dst_off + off, o, spol);
+    } else {
+        atom::store(p.out[s.dst] + s.dst_off + off, o, spol);
+    }
+}
+
+// Several units per thread (sums of 2 to 4 ranks): U = kMaxRanks / NR of them
+// for at most NR ranks (R <= NR), each warp access contiguous.  All R x U loads
+// are issued before the first add, so a small rank count keeps as many
+// independent requests in flight per thread as kMaxRanks ranks do.
 template <typename T, int ORDER, bool FAN_ALL, int BYTES, int NR, int THREADS>
 __device__ __forceinline__ void reduce_tile(const ZsParams<kSegsSmall>& p, const Segment& s,
                                             uint64_t base, int R, uint64_t lpol, uint64_t spol)
@@ -117,6 +139,17 @@ zs_reduce_kernel(const __grid_constant__ ZsParams<kSegsSmall> p)
     for (uint32_t t = blockIdx.x; t < p.ntiles; t += gridDim.x) {
         const Segment& s = segment_of(p, t);
         const int ul = s.unit_log2;
+        if constexpr (U == 1) {
+            // kept in this form: the one-unit kernels scheduled from the
+            // general tile loop below ran up to 8 % slower (fp32 AllReduce)
+            const uint64_t off = (uint64_t)(t - s.tile0) * tile_bytes(ul, THREADS) +
+                                 ((uint64_t)threadIdx.x << ul);
+            if (off >= s.bytes) continue;
+            if (ul == 5) reduce_vector<T, ORDER, FAN_ALL, 32>(p, s, off, R, lpol, spol);
+            else if (ul == 4) reduce_vector<T, ORDER, FAN_ALL, 16>(p, s, off, R, lpol, spol);
+            else reduce_element<T, ORDER, FAN_ALL>(p, s, off, R);
+            continue;
+        }
         const uint64_t base = (uint64_t)(t - s.tile0) * tile_bytes(ul, THREADS * U);
         if (ul == 5) {
             reduce_tile<T, ORDER, FAN_ALL, 32, NR, THREADS>(p, s, base, R, lpol, spol);
