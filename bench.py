@@ -62,6 +62,8 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--only", choices=["rs", "ag", "ar", "a2av"], default=None,
                     help="time one collective alone (profiling runs); prints a short line")
+    ap.add_argument("--ranks", type=int, default=R, choices=range(1, R + 1), metavar="R",
+                    help="virtual ranks of an --only run (1..8; default 8)")
     ap.add_argument("--bytes-per-rank", type=int, default=BYTES_PER_RANK,
                     help="with --only: input bytes per rank")
     ap.add_argument("--atom", choices=["auto", "vector", "bulk", "copy_engine"], default="auto",
@@ -1113,7 +1115,8 @@ def bench_e2e(args, rd, torch, h, x, y, z, counts, stream):
 
 
 def bench_only(args):
-    """One collective of the bench workload's shape, K times (for ncu runs)."""
+    """One collective of the bench workload's shape (R = --ranks virtual ranks),
+    K times (for ncu runs)."""
     import torch
 
     import reduce_datapath_gb300 as rd
@@ -1122,6 +1125,7 @@ def bench_only(args):
     torch.cuda.set_device(0)
     dev = torch.device("cuda", 0)
     rd.build()
+    R = args.ranks
     n = args.bytes_per_rank // 2
     c = n // R
     h = rd.purlin_create(R, args.staging, 0)
@@ -1171,7 +1175,7 @@ def bench_only(args):
     info = rd.purlin_last_launch(h)
     rd.purlin_destroy(h)
     us = a.elapsed_time(b) * 1e3 / K
-    print(json.dumps({"only": args.only, "variant": args.variant,
+    print(json.dumps({"only": args.only, "variant": args.variant, "R": R,
                       "bytes_per_rank": args.bytes_per_rank, "us": us,
                       "gbs": nbytes / (us / 1e6) / 1e9, "algorithmic_bytes": nbytes,
                       "launch": info}), flush=True)
