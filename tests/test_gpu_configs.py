@@ -4,7 +4,8 @@ benchmark times.
   allreduce_r2_f32     AllReduce R=2 fp32 4096 integers in [-8, 8] (exact sums),
                        plus ReduceScatter + AllGather on the same inputs.
   rs_ag_r8_bf16        ReduceScatter then AllGather, R=8 bf16, 64 MiB per rank:
-                       compared in full with the oracle.
+                       compared in full with the oracle; the same size summed
+                       over 2 and 4 ranks (bf16 and fp32), in full.
   allreduce_sweep_r8   AllReduce R=8 bf16, 4 KiB .. 256 MiB per rank, zero staging
                        and SNAC chunks of 64 KiB .. 2 MiB: in full up to 16 MiB
                        per rank, sampled above (the oracle recomputes sampled
@@ -112,6 +113,41 @@ def test_rs_ag_r8_bf16_64MiB_full(variant):
     for j in range(R):
         assert _bits_equal(host_bits(z[j]), want_z), j
 
+
+
+# ----------------------------------------------------- sums of 2 and 4 ranks
+
+@pytest.mark.parametrize("coll", ["all_reduce", "reduce_scatter"])
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("R", [2, 4])
+def test_rank_count_sums_64MiB_full(R, dtype, coll):
+    """The benchmark's rank-count study (64 MiB per rank, zero staging, 4 or 2
+    units per thread), compared in full with the oracle."""
+    esz = 2 if dtype == "bf16" else 4
+    n = 64 * MiB // esz
+    c = n // R
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    x = workloads.rank_buffers("rs_ag_r8_bf16", R, n, dtype, role=10 + R, device="cuda")
+    h = rd.purlin_create(R)
+    try:
+        if coll == "all_reduce":
+            out = [torch.empty(n, dtype=tdt, device="cuda") for _ in range(R)]
+            rd.purlin_all_reduce(h, x, out, n, dtype)
+        else:
+            out = [torch.empty(c, dtype=tdt, device="cuda") for _ in range(R)]
+            rd.purlin_reduce_scatter(h, x, out, [c] * R, None, dtype)
+        _ok(h)
+        assert rd.purlin_last_launch(h)["block"] == 256
+    finally:
+        rd.purlin_destroy(h)
+    xs = [host_bits(t) for t in x]
+    del x
+    if coll == "all_reduce":
+        want = oracle.all_reduce(xs, dtype=dtype)
+    else:
+        want = oracle.reduce_scatter(xs, [c] * R, dtype=dtype)
+    for j in range(R):
+        assert _bits_equal(host_bits(out[j]), want[j]), j
 
 # ---------------------------------------------------------- allreduce_sweep_r8
 
