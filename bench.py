@@ -83,6 +83,14 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def bench_config(world):
+    """The workload both arms measure (the reference arm reports the same)."""
+    return {"workload": "ReduceScatter then AllGather, R=8 virtual ranks, bf16, 64 MiB per "
+                        "rank (8 partitions of 8 MiB), N(0,1), fp32 accumulation in rank order",
+            "R": R, "bytes_per_rank": BYTES_PER_RANK, "parallelism": f"replicas x{world}",
+            "l2": "inputs 512 MiB > L2 per step; no flush"}
+
+
 def cpu_model():
     """The host CPU's model name (lscpu's on Arm, where /proc/cpuinfo gives
     only a part number)."""
@@ -350,8 +358,7 @@ def bench_reference(args):
         "steps": steps, "warmup": warm, "ms_per_step": el / steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": "ReduceScatter then AllGather, R=8 virtual ranks, bf16, "
-                               "64 MiB per rank, N(0,1)", "R": R, "bytes_per_rank": BYTES_PER_RANK},
+        "config": bench_config(args.gpus),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": f"{steps} full step(s), single-threaded C, {cpu_model()}"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -564,12 +571,7 @@ def bench_purlin(args):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": max(3, args.warmup), "ms_per_step": max_ms / K, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": "ReduceScatter then AllGather, R=8 virtual ranks, bf16, 64 MiB "
-                               "per rank (8 partitions of 8 MiB), N(0,1), fp32 accumulation "
-                               "in rank order",
-                   "R": R, "bytes_per_rank": BYTES_PER_RANK, "variant": args.variant,
-                   "parallelism": f"replicas x{world}",
-                   "l2": "inputs 512 MiB > L2 per step; no flush"},
+        "config": bench_config(world) | {"variant": args.variant},
         "roofline": roofline,
         "per_collective": per,
         "allreduce_4KiB": lat,
