@@ -39,6 +39,10 @@ typedef struct {
     int32_t unit;      /* bytes per access: 32 or 16 (vector body), else element /
                           byte granularity for unaligned heads and tails            */
     uint32_t tile0;    /* first tile of the segment in the launch's tile space     */
+    int32_t shift;     /* 0, or a shifted vector body: the destinations are aligned
+                          to `unit` and every source starts `shift` bytes (0 <
+                          shift < unit) past a unit boundary; the kernel reads
+                          aligned source blocks and realigns them in registers   */
 } purlin_segment_t;
 
 /* Derive the plan of one collective.

@@ -80,7 +80,7 @@ class Segment(ctypes.Structure):
     _fields_ = [("src_off", ctypes.c_uint64), ("dst_off", ctypes.c_uint64),
                 ("bytes", ctypes.c_uint64), ("src_rank", ctypes.c_int32),
                 ("dst_rank", ctypes.c_int32), ("unit", ctypes.c_int32),
-                ("tile0", ctypes.c_uint32)]
+                ("tile0", ctypes.c_uint32), ("shift", ctypes.c_int32)]
 
 
 _lock = threading.Lock()

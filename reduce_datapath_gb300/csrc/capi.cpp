@@ -179,6 +179,7 @@ purlin_status_t check_buffers(Coll coll, int R, const uint64_t* in, const uint64
 struct ZsKnobs {
     int tile_units;
     int max_unit_log2;
+    bool allow_shift;   // shifted bodies (vector kernels; the TMA bulk Atom has none)
     uint32_t l2_load;
     uint32_t l2_store;
     bool pdl;
@@ -201,6 +202,7 @@ ZsKnobs zs_knobs(const purlin_handle* h, Coll coll)
     k.tile_units = reduce ? kThreads * reduce_unroll(h->R, h->order)
                           : (h->atom == PURLIN_ATOM_BULK ? kTileUnitsBulk : kTileUnitsCopy);
     k.max_unit_log2 = h->max_unit_log2 ? h->max_unit_log2 : 5;
+    k.allow_shift = reduce ? h->order == 0 : h->atom != PURLIN_ATOM_BULK;
     k.l2_load = h->l2_load >= 0 ? (uint32_t)h->l2_load : kL2EvictFirst;
     k.l2_store = h->l2_store >= 0 ? (uint32_t)h->l2_store
                                   : (coll == Coll::ReduceScatter ? kL2Normal : kL2EvictFirst);
@@ -230,11 +232,19 @@ purlin_status_t make_params(ZsParams<MAXSEG>& p, const Piece* pieces, int npiece
     p.tile_units = (uint32_t)k.tile_units;
     uint32_t ntiles = 0;
     int n = layout_segments(pieces, npieces, R, in, out, esz, reduce, k.tile_units,
-                            max_unit_log2, p.seg, MAXSEG, &ntiles);
+                            max_unit_log2, k.allow_shift, p.seg, MAXSEG, &ntiles);
     if (n < 0) return PURLIN_ERR_UNSUPPORTED;
     p.nseg = (uint32_t)n;
     p.ntiles = ntiles;
     return PURLIN_OK;
+}
+
+template <int MAXSEG>
+bool has_shift(const ZsParams<MAXSEG>& p)
+{
+    for (uint32_t i = 0; i < p.nseg; ++i)
+        if (p.seg[i].shift) return true;
+    return false;
 }
 
 // Small messages: when the large-message plan has fewer than h->small_tiles
@@ -452,8 +462,9 @@ purlin_status_t run(purlin_handle_t h, Coll coll, const void* const in_[], void*
                 info.block = kBulkThreads;
             } else {
                 const bool small = replan_small(h, coll, p, plan, nplan, R, in, out, esz, false, knobs);
-                grid = zs_grid(h, p.ntiles, zs_copy_resident_ctas(true, false, small));
-                zs_copy_select(k, true, false, small);
+                const bool sh = has_shift(p);
+                grid = zs_grid(h, p.ntiles, zs_copy_resident_ctas(true, false, small, sh));
+                zs_copy_select(k, true, false, small, sh);
                 if (small) info.block = kSmallThreads;
             }
             k.grid = (unsigned)grid;
@@ -475,11 +486,14 @@ purlin_status_t run(purlin_handle_t h, Coll coll, const void* const in_[], void*
             } else {
                 const bool small = replan_small(h, coll, p, pieces, np, R, in, out, esz, reduce, knobs);
                 if (reduce) {
-                    grid = zs_grid(h, p.ntiles, zs_reduce_resident_ctas(dtype, h->order, fan_all, small, R));
-                    zs_reduce_select(k, dtype, h->order, fan_all, small, R);
+                    const bool sh = has_shift(p);
+                    grid = zs_grid(h, p.ntiles,
+                                   zs_reduce_resident_ctas(dtype, h->order, fan_all, small, R, sh));
+                    zs_reduce_select(k, dtype, h->order, fan_all, small, R, sh);
                 } else {
-                    grid = zs_grid(h, p.ntiles, zs_copy_resident_ctas(false, fan_all, small));
-                    zs_copy_select(k, false, fan_all, small);
+                    const bool sh = has_shift(p);
+                    grid = zs_grid(h, p.ntiles, zs_copy_resident_ctas(false, fan_all, small, sh));
+                    zs_copy_select(k, false, fan_all, small, sh);
                 }
                 if (small) info.block = kSmallThreads;
             }
@@ -826,8 +840,7 @@ purlin_status_t purlin_plan_segments(purlin_collective_t coll, int R, const uint
     uint32_t nt = 0;
     int n = layout_segments(pieces, np, R, in_addr, out_addr, esz, reduce,
                             reduce ? kThreads * reduce_unroll(R, 0) : kTileUnitsCopy,
-                            max_unit == 32 ? 5 : 4, tmp,
-                            kSegsLarge, &nt);
+                            max_unit == 32 ? 5 : 4, /*allow_shift=*/true, tmp, kSegsLarge, &nt);
     if (n < 0 || n > max_segs) return PURLIN_ERR_UNSUPPORTED;
     for (int i = 0; i < n; ++i) {
         segs[i].src_off = tmp[i].src_off;
@@ -836,6 +849,7 @@ purlin_status_t purlin_plan_segments(purlin_collective_t coll, int R, const uint
         segs[i].src_rank = tmp[i].src == kEveryRank ? -1 : tmp[i].src;
         segs[i].dst_rank = tmp[i].dst == kEveryRank ? -1 : tmp[i].dst;
         segs[i].unit = 1 << tmp[i].unit_log2;
+        segs[i].shift = tmp[i].shift;
         segs[i].tile0 = tmp[i].tile0;
     }
     *nsegs = n;

@@ -48,17 +48,20 @@ int resident_ctas_of(const void* kernel, int threads);
 // built with kTileUnitsSmall; else kThreads-thread CTAs, kTileUnitsReduce.
 // Units per thread of the kThreads-thread sum kernel for R ranks and a rank
 // order (R x units <= kMaxRanks vectors in flight per thread); the plan's tiles
-// are kThreads x reduce_unroll(R, order) units.
+// are kThreads x reduce_unroll(R, order) units.  shifted: the plan holds a
+// shifted segment (Segment::shift), which only the SHIFTED kernels serve (the
+// fixed rank order only).
 int reduce_unroll(int R, int order);
-void zs_reduce_select(KernelLaunch& k, int dtype, int order, bool fan_all, bool small, int R);
-int zs_reduce_resident_ctas(int dtype, int order, bool fan_all, bool small, int R);
+void zs_reduce_select(KernelLaunch& k, int dtype, int order, bool fan_all, bool small, int R,
+                      bool shifted);
+int zs_reduce_resident_ctas(int dtype, int order, bool fan_all, bool small, int R, bool shifted);
 
 // Copy.  fan_all: every segment goes to every output (AllGather), else to the
 // segment's destination (AllToAll(V)).  large: ZsParams<kSegsLarge> (else
 // kSegsSmall).  small: one-warp CTAs, plan built with kTileUnitsSmall; else
-// kThreads-thread CTAs, kTileUnitsCopy.
-void zs_copy_select(KernelLaunch& k, bool large, bool fan_all, bool small);
-int zs_copy_resident_ctas(bool large, bool fan_all, bool small);
+// kThreads-thread CTAs, kTileUnitsCopy.  shifted: as for the sums.
+void zs_copy_select(KernelLaunch& k, bool large, bool fan_all, bool small, bool shifted);
+int zs_copy_resident_ctas(bool large, bool fan_all, bool small, bool shifted);
 
 // Copy through TMA bulk transfers (plan built with kTileUnitsBulk tiles).
 // Returns the CUDA error of the one-time shared-memory opt-in, if any.

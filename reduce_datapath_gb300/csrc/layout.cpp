@@ -151,12 +151,14 @@ void layout_extents(Coll coll, int R, const size_t* counts, const size_t* da, co
 
 int layout_segments(const Piece* pieces, int npieces, int R, const uint64_t* in_addr,
                     const uint64_t* out_addr, size_t esz, bool reduce, int tile_units,
-                    int max_unit_log2, Segment* segs, int max_segs, uint32_t* ntiles)
+                    int max_unit_log2, bool allow_shift, Segment* segs, int max_segs,
+                    uint32_t* ntiles)
 {
     int n = 0;
     uint64_t tiles = 0;
     const int elem_log2 = log2_exact(esz);
-    auto push = [&](uint64_t so, uint64_t dof, uint64_t bytes, const Piece& p, int ulog2) {
+    auto push = [&](uint64_t so, uint64_t dof, uint64_t bytes, const Piece& p, int ulog2,
+                    int shift = 0) {
         if (bytes == 0) return true;
         if (n >= max_segs) return false;
         Segment s{};
@@ -166,26 +168,68 @@ int layout_segments(const Piece* pieces, int npieces, int R, const uint64_t* in_
         s.src = p.src;
         s.dst = p.dst;
         s.unit_log2 = (uint8_t)ulog2;
+        s.shift = (uint8_t)shift;
         s.tile0 = (uint32_t)tiles;
-        uint64_t tb = tile_bytes(ulog2, tile_units);
+        uint64_t tb = tile_bytes(ulog2, shift ? shifted_tile_units(tile_units) : tile_units);
         tiles += (bytes + tb - 1) / tb;
         if (tiles > 0xffffffffull) return false;
         segs[n++] = s;
         return true;
     };
+    auto same_residue = [](const uint64_t* a, int na, uint64_t mask) {
+        for (int i = 1; i < na; ++i)
+            if ((a[i] & mask) != (a[0] & mask)) return false;
+        return true;
+    };
     for (int i = 0; i < npieces; ++i) {
         const Piece& p = pieces[i];
-        // Every address this piece touches, at its first byte.
+        // Every address this piece touches, at its first byte: the sources
+        // first (ns of them), then the destinations.
         uint64_t addrs[2 * kMaxRanks];
         int na = 0;
         if (p.src == kEveryRank)
             for (int r = 0; r < R; ++r) addrs[na++] = in_addr[r] + p.src_off;
         else
             addrs[na++] = in_addr[p.src] + p.src_off;
+        const int ns = na;
         if (p.dst == kEveryRank)
             for (int r = 0; r < R; ++r) addrs[na++] = out_addr[r] + p.dst_off;
         else
             addrs[na++] = out_addr[p.dst] + p.dst_off;
+        const uint64_t* dsts = addrs + ns;
+        const int nd = na - ns;
+
+        // Shifted body: the sources agree on a vector alignment among
+        // themselves and so do the destinations, but not with each other.  The
+        // body's vector units are aligned to the destinations (a head of less
+        // than one unit gets there) and read the sources `shift` bytes past a
+        // unit boundary; heads and tails go element (sum) or byte-group (copy)
+        // wise.
+        auto try_shifted = [&]() {
+            for (int u_log2 = max_unit_log2; u_log2 >= 4; --u_log2) {
+                const uint64_t u = (uint64_t)1 << u_log2, mask = u - 1;
+                if (!same_residue(addrs, ns, mask) || !same_residue(dsts, nd, mask)) continue;
+                const uint64_t head = std::min<uint64_t>((u - (dsts[0] & mask)) & mask, p.bytes);
+                const uint64_t body = ((p.bytes - head) / u) * u;
+                const uint64_t tail = p.bytes - head - body;
+                const int shift = (int)((addrs[0] + head) & mask);
+                if (body == 0 || shift == 0) return 0;
+                // widest access every stream and the length allow, at offset `off`
+                auto small_log2 = [&](uint64_t off, uint64_t len) {
+                    if (reduce) return elem_log2;
+                    uint64_t v = len;
+                    for (int a = 0; a < na; ++a) v |= addrs[a] + off;
+                    return std::min(lowbit_log2(v), max_unit_log2);
+                };
+                if (!push(p.src_off, p.dst_off, head, p, small_log2(0, head))) return -1;
+                if (!push(p.src_off + head, p.dst_off + head, body, p, u_log2, shift)) return -1;
+                if (!push(p.src_off + head + body, p.dst_off + head + body, tail, p,
+                          small_log2(head + body, tail)))
+                    return -1;
+                return 1;
+            }
+            return 0;
+        };
 
         // Widest unit at which all addresses share one residue: one common head
         // then aligns every stream at once.
@@ -196,6 +240,11 @@ int layout_segments(const Piece* pieces, int npieces, int R, const uint64_t* in_
             bool same = true;
             for (int a = 1; a < na; ++a) same &= ((addrs[a] & mask) == (addrs[0] & mask));
             if (same) { body_log2 = u; break; }
+        }
+        if (allow_shift && body_log2 < 4) {
+            const int r = try_shifted();
+            if (r < 0) return -1;
+            if (r > 0) continue;
         }
         if (body_log2 < 0 || (reduce && body_log2 <= elem_log2)) {
             // Sums whose streams cannot share a vector alignment go element by element.

@@ -48,7 +48,8 @@ struct Segment {
     uint8_t src;        // source rank, or kEveryRank (sum over ranks)
     uint8_t dst;        // destination rank, or kEveryRank (every output)
     uint8_t unit_log2;  // access width = 1 << unit_log2 bytes (0..5)
-    uint8_t pad;
+    uint8_t shift;      // 0, or a shifted body: destinations aligned to the unit,
+                        // every source `shift` bytes past a unit boundary
 };
 static_assert(sizeof(Segment) == 32, "Segment is passed by value to kernels");
 
@@ -76,6 +77,14 @@ struct ZsParams {
 PURLIN_HD inline uint64_t tile_bytes(int unit_log2, int tile_units)
 {
     return (uint64_t)tile_units << unit_log2;
+}
+
+// Units per tile of a shifted segment: each warp's 32 lanes load 32 aligned
+// source blocks and write the 31 destination units that lie between them (a
+// destination unit takes the tail of one source block and the head of the next).
+PURLIN_HD constexpr int shifted_tile_units(int tile_units)
+{
+    return tile_units / 32 * 31;
 }
 
 constexpr int kUnrollBulk = 2;          // bulk-copy tiles: 256 x unit x 2 bytes (<= 16 KiB)
@@ -112,12 +121,17 @@ void layout_extents(Coll coll, int R, const size_t* counts, const size_t* da,
                     uint64_t in_extent[kMaxRanks], uint64_t out_extent[kMaxRanks]);
 
 // Split pieces into head / body / tail segments by the alignment of the actual
-// addresses, then number the tiles (tile_units x unit bytes each).  `reduce`
-// selects element-wise heads and tails (sums) or byte-wise ones (copies).  max_unit_log2 caps the vector width
-// (4 = 16 B, 5 = 32 B).  Returns the segment count or -1 if max_segs is too
-// small; *ntiles receives the tile count.
+// addresses, then number the tiles (tile_units x unit bytes each;
+// shifted_tile_units for a shifted body).  `reduce` selects element-wise heads
+// and tails (sums) or byte-wise ones (copies).  max_unit_log2 caps the vector
+// width (4 = 16 B, 5 = 32 B).  When the sources and the destinations of a piece
+// cannot share one vector alignment but each side agrees within itself,
+// `allow_shift` gives the body vector units aligned to the destinations and a
+// source shift (Segment::shift) instead of element or byte units.  Returns the
+// segment count or -1 if max_segs is too small; *ntiles receives the tile count.
 int layout_segments(const Piece* pieces, int npieces, int R, const uint64_t* in_addr,
                     const uint64_t* out_addr, size_t elem_bytes, bool reduce, int tile_units,
-                    int max_unit_log2, Segment* segs, int max_segs, uint32_t* ntiles);
+                    int max_unit_log2, bool allow_shift, Segment* segs, int max_segs,
+                    uint32_t* ntiles);
 
 }  // namespace purlin

@@ -673,8 +673,8 @@ purlin_status_t plan_into(KernelLaunch& k, const SnacRequest& rq, const SnacConf
     const bool reduce = rq.coll == Coll::ReduceScatter || rq.coll == Coll::AllReduce;
     uint32_t ntiles = 0;
     int nseg = layout_segments(rq.pieces, rq.npieces, rq.R, rq.in, rq.out, rq.esz, reduce,
-                               reduce ? kTileUnitsReduce : kTileUnitsCopy, snac_unit_log2(), p.seg,
-                               kSegsLarge, &ntiles);
+                               reduce ? kTileUnitsReduce : kTileUnitsCopy, snac_unit_log2(),
+                               /*allow_shift=*/false, p.seg, kSegsLarge, &ntiles);
     if (nseg < 0) return PURLIN_ERR_UNSUPPORTED;
 
     SnacKernel kernel = kernel_for(rq.coll, rq.dtype, rq.order, rq.stage_y);

@@ -14,48 +14,64 @@ namespace {
 using ReduceKernel = void (*)(ZsParams<kSegsSmall>);
 
 // NR = kMaxRanks / units per thread.  The pairwise rank order keeps one unit
-// per thread (NR = kMaxRanks).
-template <typename T, int THREADS, int NR>
+// per thread (NR = kMaxRanks) and has no shifted segments (SH).
+template <typename T, int THREADS, int NR, bool SH>
 ReduceKernel pick_reduce(int order, bool fan_all)
 {
     if (order == 0)
-        return fan_all ? zs_reduce_kernel<T, 0, true, THREADS, NR> : zs_reduce_kernel<T, 0, false, THREADS, NR>;
-    return fan_all ? zs_reduce_kernel<T, 1, true, THREADS, kMaxRanks>
-                   : zs_reduce_kernel<T, 1, false, THREADS, kMaxRanks>;
+        return fan_all ? zs_reduce_kernel<T, 0, true, THREADS, NR, SH>
+                       : zs_reduce_kernel<T, 0, false, THREADS, NR, SH>;
+    return fan_all ? zs_reduce_kernel<T, 1, true, THREADS, kMaxRanks, false>
+                   : zs_reduce_kernel<T, 1, false, THREADS, kMaxRanks, false>;
 }
 
-template <int THREADS, int NR>
+template <int THREADS, int NR, bool SH>
 ReduceKernel reduce_kernel_t(int dtype, int order, bool fan_all)
 {
-    if (dtype == kF32) return pick_reduce<atom::F32, THREADS, NR>(order, fan_all);
-    if (dtype == kBF16) return pick_reduce<atom::BF16, THREADS, NR>(order, fan_all);
-    return pick_reduce<atom::F16, THREADS, NR>(order, fan_all);
+    if (dtype == kF32) return pick_reduce<atom::F32, THREADS, NR, SH>(order, fan_all);
+    if (dtype == kBF16) return pick_reduce<atom::BF16, THREADS, NR, SH>(order, fan_all);
+    return pick_reduce<atom::F16, THREADS, NR, SH>(order, fan_all);
 }
 
-ReduceKernel reduce_kernel_for(int dtype, int order, bool fan_all, bool small, int unroll)
+template <bool SH>
+ReduceKernel reduce_kernel_sh(int dtype, int order, bool fan_all, bool small, int unroll)
 {
-    if (small) return reduce_kernel_t<kSmallThreads, kMaxRanks>(dtype, order, fan_all);
+    if (small) return reduce_kernel_t<kSmallThreads, kMaxRanks, SH>(dtype, order, fan_all);
     switch (unroll) {
-    case 4: return reduce_kernel_t<kThreads, kMaxRanks / 4>(dtype, order, fan_all);
-    case 2: return reduce_kernel_t<kThreads, kMaxRanks / 2>(dtype, order, fan_all);
-    default: return reduce_kernel_t<kThreads, kMaxRanks>(dtype, order, fan_all);
+    case 4: return reduce_kernel_t<kThreads, kMaxRanks / 4, SH>(dtype, order, fan_all);
+    case 2: return reduce_kernel_t<kThreads, kMaxRanks / 2, SH>(dtype, order, fan_all);
+    default: return reduce_kernel_t<kThreads, kMaxRanks, SH>(dtype, order, fan_all);
     }
 }
 
-template <int MAXSEG>
-void (*copy_kernel_for(bool fan_all, bool small))(ZsParams<MAXSEG>)
+ReduceKernel reduce_kernel_for(int dtype, int order, bool fan_all, bool small, int unroll,
+                               bool shifted)
 {
-    if (small)
-        return fan_all ? zs_copy_kernel<true, MAXSEG, kSmallThreads, 1>
-                       : zs_copy_kernel<false, MAXSEG, kSmallThreads, 1>;
-    return fan_all ? zs_copy_kernel<true, MAXSEG, kThreads, kUnrollCopy>
-                   : zs_copy_kernel<false, MAXSEG, kThreads, kUnrollCopy>;
+    return shifted ? reduce_kernel_sh<true>(dtype, order, fan_all, small, unroll)
+                   : reduce_kernel_sh<false>(dtype, order, fan_all, small, unroll);
 }
 
-const void* copy_kernel_any(bool large, bool fan_all, bool small)
+template <int MAXSEG, bool SH>
+void (*copy_kernel_sh(bool fan_all, bool small))(ZsParams<MAXSEG>)
 {
-    return large ? reinterpret_cast<const void*>(copy_kernel_for<kSegsLarge>(fan_all, small))
-                 : reinterpret_cast<const void*>(copy_kernel_for<kSegsSmall>(fan_all, small));
+    if (small)
+        return fan_all ? zs_copy_kernel<true, MAXSEG, kSmallThreads, 1, SH>
+                       : zs_copy_kernel<false, MAXSEG, kSmallThreads, 1, SH>;
+    return fan_all ? zs_copy_kernel<true, MAXSEG, kThreads, kUnrollCopy, SH>
+                   : zs_copy_kernel<false, MAXSEG, kThreads, kUnrollCopy, SH>;
+}
+
+template <int MAXSEG>
+const void* copy_kernel_for(bool fan_all, bool small, bool shifted)
+{
+    return shifted ? reinterpret_cast<const void*>(copy_kernel_sh<MAXSEG, true>(fan_all, small))
+                   : reinterpret_cast<const void*>(copy_kernel_sh<MAXSEG, false>(fan_all, small));
+}
+
+const void* copy_kernel_any(bool large, bool fan_all, bool small, bool shifted)
+{
+    return large ? copy_kernel_for<kSegsLarge>(fan_all, small, shifted)
+                 : copy_kernel_for<kSegsSmall>(fan_all, small, shifted);
 }
 
 // Resident CTAs per SM of a kernel at `threads` threads, cached per device in a
@@ -154,35 +170,37 @@ int reduce_unroll(int R, int order)
     return R >= 5 ? 1 : R >= 3 ? 2 : 4;
 }
 
-void zs_reduce_select(KernelLaunch& k, int dtype, int order, bool fan_all, bool small, int R)
+void zs_reduce_select(KernelLaunch& k, int dtype, int order, bool fan_all, bool small, int R,
+                      bool shifted)
 {
     k.func = reinterpret_cast<const void*>(
-        reduce_kernel_for(dtype, order, fan_all, small, reduce_unroll(R, order)));
+        reduce_kernel_for(dtype, order, fan_all, small, reduce_unroll(R, order), shifted));
     k.block = small ? kSmallThreads : kThreads;
     k.smem = 0;
     k.cooperative = false;
     k.params_bytes = sizeof(ZsParams<kSegsSmall>);
 }
 
-int zs_reduce_resident_ctas(int dtype, int order, bool fan_all, bool small, int R)
+int zs_reduce_resident_ctas(int dtype, int order, bool fan_all, bool small, int R, bool shifted)
 {
-    return resident_ctas(reinterpret_cast<const void*>(
-                             reduce_kernel_for(dtype, order, fan_all, small, reduce_unroll(R, order))),
+    return resident_ctas(reinterpret_cast<const void*>(reduce_kernel_for(
+                             dtype, order, fan_all, small, reduce_unroll(R, order), shifted)),
                          small ? kSmallThreads : kThreads);
 }
 
-void zs_copy_select(KernelLaunch& k, bool large, bool fan_all, bool small)
+void zs_copy_select(KernelLaunch& k, bool large, bool fan_all, bool small, bool shifted)
 {
-    k.func = copy_kernel_any(large, fan_all, small);
+    k.func = copy_kernel_any(large, fan_all, small, shifted);
     k.block = small ? kSmallThreads : kThreads;
     k.smem = 0;
     k.cooperative = false;
     k.params_bytes = large ? sizeof(ZsParams<kSegsLarge>) : sizeof(ZsParams<kSegsSmall>);
 }
 
-int zs_copy_resident_ctas(bool large, bool fan_all, bool small)
+int zs_copy_resident_ctas(bool large, bool fan_all, bool small, bool shifted)
 {
-    return resident_ctas(copy_kernel_any(large, fan_all, small), small ? kSmallThreads : kThreads);
+    return resident_ctas(copy_kernel_any(large, fan_all, small, shifted),
+                         small ? kSmallThreads : kThreads);
 }
 
 cudaError_t zs_copy_bulk_select(KernelLaunch& k, bool large, bool fan_all)

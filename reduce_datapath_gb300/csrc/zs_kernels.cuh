@@ -46,6 +46,135 @@ __device__ __forceinline__ void pdl_enter()
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// ------------------------------------------------------------ shifted bodies
+// A shifted segment (Segment::shift != 0) has its destinations aligned to its
+// unit of BYTES while every source starts `shift` bytes past a unit boundary
+// (a V-collective whose partition offsets are not multiples of the vector).
+// Lane l of a warp loads the aligned source block q + l -- for a sum, the R
+// ranks' blocks folded first: `shift` is a multiple of the element size, so the
+// realignment moves whole elements -- and destination unit q + l is that
+// block's last BYTES - shift bytes followed by the first `shift` bytes of the
+// next block, which lane l + 1 holds.  Each warp's 32 lanes thus write 31
+// units (lane 31 only lends its block); every block loaded holds a byte of the
+// segment, so no load leaves the pages the segment lies in.
+
+// out = (lo ++ hi)[shift, shift + 4W) as bytes, 0 < shift < 4W, with no
+// dynamically indexed registers: a log-depth word rotation, then a funnel
+// shift for the bytes within a word.
+template <int W>
+__device__ __forceinline__ void realign(const uint32_t (&lo)[W], const uint32_t (&hi)[W],
+                                        int shift, uint32_t (&out)[W])
+{
+    uint32_t c[2 * W];
+#pragma unroll
+    for (int i = 0; i < W; ++i) {
+        c[i] = lo[i];
+        c[W + i] = hi[i];
+    }
+    const int words = shift >> 2;
+#pragma unroll
+    for (int k = W / 2; k >= 1; k >>= 1) {
+        const bool take = (words & k) != 0;
+#pragma unroll
+        for (int i = 0; i + k < 2 * W; ++i) c[i] = take ? c[i + k] : c[i];
+    }
+    const uint32_t bits = (uint32_t)(shift & 3) * 8;
+#pragma unroll
+    for (int j = 0; j < W; ++j) out[j] = __funnelshift_r(c[j], c[j + 1], bits);
+}
+
+__device__ __forceinline__ const char* at(const char* base, uint64_t off, int back)
+{
+    return reinterpret_cast<const char*>(reinterpret_cast<uintptr_t>(base) + off - (uint64_t)back);
+}
+
+// One tile of a shifted sum: U = kMaxRanks / NR rows of 31-unit warp runs.
+template <typename T, int ORDER, bool FAN_ALL, int BYTES, int NR, int THREADS>
+__device__ __forceinline__ void reduce_shifted(const ZsParams<kSegsSmall>& p, const Segment& s,
+                                            uint32_t tile, int R, uint64_t lpol, uint64_t spol)
+{
+    constexpr int U = kMaxRanks / NR;
+    constexpr int W = BYTES / 4;
+    constexpr int WARPS = THREADS / 32;
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int shift = s.shift;
+    const uint64_t nunits = s.bytes / BYTES;
+    const uint64_t q0 = (uint64_t)tile * shifted_tile_units(THREADS * U);
+    atom::Vec<BYTES> v[U][NR];
+#pragma unroll
+    for (int k = 0; k < U; ++k) {
+        const uint64_t q = q0 + (uint64_t)(k * WARPS + warp) * 31 + lane;
+#pragma unroll
+        for (int r = 0; r < NR; ++r) {
+            if (r < R && q <= nunits) {
+                atom::load(v[k][r], at(p.in[r], s.src_off + q * BYTES, shift), lpol);
+            } else {
+#pragma unroll
+                for (int i = 0; i < W; ++i) v[k][r].w[i] = 0u;
+            }
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < U; ++k) {
+        const uint64_t q = q0 + (uint64_t)(k * WARPS + warp) * 31 + lane;
+        atom::Vec<BYTES> y, next, out;
+        atom::reduce_unit<T, ORDER, BYTES, NR>(v[k], R, y);
+#pragma unroll
+        for (int i = 0; i < W; ++i) next.w[i] = __shfl_down_sync(0xffffffffu, y.w[i], 1);
+        if (lane == 31 || q >= nunits) continue;
+        realign<W>(y.w, next.w, shift, out.w);
+        const uint64_t o = s.dst_off + q * BYTES;
+        if (FAN_ALL) {
+#pragma unroll
+            for (int r = 0; r < NR; ++r)
+                if (r < R) atom::store(p.out[r] + o, out, spol);
+        } else {
+            atom::store(p.out[s.dst] + o, out, spol);
+        }
+    }
+}
+
+// One tile of a shifted copy: UNROLL rows of 31-unit warp runs.
+template <int BYTES, bool FAN_ALL, int THREADS, int UNROLL, int MAXSEG>
+__device__ __forceinline__ void copy_shifted(const ZsParams<MAXSEG>& p, const Segment& s,
+                                          uint32_t tile, uint64_t lpol, uint64_t spol)
+{
+    constexpr int W = BYTES / 4;
+    constexpr int WARPS = THREADS / 32;
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int shift = s.shift;
+    const uint64_t nunits = s.bytes / BYTES;
+    const uint64_t q0 = (uint64_t)tile * shifted_tile_units(THREADS * UNROLL);
+    atom::Vec<BYTES> v[UNROLL];
+#pragma unroll
+    for (int k = 0; k < UNROLL; ++k) {
+        const uint64_t q = q0 + (uint64_t)(k * WARPS + warp) * 31 + lane;
+        if (q <= nunits) {
+            atom::load(v[k], at(p.in[s.src], s.src_off + q * BYTES, shift), lpol);
+        } else {
+#pragma unroll
+            for (int i = 0; i < W; ++i) v[k].w[i] = 0u;
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < UNROLL; ++k) {
+        const uint64_t q = q0 + (uint64_t)(k * WARPS + warp) * 31 + lane;
+        atom::Vec<BYTES> next, out;
+#pragma unroll
+        for (int i = 0; i < W; ++i) next.w[i] = __shfl_down_sync(0xffffffffu, v[k].w[i], 1);
+        if (lane == 31 || q >= nunits) continue;
+        realign<W>(v[k].w, next.w, shift, out.w);
+        const uint64_t o = s.dst_off + q * BYTES;
+        if (FAN_ALL) {
+            for (int r = 0; r < (int)p.R; ++r) atom::store(p.out[r] + o, out, spol);
+        } else {
+            atom::store(p.out[s.dst] + o, out, spol);
+        }
+    }
+}
+
 // ------------------------------------------------------------------ reduce
 
 // One unit per thread (sums of more than 4 ranks, and the pairwise order).
@@ -126,8 +255,9 @@ __device__ __forceinline__ void reduce_element(const ZsParams<kSegsSmall>& p, co
 // THREADS threads per CTA: kThreads for large messages, one warp
 // (kSmallThreads) for small ones.  NR bounds the rank count (R <= NR); a tile
 // holds THREADS x (kMaxRanks / NR) units, so sums of 2 or 4 ranks take 4 or 2
-// units per thread.
-template <typename T, int ORDER, bool FAN_ALL, int THREADS, int NR>
+// units per thread.  SHIFTED kernels also serve shifted segments; a launch
+// with none runs the kernel without that path.
+template <typename T, int ORDER, bool FAN_ALL, int THREADS, int NR, bool SHIFTED>
 __global__ void __launch_bounds__(THREADS, THREADS == kThreads ? 2 : 16)
 zs_reduce_kernel(const __grid_constant__ ZsParams<kSegsSmall> p)
 {
@@ -139,6 +269,13 @@ zs_reduce_kernel(const __grid_constant__ ZsParams<kSegsSmall> p)
     for (uint32_t t = blockIdx.x; t < p.ntiles; t += gridDim.x) {
         const Segment& s = segment_of(p, t);
         const int ul = s.unit_log2;
+        if constexpr (SHIFTED) {
+            if (s.shift) {
+                if (ul == 5) reduce_shifted<T, ORDER, FAN_ALL, 32, NR, THREADS>(p, s, t - s.tile0, R, lpol, spol);
+                else reduce_shifted<T, ORDER, FAN_ALL, 16, NR, THREADS>(p, s, t - s.tile0, R, lpol, spol);
+                continue;
+            }
+        }
         if constexpr (U == 1) {
             // kept in this form: the one-unit kernels scheduled from the
             // general tile loop below ran up to 8 % slower (fp32 AllReduce)
@@ -215,8 +352,8 @@ __device__ __forceinline__ void copy_tile(const ZsParams<MAXSEG>& p, const Segme
 }
 
 // THREADS x UNROLL units per tile: kThreads x kUnrollCopy for large messages,
-// one warp with one unit per thread for small ones.
-template <bool FAN_ALL, int MAXSEG, int THREADS, int UNROLL>
+// one warp with one unit per thread for small ones.  SHIFTED: as for the sums.
+template <bool FAN_ALL, int MAXSEG, int THREADS, int UNROLL, bool SHIFTED>
 __global__ void __launch_bounds__(THREADS, THREADS == kThreads ? 2 : 16)
 zs_copy_kernel(const __grid_constant__ ZsParams<MAXSEG> p)
 {
@@ -226,6 +363,13 @@ zs_copy_kernel(const __grid_constant__ ZsParams<MAXSEG> p)
     for (uint32_t t = blockIdx.x; t < p.ntiles; t += gridDim.x) {
         const Segment& s = segment_of(p, t);
         const int ul = s.unit_log2;
+        if constexpr (SHIFTED) {
+            if (s.shift) {
+                if (ul == 5) copy_shifted<32, FAN_ALL, THREADS, UNROLL>(p, s, t - s.tile0, lpol, spol);
+                else copy_shifted<16, FAN_ALL, THREADS, UNROLL>(p, s, t - s.tile0, lpol, spol);
+                continue;
+            }
+        }
         const uint64_t base = (uint64_t)(t - s.tile0) * tile_bytes(ul, THREADS * UNROLL);
         switch (ul) {
         case 5: copy_tile<32, FAN_ALL, THREADS, UNROLL>(p, s, base, lpol, spol); break;

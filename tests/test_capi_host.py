@@ -127,6 +127,16 @@ def check_alignment(segs, R, in_addr, out_addr, reduce, esz):
             else [in_addr[s["src_rank"]] + s["src_off"]]
         dsts = [out_addr[r] + s["dst_off"] for r in range(R)] if s["dst_rank"] == -1 \
             else [out_addr[s["dst_rank"]] + s["dst_off"]]
+        if s["shift"]:
+            # shifted body: destinations aligned, every source `shift` past a boundary
+            assert u in (16, 32) and 0 < s["shift"] < u, s
+            for a in dsts:
+                assert a % u == 0, (s, a)
+            for a in srcs:
+                assert a % u == s["shift"], (s, a)
+            if reduce:
+                assert s["shift"] % esz == 0, s
+            continue
         for a in srcs + dsts:
             assert a % u == 0, (s, a)
         if reduce:
@@ -139,7 +149,10 @@ def check_tiles(segs, ntiles, reduce, R):
     t = 0
     for s in segs:
         assert s["tile0"] == t
-        tb = 256 * s["unit"] * unroll
+        units = 256 * unroll
+        if s["shift"]:
+            units = units // 32 * 31   # each warp writes 31 units of 32 lanes' blocks
+        tb = units * s["unit"]
         t += -(-s["bytes"] // tb)
     assert t == ntiles
 
@@ -261,3 +274,26 @@ def test_plan_at_maximum_sizes(lib):
     C = np.full(R * R, 1001)
     segs, _ = rd.purlin_plan_segments(rd.COLL_ALL_TO_ALL_V, R, odd, b, C, dtype="u8")
     assert len(segs) <= 3 * R * R
+
+
+def test_offset_partitions_get_shifted_bodies(lib):
+    """ReduceScatter of 3 ranks whose partitions start 20 bytes past a 32-byte
+    boundary: aligned outputs take 32-byte vector bodies that read the sources
+    shifted by 20 (not element by element); the aligned partition 0 is plain.
+    AllGather placing such blocks, the copy analogue, and the TMA bulk plan
+    (never shifted) are checked by the kernels' parity tests."""
+    R, esz = 3, 2
+    c = 16 * 1000 + 10                          # 32,020 B per partition: 20 mod 32
+    in_addr = [(1 << 32) * (r + 1) for r in range(R)]
+    out_addr = [(1 << 32) * (r + 9) for r in range(R)]
+    segs, ntiles = rd.purlin_plan_segments(rd.COLL_REDUCE_SCATTER, R, in_addr, out_addr,
+                                           [c] * R, dtype="bf16")
+    check_alignment(segs, R, in_addr, out_addr, True, esz)
+    check_tiles(segs, ntiles, True, R)
+    body = {s["dst_rank"]: s for s in segs if s["unit"] == 32}
+    assert body[0]["shift"] == 0 and body[0]["bytes"] >= c * esz - 32
+    for k in (1, 2):
+        assert body[k]["shift"] == (k * c * esz) % 32 and body[k]["shift"] != 0
+        assert body[k]["bytes"] >= c * esz - 64     # only a sub-vector head and tail
+    assert plan_map(segs, R) == expected_map(rd.COLL_REDUCE_SCATTER, R, [c] * R, None, None, 0,
+                                             esz)

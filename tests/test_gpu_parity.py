@@ -588,3 +588,83 @@ def test_launch_shape_follows_message_size(coll, nbytes, small, R):
     assert info["block"] == (32 if small else 256), info
     for j in range(R):
         assert same_bits(host_bits(out[j]), want[j]), j
+
+
+# ------------------------------------------------------------ shifted bodies
+
+@pytest.mark.parametrize("policy", ["zs", "zs_large", "zs_small"])
+@pytest.mark.parametrize("dtype", ["bf16", "f32", "f16"])
+@pytest.mark.parametrize("R", [2, 3, 5, 8])
+def test_reduce_scatter_shifted_partitions(policy, dtype, R):
+    """Partitions whose starts sit off the 32-byte grid while the outputs are
+    aligned: the bodies are summed at the sources' alignment and realigned to
+    the outputs' (several tiles of warps, a ragged end)."""
+    h = handle(R)
+    set_variant(h, *POLICIES[policy])
+    c = 9 * 1024 + 7 if dtype != "f32" else 5 * 1024 + 3
+    x = inputs(R, R * c, dtype, seed=31 * R + len(dtype))
+    outs = [Guarded(c, dtype) for _ in range(R)]
+    rd.purlin_reduce_scatter(h, x, [o.view for o in outs], [c] * R, None, dtype)
+    run_ok(h)
+    want = oracle.reduce_scatter(oracle_in(x), [c] * R, dtype=dtype)
+    for k in range(R):
+        assert same_bits(host_bits(outs[k].view), want[k]), k
+        assert outs[k].guards_intact()
+
+
+@pytest.mark.parametrize("policy", ["zs", "zs_large", "zs_small"])
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("R", [2, 4, 8])
+@pytest.mark.parametrize("offset", [1, 3, 6])
+def test_all_reduce_shifted_outputs(policy, dtype, R, offset):
+    """Aligned inputs, outputs `offset` elements into their allocations."""
+    n = 40000 + 11
+    h = handle(R)
+    set_variant(h, *POLICIES[policy])
+    x = inputs(R, n, dtype, seed=700 + R + offset)
+    outs = [Guarded(n, dtype, offset=offset) for _ in range(R)]
+    rd.purlin_all_reduce(h, x, [o.view for o in outs], n, dtype)
+    run_ok(h)
+    want = oracle.all_reduce(oracle_in(x), dtype=dtype)
+    for j in range(R):
+        assert same_bits(host_bits(outs[j].view), want[j]), j
+        assert outs[j].guards_intact()
+
+
+@pytest.mark.parametrize("policy", ["zs", "zs_large", "zs_small", "zs_pull"])
+@pytest.mark.parametrize("R", [2, 3, 8])
+@pytest.mark.parametrize("dtype", ["bf16", "u8"])
+def test_all_gather_shifted_blocks(policy, R, dtype):
+    """Blocks of lengths that place each rank's block off the 32-byte grid of
+    the outputs (copies realigned in registers), several tiles long."""
+    h = handle(R)
+    set_variant(h, *POLICIES[policy])
+    counts = [20000 + 13 * k + (5 if dtype == "u8" else 3) for k in range(R)]
+    x = [inputs(1, c, dtype, seed=50 + k)[0] for k, c in enumerate(counts)]
+    total = sum(counts)
+    outs = [Guarded(total, dtype) for _ in range(R)]
+    rd.purlin_all_gather(h, x, [o.view for o in outs], counts, None, dtype)
+    run_ok(h)
+    want = oracle.all_gather(oracle_in(x))
+    for j in range(R):
+        assert same_bits(host_bits(outs[j].view), want[j]), j
+        assert outs[j].guards_intact()
+
+
+@pytest.mark.parametrize("policy", ["zs", "zs_large", "zs_small"])
+@pytest.mark.parametrize("R", [3, 8])
+def test_all_to_all_v_shifted_blocks(policy, R):
+    """Per-pair counts that are not multiples of 16 bytes: send and receive
+    offsets fall on different residues."""
+    h = handle(R)
+    set_variant(h, *POLICIES[policy])
+    rng = np.random.default_rng(R)
+    C = rng.integers(3000, 9000, size=(R, R)) | 1
+    x = [inputs(1, int(C[s].sum()), "bf16", seed=90 + s)[0] for s in range(R)]
+    outs = [Guarded(int(C[:, j].sum()), "bf16") for j in range(R)]
+    rd.purlin_all_to_all_v(h, x, [o.view for o in outs], C, None, None, "bf16")
+    run_ok(h)
+    want = oracle.all_to_all_v(oracle_in(x), C)
+    for j in range(R):
+        assert same_bits(host_bits(outs[j].view), want[j]), j
+        assert outs[j].guards_intact()
