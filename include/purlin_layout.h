@@ -42,7 +42,8 @@ typedef struct {
     int32_t shift;     /* 0, or a shifted vector body: the destinations are aligned
                           to `unit` and every source starts `shift` bytes (0 <
                           shift < unit) past a unit boundary; the kernel reads
-                          aligned source blocks and realigns them in registers   */
+                          aligned source blocks and realigns them in registers.
+                          A sum plan holding one has 16-byte bodies throughout  */
 } purlin_segment_t;
 
 /* Derive the plan of one collective.

@@ -234,6 +234,15 @@ purlin_status_t make_params(ZsParams<MAXSEG>& p, const Piece* pieces, int npiece
     int n = layout_segments(pieces, npieces, R, in, out, esz, reduce, k.tile_units,
                             max_unit_log2, k.allow_shift, p.seg, MAXSEG, &ntiles);
     if (n < 0) return PURLIN_ERR_UNSUPPORTED;
+    if (reduce && max_unit_log2 > 4) {
+        // the kernels that serve shifted sums take 16-byte vector bodies only
+        bool shifted = false;
+        for (int i = 0; i < n; ++i) shifted |= p.seg[i].shift != 0;
+        if (shifted)
+            n = layout_segments(pieces, npieces, R, in, out, esz, reduce, k.tile_units, 4,
+                                k.allow_shift, p.seg, MAXSEG, &ntiles);
+        if (n < 0) return PURLIN_ERR_UNSUPPORTED;
+    }
     p.nseg = (uint32_t)n;
     p.ntiles = ntiles;
     return PURLIN_OK;
@@ -838,9 +847,16 @@ purlin_status_t purlin_plan_segments(purlin_collective_t coll, int R, const uint
     if (np < 0) return PURLIN_ERR_INVALID_ARG;
     Segment tmp[kSegsLarge];
     uint32_t nt = 0;
-    int n = layout_segments(pieces, np, R, in_addr, out_addr, esz, reduce,
-                            reduce ? kThreads * reduce_unroll(R, 0) : kTileUnitsCopy,
+    const int tile_units = reduce ? kThreads * reduce_unroll(R, 0) : kTileUnitsCopy;
+    int n = layout_segments(pieces, np, R, in_addr, out_addr, esz, reduce, tile_units,
                             max_unit == 32 ? 5 : 4, /*allow_shift=*/true, tmp, kSegsLarge, &nt);
+    if (n > 0 && reduce && max_unit == 32) {
+        bool shifted = false;   // as the launch: 16-byte bodies when a sum is shifted
+        for (int i = 0; i < n; ++i) shifted |= tmp[i].shift != 0;
+        if (shifted)
+            n = layout_segments(pieces, np, R, in_addr, out_addr, esz, reduce, tile_units, 4,
+                                /*allow_shift=*/true, tmp, kSegsLarge, &nt);
+    }
     if (n < 0 || n > max_segs) return PURLIN_ERR_UNSUPPORTED;
     for (int i = 0; i < n; ++i) {
         segs[i].src_off = tmp[i].src_off;

@@ -206,7 +206,10 @@ int layout_segments(const Piece* pieces, int npieces, int R, const uint64_t* in_
         // unit boundary; heads and tails go element (sum) or byte-group (copy)
         // wise.
         auto try_shifted = [&]() {
-            for (int u_log2 = max_unit_log2; u_log2 >= 4; --u_log2) {
+            // shifted sums take 16-byte units: with 32-byte ones the R blocks,
+            // their neighbours' and the realignment outgrow the registers
+            const int widest = reduce ? std::min(max_unit_log2, 4) : max_unit_log2;
+            for (int u_log2 = widest; u_log2 >= 4; --u_log2) {
                 const uint64_t u = (uint64_t)1 << u_log2, mask = u - 1;
                 if (!same_residue(addrs, ns, mask) || !same_residue(dsts, nd, mask)) continue;
                 const uint64_t head = std::min<uint64_t>((u - (dsts[0] & mask)) & mask, p.bytes);

@@ -65,7 +65,7 @@ struct ZsParams {
     uint32_t l2_load;   // eviction priority of source loads (kL2*)
     uint32_t l2_store;  // ... and of destination stores
     uint32_t pdl;       // launched with programmatic stream serialization
-    int* status;        // device status word (bounded waits of the bulk kernel)
+    int* status;        // device status word (bounded waits of the bulk kernel, plan checks)
     uint32_t R;
     uint32_t nseg;
     uint32_t ntiles;

@@ -88,9 +88,11 @@ __device__ __forceinline__ const char* at(const char* base, uint64_t off, int ba
     return reinterpret_cast<const char*>(reinterpret_cast<uintptr_t>(base) + off - (uint64_t)back);
 }
 
-// One tile of a shifted sum: U = kMaxRanks / NR rows of 31-unit warp runs.
+// One tile of a 16- or 32-byte vector body in a launch that holds a shifted
+// sum: U = kMaxRanks / NR rows of warp runs, 31 units a warp for a shifted
+// body, 32 for an aligned one (no exchange between lanes).
 template <typename T, int ORDER, bool FAN_ALL, int BYTES, int NR, int THREADS>
-__device__ __forceinline__ void reduce_shifted(const ZsParams<kSegsSmall>& p, const Segment& s,
+__device__ __forceinline__ void reduce_rows(const ZsParams<kSegsSmall>& p, const Segment& s,
                                             uint32_t tile, int R, uint64_t lpol, uint64_t spol)
 {
     constexpr int U = kMaxRanks / NR;
@@ -99,15 +101,18 @@ __device__ __forceinline__ void reduce_shifted(const ZsParams<kSegsSmall>& p, co
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int shift = s.shift;
+    const int per_warp = shift ? 31 : 32;
     const uint64_t nunits = s.bytes / BYTES;
-    const uint64_t q0 = (uint64_t)tile * shifted_tile_units(THREADS * U);
+    // a shifted body also reads the block after its last unit
+    const uint64_t nblocks = shift ? nunits + 1 : nunits;
+    const uint64_t q0 = (uint64_t)tile * (shift ? shifted_tile_units(THREADS * U) : THREADS * U);
     atom::Vec<BYTES> v[U][NR];
 #pragma unroll
     for (int k = 0; k < U; ++k) {
-        const uint64_t q = q0 + (uint64_t)(k * WARPS + warp) * 31 + lane;
+        const uint64_t q = q0 + (uint64_t)(k * WARPS + warp) * per_warp + lane;
 #pragma unroll
         for (int r = 0; r < NR; ++r) {
-            if (r < R && q <= nunits) {
+            if (r < R && q < nblocks) {
                 atom::load(v[k][r], at(p.in[r], s.src_off + q * BYTES, shift), lpol);
             } else {
 #pragma unroll
@@ -117,13 +122,19 @@ __device__ __forceinline__ void reduce_shifted(const ZsParams<kSegsSmall>& p, co
     }
 #pragma unroll
     for (int k = 0; k < U; ++k) {
-        const uint64_t q = q0 + (uint64_t)(k * WARPS + warp) * 31 + lane;
-        atom::Vec<BYTES> y, next, out;
+        const uint64_t q = q0 + (uint64_t)(k * WARPS + warp) * per_warp + lane;
+        atom::Vec<BYTES> y, out;
         atom::reduce_unit<T, ORDER, BYTES, NR>(v[k], R, y);
+        if (shift) {
+            atom::Vec<BYTES> next;
 #pragma unroll
-        for (int i = 0; i < W; ++i) next.w[i] = __shfl_down_sync(0xffffffffu, y.w[i], 1);
-        if (lane == 31 || q >= nunits) continue;
-        realign<W>(y.w, next.w, shift, out.w);
+            for (int i = 0; i < W; ++i) next.w[i] = __shfl_down_sync(0xffffffffu, y.w[i], 1);
+            if (lane == 31 || q >= nunits) continue;
+            realign<W>(y.w, next.w, shift, out.w);
+        } else {
+            if (q >= nunits) continue;
+            out = y;
+        }
         const uint64_t o = s.dst_off + q * BYTES;
         if (FAN_ALL) {
 #pragma unroll
@@ -270,11 +281,21 @@ zs_reduce_kernel(const __grid_constant__ ZsParams<kSegsSmall> p)
         const Segment& s = segment_of(p, t);
         const int ul = s.unit_log2;
         if constexpr (SHIFTED) {
-            if (s.shift) {
-                if (ul == 5) reduce_shifted<T, ORDER, FAN_ALL, 32, NR, THREADS>(p, s, t - s.tile0, R, lpol, spol);
-                else reduce_shifted<T, ORDER, FAN_ALL, 16, NR, THREADS>(p, s, t - s.tile0, R, lpol, spol);
-                continue;
+            // a launch holding a shifted sum is planned with 16-byte vector
+            // bodies only (and element heads and tails)
+            if (ul == 4) {
+                reduce_rows<T, ORDER, FAN_ALL, 16, NR, THREADS>(p, s, t - s.tile0, R, lpol, spol);
+            } else if (ul < 4) {
+                const uint64_t base = (uint64_t)(t - s.tile0) * tile_bytes(ul, THREADS * U);
+#pragma unroll
+                for (int k = 0; k < U; ++k) {
+                    const uint64_t off = base + ((uint64_t)(k * THREADS + threadIdx.x) << ul);
+                    if (off < s.bytes) reduce_element<T, ORDER, FAN_ALL>(p, s, off, R);
+                }
+            } else if (threadIdx.x == 0) {
+                atomicCAS(p.status, 0, (int)PURLIN_ERR_UNSUPPORTED);  // not planned this way
             }
+            continue;
         }
         if constexpr (U == 1) {
             // kept in this form: the one-unit kernels scheduled from the

@@ -278,10 +278,10 @@ def test_plan_at_maximum_sizes(lib):
 
 def test_offset_partitions_get_shifted_bodies(lib):
     """ReduceScatter of 3 ranks whose partitions start 20 bytes past a 32-byte
-    boundary: aligned outputs take 32-byte vector bodies that read the sources
-    shifted by 20 (not element by element); the aligned partition 0 is plain.
-    AllGather placing such blocks, the copy analogue, and the TMA bulk plan
-    (never shifted) are checked by the kernels' parity tests."""
+    boundary: aligned outputs take 16-byte vector bodies that read the sources
+    shifted by 4 (not element by element), and the plan's other bodies are
+    16-byte too; the aligned partition 0 is plain.  AllGather placing such
+    blocks, the copy analogue, keeps 32-byte units."""
     R, esz = 3, 2
     c = 16 * 1000 + 10                          # 32,020 B per partition: 20 mod 32
     in_addr = [(1 << 32) * (r + 1) for r in range(R)]
@@ -290,10 +290,18 @@ def test_offset_partitions_get_shifted_bodies(lib):
                                            [c] * R, dtype="bf16")
     check_alignment(segs, R, in_addr, out_addr, True, esz)
     check_tiles(segs, ntiles, True, R)
-    body = {s["dst_rank"]: s for s in segs if s["unit"] == 32}
-    assert body[0]["shift"] == 0 and body[0]["bytes"] >= c * esz - 32
+    assert all(s["unit"] in (esz, 16) for s in segs)
+    body = {s["dst_rank"]: s for s in segs if s["unit"] == 16}
+    assert body[0]["shift"] == 0 and body[0]["bytes"] >= c * esz - 16
     for k in (1, 2):
-        assert body[k]["shift"] == (k * c * esz) % 32 and body[k]["shift"] != 0
-        assert body[k]["bytes"] >= c * esz - 64     # only a sub-vector head and tail
+        assert body[k]["shift"] == (k * c * esz) % 16 and body[k]["shift"] != 0
+        assert body[k]["bytes"] >= c * esz - 32     # only a sub-vector head and tail
     assert plan_map(segs, R) == expected_map(rd.COLL_REDUCE_SCATTER, R, [c] * R, None, None, 0,
                                              esz)
+    # the copy back (AllGather of those partitions into packed outputs): 32-byte
+    # bodies shifted by the partitions' offsets
+    segs, ntiles = rd.purlin_plan_segments(rd.COLL_ALL_GATHER, R, out_addr, in_addr, [c] * R,
+                                           dtype="bf16")
+    check_alignment(segs, R, out_addr, in_addr, False, esz)
+    check_tiles(segs, ntiles, False, R)
+    assert any(s["unit"] == 32 and s["shift"] for s in segs)
