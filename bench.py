@@ -534,6 +534,7 @@ def bench_purlin(args):
         # ---- the other workload configurations, zero staging (default policy)
         configs = other_configs(rd, torch, dev, stream, peak)
         configs["zs_by_rank_count"] = rank_scaling(rd, torch, dev, stream, peak)
+        configs["off_grid_partitions"] = off_grid_partitions(rd, torch, dev, stream, peak)
 
         # ---- AllReduce size sweep: zero staging vs SNAC (default policy)
         sweep = allreduce_sweep(rd, torch, dev, stream, peak)
@@ -793,6 +794,48 @@ def rank_scaling(rd, torch, dev, stream, peak):
             finally:
                 rd.purlin_destroy(h)
                 torch.cuda.empty_cache()
+    return out
+
+
+def off_grid_partitions(rd, torch, dev, stream, peak):
+    """Layouts whose partitions start off the 32-byte grid (64 MiB per rank,
+    bf16): 3 ranks (partitions of n/3 elements start 20 bytes past a
+    boundary), 8 ranks with partitions 3 elements short, and an AllReduce into
+    outputs one element into their allocations.  The plans read the sources
+    through shifted vector bodies."""
+    out = []
+    for R_, trim in ((3, 0), (8, 3)):
+        n = BYTES_PER_RANK // 2
+        c = n // R_ - trim
+        h = rd.purlin_create(R_, 0, dev.index)
+        try:
+            x = [torch.randn(R_ * c, device=dev).to(torch.bfloat16) for _ in range(R_)]
+            y = [torch.empty(c, dtype=torch.bfloat16, device=dev) for _ in range(R_)]
+            zf = [torch.empty(R_ * c + 1, dtype=torch.bfloat16, device=dev) for _ in range(R_)]
+            z = [t[:R_ * c] for t in zf]
+            zo = [t[1:] for t in zf]
+            m = R_ * c
+            runs = (("reduce_scatter", lambda: rd.purlin_reduce_scatter(
+                        h, x, y, [c] * R_, None, "bf16", stream=stream), (R_ + 1) * c * R_ * 2),
+                    ("all_gather", lambda: rd.purlin_all_gather(
+                        h, y, z, [c] * R_, None, "bf16", stream=stream), (R_ + 1) * c * R_ * 2),
+                    ("all_reduce_off_grid_outputs", lambda: rd.purlin_all_reduce(
+                        h, x, zo, m, "bf16", stream=stream), 2 * R_ * m * 2))
+            for name, fn, nbytes in runs:
+                with torch.cuda.stream(stream):
+                    for _ in range(3):
+                        fn()
+                torch.cuda.synchronize()
+                us = _events_us(torch, stream, fn, 20)
+                gbs = nbytes / (us / 1e6) / 1e9
+                out.append({"R": R_, "partition_elems": c, "collective": name, "us": round(us, 1),
+                            "gbs": round(gbs, 1), "frac_of_peak": round(gbs / peak, 3)})
+            if rd.purlin_query_status(h) != rd.OK:
+                raise RuntimeError("off-grid partitions: device status not ok")
+            del x, y, zf, z, zo
+        finally:
+            rd.purlin_destroy(h)
+            torch.cuda.empty_cache()
     return out
 
 
