@@ -40,9 +40,11 @@ typedef struct {
                           byte granularity for unaligned heads and tails            */
     uint32_t tile0;    /* first tile of the segment in the launch's tile space     */
     int32_t shift;     /* 0, or a shifted vector body: the destinations are aligned
-                          to `unit` and every source starts `shift` bytes (0 <
-                          shift < unit) past a unit boundary; the kernel reads
-                          aligned source blocks and realigns them in registers.
+                          to `unit`; the first source off that grid starts
+                          `shift` bytes (0 < shift < unit) past a unit boundary.
+                          The kernel reads aligned source blocks and realigns
+                          them in registers (a sum realigns each rank on its own
+                          offset, so its sources may sit on different grids).
                           A sum plan holding one has 16-byte bodies throughout  */
 } purlin_segment_t;
 

@@ -248,12 +248,17 @@ purlin_status_t make_params(ZsParams<MAXSEG>& p, const Piece* pieces, int npiece
     return PURLIN_OK;
 }
 
+// Which kernels a plan needs: 0 no shifted body, 1 shifted bodies whose
+// sources share one offset, 2 a sum whose ranks' sources sit on different ones.
 template <int MAXSEG>
-bool has_shift(const ZsParams<MAXSEG>& p)
+int has_shift(const ZsParams<MAXSEG>& p)
 {
-    for (uint32_t i = 0; i < p.nseg; ++i)
-        if (p.seg[i].shift) return true;
-    return false;
+    int mode = 0;
+    for (uint32_t i = 0; i < p.nseg; ++i) {
+        if (p.seg[i].shift & kShiftPerRank) return 2;
+        if (p.seg[i].shift) mode = 1;
+    }
+    return mode;
 }
 
 // Small messages: when the large-message plan has fewer than h->small_tiles
@@ -327,6 +332,30 @@ int zs_grid(const purlin_handle* h, uint32_t ntiles, int resident, long waves = 
     if (ntiles == 0) return 0;
     long g = h->ctas > 0 ? h->ctas : (long)h->sms * resident * waves;
     return (int)std::max<long>(1, std::min<long>(g, (long)ntiles));
+}
+
+// The AllGather's pieces by destination: one per (destination, source),
+// destination by destination, in-place blocks dropped.  Returns their count.
+int pull_pieces(const Piece* pieces, int np, int R, const uint64_t* in, const uint64_t* out,
+                Piece* pulled)
+{
+    int n = 0;
+    for (int j = 0; j < R; ++j)
+        for (int i = 0; i < np; ++i) {
+            Piece e = pieces[i];
+            e.dst = (uint8_t)j;
+            if (in[e.src] + e.src_off == out[j] + e.dst_off) continue;  // in place
+            pulled[n++] = e;
+        }
+    return n;
+}
+
+// Whether the R output buffers share one 16-byte alignment.
+bool outputs_share_grid(const uint64_t* out, int R)
+{
+    for (int r = 1; r < R; ++r)
+        if ((out[r] ^ out[0]) & 15u) return false;
+    return true;
 }
 
 bool wants_staged(const purlin_handle* h)
@@ -442,7 +471,13 @@ purlin_status_t run(purlin_handle_t h, Coll coll, const void* const in_[], void*
             info.block = 0;
             info.chunk_bytes = 0;
         } else if (coll == Coll::AllToAllV ||
-                   (coll == Coll::AllGather && h->direction == PURLIN_DIRECTION_PULL)) {
+                   (coll == Coll::AllGather &&
+                    (h->direction == PURLIN_DIRECTION_PULL ||
+                     (h->direction == PURLIN_DIRECTION_AUTO && !bulk &&
+                      !outputs_share_grid(out, R))))) {
+            // AllGather outputs on different 16-byte alignments: one fan-out
+            // body cannot be aligned to all of them, single-destination pieces
+            // can (each a shifted body where its source is off its grid)
             ZsParams<kSegsLarge>& p = *reinterpret_cast<ZsParams<kSegsLarge>*>(k.params);
             const Piece* plan = pieces;
             int nplan = np;
@@ -451,14 +486,7 @@ purlin_status_t run(purlin_handle_t h, Coll coll, const void* const in_[], void*
                 // pull: one piece per (destination, source), destination by
                 // destination; every source is read R times (from L2 after
                 // the first read, hence normal priority for the loads)
-                nplan = 0;
-                for (int j = 0; j < R; ++j)
-                    for (int i = 0; i < np; ++i) {
-                        Piece e = pieces[i];
-                        e.dst = (uint8_t)j;
-                        if (in[e.src] + e.src_off == out[j] + e.dst_off) continue;  // in place
-                        pulled[nplan++] = e;
-                    }
+                nplan = pull_pieces(pieces, np, R, in, out, pulled);
                 plan = pulled;
                 if (h->l2_load < 0 && h->l2_coll_load[(int)coll] < 0) knobs.l2_load = kL2Normal;
             }
@@ -471,7 +499,7 @@ purlin_status_t run(purlin_handle_t h, Coll coll, const void* const in_[], void*
                 info.block = kBulkThreads;
             } else {
                 const bool small = replan_small(h, coll, p, plan, nplan, R, in, out, esz, false, knobs);
-                const bool sh = has_shift(p);
+                const bool sh = has_shift(p) != 0;
                 grid = zs_grid(h, p.ntiles, zs_copy_resident_ctas(true, false, small, sh));
                 zs_copy_select(k, true, false, small, sh);
                 if (small) info.block = kSmallThreads;
@@ -495,12 +523,12 @@ purlin_status_t run(purlin_handle_t h, Coll coll, const void* const in_[], void*
             } else {
                 const bool small = replan_small(h, coll, p, pieces, np, R, in, out, esz, reduce, knobs);
                 if (reduce) {
-                    const bool sh = has_shift(p);
+                    const int sh = has_shift(p);
                     grid = zs_grid(h, p.ntiles,
                                    zs_reduce_resident_ctas(dtype, h->order, fan_all, small, R, sh));
                     zs_reduce_select(k, dtype, h->order, fan_all, small, R, sh);
                 } else {
-                    const bool sh = has_shift(p);
+                    const bool sh = has_shift(p) != 0;
                     grid = zs_grid(h, p.ntiles, zs_copy_resident_ctas(false, fan_all, small, sh));
                     zs_copy_select(k, false, fan_all, small, sh);
                 }
@@ -845,6 +873,13 @@ purlin_status_t purlin_plan_segments(purlin_collective_t coll, int R, const uint
     Piece pieces[kSegsLarge];
     int np = layout_pieces(c, R, counts, displs_a, displs_b, count, esz, pieces, kSegsLarge);
     if (np < 0) return PURLIN_ERR_INVALID_ARG;
+    Piece pulled[kMaxRanks * kMaxRanks];
+    if (c == Coll::AllGather && !outputs_share_grid(out_addr, R)) {
+        // as the launch (automatic direction): outputs on different 16-byte
+        // alignments take the AllGather by destination
+        np = pull_pieces(pieces, np, R, in_addr, out_addr, pulled);
+        std::memcpy(pieces, pulled, sizeof(Piece) * (size_t)np);
+    }
     Segment tmp[kSegsLarge];
     uint32_t nt = 0;
     const int tile_units = reduce ? kThreads * reduce_unroll(R, 0) : kTileUnitsCopy;
@@ -865,7 +900,7 @@ purlin_status_t purlin_plan_segments(purlin_collective_t coll, int R, const uint
         segs[i].src_rank = tmp[i].src == kEveryRank ? -1 : tmp[i].src;
         segs[i].dst_rank = tmp[i].dst == kEveryRank ? -1 : tmp[i].dst;
         segs[i].unit = 1 << tmp[i].unit_log2;
-        segs[i].shift = tmp[i].shift;
+        segs[i].shift = tmp[i].shift & ~kShiftPerRank;
         segs[i].tile0 = tmp[i].tile0;
     }
     *nsegs = n;

@@ -48,13 +48,14 @@ int resident_ctas_of(const void* kernel, int threads);
 // built with kTileUnitsSmall; else kThreads-thread CTAs, kTileUnitsReduce.
 // Units per thread of the kThreads-thread sum kernel for R ranks and a rank
 // order (R x units <= kMaxRanks vectors in flight per thread); the plan's tiles
-// are kThreads x reduce_unroll(R, order) units.  shifted: the plan holds a
-// shifted segment (Segment::shift), which only the SHIFTED kernels serve (the
-// fixed rank order only).
+// are kThreads x reduce_unroll(R, order) units.  shift_mode: 0 the plan holds
+// no shifted segment (Segment::shift); 1 shifted segments whose sources share
+// one offset; 2 one whose ranks' sources sit on different offsets (kernels of
+// the fixed rank order only serve 1 and 2).
 int reduce_unroll(int R, int order);
 void zs_reduce_select(KernelLaunch& k, int dtype, int order, bool fan_all, bool small, int R,
-                      bool shifted);
-int zs_reduce_resident_ctas(int dtype, int order, bool fan_all, bool small, int R, bool shifted);
+                      int shift_mode);
+int zs_reduce_resident_ctas(int dtype, int order, bool fan_all, bool small, int R, int shift_mode);
 
 // Copy.  fan_all: every segment goes to every output (AllGather), else to the
 // segment's destination (AllToAll(V)).  large: ZsParams<kSegsLarge> (else

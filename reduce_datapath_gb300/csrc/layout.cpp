@@ -199,24 +199,29 @@ int layout_segments(const Piece* pieces, int npieces, int R, const uint64_t* in_
         const uint64_t* dsts = addrs + ns;
         const int nd = na - ns;
 
-        // Shifted body: the sources agree on a vector alignment among
-        // themselves and so do the destinations, but not with each other.  The
-        // body's vector units are aligned to the destinations (a head of less
-        // than one unit gets there) and read the sources `shift` bytes past a
-        // unit boundary; heads and tails go element (sum) or byte-group (copy)
-        // wise.
+        // Shifted body: the destinations agree on a vector alignment among
+        // themselves but the sources do not share it.  The body's vector units
+        // are aligned to the destinations (a head of less than one unit gets
+        // there); every source is read from the unit boundary at or before it
+        // and realigned in registers -- for a sum each rank on its own shift, so
+        // its ranks' buffers may sit on different alignments.  Heads and tails
+        // go element (sum) or byte-group (copy) wise.
         auto try_shifted = [&]() {
             // shifted sums take 16-byte units: with 32-byte ones the R blocks,
             // their neighbours' and the realignment outgrow the registers
             const int widest = reduce ? std::min(max_unit_log2, 4) : max_unit_log2;
             for (int u_log2 = widest; u_log2 >= 4; --u_log2) {
                 const uint64_t u = (uint64_t)1 << u_log2, mask = u - 1;
-                if (!same_residue(addrs, ns, mask) || !same_residue(dsts, nd, mask)) continue;
+                if (!same_residue(dsts, nd, mask)) continue;
+                if (!reduce && !same_residue(addrs, ns, mask)) continue;
                 const uint64_t head = std::min<uint64_t>((u - (dsts[0] & mask)) & mask, p.bytes);
                 const uint64_t body = ((p.bytes - head) / u) * u;
                 const uint64_t tail = p.bytes - head - body;
-                const int shift = (int)((addrs[0] + head) & mask);
+                // the first source off the destinations' grid (0: none is)
+                int shift = 0;
+                for (int a = 0; a < ns && shift == 0; ++a) shift = (int)((addrs[a] + head) & mask);
                 if (body == 0 || shift == 0) return 0;
+                if (!same_residue(addrs, ns, mask)) shift |= kShiftPerRank;
                 // widest access every stream and the length allow, at offset `off`
                 auto small_log2 = [&](uint64_t off, uint64_t len) {
                     if (reduce) return elem_log2;

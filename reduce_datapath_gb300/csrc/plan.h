@@ -49,8 +49,13 @@ struct Segment {
     uint8_t dst;        // destination rank, or kEveryRank (every output)
     uint8_t unit_log2;  // access width = 1 << unit_log2 bytes (0..5)
     uint8_t shift;      // 0, or a shifted body: destinations aligned to the unit,
-                        // every source `shift` bytes past a unit boundary
+                        // every source `shift` bytes past a unit boundary; with
+                        // kShiftPerRank set (sums), the sources sit on different
+                        // offsets (the low bits: the first non-zero one), which
+                        // the kernel reads from their addresses
 };
+
+constexpr uint8_t kShiftPerRank = 0x80;
 static_assert(sizeof(Segment) == 32, "Segment is passed by value to kernels");
 
 // Kernel parameter block of the zero-staging Atom kernels (passed as a

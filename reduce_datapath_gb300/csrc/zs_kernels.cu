@@ -14,18 +14,19 @@ namespace {
 using ReduceKernel = void (*)(ZsParams<kSegsSmall>);
 
 // NR = kMaxRanks / units per thread.  The pairwise rank order keeps one unit
-// per thread (NR = kMaxRanks) and has no shifted segments (SH).
-template <typename T, int THREADS, int NR, bool SH>
+// per thread (NR = kMaxRanks) and has no shifted segments (SH: 0 none, 1 one
+// offset, 2 one per rank).
+template <typename T, int THREADS, int NR, int SH>
 ReduceKernel pick_reduce(int order, bool fan_all)
 {
     if (order == 0)
         return fan_all ? zs_reduce_kernel<T, 0, true, THREADS, NR, SH>
                        : zs_reduce_kernel<T, 0, false, THREADS, NR, SH>;
-    return fan_all ? zs_reduce_kernel<T, 1, true, THREADS, kMaxRanks, false>
-                   : zs_reduce_kernel<T, 1, false, THREADS, kMaxRanks, false>;
+    return fan_all ? zs_reduce_kernel<T, 1, true, THREADS, kMaxRanks, 0>
+                   : zs_reduce_kernel<T, 1, false, THREADS, kMaxRanks, 0>;
 }
 
-template <int THREADS, int NR, bool SH>
+template <int THREADS, int NR, int SH>
 ReduceKernel reduce_kernel_t(int dtype, int order, bool fan_all)
 {
     if (dtype == kF32) return pick_reduce<atom::F32, THREADS, NR, SH>(order, fan_all);
@@ -33,7 +34,7 @@ ReduceKernel reduce_kernel_t(int dtype, int order, bool fan_all)
     return pick_reduce<atom::F16, THREADS, NR, SH>(order, fan_all);
 }
 
-template <bool SH>
+template <int SH>
 ReduceKernel reduce_kernel_sh(int dtype, int order, bool fan_all, bool small, int unroll)
 {
     if (small) return reduce_kernel_t<kSmallThreads, kMaxRanks, SH>(dtype, order, fan_all);
@@ -45,10 +46,11 @@ ReduceKernel reduce_kernel_sh(int dtype, int order, bool fan_all, bool small, in
 }
 
 ReduceKernel reduce_kernel_for(int dtype, int order, bool fan_all, bool small, int unroll,
-                               bool shifted)
+                               int shift_mode)
 {
-    return shifted ? reduce_kernel_sh<true>(dtype, order, fan_all, small, unroll)
-                   : reduce_kernel_sh<false>(dtype, order, fan_all, small, unroll);
+    if (shift_mode == 2) return reduce_kernel_sh<2>(dtype, order, fan_all, small, unroll);
+    if (shift_mode == 1) return reduce_kernel_sh<1>(dtype, order, fan_all, small, unroll);
+    return reduce_kernel_sh<0>(dtype, order, fan_all, small, unroll);
 }
 
 template <int MAXSEG, bool SH>
@@ -171,20 +173,20 @@ int reduce_unroll(int R, int order)
 }
 
 void zs_reduce_select(KernelLaunch& k, int dtype, int order, bool fan_all, bool small, int R,
-                      bool shifted)
+                      int shift_mode)
 {
     k.func = reinterpret_cast<const void*>(
-        reduce_kernel_for(dtype, order, fan_all, small, reduce_unroll(R, order), shifted));
+        reduce_kernel_for(dtype, order, fan_all, small, reduce_unroll(R, order), shift_mode));
     k.block = small ? kSmallThreads : kThreads;
     k.smem = 0;
     k.cooperative = false;
     k.params_bytes = sizeof(ZsParams<kSegsSmall>);
 }
 
-int zs_reduce_resident_ctas(int dtype, int order, bool fan_all, bool small, int R, bool shifted)
+int zs_reduce_resident_ctas(int dtype, int order, bool fan_all, bool small, int R, int shift_mode)
 {
     return resident_ctas(reinterpret_cast<const void*>(reduce_kernel_for(
-                             dtype, order, fan_all, small, reduce_unroll(R, order), shifted)),
+                             dtype, order, fan_all, small, reduce_unroll(R, order), shift_mode)),
                          small ? kSmallThreads : kThreads);
 }
 

@@ -90,8 +90,11 @@ __device__ __forceinline__ const char* at(const char* base, uint64_t off, int ba
 
 // One tile of a 16- or 32-byte vector body in a launch that holds a shifted
 // sum: U = kMaxRanks / NR rows of warp runs, 31 units a warp for a shifted
-// body, 32 for an aligned one (no exchange between lanes).
-template <typename T, int ORDER, bool FAN_ALL, int BYTES, int NR, int THREADS>
+// body, 32 for an aligned one (no exchange between lanes).  PER_RANK: the
+// launch holds a body whose ranks' sources sit on different offsets; each
+// rank's offset is then read from its address and its blocks realigned before
+// the fold (a body on one offset folds first and realigns the sum once).
+template <typename T, int ORDER, bool FAN_ALL, int BYTES, int NR, int THREADS, bool PER_RANK>
 __device__ __forceinline__ void reduce_rows(const ZsParams<kSegsSmall>& p, const Segment& s,
                                             uint32_t tile, int R, uint64_t lpol, uint64_t spol)
 {
@@ -100,48 +103,100 @@ __device__ __forceinline__ void reduce_rows(const ZsParams<kSegsSmall>& p, const
     constexpr int WARPS = THREADS / 32;
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
-    const int shift = s.shift;
-    const int per_warp = shift ? 31 : 32;
+    const bool shifted = s.shift != 0;
+    const int per_warp = shifted ? 31 : 32;
     const uint64_t nunits = s.bytes / BYTES;
-    // a shifted body also reads the block after its last unit
-    const uint64_t nblocks = shift ? nunits + 1 : nunits;
-    const uint64_t q0 = (uint64_t)tile * (shift ? shifted_tile_units(THREADS * U) : THREADS * U);
+    const uint64_t q0 =
+        (uint64_t)tile * (shifted ? shifted_tile_units(THREADS * U) : THREADS * U);
     atom::Vec<BYTES> v[U][NR];
+    if constexpr (!PER_RANK) {
+        const int shift = s.shift;
+        // a shifted body also reads the block after its last unit
+        const uint64_t nblocks = shifted ? nunits + 1 : nunits;
 #pragma unroll
-    for (int k = 0; k < U; ++k) {
-        const uint64_t q = q0 + (uint64_t)(k * WARPS + warp) * per_warp + lane;
+        for (int k = 0; k < U; ++k) {
+            const uint64_t q = q0 + (uint64_t)(k * WARPS + warp) * per_warp + lane;
 #pragma unroll
-        for (int r = 0; r < NR; ++r) {
-            if (r < R && q < nblocks) {
-                atom::load(v[k][r], at(p.in[r], s.src_off + q * BYTES, shift), lpol);
-            } else {
+            for (int r = 0; r < NR; ++r) {
+                if (r < R && q < nblocks) {
+                    atom::load(v[k][r], at(p.in[r], s.src_off + q * BYTES, shift), lpol);
+                } else {
 #pragma unroll
-                for (int i = 0; i < W; ++i) v[k][r].w[i] = 0u;
+                    for (int i = 0; i < W; ++i) v[k][r].w[i] = 0u;
+                }
             }
         }
-    }
 #pragma unroll
-    for (int k = 0; k < U; ++k) {
-        const uint64_t q = q0 + (uint64_t)(k * WARPS + warp) * per_warp + lane;
-        atom::Vec<BYTES> y, out;
-        atom::reduce_unit<T, ORDER, BYTES, NR>(v[k], R, y);
-        if (shift) {
-            atom::Vec<BYTES> next;
+        for (int k = 0; k < U; ++k) {
+            const uint64_t q = q0 + (uint64_t)(k * WARPS + warp) * per_warp + lane;
+            atom::Vec<BYTES> y, out;
+            atom::reduce_unit<T, ORDER, BYTES, NR>(v[k], R, y);
+            if (shifted) {
+                atom::Vec<BYTES> next;
 #pragma unroll
-            for (int i = 0; i < W; ++i) next.w[i] = __shfl_down_sync(0xffffffffu, y.w[i], 1);
-            if (lane == 31 || q >= nunits) continue;
-            realign<W>(y.w, next.w, shift, out.w);
-        } else {
-            if (q >= nunits) continue;
-            out = y;
+                for (int i = 0; i < W; ++i) next.w[i] = __shfl_down_sync(0xffffffffu, y.w[i], 1);
+                if (lane == 31 || q >= nunits) continue;
+                realign<W>(y.w, next.w, shift, out.w);
+            } else {
+                if (q >= nunits) continue;
+                out = y;
+            }
+            const uint64_t o = s.dst_off + q * BYTES;
+            if (FAN_ALL) {
+#pragma unroll
+                for (int r = 0; r < NR; ++r)
+                    if (r < R) atom::store(p.out[r] + o, out, spol);
+            } else {
+                atom::store(p.out[s.dst] + o, out, spol);
+            }
         }
-        const uint64_t o = s.dst_off + q * BYTES;
-        if (FAN_ALL) {
+    } else {
+        // Each rank's offset from the destinations' grid (0 on an aligned
+        // body).  A rank off the grid also reads the block after the body's
+        // last unit (it holds the body's last bytes); one on the grid stops at
+        // the last unit.
+        int sh[NR];
 #pragma unroll
-            for (int r = 0; r < NR; ++r)
-                if (r < R) atom::store(p.out[r] + o, out, spol);
-        } else {
-            atom::store(p.out[s.dst] + o, out, spol);
+        for (int r = 0; r < NR; ++r)
+            sh[r] = (shifted && r < R)
+                        ? (int)((reinterpret_cast<uintptr_t>(p.in[r]) + s.src_off) & (BYTES - 1))
+                        : 0;
+#pragma unroll
+        for (int k = 0; k < U; ++k) {
+            const uint64_t q = q0 + (uint64_t)(k * WARPS + warp) * per_warp + lane;
+#pragma unroll
+            for (int r = 0; r < NR; ++r) {
+                if (r < R && q < (sh[r] ? nunits + 1 : nunits)) {
+                    atom::load(v[k][r], at(p.in[r], s.src_off + q * BYTES, sh[r]), lpol);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < W; ++i) v[k][r].w[i] = 0u;
+                }
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < U; ++k) {
+            const uint64_t q = q0 + (uint64_t)(k * WARPS + warp) * per_warp + lane;
+#pragma unroll
+            for (int r = 0; r < NR; ++r) {
+                if (r >= R || sh[r] == 0) continue;
+                atom::Vec<BYTES> next;
+#pragma unroll
+                for (int i = 0; i < W; ++i)
+                    next.w[i] = __shfl_down_sync(0xffffffffu, v[k][r].w[i], 1);
+                realign<W>(v[k][r].w, next.w, sh[r], v[k][r].w);
+            }
+            if ((shifted && lane == 31) || q >= nunits) continue;
+            atom::Vec<BYTES> out;
+            atom::reduce_unit<T, ORDER, BYTES, NR>(v[k], R, out);
+            const uint64_t o = s.dst_off + q * BYTES;
+            if (FAN_ALL) {
+#pragma unroll
+                for (int r = 0; r < NR; ++r)
+                    if (r < R) atom::store(p.out[r] + o, out, spol);
+            } else {
+                atom::store(p.out[s.dst] + o, out, spol);
+            }
         }
     }
 }
@@ -266,9 +321,10 @@ __device__ __forceinline__ void reduce_element(const ZsParams<kSegsSmall>& p, co
 // THREADS threads per CTA: kThreads for large messages, one warp
 // (kSmallThreads) for small ones.  NR bounds the rank count (R <= NR); a tile
 // holds THREADS x (kMaxRanks / NR) units, so sums of 2 or 4 ranks take 4 or 2
-// units per thread.  SHIFTED kernels also serve shifted segments; a launch
-// with none runs the kernel without that path.
-template <typename T, int ORDER, bool FAN_ALL, int THREADS, int NR, bool SHIFTED>
+// units per thread.  SHIFTED kernels (1: sources on one offset; 2: ranks'
+// sources on different offsets) also serve shifted segments; a launch with
+// none runs the kernel without that path.
+template <typename T, int ORDER, bool FAN_ALL, int THREADS, int NR, int SHIFTED>
 __global__ void __launch_bounds__(THREADS, THREADS == kThreads ? 2 : 16)
 zs_reduce_kernel(const __grid_constant__ ZsParams<kSegsSmall> p)
 {
@@ -280,11 +336,12 @@ zs_reduce_kernel(const __grid_constant__ ZsParams<kSegsSmall> p)
     for (uint32_t t = blockIdx.x; t < p.ntiles; t += gridDim.x) {
         const Segment& s = segment_of(p, t);
         const int ul = s.unit_log2;
-        if constexpr (SHIFTED) {
+        if constexpr (SHIFTED != 0) {
             // a launch holding a shifted sum is planned with 16-byte vector
             // bodies only (and element heads and tails)
             if (ul == 4) {
-                reduce_rows<T, ORDER, FAN_ALL, 16, NR, THREADS>(p, s, t - s.tile0, R, lpol, spol);
+                reduce_rows<T, ORDER, FAN_ALL, 16, NR, THREADS, SHIFTED == 2>(p, s, t - s.tile0, R,
+                                                                             lpol, spol);
             } else if (ul < 4) {
                 const uint64_t base = (uint64_t)(t - s.tile0) * tile_bytes(ul, THREADS * U);
 #pragma unroll

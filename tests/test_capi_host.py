@@ -128,14 +128,18 @@ def check_alignment(segs, R, in_addr, out_addr, reduce, esz):
         dsts = [out_addr[r] + s["dst_off"] for r in range(R)] if s["dst_rank"] == -1 \
             else [out_addr[s["dst_rank"]] + s["dst_off"]]
         if s["shift"]:
-            # shifted body: destinations aligned, every source `shift` past a boundary
+            # shifted body: destinations aligned; the first source off their grid
+            # is `shift` past a boundary (a copy's one source; a sum's sources
+            # each on their own offset, element-aligned)
             assert u in (16, 32) and 0 < s["shift"] < u, s
             for a in dsts:
                 assert a % u == 0, (s, a)
-            for a in srcs:
-                assert a % u == s["shift"], (s, a)
+            first = next(a % u for a in srcs if a % u)
+            assert first == s["shift"], s
             if reduce:
-                assert s["shift"] % esz == 0, s
+                assert all(a % esz == 0 for a in srcs), s
+            else:
+                assert len(srcs) == 1
             continue
         for a in srcs + dsts:
             assert a % u == 0, (s, a)
@@ -230,8 +234,14 @@ def test_aligned_bodies_use_wide_units(lib):
     segs, _ = rd.purlin_plan_segments(rd.COLL_ALL_REDUCE, R, in_addr, out_addr, count=n,
                                       dtype="bf16", max_unit=16)
     assert segs[0]["unit"] == 16
-    # one stream off by one element: sums fall back to element units
+    # one source off by one element: a 16-byte body shifted for that rank
     in_addr[3] += 2
+    segs, _ = rd.purlin_plan_segments(rd.COLL_ALL_REDUCE, R, in_addr, out_addr, count=n,
+                                      dtype="bf16")
+    assert [(s["unit"], s["shift"]) for s in segs] == [(16, 2)]
+    check_alignment(segs, R, in_addr, out_addr, True, 2)
+    # outputs on different alignments: no body fits all of them, element units
+    out_addr[5] += 2
     segs, _ = rd.purlin_plan_segments(rd.COLL_ALL_REDUCE, R, in_addr, out_addr, count=n,
                                       dtype="bf16")
     assert [s["unit"] for s in segs] == [2]

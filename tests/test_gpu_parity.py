@@ -668,3 +668,49 @@ def test_all_to_all_v_shifted_blocks(policy, R):
     for j in range(R):
         assert same_bits(host_bits(outs[j].view), want[j]), j
         assert outs[j].guards_intact()
+
+
+@pytest.mark.parametrize("policy", ["zs", "zs_large", "zs_small"])
+@pytest.mark.parametrize("dtype", ["bf16", "f32", "f16"])
+@pytest.mark.parametrize("R", [2, 3, 5, 8])
+@pytest.mark.parametrize("coll", ["reduce_scatter", "all_reduce"])
+def test_sums_with_sources_on_different_grids(policy, dtype, R, coll):
+    """Each rank's input `r % 4` elements into its allocation: the ranks' shifts
+    differ, so each rank's blocks are realigned on their own before the fold."""
+    h = handle(R)
+    set_variant(h, *POLICIES[policy])
+    c = 6 * 1024 + 5
+    n = R * c
+    x = [inputs(1, n, dtype, seed=400 + 7 * R + r, offset=r % 4)[0] for r in range(R)]
+    if coll == "reduce_scatter":
+        outs = [Guarded(c, dtype) for _ in range(R)]
+        rd.purlin_reduce_scatter(h, x, [o.view for o in outs], [c] * R, None, dtype)
+        want = oracle.reduce_scatter(oracle_in(x), [c] * R, dtype=dtype)
+    else:
+        outs = [Guarded(n, dtype, offset=1) for _ in range(R)]
+        rd.purlin_all_reduce(h, x, [o.view for o in outs], n, dtype)
+        want = oracle.all_reduce(oracle_in(x), dtype=dtype)
+    run_ok(h)
+    for j in range(R):
+        assert same_bits(host_bits(outs[j].view), want[j]), j
+        assert outs[j].guards_intact()
+
+
+@pytest.mark.parametrize("policy", ["zs", "zs_large", "zs_small"])
+@pytest.mark.parametrize("R", [2, 3, 8])
+@pytest.mark.parametrize("dtype", ["bf16", "u8"])
+def test_all_gather_outputs_on_different_grids(policy, R, dtype):
+    """Outputs `j % 5` elements into their allocations: the gather runs by
+    destination, each block realigned to its own output."""
+    h = handle(R)
+    set_variant(h, *POLICIES[policy])
+    counts = [12000 + 7 * k for k in range(R)]
+    x = [inputs(1, c, dtype, seed=60 + k)[0] for k, c in enumerate(counts)]
+    total = sum(counts)
+    outs = [Guarded(total, dtype, offset=j % 5) for j in range(R)]
+    rd.purlin_all_gather(h, x, [o.view for o in outs], counts, None, dtype)
+    run_ok(h)
+    want = oracle.all_gather(oracle_in(x))
+    for j in range(R):
+        assert same_bits(host_bits(outs[j].view), want[j]), j
+        assert outs[j].guards_intact()
