@@ -177,8 +177,19 @@ def _ptrs(bufs):
 def _sizes(vals):
     if vals is None:
         return None
+    if hasattr(vals, "__array_interface__"):
+        # a numpy array: a ctypes view of a contiguous size_t copy (the view
+        # keeps that array alive for the call)
+        import numpy as np
+        arr = np.ascontiguousarray(np.asarray(vals).reshape(-1), dtype=_SIZE_T_NP)
+        if not arr.flags.writeable:
+            arr = arr.copy()
+        return (ctypes.c_size_t * arr.size).from_buffer(arr)
     flat = [int(v) for v in (vals.reshape(-1).tolist() if hasattr(vals, "reshape") else vals)]
     return (ctypes.c_size_t * len(flat))(*flat)
+
+
+_SIZE_T_NP = "u%d" % ctypes.sizeof(ctypes.c_size_t)
 
 
 def _dtype(dt) -> int:

@@ -15,6 +15,8 @@
 // in the kernel's constant parameter bank.
 #pragma once
 
+#include <type_traits>
+
 #include "atom.cuh"
 #include "internal.h"
 #include "purlin.h"
@@ -81,6 +83,48 @@ __device__ __forceinline__ void realign(const uint32_t (&lo)[W], const uint32_t 
     const uint32_t bits = (uint32_t)(shift & 3) * 8;
 #pragma unroll
     for (int j = 0; j < W; ++j) out[j] = __funnelshift_r(c[j], c[j + 1], bits);
+}
+
+// Calls f(std::integral_constant<int, a>) for a runtime word offset a in
+// [0, W): a segment's shift is uniform, so the realignment below is compiled
+// once per word offset and a tile branches once.
+template <int W, typename F>
+__device__ __forceinline__ void with_word_offset(int a, F&& f)
+{
+    switch (a) {
+    case 0: f(std::integral_constant<int, 0>{}); break;
+    case 1: f(std::integral_constant<int, 1>{}); break;
+    case 2: f(std::integral_constant<int, 2>{}); break;
+    case 3: f(std::integral_constant<int, 3>{}); break;
+    default:
+        if constexpr (W > 4) {
+            switch (a) {
+            case 4: f(std::integral_constant<int, 4>{}); break;
+            case 5: f(std::integral_constant<int, 5>{}); break;
+            case 6: f(std::integral_constant<int, 6>{}); break;
+            default: f(std::integral_constant<int, 7>{}); break;
+            }
+        }
+        break;
+    }
+}
+
+// realign() for a word offset A known at compile time: the neighbour lane's
+// words 0..A by shuffle (every lane calls this), then one funnel shift per
+// output word.  Returns in out the unit (lo ++ next)[4A + bytes, ...).
+template <int W, int A>
+__device__ __forceinline__ void realign_from_next(const uint32_t (&lo)[W], uint32_t bits,
+                                                  uint32_t (&out)[W])
+{
+    uint32_t next[A + 1];
+#pragma unroll
+    for (int i = 0; i <= A; ++i) next[i] = __shfl_down_sync(0xffffffffu, lo[i], 1);
+#pragma unroll
+    for (int j = 0; j < W; ++j) {
+        const uint32_t a = (A + j < W) ? lo[A + j] : next[A + j - W];
+        const uint32_t b = (A + j + 1 < W) ? lo[A + j + 1] : next[A + j + 1 - W];
+        out[j] = __funnelshift_r(a, b, bits);
+    }
 }
 
 __device__ __forceinline__ const char* at(const char* base, uint64_t off, int back)
@@ -224,21 +268,22 @@ __device__ __forceinline__ void copy_shifted(const ZsParams<MAXSEG>& p, const Se
             for (int i = 0; i < W; ++i) v[k].w[i] = 0u;
         }
     }
+    const uint32_t bits = (uint32_t)(shift & 3) * 8;
+    with_word_offset<W>(shift >> 2, [&](auto A) {
 #pragma unroll
-    for (int k = 0; k < UNROLL; ++k) {
-        const uint64_t q = q0 + (uint64_t)(k * WARPS + warp) * 31 + lane;
-        atom::Vec<BYTES> next, out;
-#pragma unroll
-        for (int i = 0; i < W; ++i) next.w[i] = __shfl_down_sync(0xffffffffu, v[k].w[i], 1);
-        if (lane == 31 || q >= nunits) continue;
-        realign<W>(v[k].w, next.w, shift, out.w);
-        const uint64_t o = s.dst_off + q * BYTES;
-        if (FAN_ALL) {
-            for (int r = 0; r < (int)p.R; ++r) atom::store(p.out[r] + o, out, spol);
-        } else {
-            atom::store(p.out[s.dst] + o, out, spol);
+        for (int k = 0; k < UNROLL; ++k) {
+            const uint64_t q = q0 + (uint64_t)(k * WARPS + warp) * 31 + lane;
+            atom::Vec<BYTES> out;
+            realign_from_next<W, decltype(A)::value>(v[k].w, bits, out.w);
+            if (lane == 31 || q >= nunits) continue;
+            const uint64_t o = s.dst_off + q * BYTES;
+            if (FAN_ALL) {
+                for (int r = 0; r < (int)p.R; ++r) atom::store(p.out[r] + o, out, spol);
+            } else {
+                atom::store(p.out[s.dst] + o, out, spol);
+            }
         }
-    }
+    });
 }
 
 // ------------------------------------------------------------------ reduce
