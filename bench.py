@@ -374,13 +374,45 @@ KERNEL_SOURCES = {
 }
 
 
-def sources_digest(family):
+def code_tokens(text):
+    """C/C++ source with comments removed and whitespace runs collapsed (string
+    and character literals kept as written): what the compiler sees."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        elif c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
+def sources_digest(family, read=None):
+    """Digest of a kernel family's sources as compiled (comments and layout do
+    not count), which ties an ncu summary's traffic to the code it measured."""
     import hashlib
     src = os.path.join(ROOT, "reduce_datapath_gb300", "csrc")
     h = hashlib.sha256()
     for f in KERNEL_SOURCES[family]:
-        with open(os.path.join(src, f), "rb") as fh:
-            h.update(fh.read())
+        if read is None:
+            with open(os.path.join(src, f), encoding="utf-8") as fh:
+                text = fh.read()
+        else:
+            text = read(f)
+        h.update(code_tokens(text).encode())
+        h.update(b"\0")
     return h.hexdigest()[:16]
 
 

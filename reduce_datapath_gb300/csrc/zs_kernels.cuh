@@ -50,15 +50,17 @@ __device__ __forceinline__ void pdl_enter()
 
 // ------------------------------------------------------------ shifted bodies
 // A shifted segment (Segment::shift != 0) has its destinations aligned to its
-// unit of BYTES while every source starts `shift` bytes past a unit boundary
-// (a V-collective whose partition offsets are not multiples of the vector).
-// Lane l of a warp loads the aligned source block q + l -- for a sum, the R
-// ranks' blocks folded first: `shift` is a multiple of the element size, so the
-// realignment moves whole elements -- and destination unit q + l is that
-// block's last BYTES - shift bytes followed by the first `shift` bytes of the
-// next block, which lane l + 1 holds.  Each warp's 32 lanes thus write 31
-// units (lane 31 only lends its block); every block loaded holds a byte of the
-// segment, so no load leaves the pages the segment lies in.
+// unit of BYTES while its sources start `shift` bytes past a unit boundary (a
+// V-collective whose partition offsets are not multiples of the vector).
+// Lane l of a warp loads the aligned source block q + l -- for a sum on one
+// offset, the R ranks' blocks folded first: `shift` is a multiple of the
+// element size, so the realignment moves whole elements -- and destination unit
+// q + l is that block's last BYTES - shift bytes followed by the first `shift`
+// bytes of the next block, which lane l + 1 holds.  (A sum whose ranks sit on
+// different offsets, kShiftPerRank, realigns each rank's block the same way
+// before the fold.)  Each warp's 32 lanes thus write 31 units (lane 31 only
+// lends its block); every block loaded holds a byte of the segment, so no load
+// leaves the pages the segment lies in.
 
 // out = (lo ++ hi)[shift, shift + 4W) as bytes, 0 < shift < 4W, with no
 // dynamically indexed registers: a log-depth word rotation, then a funnel

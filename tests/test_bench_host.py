@@ -91,3 +91,21 @@ def test_threaded_oracle_baseline_is_bit_identical(monkeypatch, cores):
     assert c2["cores"] == min(cores, bench.R) and c2["kind"].startswith("oracle")
     assert all(np.array_equal(a, b) for a, b in zip(y1, y2))
     assert all(np.array_equal(a, b) for a, b in zip(z1, z2))
+
+
+def test_sources_digest_ignores_comments_not_code():
+    """The digest that ties an ncu summary's traffic to the kernel sources
+    changes with the code but not with comments or layout."""
+    import bench
+    base = 'int f(int x) { return x + 1; } // one\n/* two */ const char* s = "a // b";\n'
+    same = '/* header */\nint f(int x)\n{\n    return x + 1;   // the increment\n}\nconst char* s = "a // b";'
+    other = 'int f(int x) { return x + 2; } const char* s = "a // b";'
+    strs = 'int f(int x) { return x + 1; } const char* s = "a // c";'
+    assert bench.code_tokens(base) == bench.code_tokens(same)
+    assert bench.code_tokens(base) != bench.code_tokens(other)
+    assert bench.code_tokens(base) != bench.code_tokens(strs)
+    files = {f: base for f in bench.KERNEL_SOURCES["zs"]}
+    d1 = bench.sources_digest("zs", read=files.get)
+    d2 = bench.sources_digest("zs", read={f: same for f in files}.get)
+    d3 = bench.sources_digest("zs", read={f: other for f in files}.get)
+    assert d1 == d2 != d3
