@@ -195,6 +195,9 @@ PURLIN_API purlin_status_t purlin_all_gather(purlin_handle_t h, const void* cons
  *   dtype        PURLIN_F32, PURLIN_BF16 or PURLIN_F16.
  *   op           PURLIN_OP_SUM.
  *   In-place: out[r] == in[r] for every r is allowed.
+ * Zero staging runs one kernel that writes each sum to all R outputs; when the
+ * outputs sit on different 16-byte alignments it runs two, in stream order: the
+ * sum into out[0], then copies of out[0] to the other outputs.
  */
 PURLIN_API purlin_status_t purlin_all_reduce(purlin_handle_t h, const void* const in[],
                                   void* const out[], size_t count, purlin_dtype_t dtype,

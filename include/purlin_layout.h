@@ -66,6 +66,10 @@ typedef struct {
  *              with fewer than the small-message threshold of them
  *              (purlin_set_small_tiles) runs one-warp tiles of 32 units over the
  *              same segments.
+ * An AllGather whose outputs sit on different 16-byte alignments is planned by
+ * destination (one piece per destination and source), as its launch is.  An
+ * AllReduce whose outputs do is launched as a sum into output 0 followed by
+ * copies to the others; the plan shown here is then the single fan-out plan.
  * Returns PURLIN_OK, PURLIN_ERR_INVALID_ARG (bad R, dtype, NULL array, element
  * misalignment for a sum, byte overflow) or PURLIN_ERR_UNSUPPORTED (more
  * segments than max_segs).  Never calls CUDA. */

@@ -78,8 +78,9 @@ struct CopyOp {
 struct purlin_plan {
     purlin_handle_t h = nullptr;
     int device = 0;
-    int kind = 0;  // 0 nothing, 1 kernel, 2 copies
+    int kind = 0;  // 0 nothing, 1 kernel, 2 copies, 3 kernel k then kernel k2
     purlin::KernelLaunch k;
+    purlin::KernelLaunch k2;
     std::vector<CopyOp> copies;
     purlin_launch_info_t info{};
 };
@@ -407,10 +408,12 @@ purlin_status_t run(purlin_handle_t h, Coll coll, const void* const in_[], void*
     // The call's launch is built in thread-local storage (no copy of the
     // parameter block on the way to the launch), then made at once or, while
     // a plan is being recorded, kept.
-    static thread_local KernelLaunch tl_k;
+    static thread_local KernelLaunch tl_k, tl_k2;
     static thread_local std::vector<CopyOp> tl_copies;
     KernelLaunch& k = tl_k;
+    KernelLaunch& k2 = tl_k2;
     k.grid = 0;
+    k2.grid = 0;
     tl_copies.clear();
     int kind = 0;
 
@@ -510,6 +513,52 @@ purlin_status_t run(purlin_handle_t h, Coll coll, const void* const in_[], void*
             info.grid = grid;
             info.kernels = grid > 0;
             info.chunk_bytes = tile_bytes(knobs.max_unit_log2, knobs.tile_units);
+        } else if (coll == Coll::AllReduce && np == 1 && R > 1 && h->order == 0 &&
+                   !outputs_share_grid(out, R)) {
+            // Outputs on different 16-byte alignments: no fan-out body fits
+            // them all.  Sum into out[0] (one destination: a shifted body where
+            // the sources are off its grid), then copy out[0] to the other
+            // outputs (single-destination shifted copies).  (2R + 1) / 2R of
+            // the fused traffic instead of element accesses.
+            ZsParams<kSegsSmall>& p = *reinterpret_cast<ZsParams<kSegsSmall>*>(k.params);
+            Piece sum = pieces[0];
+            sum.dst = 0;
+            ZsKnobs ks = knobs;
+            if (h->l2_store < 0 && h->l2_coll_store[(int)coll] < 0) ks.l2_store = kL2Normal;
+            st = make_params(p, &sum, 1, R, in, out, esz, true, ks, h->status);
+            if (st != PURLIN_OK) return st;
+            const bool small = replan_small(h, coll, p, &sum, 1, R, in, out, esz, true, ks);
+            const int sh = has_shift(p);
+            const int grid = zs_grid(h, p.ntiles,
+                                     zs_reduce_resident_ctas(dtype, 0, false, small, R, sh));
+            zs_reduce_select(k, dtype, 0, false, small, R, sh);
+            k.grid = (unsigned)grid;
+            k.pdl = p.pdl != 0;
+
+            ZsParams<kSegsSmall>& p2 = *reinterpret_cast<ZsParams<kSegsSmall>*>(k2.params);
+            uint64_t from[kMaxRanks];
+            Piece copies[kMaxRanks];
+            int nc = 0;
+            for (int r = 0; r < R; ++r) from[r] = out[0];
+            for (int j = 1; j < R; ++j) {
+                if (out[j] == out[0]) continue;
+                copies[nc++] = Piece{sum.dst_off, sum.dst_off, sum.bytes, 0, (uint8_t)j};
+            }
+            ZsKnobs kc = zs_knobs(h, Coll::AllToAllV);
+            st = make_params(p2, copies, nc, R, from, out, esz, false, kc, h->status);
+            if (st != PURLIN_OK) return st;
+            const bool small2 = replan_small(h, Coll::AllToAllV, p2, copies, nc, R, from, out, esz,
+                                             false, kc);
+            const bool sh2 = has_shift(p2) != 0;
+            const int grid2 = zs_grid(h, p2.ntiles, zs_copy_resident_ctas(false, false, small2, sh2));
+            zs_copy_select(k2, false, false, small2, sh2);
+            k2.grid = (unsigned)grid2;
+            k2.pdl = p2.pdl != 0;
+            kind = grid > 0 ? (grid2 > 0 ? 3 : 1) : 0;
+            info.grid = grid;
+            info.kernels = (grid > 0) + (grid2 > 0);
+            if (small) info.block = kSmallThreads;
+            info.chunk_bytes = tile_bytes(ks.max_unit_log2, ks.tile_units);
         } else {
             ZsParams<kSegsSmall>& p = *reinterpret_cast<ZsParams<kSegsSmall>*>(k.params);
             st = make_params(p, pieces, np, R, in, out, esz, reduce, knobs, h->status);
@@ -550,24 +599,27 @@ purlin_status_t run(purlin_handle_t h, Coll coll, const void* const in_[], void*
         plan->h = h;
         plan->device = h->device;
         plan->kind = kind;
-        if (kind == 1) {
-            plan->k.func = k.func;
-            plan->k.grid = k.grid;
-            plan->k.block = k.block;
-            plan->k.smem = k.smem;
-            plan->k.pdl = k.pdl;
-            plan->k.cooperative = k.cooperative;
-            plan->k.params_bytes = k.params_bytes;
-            std::memcpy(plan->k.params, k.params, k.params_bytes);
-        }
+        auto keep = [](KernelLaunch& to, const KernelLaunch& from) {
+            to.func = from.func;
+            to.grid = from.grid;
+            to.block = from.block;
+            to.smem = from.smem;
+            to.pdl = from.pdl;
+            to.cooperative = from.cooperative;
+            to.params_bytes = from.params_bytes;
+            std::memcpy(to.params, from.params, from.params_bytes);
+        };
+        if (kind == 1 || kind == 3) keep(plan->k, k);
+        if (kind == 3) keep(plan->k2, k2);
         plan->copies = tl_copies;
         plan->info = info;
         h->recorded = plan;
         return PURLIN_OK;
     }
     cudaError_t ce = cudaSuccess;
-    if (kind == 1) {
+    if (kind == 1 || kind == 3) {
         ce = launch_kernel(k, s);
+        if (ce == cudaSuccess && kind == 3) ce = launch_kernel(k2, s);
     } else if (kind == 2) {
         for (const CopyOp& c : tl_copies) {
             ce = cudaMemcpyAsync(c.dst, c.src, c.bytes, cudaMemcpyDefault, s);
@@ -795,8 +847,9 @@ purlin_status_t purlin_plan_launch(purlin_plan_t plan, purlin_stream_t stream)
     if (!guard.ok) return PURLIN_ERR_CUDA;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t ce = cudaSuccess;
-    if (plan->kind == 1) {
+    if (plan->kind == 1 || plan->kind == 3) {
         ce = launch_kernel(plan->k, s);
+        if (ce == cudaSuccess && plan->kind == 3) ce = launch_kernel(plan->k2, s);
     } else if (plan->kind == 2) {
         for (const CopyOp& c : plan->copies) {
             ce = cudaMemcpyAsync(c.dst, c.src, c.bytes, cudaMemcpyDefault, s);

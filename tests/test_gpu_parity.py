@@ -714,3 +714,37 @@ def test_all_gather_outputs_on_different_grids(policy, R, dtype):
     for j in range(R):
         assert same_bits(host_bits(outs[j].view), want[j]), j
         assert outs[j].guards_intact()
+
+
+@pytest.mark.parametrize("policy", ["zs", "zs_large", "zs_small"])
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("R", [2, 3, 8])
+def test_all_reduce_outputs_on_different_grids(policy, dtype, R):
+    """Outputs `j % 3` elements into their allocations (and inputs `r % 2`):
+    the sum goes to output 0, then copies to the others -- two launches."""
+    n = 30000 + 7
+    h = handle(R)
+    set_variant(h, *POLICIES[policy])
+    x = [inputs(1, n, dtype, seed=800 + 3 * R + r, offset=r % 2)[0] for r in range(R)]
+    outs = [Guarded(n, dtype, offset=j % 3) for j in range(R)]
+    rd.purlin_all_reduce(h, x, [o.view for o in outs], n, dtype)
+    run_ok(h)
+    assert rd.purlin_last_launch(h)["kernels"] == 2
+    want = oracle.all_reduce(oracle_in(x), dtype=dtype)
+    for j in range(R):
+        assert same_bits(host_bits(outs[j].view), want[j]), j
+        assert outs[j].guards_intact()
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_all_reduce_in_place_on_different_grids(dtype):
+    """In place (out[r] is in[r]) with the ranks' buffers on different offsets."""
+    R, n = 8, 20000 + 3
+    h = handle(R)
+    set_variant(h, *POLICIES["zs"])
+    x = [inputs(1, n, dtype, seed=900 + r, offset=r % 3)[0] for r in range(R)]
+    want = oracle.all_reduce(oracle_in(x), dtype=dtype)
+    rd.purlin_all_reduce(h, x, x, n, dtype)
+    run_ok(h)
+    for j in range(R):
+        assert same_bits(host_bits(x[j]), want[j]), j

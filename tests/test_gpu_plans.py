@@ -194,3 +194,41 @@ def test_plan_launches_in_a_cuda_graph(variant):
         rs.destroy()
         ag.destroy()
         set_variant(h, rd.VARIANT_AUTO)
+
+
+def test_two_launch_plan_all_reduce_in_a_cuda_graph():
+    """An AllReduce into outputs on different alignments plans two kernels (a
+    sum into output 0, then copies): a kept plan launches both, each launch and
+    each replay of a captured graph gives the oracle's bits."""
+    R, n, dtype = 8, 50000 + 5, "bf16"
+    h = handle(R)
+    set_variant(h, rd.VARIANT_ZS)
+    x = [inputs(1, n, dtype, seed=70 + r, offset=r % 2)[0] for r in range(R)]
+    full = [torch.zeros(n + 8, dtype=torch.bfloat16, device="cuda") for _ in range(R)]
+    out = [t[j % 3:j % 3 + n] for j, t in enumerate(full)]
+    stream = torch.cuda.Stream()
+    p = rd.plan(rd.purlin_all_reduce, h, x, out, n, dtype, stream=stream)
+    try:
+        for rep in range(2):
+            _refill(x, dtype, seed=700 + rep)
+            torch.cuda.synchronize()
+            p()
+            _ok(h)
+            assert rd.purlin_last_launch(h)["kernels"] == 2
+            want = oracle.all_reduce([host_bits(t) for t in x], dtype=dtype)
+            for j in range(R):
+                assert same_bits(host_bits(out[j]), want[j]), (rep, j)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            p()
+        for rep in range(2):
+            _refill(x, dtype, seed=710 + rep)
+            torch.cuda.synchronize()
+            g.replay()
+            _ok(h)
+            want = oracle.all_reduce([host_bits(t) for t in x], dtype=dtype)
+            for j in range(R):
+                assert same_bits(host_bits(out[j]), want[j]), (rep, j)
+        del g
+    finally:
+        p.destroy()
