@@ -567,6 +567,7 @@ def bench_purlin(args):
         configs = other_configs(rd, torch, dev, stream, peak)
         configs["zs_by_rank_count"] = rank_scaling(rd, torch, dev, stream, peak)
         configs["off_grid_partitions"] = off_grid_partitions(rd, torch, dev, stream, peak)
+        configs["layout_fuzz"] = layout_fuzz(rd, torch, dev, stream, peak)
 
         # ---- AllReduce size sweep: zero staging vs SNAC (default policy)
         sweep = allreduce_sweep(rd, torch, dev, stream, peak)
@@ -869,6 +870,80 @@ def off_grid_partitions(rd, torch, dev, stream, peak):
             rd.purlin_destroy(h)
             torch.cuda.empty_cache()
     return out
+
+
+def layout_fuzz(rd, torch, dev, stream, peak, trials=16, seed=7):
+    """Bandwidth over random layouts (seeded): R in 2..8, a random collective
+    (ReduceScatterV, AllGatherV, AllReduce, AllToAllV), bf16 / fp32 (and bytes
+    for copies), 16-64 MiB per rank, random counts, each rank's input and output
+    buffer 0-2 elements into its allocation with probability 0.3.  Reports
+    every trial and the minimum and median fraction of the peak."""
+    import numpy as np
+    rng = np.random.default_rng(seed)
+    tdt = {"bf16": torch.bfloat16, "f32": torch.float32, "u8": torch.uint8}
+    esz = {"bf16": 2, "f32": 4, "u8": 1}
+    out, handles = [], {}
+    try:
+        for trial in range(trials):
+            R_ = int(rng.integers(2, R + 1))
+            coll = ("rs", "ag", "ar", "a2av")[int(rng.integers(0, 4))]
+            dts = ("bf16", "f32") if coll in ("rs", "ar") else ("bf16", "f32", "u8")
+            dtype = dts[int(rng.integers(0, len(dts)))]
+            e = esz[dtype]
+            n = (int(rng.integers(16, 65)) << 20) // e
+            in_off = [int(rng.integers(0, 3)) * int(rng.random() < 0.3) for _ in range(R_)]
+            out_off = [int(rng.integers(0, 3)) * int(rng.random() < 0.3) for _ in range(R_)]
+            h = handles.setdefault(R_, rd.purlin_create(R_, 0, dev.index))
+
+            def buf(m, off, fill=False):
+                t = torch.empty(m + off + 16, dtype=tdt[dtype], device=dev)
+                if fill:
+                    t.copy_(torch.randn(t.numel(), device=dev).to(tdt[dtype]))
+                return t[off:off + m]
+
+            if coll in ("rs", "ag"):
+                counts = rng.integers(1, 2 * n // R_, size=R_)
+                counts = (counts * (n / counts.sum())).astype(np.int64) + 1
+                total = int(counts.sum())
+                if coll == "rs":
+                    x = [buf(total, in_off[r], True) for r in range(R_)]
+                    y = [buf(int(c), out_off[k]) for k, c in enumerate(counts)]
+                    fn = lambda: rd.purlin_reduce_scatter(h, x, y, counts, None, dtype, stream=stream)
+                else:
+                    x = [buf(int(c), in_off[k]) for k, c in enumerate(counts)]
+                    y = [buf(total, out_off[j]) for j in range(R_)]
+                    fn = lambda: rd.purlin_all_gather(h, x, y, counts, None, dtype, stream=stream)
+                nbytes = (R_ + 1) * total * e
+            elif coll == "ar":
+                x = [buf(n, in_off[r], True) for r in range(R_)]
+                y = [buf(n, out_off[r]) for r in range(R_)]
+                fn = lambda: rd.purlin_all_reduce(h, x, y, n, dtype, stream=stream)
+                nbytes = 2 * R_ * n * e
+            else:
+                C = rng.integers(1, 2 * n // (R_ * R_), size=(R_, R_))
+                x = [buf(int(C[a].sum()), in_off[a]) for a in range(R_)]
+                y = [buf(int(C[:, j].sum()), out_off[j]) for j in range(R_)]
+                fn = lambda: rd.purlin_all_to_all_v(h, x, y, C, None, None, dtype, stream=stream)
+                nbytes = 2 * int(C.sum()) * e
+            with torch.cuda.stream(stream):
+                for _ in range(2):
+                    fn()
+            torch.cuda.synchronize()
+            us = _events_us(torch, stream, fn, 10)
+            if rd.purlin_query_status(h) != rd.OK:
+                raise RuntimeError("layout fuzz: device status not ok")
+            gbs = nbytes / (us / 1e6) / 1e9
+            out.append({"R": R_, "collective": coll, "dtype": dtype, "mbytes_moved": round(nbytes / 1e6, 1),
+                        "in_off": in_off, "out_off": out_off, "us": round(us, 1),
+                        "frac_of_peak": round(gbs / peak, 3)})
+            del x, y
+            torch.cuda.empty_cache()
+    finally:
+        for h in handles.values():
+            rd.purlin_destroy(h)
+    fr = sorted(r["frac_of_peak"] for r in out)
+    return {"trials": out, "min_frac": fr[0], "median_frac": fr[len(fr) // 2],
+            "timing": "events over 10 launches from Python (small calls include host time)"}
 
 
 def other_configs(rd, torch, dev, stream, peak):
