@@ -119,7 +119,10 @@ typedef enum {
  * destinations.  PULL: work is split by destination; each destination pulls
  * every source's block (R reads of each source, from L2 after the first). */
 typedef enum {
-    PURLIN_DIRECTION_AUTO = 0,  /* library's choice (measured best: PUSH)        */
+    PURLIN_DIRECTION_AUTO = 0,  /* library's choice: PUSH (measured best), PULL
+                                   when the outputs sit on different 16-byte
+                                   alignments (then one push body cannot be
+                                   aligned to all of them)                     */
     PURLIN_DIRECTION_PUSH = 1,
     PURLIN_DIRECTION_PULL = 2
 } purlin_direction_t;
