@@ -364,6 +364,269 @@ bool wants_staged(const purlin_handle* h)
     return h->variant == PURLIN_VARIANT_STAGED || h->variant == PURLIN_VARIANT_STAGED_Y;
 }
 
+// One collective call as planned: its arguments after validation.
+struct Call {
+    purlin_handle_t h;
+    Coll coll;
+    int R;
+    int dtype;
+    size_t esz;
+    bool reduce;
+    const uint64_t* in;
+    const uint64_t* out;
+    const Piece* pieces;
+    int np;
+};
+
+// What a call launches: nothing (kind 0), kernel k (1), copy-engine copies
+// (2), or kernel k then kernel k2 (3), with the launch record.
+struct Launches {
+    KernelLaunch& k;
+    KernelLaunch& k2;
+    std::vector<CopyOp>& copies;
+    purlin_launch_info_t& info;
+    int kind = 0;
+};
+
+// SNAC: one cooperative launch of producer / consumer (/ gatherer) CTAs.
+purlin_status_t plan_staged(const Call& c, Launches& L)
+{
+    purlin_handle_t h = c.h;
+    SnacRequest rq{};
+    rq.coll = c.coll;
+    rq.R = c.R;
+    rq.dtype = c.dtype;
+    rq.order = h->order;
+    rq.esz = c.esz;
+    rq.pieces = c.pieces;
+    rq.npieces = c.np;
+    rq.stage_y = h->variant == PURLIN_VARIANT_STAGED_Y;
+    for (int r = 0; r < c.R; ++r) { rq.in[r] = c.in[r]; rq.out[r] = c.out[r]; }
+    SnacConfig cfg{};
+    cfg.staging = h->staging;
+    cfg.staging_bytes = h->staging_bytes;
+    cfg.flags = h->flags;
+    cfg.flag_words = h->flag_words;
+    cfg.status = h->status;
+    cfg.chunk_bytes = h->chunk_bytes;
+    cfg.depth = h->depth;
+    cfg.channels = h->ctas;
+    cfg.sms = h->sms;
+    cfg.timeout_ns = h->timeout_ns;
+    cfg.inject_skip_notify = h->inject;
+    SnacLaunch sl{};
+    purlin_status_t st = snac_plan(rq, cfg, L.k, &sl);
+    if (st != PURLIN_OK) return st;
+    h->inject = 0;
+    L.kind = L.k.grid > 0 ? 1 : 0;
+    L.info.variant = h->variant;
+    L.info.kernels = sl.kernels;
+    L.info.grid = sl.grid;
+    L.info.block = sl.block;
+    L.info.depth = sl.depth;
+    L.info.chunk_bytes = sl.chunk_bytes;
+    return PURLIN_OK;
+}
+
+// No kernel: every block goes to every destination through the copy engines,
+// one asynchronous copy each, in stream order.
+void plan_copy_engine(const Call& c, Launches& L)
+{
+    for (int i = 0; i < c.np; ++i) {
+        const Piece& pc = c.pieces[i];
+        const char* src = reinterpret_cast<const char*>(c.in[pc.src]) + pc.src_off;
+        for (int j = 0; j < c.R; ++j) {
+            if (pc.dst != kEveryRank && pc.dst != j) continue;
+            char* dst = reinterpret_cast<char*>(c.out[j]) + pc.dst_off;
+            if (dst == src) continue;  // in-place AllGather block
+            L.copies.push_back(CopyOp{dst, src, (size_t)pc.bytes});
+        }
+    }
+    L.kind = L.copies.empty() ? 0 : 2;
+    L.info.kernels = 0;
+    L.info.grid = 0;
+    L.info.block = 0;
+    L.info.chunk_bytes = 0;
+}
+
+// Copies with one destination per piece: AllToAll(V), and AllGather by
+// destination (pull, or outputs on different 16-byte alignments, which no one
+// fan-out body can be aligned to; single-destination pieces can each take a
+// shifted body where their source is off their output's grid).
+purlin_status_t plan_by_destination(const Call& c, ZsKnobs knobs, bool bulk, Launches& L)
+{
+    purlin_handle_t h = c.h;
+    ZsParams<kSegsLarge>& p = *reinterpret_cast<ZsParams<kSegsLarge>*>(L.k.params);
+    const Piece* plan = c.pieces;
+    int nplan = c.np;
+    Piece pulled[kMaxRanks * kMaxRanks];
+    if (c.coll == Coll::AllGather) {
+        // one piece per (destination, source), destination by destination;
+        // every source is read R times (from L2 after the first read, hence
+        // normal priority for the loads)
+        nplan = pull_pieces(c.pieces, c.np, c.R, c.in, c.out, pulled);
+        plan = pulled;
+        if (h->l2_load < 0 && h->l2_coll_load[(int)c.coll] < 0) knobs.l2_load = kL2Normal;
+    }
+    purlin_status_t st = make_params(p, plan, nplan, c.R, c.in, c.out, c.esz, false, knobs, h->status);
+    if (st != PURLIN_OK) return st;
+    int grid;
+    if (bulk) {
+        grid = zs_grid(h, p.ntiles, zs_copy_bulk_resident_ctas(true, false), kGridWavesBulk);
+        if (zs_copy_bulk_select(L.k, true, false) != cudaSuccess) return PURLIN_ERR_CUDA;
+        L.info.block = kBulkThreads;
+    } else {
+        const bool small = replan_small(h, c.coll, p, plan, nplan, c.R, c.in, c.out, c.esz, false,
+                                        knobs);
+        const bool sh = has_shift(p) != 0;
+        grid = zs_grid(h, p.ntiles, zs_copy_resident_ctas(true, false, small, sh));
+        zs_copy_select(L.k, true, false, small, sh);
+        if (small) L.info.block = kSmallThreads;
+    }
+    L.k.grid = (unsigned)grid;
+    L.k.pdl = p.pdl != 0;
+    L.kind = grid > 0 ? 1 : 0;
+    L.info.grid = grid;
+    L.info.kernels = grid > 0;
+    L.info.chunk_bytes = tile_bytes(knobs.max_unit_log2, knobs.tile_units);
+    return PURLIN_OK;
+}
+
+// AllReduce into outputs on different 16-byte alignments: no fan-out body
+// fits them all.  Sum into out[0] (one destination: a shifted body where the
+// sources are off its grid), then copy out[0] to the other outputs
+// (single-destination shifted copies): (2R + 1) / 2R of the fused traffic
+// instead of element accesses.
+purlin_status_t plan_all_reduce_split(const Call& c, const ZsKnobs& knobs, Launches& L)
+{
+    purlin_handle_t h = c.h;
+    const int R = c.R;
+    ZsParams<kSegsSmall>& p = *reinterpret_cast<ZsParams<kSegsSmall>*>(L.k.params);
+    Piece sum = c.pieces[0];
+    sum.dst = 0;
+    ZsKnobs ks = knobs;
+    if (h->l2_store < 0 && h->l2_coll_store[(int)c.coll] < 0) ks.l2_store = kL2Normal;
+    purlin_status_t st = make_params(p, &sum, 1, R, c.in, c.out, c.esz, true, ks, h->status);
+    if (st != PURLIN_OK) return st;
+    const bool small = replan_small(h, c.coll, p, &sum, 1, R, c.in, c.out, c.esz, true, ks);
+    const int sh = has_shift(p);
+    const int grid = zs_grid(h, p.ntiles, zs_reduce_resident_ctas(c.dtype, 0, false, small, R, sh));
+    zs_reduce_select(L.k, c.dtype, 0, false, small, R, sh);
+    L.k.grid = (unsigned)grid;
+    L.k.pdl = p.pdl != 0;
+
+    ZsParams<kSegsSmall>& p2 = *reinterpret_cast<ZsParams<kSegsSmall>*>(L.k2.params);
+    uint64_t from[kMaxRanks];
+    Piece copies[kMaxRanks];
+    int nc = 0;
+    for (int r = 0; r < R; ++r) from[r] = c.out[0];
+    for (int j = 1; j < R; ++j) {
+        if (c.out[j] == c.out[0]) continue;
+        copies[nc++] = Piece{sum.dst_off, sum.dst_off, sum.bytes, 0, (uint8_t)j};
+    }
+    ZsKnobs kc = zs_knobs(h, Coll::AllToAllV);
+    st = make_params(p2, copies, nc, R, from, c.out, c.esz, false, kc, h->status);
+    if (st != PURLIN_OK) return st;
+    const bool small2 = replan_small(h, Coll::AllToAllV, p2, copies, nc, R, from, c.out, c.esz,
+                                     false, kc);
+    const bool sh2 = has_shift(p2) != 0;
+    const int grid2 = zs_grid(h, p2.ntiles, zs_copy_resident_ctas(false, false, small2, sh2));
+    zs_copy_select(L.k2, false, false, small2, sh2);
+    L.k2.grid = (unsigned)grid2;
+    L.k2.pdl = p2.pdl != 0;
+    L.kind = grid > 0 ? (grid2 > 0 ? 3 : 1) : 0;
+    L.info.grid = grid;
+    L.info.kernels = (grid > 0) + (grid2 > 0);
+    if (small) L.info.block = kSmallThreads;
+    L.info.chunk_bytes = tile_bytes(ks.max_unit_log2, ks.tile_units);
+    return PURLIN_OK;
+}
+
+// The zero-staging kernel of ReduceScatter(V), AllReduce (fused: each sum
+// written to all R outputs) and AllGather(V) (push: each source tile written
+// to all R outputs).
+purlin_status_t plan_zs(const Call& c, const ZsKnobs& knobs, bool bulk, Launches& L)
+{
+    purlin_handle_t h = c.h;
+    ZsKnobs kn = knobs;
+    ZsParams<kSegsSmall>& p = *reinterpret_cast<ZsParams<kSegsSmall>*>(L.k.params);
+    purlin_status_t st = make_params(p, c.pieces, c.np, c.R, c.in, c.out, c.esz, c.reduce, kn,
+                                     h->status);
+    if (st != PURLIN_OK) return st;
+    const bool fan_all = c.coll == Coll::AllGather || c.coll == Coll::AllReduce;
+    int grid;
+    if (bulk) {
+        grid = zs_grid(h, p.ntiles, zs_copy_bulk_resident_ctas(false, fan_all), kGridWavesBulk);
+        if (zs_copy_bulk_select(L.k, false, fan_all) != cudaSuccess) return PURLIN_ERR_CUDA;
+        L.info.block = kBulkThreads;
+    } else {
+        const bool small = replan_small(h, c.coll, p, c.pieces, c.np, c.R, c.in, c.out, c.esz,
+                                        c.reduce, kn);
+        if (c.reduce) {
+            const int sh = has_shift(p);
+            grid = zs_grid(h, p.ntiles,
+                           zs_reduce_resident_ctas(c.dtype, h->order, fan_all, small, c.R, sh));
+            zs_reduce_select(L.k, c.dtype, h->order, fan_all, small, c.R, sh);
+        } else {
+            const bool sh = has_shift(p) != 0;
+            grid = zs_grid(h, p.ntiles, zs_copy_resident_ctas(false, fan_all, small, sh));
+            zs_copy_select(L.k, false, fan_all, small, sh);
+        }
+        if (small) L.info.block = kSmallThreads;
+    }
+    L.k.grid = (unsigned)grid;
+    L.k.pdl = p.pdl != 0;
+    L.kind = grid > 0 ? 1 : 0;
+    L.info.chunk_bytes = tile_bytes(kn.max_unit_log2, kn.tile_units);
+    L.info.grid = grid;
+    L.info.kernels = grid > 0;
+    return PURLIN_OK;
+}
+
+// Keep a recorded call as a plan (one call per plan).
+purlin_status_t keep_plan(purlin_handle_t h, const Launches& L)
+{
+    if (h->recorded) return PURLIN_ERR_INVALID_ARG;
+    purlin_plan* plan = new (std::nothrow) purlin_plan;
+    if (!plan) return PURLIN_ERR_OOM;
+    plan->h = h;
+    plan->device = h->device;
+    plan->kind = L.kind;
+    auto keep = [](KernelLaunch& to, const KernelLaunch& from) {
+        to.func = from.func;
+        to.grid = from.grid;
+        to.block = from.block;
+        to.smem = from.smem;
+        to.pdl = from.pdl;
+        to.cooperative = from.cooperative;
+        to.params_bytes = from.params_bytes;
+        std::memcpy(to.params, from.params, from.params_bytes);
+    };
+    if (L.kind == 1 || L.kind == 3) keep(plan->k, L.k);
+    if (L.kind == 3) keep(plan->k2, L.k2);
+    plan->copies = L.copies;
+    plan->info = L.info;
+    h->recorded = plan;
+    return PURLIN_OK;
+}
+
+// Launch what a call or a plan holds, in stream order.
+cudaError_t launch_all(int kind, const KernelLaunch& k, const KernelLaunch& k2,
+                       const std::vector<CopyOp>& copies, cudaStream_t s)
+{
+    cudaError_t ce = cudaSuccess;
+    if (kind == 1 || kind == 3) {
+        ce = launch_kernel(k, s);
+        if (ce == cudaSuccess && kind == 3) ce = launch_kernel(k2, s);
+    } else if (kind == 2) {
+        for (const CopyOp& c : copies) {
+            ce = cudaMemcpyAsync(c.dst, c.src, c.bytes, cudaMemcpyDefault, s);
+            if (ce != cudaSuccess) break;
+        }
+    }
+    return ce;
+}
+
 purlin_status_t run(purlin_handle_t h, Coll coll, const void* const in_[], void* const out_[],
                     const size_t* counts, const size_t* da, const size_t* db, size_t count,
                     int dtype, bool reduce, purlin_stream_t stream)
@@ -405,228 +668,42 @@ purlin_status_t run(purlin_handle_t h, Coll coll, const void* const in_[], void*
     info.block = kThreads;
     info.bytes_moved = algorithmic_bytes(coll, R, counts, count, esz);
 
-    // The call's launch is built in thread-local storage (no copy of the
+    // The call's launches are built in thread-local storage (no copy of a
     // parameter block on the way to the launch), then made at once or, while
     // a plan is being recorded, kept.
     static thread_local KernelLaunch tl_k, tl_k2;
     static thread_local std::vector<CopyOp> tl_copies;
-    KernelLaunch& k = tl_k;
-    KernelLaunch& k2 = tl_k2;
-    k.grid = 0;
-    k2.grid = 0;
+    tl_k.grid = 0;
+    tl_k2.grid = 0;
     tl_copies.clear();
-    int kind = 0;
+    Launches L{tl_k, tl_k2, tl_copies, info};
+    const Call c{h, coll, R, dtype, esz, reduce, in, out, pieces, np};
 
     if (wants_staged(h) && np > 0) {
-        SnacRequest rq{};
-        rq.coll = coll;
-        rq.R = R;
-        rq.dtype = dtype;
-        rq.order = h->order;
-        rq.esz = esz;
-        rq.pieces = pieces;
-        rq.npieces = np;
-        rq.stage_y = h->variant == PURLIN_VARIANT_STAGED_Y;
-        for (int r = 0; r < R; ++r) { rq.in[r] = in[r]; rq.out[r] = out[r]; }
-        SnacConfig cfg{};
-        cfg.staging = h->staging;
-        cfg.staging_bytes = h->staging_bytes;
-        cfg.flags = h->flags;
-        cfg.flag_words = h->flag_words;
-        cfg.status = h->status;
-        cfg.chunk_bytes = h->chunk_bytes;
-        cfg.depth = h->depth;
-        cfg.channels = h->ctas;
-        cfg.sms = h->sms;
-        cfg.timeout_ns = h->timeout_ns;
-        cfg.inject_skip_notify = h->inject;
-        SnacLaunch sl{};
-        purlin_status_t ss = snac_plan(rq, cfg, k, &sl);
-        if (ss != PURLIN_OK) return ss;
-        h->inject = 0;
-        kind = k.grid > 0 ? 1 : 0;
-        info.variant = h->variant;
-        info.kernels = sl.kernels;
-        info.grid = sl.grid;
-        info.block = sl.block;
-        info.depth = sl.depth;
-        info.chunk_bytes = sl.chunk_bytes;
+        st = plan_staged(c, L);
     } else {
         info.variant = PURLIN_VARIANT_ZS;
-        ZsKnobs knobs = zs_knobs(h, coll);
+        const ZsKnobs knobs = zs_knobs(h, coll);
         const bool bulk = !reduce && h->atom == PURLIN_ATOM_BULK;
-        if (!reduce && h->atom == PURLIN_ATOM_COPY_ENGINE) {
-            // No kernel: every block goes to every destination through the
-            // copy engines, one asynchronous copy each, in stream order.
-            for (int i = 0; i < np; ++i) {
-                const Piece& pc = pieces[i];
-                const char* src = reinterpret_cast<const char*>(in[pc.src]) + pc.src_off;
-                for (int j = 0; j < R; ++j) {
-                    if (pc.dst != kEveryRank && pc.dst != j) continue;
-                    char* dst = reinterpret_cast<char*>(out[j]) + pc.dst_off;
-                    if (dst == src) continue;  // in-place AllGather block
-                    tl_copies.push_back(CopyOp{dst, src, (size_t)pc.bytes});
-                }
-            }
-            kind = tl_copies.empty() ? 0 : 2;
-            info.kernels = 0;
-            info.grid = 0;
-            info.block = 0;
-            info.chunk_bytes = 0;
-        } else if (coll == Coll::AllToAllV ||
-                   (coll == Coll::AllGather &&
-                    (h->direction == PURLIN_DIRECTION_PULL ||
-                     (h->direction == PURLIN_DIRECTION_AUTO && !bulk &&
-                      !outputs_share_grid(out, R))))) {
-            // AllGather outputs on different 16-byte alignments: one fan-out
-            // body cannot be aligned to all of them, single-destination pieces
-            // can (each a shifted body where its source is off its grid)
-            ZsParams<kSegsLarge>& p = *reinterpret_cast<ZsParams<kSegsLarge>*>(k.params);
-            const Piece* plan = pieces;
-            int nplan = np;
-            Piece pulled[kMaxRanks * kMaxRanks];
-            if (coll == Coll::AllGather) {
-                // pull: one piece per (destination, source), destination by
-                // destination; every source is read R times (from L2 after
-                // the first read, hence normal priority for the loads)
-                nplan = pull_pieces(pieces, np, R, in, out, pulled);
-                plan = pulled;
-                if (h->l2_load < 0 && h->l2_coll_load[(int)coll] < 0) knobs.l2_load = kL2Normal;
-            }
-            st = make_params(p, plan, nplan, R, in, out, esz, false, knobs, h->status);
-            if (st != PURLIN_OK) return st;
-            int grid;
-            if (bulk) {
-                grid = zs_grid(h, p.ntiles, zs_copy_bulk_resident_ctas(true, false), kGridWavesBulk);
-                if (zs_copy_bulk_select(k, true, false) != cudaSuccess) return PURLIN_ERR_CUDA;
-                info.block = kBulkThreads;
-            } else {
-                const bool small = replan_small(h, coll, p, plan, nplan, R, in, out, esz, false, knobs);
-                const bool sh = has_shift(p) != 0;
-                grid = zs_grid(h, p.ntiles, zs_copy_resident_ctas(true, false, small, sh));
-                zs_copy_select(k, true, false, small, sh);
-                if (small) info.block = kSmallThreads;
-            }
-            k.grid = (unsigned)grid;
-            k.pdl = p.pdl != 0;
-            kind = grid > 0 ? 1 : 0;
-            info.grid = grid;
-            info.kernels = grid > 0;
-            info.chunk_bytes = tile_bytes(knobs.max_unit_log2, knobs.tile_units);
-        } else if (coll == Coll::AllReduce && np == 1 && R > 1 && h->order == 0 &&
-                   !outputs_share_grid(out, R)) {
-            // Outputs on different 16-byte alignments: no fan-out body fits
-            // them all.  Sum into out[0] (one destination: a shifted body where
-            // the sources are off its grid), then copy out[0] to the other
-            // outputs (single-destination shifted copies).  (2R + 1) / 2R of
-            // the fused traffic instead of element accesses.
-            ZsParams<kSegsSmall>& p = *reinterpret_cast<ZsParams<kSegsSmall>*>(k.params);
-            Piece sum = pieces[0];
-            sum.dst = 0;
-            ZsKnobs ks = knobs;
-            if (h->l2_store < 0 && h->l2_coll_store[(int)coll] < 0) ks.l2_store = kL2Normal;
-            st = make_params(p, &sum, 1, R, in, out, esz, true, ks, h->status);
-            if (st != PURLIN_OK) return st;
-            const bool small = replan_small(h, coll, p, &sum, 1, R, in, out, esz, true, ks);
-            const int sh = has_shift(p);
-            const int grid = zs_grid(h, p.ntiles,
-                                     zs_reduce_resident_ctas(dtype, 0, false, small, R, sh));
-            zs_reduce_select(k, dtype, 0, false, small, R, sh);
-            k.grid = (unsigned)grid;
-            k.pdl = p.pdl != 0;
+        const bool by_destination =
+            coll == Coll::AllToAllV ||
+            (coll == Coll::AllGather &&
+             (h->direction == PURLIN_DIRECTION_PULL ||
+              (h->direction == PURLIN_DIRECTION_AUTO && !bulk && !outputs_share_grid(out, R))));
+        if (!reduce && h->atom == PURLIN_ATOM_COPY_ENGINE)
+            plan_copy_engine(c, L);
+        else if (by_destination)
+            st = plan_by_destination(c, knobs, bulk, L);
+        else if (coll == Coll::AllReduce && np == 1 && R > 1 && h->order == 0 &&
+                 !outputs_share_grid(out, R))
+            st = plan_all_reduce_split(c, knobs, L);
+        else
+            st = plan_zs(c, knobs, bulk, L);
+    }
+    if (st != PURLIN_OK) return st;
 
-            ZsParams<kSegsSmall>& p2 = *reinterpret_cast<ZsParams<kSegsSmall>*>(k2.params);
-            uint64_t from[kMaxRanks];
-            Piece copies[kMaxRanks];
-            int nc = 0;
-            for (int r = 0; r < R; ++r) from[r] = out[0];
-            for (int j = 1; j < R; ++j) {
-                if (out[j] == out[0]) continue;
-                copies[nc++] = Piece{sum.dst_off, sum.dst_off, sum.bytes, 0, (uint8_t)j};
-            }
-            ZsKnobs kc = zs_knobs(h, Coll::AllToAllV);
-            st = make_params(p2, copies, nc, R, from, out, esz, false, kc, h->status);
-            if (st != PURLIN_OK) return st;
-            const bool small2 = replan_small(h, Coll::AllToAllV, p2, copies, nc, R, from, out, esz,
-                                             false, kc);
-            const bool sh2 = has_shift(p2) != 0;
-            const int grid2 = zs_grid(h, p2.ntiles, zs_copy_resident_ctas(false, false, small2, sh2));
-            zs_copy_select(k2, false, false, small2, sh2);
-            k2.grid = (unsigned)grid2;
-            k2.pdl = p2.pdl != 0;
-            kind = grid > 0 ? (grid2 > 0 ? 3 : 1) : 0;
-            info.grid = grid;
-            info.kernels = (grid > 0) + (grid2 > 0);
-            if (small) info.block = kSmallThreads;
-            info.chunk_bytes = tile_bytes(ks.max_unit_log2, ks.tile_units);
-        } else {
-            ZsParams<kSegsSmall>& p = *reinterpret_cast<ZsParams<kSegsSmall>*>(k.params);
-            st = make_params(p, pieces, np, R, in, out, esz, reduce, knobs, h->status);
-            if (st != PURLIN_OK) return st;
-            bool fan_all = coll == Coll::AllGather || coll == Coll::AllReduce;
-            int grid;
-            if (bulk) {
-                grid = zs_grid(h, p.ntiles, zs_copy_bulk_resident_ctas(false, fan_all), kGridWavesBulk);
-                if (zs_copy_bulk_select(k, false, fan_all) != cudaSuccess) return PURLIN_ERR_CUDA;
-                info.block = kBulkThreads;
-            } else {
-                const bool small = replan_small(h, coll, p, pieces, np, R, in, out, esz, reduce, knobs);
-                if (reduce) {
-                    const int sh = has_shift(p);
-                    grid = zs_grid(h, p.ntiles,
-                                   zs_reduce_resident_ctas(dtype, h->order, fan_all, small, R, sh));
-                    zs_reduce_select(k, dtype, h->order, fan_all, small, R, sh);
-                } else {
-                    const bool sh = has_shift(p) != 0;
-                    grid = zs_grid(h, p.ntiles, zs_copy_resident_ctas(false, fan_all, small, sh));
-                    zs_copy_select(k, false, fan_all, small, sh);
-                }
-                if (small) info.block = kSmallThreads;
-            }
-            k.grid = (unsigned)grid;
-            k.pdl = p.pdl != 0;
-            kind = grid > 0 ? 1 : 0;
-            info.chunk_bytes = tile_bytes(knobs.max_unit_log2, knobs.tile_units);
-            info.grid = grid;
-            info.kernels = grid > 0;
-        }
-    }
-
-    if (h->recording) {
-        if (h->recorded) return PURLIN_ERR_INVALID_ARG;  // one call per plan
-        purlin_plan* plan = new (std::nothrow) purlin_plan;
-        if (!plan) return PURLIN_ERR_OOM;
-        plan->h = h;
-        plan->device = h->device;
-        plan->kind = kind;
-        auto keep = [](KernelLaunch& to, const KernelLaunch& from) {
-            to.func = from.func;
-            to.grid = from.grid;
-            to.block = from.block;
-            to.smem = from.smem;
-            to.pdl = from.pdl;
-            to.cooperative = from.cooperative;
-            to.params_bytes = from.params_bytes;
-            std::memcpy(to.params, from.params, from.params_bytes);
-        };
-        if (kind == 1 || kind == 3) keep(plan->k, k);
-        if (kind == 3) keep(plan->k2, k2);
-        plan->copies = tl_copies;
-        plan->info = info;
-        h->recorded = plan;
-        return PURLIN_OK;
-    }
-    cudaError_t ce = cudaSuccess;
-    if (kind == 1 || kind == 3) {
-        ce = launch_kernel(k, s);
-        if (ce == cudaSuccess && kind == 3) ce = launch_kernel(k2, s);
-    } else if (kind == 2) {
-        for (const CopyOp& c : tl_copies) {
-            ce = cudaMemcpyAsync(c.dst, c.src, c.bytes, cudaMemcpyDefault, s);
-            if (ce != cudaSuccess) break;
-        }
-    }
-    if (ce != cudaSuccess) return PURLIN_ERR_CUDA;
+    if (h->recording) return keep_plan(h, L);
+    if (launch_all(L.kind, tl_k, tl_k2, tl_copies, s) != cudaSuccess) return PURLIN_ERR_CUDA;
     h->last = info;
     return PURLIN_OK;
 }
@@ -846,17 +923,8 @@ purlin_status_t purlin_plan_launch(purlin_plan_t plan, purlin_stream_t stream)
     DeviceGuard guard(plan->device);
     if (!guard.ok) return PURLIN_ERR_CUDA;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    cudaError_t ce = cudaSuccess;
-    if (plan->kind == 1 || plan->kind == 3) {
-        ce = launch_kernel(plan->k, s);
-        if (ce == cudaSuccess && plan->kind == 3) ce = launch_kernel(plan->k2, s);
-    } else if (plan->kind == 2) {
-        for (const CopyOp& c : plan->copies) {
-            ce = cudaMemcpyAsync(c.dst, c.src, c.bytes, cudaMemcpyDefault, s);
-            if (ce != cudaSuccess) break;
-        }
-    }
-    if (ce != cudaSuccess) return PURLIN_ERR_CUDA;
+    if (launch_all(plan->kind, plan->k, plan->k2, plan->copies, s) != cudaSuccess)
+        return PURLIN_ERR_CUDA;
     plan->h->last = plan->info;
     return PURLIN_OK;
 }
