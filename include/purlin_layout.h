@@ -62,7 +62,9 @@ typedef struct {
  *              *ntiles the number of tiles.  Tiles are those of the 256-thread
  *              zero-staging launch: 1024 units for copies; for sums in the fixed
  *              rank order 256 x U units, U = 4 for R <= 2, 2 for R = 3..4 and 1
- *              above (the pairwise order keeps U = 1, so its tiles differ); a call
+ *              above (the pairwise order keeps U = 1, so its tiles differ); a
+ *              shifted body's tiles hold 31/32 of those units (each warp's 32
+ *              lanes write 31 units between the 32 source blocks they load); a call
  *              with fewer than the small-message threshold of them
  *              (purlin_set_small_tiles) runs one-warp tiles of 32 units over the
  *              same segments.
