@@ -38,6 +38,7 @@
 #include "atom.cuh"
 #include "internal.h"
 #include "snac.h"
+#include "zs_kernels.cuh"  // register realignment of shifted bodies
 
 #include <algorithm>
 #include <cstdlib>
@@ -378,6 +379,96 @@ __device__ void cta_reduce_src(const SnacParams& p, int unit_log2, char* dst, ui
     else cta_reduce_src_elem<T, ORDER>(p, dst, src_off, len);
 }
 
+// ------------------------------------------------ shifted bodies (producer)
+// A step of a shifted body (Segment::shift != 0): the producer reads aligned
+// source blocks and writes the step's units, realigned to the destinations'
+// grid, into the slot, so the consumer works on aligned data.  Lanes as in the
+// zero-staging kernels: a warp loads 32 blocks and writes the 31 units between
+// them.  The block after a step's last unit is the next step's first (or the
+// segment's last one, which holds its last bytes): within the segment.  A
+// shifted step is a whole number of units.
+
+// Copy a step's len bytes from src (any offset) to dst (unit-aligned).
+template <int B>
+__device__ void cta_copy_shifted(const char* src, char* dst, uint64_t len, uint64_t lpol,
+                                 uint64_t spol)
+{
+    constexpr int W = B / 4;
+    constexpr int WARPS = kThreads / 32;
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int shift = (int)(reinterpret_cast<uintptr_t>(src) & (B - 1));
+    const uint64_t n = len / B;
+    const uint64_t nblocks = shift ? n + 1 : n;
+    for (uint64_t row = 0; row < n; row += (uint64_t)WARPS * 31) {
+        const uint64_t q = row + (uint64_t)warp * 31 + lane;
+        atom::Vec<B> v, next, out;
+        if (q < nblocks) {
+            atom::load(v, at(src, q * B, shift), lpol);
+        } else {
+#pragma unroll
+            for (int i = 0; i < W; ++i) v.w[i] = 0u;
+        }
+#pragma unroll
+        for (int i = 0; i < W; ++i) next.w[i] = __shfl_down_sync(0xffffffffu, v.w[i], 1);
+        if (lane == 31 || q >= n) continue;
+        if (shift) realign<W>(v.w, next.w, shift, out.w);
+        else out = v;
+        atom::store(dst + q * B, out, spol);
+    }
+}
+
+__device__ void cta_copy_shifted_any(int unit_log2, const char* src, char* dst, uint64_t len,
+                                     uint64_t lpol, uint64_t spol)
+{
+    if (unit_log2 == 5) cta_copy_shifted<32>(src, dst, len, lpol, spol);
+    else cta_copy_shifted<16>(src, dst, len, lpol, spol);
+}
+
+// Fold a step of the R sources into dst (unit-aligned), each rank realigned on
+// its own offset before the fold (16-byte units: a shifted sum's width).
+template <typename T, int ORDER>
+__device__ void cta_reduce_src_shifted(const SnacParams& p, char* dst, uint64_t src_off,
+                                       uint64_t len, uint64_t lpol, uint64_t spol)
+{
+    constexpr int B = 16;
+    constexpr int W = B / 4;
+    constexpr int WARPS = kThreads / 32;
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int R = (int)p.R;
+    const uint64_t n = len / B;
+    int sh[kMaxRanks];
+#pragma unroll
+    for (int r = 0; r < kMaxRanks; ++r)
+        sh[r] = r < R ? (int)((reinterpret_cast<uintptr_t>(p.in[r]) + src_off) & (B - 1)) : 0;
+    for (uint64_t row = 0; row < n; row += (uint64_t)WARPS * 31) {
+        const uint64_t q = row + (uint64_t)warp * 31 + lane;
+        atom::Vec<B> v[kMaxRanks];
+#pragma unroll
+        for (int r = 0; r < kMaxRanks; ++r) {
+            if (r < R && q < (sh[r] ? n + 1 : n)) {
+                atom::load(v[r], at(p.in[r], src_off + q * B, sh[r]), lpol);
+            } else {
+#pragma unroll
+                for (int i = 0; i < W; ++i) v[r].w[i] = 0u;
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < kMaxRanks; ++r) {
+            if (r >= R || sh[r] == 0) continue;
+            atom::Vec<B> next;
+#pragma unroll
+            for (int i = 0; i < W; ++i) next.w[i] = __shfl_down_sync(0xffffffffu, v[r].w[i], 1);
+            realign<W>(v[r].w, next.w, sh[r], v[r].w);
+        }
+        if (lane == 31 || q >= n) continue;
+        atom::Vec<B> out;
+        atom::reduce_unit<T, ORDER, B>(v, R, out);
+        atom::store(dst + q * B, out, spol);
+    }
+}
+
 // ------------------------------------------------------------------ roles
 
 // Relaxed access to a flag-area word that a release / acquire pair orders.
@@ -397,7 +488,7 @@ __device__ __forceinline__ void st_relaxed(uint64_t* w, uint64_t v)
 // round-robin: a channel whose SM drains faster takes more steps, so the
 // slowest SMs do not set the time.  The producer records the step in the slot's step
 // word before notifying; the consumer reads it after the acquire.
-template <typename T, int ORDER, int KIND>
+template <typename T, int ORDER, int KIND, bool SHIFTED>
 __device__ void producer_dynamic(const SnacParams& p, uint32_t ch, uint64_t epoch)
 {
     __shared__ uint64_t step_s;
@@ -424,6 +515,25 @@ __device__ void producer_dynamic(const SnacParams& p, uint32_t ch, uint64_t epoc
         const Segment& s = step_segment(p, (uint32_t)i);
         const uint64_t off = (uint64_t)((uint32_t)i - s.tile0) * p.chunk;
         const uint64_t len = min(p.chunk, s.bytes - off);
+        if constexpr (SHIFTED) {
+            if (s.shift) {
+                // realigned to the destinations' grid while staged
+                char* slot_p = slot_data(p, ch, slot);
+                if (KIND == kRSY || KIND == kARY) {
+                    cta_reduce_src_shifted<T, ORDER>(p, slot_p, s.src_off + off, len, lpol, spol);
+                } else if (KIND == kRS || KIND == kAR) {
+                    for (int r = 0; r < (int)p.R; ++r)
+                        cta_copy_shifted_any(s.unit_log2, p.in[r] + s.src_off + off,
+                                             slot_p + (uint64_t)r * p.chunk, len, lpol, spol);
+                } else {
+                    cta_copy_shifted_any(s.unit_log2, p.in[s.src] + s.src_off + off, slot_p, len,
+                                         lpol, spol);
+                }
+                if (threadIdx.x == 0) st_relaxed(f + kStepOf, i);
+                cta_notify(f + kReady, tag_of(epoch, n));
+                continue;
+            }
+        }
         if (KIND == kRSY || KIND == kARY) {
             cta_reduce_src<T, ORDER>(p, s.unit_log2, slot_data(p, ch, slot), s.src_off + off, len,
                                      lpol, spol);
@@ -541,7 +651,8 @@ __device__ void gatherer(const SnacParams& p, uint32_t ch, uint64_t epoch)
     }
 }
 
-template <typename T, int ORDER, int KIND>
+// SHIFTED: the plan holds a shifted body (only such launches carry that path).
+template <typename T, int ORDER, int KIND, bool SHIFTED>
 __global__ void __launch_bounds__(kThreads, 2) snac_kernel(const __grid_constant__ SnacParams p)
 {
     __shared__ uint64_t epoch_s;
@@ -555,7 +666,7 @@ __global__ void __launch_bounds__(kThreads, 2) snac_kernel(const __grid_constant
     const uint32_t role = blockIdx.x / p.nch;
     const uint32_t ch = blockIdx.x % p.nch;
     if (role == 0) {
-        producer_dynamic<T, ORDER, KIND>(p, ch, epoch);
+        producer_dynamic<T, ORDER, KIND, SHIFTED>(p, ch, epoch);
     } else if constexpr (KIND == kAR) {
         if (role == 1) consumer_ar<T, ORDER>(p, ch, epoch);
         else gatherer(p, ch, epoch);
@@ -580,28 +691,38 @@ __global__ void __launch_bounds__(kThreads, 2) snac_kernel(const __grid_constant
 
 using SnacKernel = void (*)(SnacParams);
 
-template <typename T, int KIND>
+template <typename T, int KIND, bool SH>
 SnacKernel pick_order(int order)
 {
-    return order == 0 ? snac_kernel<T, 0, KIND> : snac_kernel<T, 1, KIND>;
+    // the pairwise order never has shifted bodies
+    return order == 0 ? snac_kernel<T, 0, KIND, SH> : snac_kernel<T, 1, KIND, false>;
 }
 
-template <int KIND>
+template <int KIND, bool SH>
 SnacKernel pick_dtype(int dtype, int order)
 {
-    if (dtype == kF32) return pick_order<atom::F32, KIND>(order);
-    if (dtype == kBF16) return pick_order<atom::BF16, KIND>(order);
-    return pick_order<atom::F16, KIND>(order);
+    if (dtype == kF32) return pick_order<atom::F32, KIND, SH>(order);
+    if (dtype == kBF16) return pick_order<atom::BF16, KIND, SH>(order);
+    return pick_order<atom::F16, KIND, SH>(order);
 }
 
-SnacKernel kernel_for(Coll coll, int dtype, int order, bool stage_y)
+template <bool SH>
+SnacKernel kernel_for_sh(Coll coll, int dtype, int order, bool stage_y)
 {
     switch (coll) {
-    case Coll::ReduceScatter: return stage_y ? pick_dtype<kRSY>(dtype, order) : pick_dtype<kRS>(dtype, order);
-    case Coll::AllReduce: return stage_y ? pick_dtype<kARY>(dtype, order) : pick_dtype<kAR>(dtype, order);
-    case Coll::AllGather: return snac_kernel<atom::F32, 0, kAG>;
-    default: return snac_kernel<atom::F32, 0, kA2A>;
+    case Coll::ReduceScatter:
+        return stage_y ? pick_dtype<kRSY, SH>(dtype, order) : pick_dtype<kRS, SH>(dtype, order);
+    case Coll::AllReduce:
+        return stage_y ? pick_dtype<kARY, SH>(dtype, order) : pick_dtype<kAR, SH>(dtype, order);
+    case Coll::AllGather: return snac_kernel<atom::F32, 0, kAG, SH>;
+    default: return snac_kernel<atom::F32, 0, kA2A, SH>;
     }
+}
+
+SnacKernel kernel_for(Coll coll, int dtype, int order, bool stage_y, bool shifted)
+{
+    return shifted ? kernel_for_sh<true>(coll, dtype, order, stage_y)
+                   : kernel_for_sh<false>(coll, dtype, order, stage_y);
 }
 
 int roles_of(Coll coll, bool stage_y) { return coll == Coll::AllReduce && !stage_y ? 3 : 2; }
@@ -672,12 +793,17 @@ purlin_status_t plan_into(KernelLaunch& k, const SnacRequest& rq, const SnacConf
     k.grid = 0;
     const bool reduce = rq.coll == Coll::ReduceScatter || rq.coll == Coll::AllReduce;
     uint32_t ntiles = 0;
+    // shifted bodies for the fixed rank order and for copies: the producer
+    // realigns them while staging
+    const bool allow_shift = !reduce || rq.order == 0;
     int nseg = layout_segments(rq.pieces, rq.npieces, rq.R, rq.in, rq.out, rq.esz, reduce,
                                reduce ? kTileUnitsReduce : kTileUnitsCopy, snac_unit_log2(),
-                               /*allow_shift=*/false, p.seg, kSegsLarge, &ntiles);
+                               allow_shift, p.seg, kSegsLarge, &ntiles);
     if (nseg < 0) return PURLIN_ERR_UNSUPPORTED;
+    bool shifted = false;
+    for (int i = 0; i < nseg; ++i) shifted |= p.seg[i].shift != 0;
 
-    SnacKernel kernel = kernel_for(rq.coll, rq.dtype, rq.order, rq.stage_y);
+    SnacKernel kernel = kernel_for(rq.coll, rq.dtype, rq.order, rq.stage_y, shifted);
     const int resident = resident_ctas_of(reinterpret_cast<const void*>(kernel), kThreads);
     if (resident < 1) return PURLIN_ERR_CUDA;
     size_t chunk = 0;
