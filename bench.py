@@ -370,7 +370,7 @@ def bench_reference(args):
 # Source files whose content determines each kernel family's device code.
 KERNEL_SOURCES = {
     "zs": ["atom.cuh", "plan.h", "zs_kernels.cuh"],
-    "snac": ["atom.cuh", "plan.h", "snac.h", "snac_kernels.cu"],
+    "snac": ["atom.cuh", "plan.h", "snac.h", "snac_kernels.cu", "zs_kernels.cuh"],
 }
 
 
