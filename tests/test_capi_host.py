@@ -120,6 +120,9 @@ def plan_map(segs, R):
 
 
 def check_alignment(segs, R, in_addr, out_addr, reduce, esz):
+    if reduce and any(s["shift"] for s in segs):
+        # a sum plan holding a shifted body has 16-byte vector bodies throughout
+        assert all(s["unit"] in (esz, 16) for s in segs), segs
     for s in segs:
         u = s["unit"]
         assert s["bytes"] % u == 0
