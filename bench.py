@@ -35,6 +35,7 @@ sys.path.insert(0, ROOT)
 METRIC = "effective HBM GB/s (% of GB300 peak) per collective @R=8; µs at 4 KiB/rank"
 UNIT = "GB/s"
 WORKLOAD = "rs_ag_r8_bf16"
+WORKLOAD_SHORT = "RS+AG, R=8, bf16, 64 MiB/rank, N(0,1)"
 R = 8
 BYTES_PER_RANK = 64 << 20
 ELEMS_PER_RANK = BYTES_PER_RANK // 2
@@ -60,6 +61,9 @@ def parse_args():
                          "(no side studies, no CPU baseline)")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--studies-out", default=None,
+                    help="write the side studies to this JSON file instead of an earlier "
+                         "stdout line")
     ap.add_argument("--only", choices=["rs", "ag", "ar", "a2av"], default=None,
                     help="time one collective alone (profiling runs); prints a short line")
     ap.add_argument("--ranks", type=int, default=R, choices=range(1, R + 1), metavar="R",
@@ -85,10 +89,8 @@ def measured_peaks():
 
 def bench_config(world):
     """The workload both arms measure (the reference arm reports the same)."""
-    return {"workload": "ReduceScatter then AllGather, R=8 virtual ranks, bf16, 64 MiB per "
-                        "rank (8 partitions of 8 MiB), N(0,1), fp32 accumulation in rank order",
-            "R": R, "bytes_per_rank": BYTES_PER_RANK, "parallelism": f"replicas x{world}",
-            "l2": "inputs 512 MiB > L2 per step; no flush"}
+    return {"workload": WORKLOAD_SHORT, "parallelism": f"replicas x{world}",
+            "l2": "inputs>L2"}
 
 
 def cpu_model():
@@ -284,6 +286,7 @@ def run_cpu_oracle(xh, budget_s, max_reps=20):
     return {"value": reps * (rs + ag) / el / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": f"{reps} full step(s) of the workload (RS then AG, R=8, 8 x 64 MiB bf16) "
                       f"in {el:.1f} s, single-threaded C, {cpu_model()}",
+            "short": f"{reps} steps, {el:.1f} s, {cpu_model()[:16]}",
             "seconds": el}, y, z
 
 
@@ -417,24 +420,96 @@ def sources_digest(family, read=None):
 
 
 def traffic_from_profiles(kernel_key):
-    """Per-launch DRAM bytes of a kernel from the committed ncu summary, if it
-    was taken on the current sources of that kernel family (else None)."""
+    """Per-launch DRAM bytes of a kernel from the committed ncu summaries, if
+    taken on the current sources of that kernel family: (bytes, kind, digest),
+    bytes None if there is none.  A summary line reads
+    "traffic: <kernel_key> <bytes per launch> sources=<digest>" (one launch
+    captured alone, caches flushed) or "traffic-in-step: ..." (one launch of the
+    benchmark step, caches as the step leaves them), which is preferred."""
     family = "snac" if kernel_key.startswith("snac") else "zs"
     digest = sources_digest(family)
     pdir = os.path.join(ROOT, "profiles")
-    if not os.path.isdir(pdir):
-        return None, digest
-    for f in sorted(os.listdir(pdir)):
-        if not f.endswith((".md", ".txt")):
-            continue
-        with open(os.path.join(pdir, f)) as fh:
-            for line in fh:
-                # "traffic: <kernel_key> <bytes_per_launch> sources=<digest>"
-                parts = line.strip().strip("`").split()
-                if len(parts) == 4 and parts[0] == "traffic:" and parts[1] == kernel_key \
-                        and parts[3] == f"sources={digest}":
-                    return int(parts[2]), digest
-    return None, digest
+    found = {}
+    if os.path.isdir(pdir):
+        for f in sorted(os.listdir(pdir)):
+            if not f.endswith((".md", ".txt")):
+                continue
+            with open(os.path.join(pdir, f)) as fh:
+                for line in fh:
+                    parts = line.strip().strip("`").split()
+                    if len(parts) == 4 and parts[0] in ("traffic:", "traffic-in-step:") \
+                            and parts[1] == kernel_key and parts[3] == f"sources={digest}":
+                        found[parts[0]] = int(parts[2])
+    if "traffic-in-step:" in found:
+        return found["traffic-in-step:"], "in step", digest
+    if "traffic:" in found:
+        return found["traffic:"], "alone, cold L2", digest
+    return None, None, digest
+
+
+def roofline_entry(coll, peak, peak_kind, name, traffic, traffic_kind):
+    """The roofline object of the dominant kernel: algorithmic bytes per launch
+    over its event-timed duration, against the measured copy peak; beside it
+    the DRAM bytes ncu counted for one launch over the same duration
+    (dram_frac), which tells bytes served by HBM from bytes served by L2."""
+    dur_s = coll["us"] / 1e6
+    out = {"bound": "hbm", "achieved": coll["gbs"], "peak": peak, "unit": "GB/s",
+           "frac": coll["gbs"] / peak, "traffic": traffic, "kernel": name,
+           "algorithmic_bytes_per_launch": coll["bytes"],
+           "peak_kind": "of measured" if peak_kind == "measured" else "of fallback"}
+    if traffic is not None:
+        out["dram_frac"] = traffic / dur_s / 1e9 / peak
+        out["traffic_kind"] = traffic_kind
+    return out
+
+
+def _r(v, nd=4):
+    return round(v, nd) if isinstance(v, float) else v
+
+
+def compact_line(*, world, steps, warmup, value, ms_per_step, variant, roofline, per, e2e,
+                 cpu, parity, lat, launches, clocks, peak, step_traffic):
+    """The benchmark's result line: the contract keys and the figures that
+    back them, short enough to be read whole from the end of a log."""
+    rf = {k: roofline.get(k) for k in ("bound", "achieved", "peak", "unit", "frac", "traffic",
+                                       "dram_frac", "kernel", "algorithmic_bytes_per_launch")}
+    for k in ("achieved", "peak"):
+        rf[k] = _r(rf[k], 1)
+    for k in ("frac", "dram_frac"):
+        rf[k] = _r(rf[k], 4)
+    line = {
+        "metric": METRIC, "value": _r(value, 1), "unit": UNIT, "n_gpus": world, "steps": steps,
+        "warmup": warmup, "ms_per_step": _r(ms_per_step, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": bench_config(world) | {"variant": variant},
+        "roofline": rf,
+        "e2e": {"value": _r(e2e["value"], 1), "unit": e2e["unit"],
+                "h2d_bytes_per_step": e2e["h2d_bytes_per_step"],
+                "d2h_bytes_per_step": e2e["d2h_bytes_per_step"],
+                "ms_per_step": _r(e2e.get("ms_per_step"), 3), "steps": e2e.get("steps")},
+        "cpu_baseline": None if cpu is None else
+        {"value": _r(cpu["value"], 3), "unit": cpu["unit"], "cores": cpu["cores"],
+         "kind": cpu["kind"], "sample": cpu.get("short", "full steps")},
+        "allreduce_4KiB_us": None if lat is None else _r(lat.get("us_graph_per_launch"), 3),
+        "parity_vs_oracle": parity,
+        "gpu_launches": launches,
+        "clocks": {"sm_mhz": clocks.get("sm_mhz"), "sm_max_mhz": clocks.get("sm_max_mhz"),
+                   "reasons": clocks.get("reasons", [])},
+    }
+    if step_traffic is not None:
+        line["step_dram_frac"] = _r(step_traffic / (ms_per_step / 1e3) / 1e9 / peak)
+    return line
+
+
+def emit(line, studies, studies_out=None):
+    """Side studies go to a file (or an earlier stdout line); the result line
+    is always the last line on stdout."""
+    if studies_out:
+        with open(studies_out, "w") as f:
+            json.dump(studies, f)
+    else:
+        print(json.dumps({"studies": studies}), flush=True)
+    print(json.dumps(line, separators=(",", ":")), flush=True)
 
 
 def bench_purlin(args):
@@ -537,15 +612,22 @@ def bench_purlin(args):
         v["frac_of_peak"] = v["gbs"] / peak
         v["sm_bound"] = min(v["grid"], rs_info["sms"])
     dom = "reduce_scatter" if rs_avg >= ag_avg else "all_gather"
-    kernel_key = ("zs_reduce" if dom == "reduce_scatter" else "zs_copy") \
-        if args.variant == "zs" else "snac"
-    traffic, digest = traffic_from_profiles(f"{kernel_key}:{WORKLOAD}")
-    roofline = {"bound": "hbm", "achieved": per[dom]["gbs"], "peak": peak, "unit": "GB/s",
-                "frac": per[dom]["gbs"] / peak, "traffic": traffic, "kernel": dom,
-                "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs, copy burst)"
-                if peak_kind == "measured" else "fallback 6.8 TB/s",
-                "algorithmic_bytes_per_launch": per[dom]["bytes"]}
-
+    family = "zs" if args.variant == "zs" else "snac"
+    keys = {"reduce_scatter": ("zs_reduce" if family == "zs" else "snac") + ":" + WORKLOAD,
+            "all_gather": ("zs_copy" if family == "zs" else "snac_ag") + ":" + WORKLOAD}
+    # DRAM bytes per launch from the committed ncu summaries: the in-step
+    # capture (caches as the step leaves them) where there is one, else the
+    # cold one-launch capture; None once the kernel sources have changed.
+    traffic = {}
+    digest = None
+    for coll, key in keys.items():
+        t, kind, digest = traffic_from_profiles(key)
+        traffic[coll] = (t, kind)
+    roofline = roofline_entry(per[dom], peak, peak_kind, "rs" if dom == "reduce_scatter" else "ag",
+                              *traffic[dom])
+    step_traffic = None
+    if all(t is not None for t, _ in traffic.values()):
+        step_traffic = sum(t for t, _ in traffic.values())
     per["split_run_step_us"] = split_ms / Kb * 1e3
 
     lat = staged = frugal = tree = configs = sweep = None
@@ -601,12 +683,12 @@ def bench_purlin(args):
     rd.purlin_destroy(h)
     if rank != 0:
         return
-    line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
-        "warmup": max(3, args.warmup), "ms_per_step": max_ms / K, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": bench_config(world) | {"variant": args.variant},
-        "roofline": roofline,
+    line = compact_line(
+        world=world, steps=K, warmup=max(3, args.warmup), value=value, ms_per_step=max_ms / K,
+        variant=args.variant, roofline=roofline, per=per, e2e=e2e, cpu=cpu, parity=parity,
+        lat=lat, launches=launches, clocks=clocks.summary(), peak=peak,
+        step_traffic=step_traffic)
+    studies = {
         "per_collective": per,
         "allreduce_4KiB": lat,
         "staged_step": staged,
@@ -617,12 +699,10 @@ def bench_purlin(args):
         "e2e": e2e,
         "cpu_baseline": cpu,
         "cpu_baseline_threads": cpu_threads,
-        "parity_vs_oracle": parity,
-        "gpu_launches": launches,
-        "clocks": clocks.summary(),
+        "roofline": roofline,
         "sources": digest,
     }
-    print(json.dumps(line), flush=True)
+    emit(line, studies, args.studies_out)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()

@@ -7,6 +7,7 @@ and the reference arm does no work on ranks other than 0.  The CPU baseline's
 partition-split timing must give the single-threaded oracle's bits.
 """
 import io
+import json
 import os
 import socket
 import sys
@@ -109,3 +110,86 @@ def test_sources_digest_ignores_comments_not_code():
     d2 = bench.sources_digest("zs", read={f: same for f in files}.get)
     d3 = bench.sources_digest("zs", read={f: other for f in files}.get)
     assert d1 == d2 != d3
+
+
+def _worst_case_line(bench):
+    """A result line built from stub figures with every optional part present
+    and long values where values can be long."""
+    per = {"reduce_scatter": {"us": 97.12345678, "gbs": 6219.123456789, "bytes": 603979776},
+           "all_gather": {"us": 83.98765432, "gbs": 7191.987654321, "bytes": 603979776}}
+    roofline = bench.roofline_entry(per["reduce_scatter"], 6785.9, "measured", "rs",
+                                    551648256, "in step")
+    e2e = {"value": 363.61234567, "unit": "GB/s", "h2d_bytes_per_step": 536870912,
+           "d2h_bytes_per_step": 536870912, "ms_per_step": 3.3212345678, "steps": 20,
+           "note": "a long note that must not reach the line " * 4}
+    cpu = {"value": 1.7871234567, "unit": "GB/s", "cores": 1, "kind": "oracle",
+           "sample": "a long sample description " * 10,
+           "short": "20 steps, 13.5 s, " + "x" * 16}
+    lat = {"us_graph_per_launch": 1.5123456789, "us_back_to_back": 2.0}
+    clocks = {"sm_mhz": 2070.0, "sm_max_mhz": 2070, "samples": 900,
+              "reasons": ["sw_power_cap"]}
+    return bench.compact_line(
+        world=8, steps=500, warmup=10, value=56000.123456789, ms_per_step=0.17212345678,
+        variant="staged_y", roofline=roofline, per=per, e2e=e2e, cpu=cpu, parity=True,
+        lat=lat, launches=1000, clocks=clocks, peak=6785.9,
+        step_traffic=1141000000)
+
+
+def test_result_line_is_last_short_and_parses():
+    """The driver reads the benchmark's result from the end of its log: the
+    result line must come last, parse alone and stay under 1000 characters,
+    with the contract keys and the roofline in it; the side studies go to an
+    earlier line."""
+    import json
+    import bench
+    line = _worst_case_line(bench)
+    studies = {"allreduce_sweep": [{"bytes_per_rank": 4096 << (2 * i), "us": 1.5 * i}
+                                   for i in range(9)] * 50}
+    buf = io.StringIO()
+    with redirect_stdout(buf):
+        bench.emit(line, studies)
+    out = buf.getvalue().splitlines()
+    assert len(out) == 2 and len(out[0]) > 1000
+    last = out[-1]
+    assert len(last) < 1000, len(last)
+    got = json.loads(last)
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "roofline", "e2e", "cpu_baseline", "gpu_launches", "clocks",
+                "parity_vs_oracle", "allreduce_4KiB_us", "step_dram_frac"):
+        assert key in got, key
+    assert got["config"]["workload"]
+    rf = got["roofline"]
+    assert rf["bound"] == "hbm" and rf["unit"] == "GB/s"
+    assert rf["frac"] == pytest.approx(rf["achieved"] / rf["peak"], rel=1e-3)
+    # DRAM bytes over the same duration: 551648256 B / 97.12 us / 6785.9 GB/s
+    assert rf["dram_frac"] == pytest.approx(551648256 / 97.12345678e-6 / 1e9 / 6785.9, rel=1e-3)
+    assert got["step_dram_frac"] == pytest.approx(1141000000 / 0.17212345678e-3 / 1e9 / 6785.9,
+                                                  rel=1e-3)
+    for key in ("value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step"):
+        assert key in got["e2e"]
+    for key in ("value", "unit", "cores", "kind", "sample"):
+        assert key in got["cpu_baseline"]
+    assert json.loads(out[0])["studies"] == studies
+
+
+def test_studies_can_go_to_a_file(tmp_path):
+    import json
+    import bench
+    line = _worst_case_line(bench)
+    path = tmp_path / "studies.json"
+    buf = io.StringIO()
+    with redirect_stdout(buf):
+        bench.emit(line, {"cta_study": [1, 2, 3]}, str(path))
+    out = buf.getvalue().splitlines()
+    assert len(out) == 1 and json.loads(out[0])["metric"] == bench.METRIC
+    assert json.loads(path.read_text()) == {"cta_study": [1, 2, 3]}
+
+
+def test_reference_line_is_short_and_shares_the_config():
+    """Both arms name one workload configuration, and the reference line is
+    short as well."""
+    import bench
+    ours = bench.bench_config(1)
+    assert ours["workload"] == bench.WORKLOAD_SHORT
+    assert len(json.dumps(bench.bench_config(8))) < 200
