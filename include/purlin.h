@@ -253,7 +253,9 @@ PURLIN_API purlin_status_t purlin_all_to_all_v(purlin_handle_t h, const void* co
  *                and not reported).
  *   stream       runs on the current device, on this stream.
  * The first call on a device looks up the static array's device address (with
- * that device current); make that first call before any stream capture.  Every
+ * that device current); make that first call before any stream capture.  If
+ * the lookup fails the call returns PURLIN_ERR_CUDA having enqueued nothing,
+ * and the next call on that device tries the lookup again.  Every
  * call on a device shares the one array: calls whose kernels overlap on the GPU
  * (e.g. on two streams at once) race and produce wrong results; serialize them.
  * Flags hold per-call epoch tags and the status word is cleared at each call, so

@@ -43,22 +43,35 @@ static_assert(kFlagsOffset + kFlagWords * sizeof(uint64_t) <= kStagingOffset, "l
 static __device__ __align__(256) char g_noalloc_scratch[kScratchBytes];
 
 struct DeviceScratch {
-    std::once_flag once;
-    cudaError_t setup_error = cudaSuccess;
+    std::mutex lock;
+    bool ready = false;     // set once a lookup has succeeded; a failed one is retried
     char* base = nullptr;   // device address of g_noalloc_scratch on this device
     int sms = 0;
 };
 
 DeviceScratch g_devices[kMaxDevices];
 
-void set_up(DeviceScratch& d, int device)
+// Look up the array's device address on the current device, once it succeeds.
+// A failure (e.g. a first call made while a stream is being captured, where
+// the lookup may be refused) is not remembered: the next call tries again.
+bool set_up(DeviceScratch& d, int device)
 {
+    std::lock_guard<std::mutex> g(d.lock);
+    if (d.ready) return true;
     void* ptr = nullptr;
-    cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
-    if (e == cudaSuccess)
-        e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, device);
+    int sms = 0;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) {
+        (void)cudaGetLastError();   // do not leave the failure for the caller's next check
+        return false;
+    }
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return false;
+    }
     d.base = static_cast<char*>(ptr);
-    d.setup_error = e;
+    d.sms = sms;
+    d.ready = true;
+    return true;
 }
 
 bool overlaps(uint64_t a, uint64_t alen, uint64_t b, uint64_t blen)
@@ -104,8 +117,7 @@ extern "C" PURLIN_API purlin_status_t purlin_all_reduce_noalloc(
     if (cudaGetDevice(&device) != cudaSuccess) return PURLIN_ERR_CUDA;
     if (device < 0 || device >= kMaxDevices) return PURLIN_ERR_UNSUPPORTED;
     DeviceScratch& d = g_devices[device];
-    std::call_once(d.once, [&d, device] { set_up(d, device); });
-    if (d.setup_error != cudaSuccess || !d.base) return PURLIN_ERR_CUDA;
+    if (!set_up(d, device)) return PURLIN_ERR_CUDA;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     int* status = device_status ? device_status

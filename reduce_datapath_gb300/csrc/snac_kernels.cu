@@ -515,6 +515,7 @@ __device__ void producer_dynamic(const SnacParams& p, uint32_t ch, uint64_t epoc
         const Segment& s = step_segment(p, (uint32_t)i);
         const uint64_t off = (uint64_t)((uint32_t)i - s.tile0) * p.chunk;
         const uint64_t len = min(p.chunk, s.bytes - off);
+        bool staged = false;
         if constexpr (SHIFTED) {
             if (s.shift) {
                 // realigned to the destinations' grid while staged
@@ -529,19 +530,19 @@ __device__ void producer_dynamic(const SnacParams& p, uint32_t ch, uint64_t epoc
                     cta_copy_shifted_any(s.unit_log2, p.in[s.src] + s.src_off + off, slot_p, len,
                                          lpol, spol);
                 }
-                if (threadIdx.x == 0) st_relaxed(f + kStepOf, i);
-                cta_notify(f + kReady, tag_of(epoch, n));
-                continue;
+                staged = true;
             }
         }
-        if (KIND == kRSY || KIND == kARY) {
-            cta_reduce_src<T, ORDER>(p, s.unit_log2, slot_data(p, ch, slot), s.src_off + off, len,
-                                     lpol, spol);
-        } else if (KIND == kRS || KIND == kAR) {
-            cta_stage_any(p, s.unit_log2, slot_data(p, ch, slot), s.src_off + off, len, lpol);
-        } else {
-            cta_copy_any<false, false>(p, s.unit_log2, slot_data(p, ch, slot), 0,
-                                       p.in[s.src] + s.src_off + off, len, 0, lpol, spol);
+        if (!staged) {
+            if (KIND == kRSY || KIND == kARY) {
+                cta_reduce_src<T, ORDER>(p, s.unit_log2, slot_data(p, ch, slot), s.src_off + off,
+                                         len, lpol, spol);
+            } else if (KIND == kRS || KIND == kAR) {
+                cta_stage_any(p, s.unit_log2, slot_data(p, ch, slot), s.src_off + off, len, lpol);
+            } else {
+                cta_copy_any<false, false>(p, s.unit_log2, slot_data(p, ch, slot), 0,
+                                           p.in[s.src] + s.src_off + off, len, 0, lpol, spol);
+            }
         }
         if (threadIdx.x == 0) st_relaxed(f + kStepOf, i);
         if (p.inject && ch == 0 && n == 0) continue;  // testing: this notify never happens

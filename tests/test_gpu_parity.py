@@ -592,7 +592,7 @@ def test_launch_shape_follows_message_size(coll, nbytes, small, R):
 
 # ------------------------------------------------------------ shifted bodies
 
-@pytest.mark.parametrize("policy", ["zs", "zs_large", "zs_small"])
+@pytest.mark.parametrize("policy", ["zs", "zs_large", "zs_small", "snac_default", "snac_tiny_chunks", "snac_deep", "snac_y_default", "snac_y_tiny_chunks"])
 @pytest.mark.parametrize("dtype", ["bf16", "f32", "f16"])
 @pytest.mark.parametrize("R", [2, 3, 5, 8])
 def test_reduce_scatter_shifted_partitions(policy, dtype, R):
@@ -612,7 +612,7 @@ def test_reduce_scatter_shifted_partitions(policy, dtype, R):
         assert outs[k].guards_intact()
 
 
-@pytest.mark.parametrize("policy", ["zs", "zs_large", "zs_small"])
+@pytest.mark.parametrize("policy", ["zs", "zs_large", "zs_small", "snac_default", "snac_tiny_chunks", "snac_deep", "snac_y_default", "snac_y_tiny_chunks"])
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 @pytest.mark.parametrize("R", [2, 4, 8])
 @pytest.mark.parametrize("offset", [1, 3, 6])
@@ -631,7 +631,7 @@ def test_all_reduce_shifted_outputs(policy, dtype, R, offset):
         assert outs[j].guards_intact()
 
 
-@pytest.mark.parametrize("policy", ["zs", "zs_large", "zs_small", "zs_pull"])
+@pytest.mark.parametrize("policy", ["zs", "zs_large", "zs_small", "zs_pull", "snac_default", "snac_tiny_chunks", "snac_deep", "snac_y_default", "snac_y_tiny_chunks"])
 @pytest.mark.parametrize("R", [2, 3, 8])
 @pytest.mark.parametrize("dtype", ["bf16", "u8"])
 def test_all_gather_shifted_blocks(policy, R, dtype):
@@ -651,7 +651,7 @@ def test_all_gather_shifted_blocks(policy, R, dtype):
         assert outs[j].guards_intact()
 
 
-@pytest.mark.parametrize("policy", ["zs", "zs_large", "zs_small"])
+@pytest.mark.parametrize("policy", ["zs", "zs_large", "zs_small", "snac_default", "snac_tiny_chunks", "snac_deep", "snac_y_default", "snac_y_tiny_chunks"])
 @pytest.mark.parametrize("R", [3, 8])
 def test_all_to_all_v_shifted_blocks(policy, R):
     """Per-pair counts that are not multiples of 16 bytes: send and receive
@@ -670,7 +670,7 @@ def test_all_to_all_v_shifted_blocks(policy, R):
         assert outs[j].guards_intact()
 
 
-@pytest.mark.parametrize("policy", ["zs", "zs_large", "zs_small"])
+@pytest.mark.parametrize("policy", ["zs", "zs_large", "zs_small", "snac_default", "snac_tiny_chunks", "snac_deep", "snac_y_default", "snac_y_tiny_chunks"])
 @pytest.mark.parametrize("dtype", ["bf16", "f32", "f16"])
 @pytest.mark.parametrize("R", [2, 3, 5, 8])
 @pytest.mark.parametrize("coll", ["reduce_scatter", "all_reduce"])
