@@ -72,6 +72,9 @@ def parse_args():
                     help="with --only: input bytes per rank")
     ap.add_argument("--atom", choices=["auto", "vector", "bulk", "copy_engine"], default="auto",
                     help="with --only: copy Atom of the zero-staging path")
+    ap.add_argument("--trim", type=int, default=0,
+                    help="with --only: elements taken off every partition (rs, ag) or every "
+                         "non-empty block (a2av), which puts partitions off the vector grid")
     return ap.parse_args()
 
 
@@ -1359,7 +1362,7 @@ def bench_only(args):
     rd.build()
     R = args.ranks
     n = args.bytes_per_rank // 2
-    c = n // R
+    c = n // R - args.trim
     h = rd.purlin_create(R, args.staging, 0)
     variant = {"zs": rd.VARIANT_ZS, "staged": rd.VARIANT_STAGED,
                "staged_y": rd.VARIANT_STAGED_Y}[args.variant]
@@ -1386,11 +1389,12 @@ def bench_only(args):
         H = workloads.HIDDEN
         T = max(1, n // H)
         C = workloads.zipf_pair_counts(R, T, workloads.ZIPF_S, workloads.seed_for("moe_a2av_r8", 9))
+        E = C * H
+        E[E > 0] -= args.trim
         x = workloads.rank_buffers("moe_a2av_r8", R, T * H, "bf16", device=dev)
-        o = [torch.empty(int(C[:, j].sum()) * H, dtype=torch.bfloat16, device=dev)
-             for j in range(R)]
-        fn = lambda: rd.purlin_all_to_all_v(h, x, o, C * H, None, None, "bf16", stream=stream)
-        nbytes = 2 * int(C.sum()) * H * 2
+        o = [torch.empty(int(E[:, j].sum()), dtype=torch.bfloat16, device=dev) for j in range(R)]
+        fn = lambda: rd.purlin_all_to_all_v(h, x, o, E, None, None, "bf16", stream=stream)
+        nbytes = 2 * int(E.sum()) * 2
     with torch.cuda.stream(stream):
         for _ in range(max(1, args.warmup)):
             fn()
@@ -1408,7 +1412,7 @@ def bench_only(args):
     rd.purlin_destroy(h)
     us = a.elapsed_time(b) * 1e3 / K
     print(json.dumps({"only": args.only, "variant": args.variant, "R": R,
-                      "bytes_per_rank": args.bytes_per_rank, "us": us,
+                      "bytes_per_rank": args.bytes_per_rank, "trim": args.trim, "us": us,
                       "gbs": nbytes / (us / 1e6) / 1e9, "algorithmic_bytes": nbytes,
                       "launch": info}), flush=True)
 

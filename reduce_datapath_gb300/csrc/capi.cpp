@@ -196,14 +196,16 @@ struct ZsKnobs {
 //    next.  In that pair the AllGather's reads then hit L2 and DRAM sees
 //    almost only its writes: AllGather 104.3 -> 90.2 us, ReduceScatter
 //    108.8 -> 98.5 us, the pair 5599 -> 6332 GB/s.
-ZsKnobs zs_knobs(const purlin_handle* h, Coll coll)
+// bulk: the plan is for the TMA bulk Atom (copies only).
+ZsKnobs zs_knobs(const purlin_handle* h, Coll coll, bool bulk)
 {
     ZsKnobs k;
     const bool reduce = coll == Coll::ReduceScatter || coll == Coll::AllReduce;
+    bulk = bulk && !reduce;
     k.tile_units = reduce ? kThreads * reduce_unroll(h->R, h->order)
-                          : (h->atom == PURLIN_ATOM_BULK ? kTileUnitsBulk : kTileUnitsCopy);
+                          : (bulk ? kTileUnitsBulk : kTileUnitsCopy);
     k.max_unit_log2 = h->max_unit_log2 ? h->max_unit_log2 : 5;
-    k.allow_shift = reduce ? h->order == 0 : h->atom != PURLIN_ATOM_BULK;
+    k.allow_shift = !bulk;
     k.l2_load = h->l2_load >= 0 ? (uint32_t)h->l2_load : kL2EvictFirst;
     k.l2_store = h->l2_store >= 0 ? (uint32_t)h->l2_store
                                   : (coll == Coll::ReduceScatter ? kL2Normal : kL2EvictFirst);
@@ -359,6 +361,19 @@ bool outputs_share_grid(const uint64_t* out, int R)
     return true;
 }
 
+// Whether a copy's plan on the vector kernels holds a shifted body.
+bool needs_shift(const Piece* pieces, int np, int R, const uint64_t* in, const uint64_t* out,
+                 size_t esz, const ZsKnobs& knobs)
+{
+    Segment segs[kSegsLarge];
+    uint32_t ntiles = 0;
+    const int n = layout_segments(pieces, np, R, in, out, esz, false, kTileUnitsCopy,
+                                  knobs.max_unit_log2, true, segs, kSegsLarge, &ntiles);
+    for (int i = 0; i < n; ++i)
+        if (segs[i].shift) return true;
+    return false;
+}
+
 bool wants_staged(const purlin_handle* h)
 {
     return h->variant == PURLIN_VARIANT_STAGED || h->variant == PURLIN_VARIANT_STAGED_Y;
@@ -510,8 +525,9 @@ purlin_status_t plan_all_reduce_split(const Call& c, const ZsKnobs& knobs, Launc
     if (st != PURLIN_OK) return st;
     const bool small = replan_small(h, c.coll, p, &sum, 1, R, c.in, c.out, c.esz, true, ks);
     const int sh = has_shift(p);
-    const int grid = zs_grid(h, p.ntiles, zs_reduce_resident_ctas(c.dtype, 0, false, small, R, sh));
-    zs_reduce_select(L.k, c.dtype, 0, false, small, R, sh);
+    const int grid =
+        zs_grid(h, p.ntiles, zs_reduce_resident_ctas(c.dtype, h->order, false, small, R, sh));
+    zs_reduce_select(L.k, c.dtype, h->order, false, small, R, sh);
     L.k.grid = (unsigned)grid;
     L.k.pdl = p.pdl != 0;
 
@@ -524,7 +540,7 @@ purlin_status_t plan_all_reduce_split(const Call& c, const ZsKnobs& knobs, Launc
         if (c.out[j] == c.out[0]) continue;
         copies[nc++] = Piece{sum.dst_off, sum.dst_off, sum.bytes, 0, (uint8_t)j};
     }
-    ZsKnobs kc = zs_knobs(h, Coll::AllToAllV);
+    ZsKnobs kc = zs_knobs(h, Coll::AllToAllV, false);  // vector copies
     st = make_params(p2, copies, nc, R, from, c.out, c.esz, false, kc, h->status);
     if (st != PURLIN_OK) return st;
     const bool small2 = replan_small(h, Coll::AllToAllV, p2, copies, nc, R, from, c.out, c.esz,
@@ -683,8 +699,12 @@ purlin_status_t run(purlin_handle_t h, Coll coll, const void* const in_[], void*
         st = plan_staged(c, L);
     } else {
         info.variant = PURLIN_VARIANT_ZS;
-        const ZsKnobs knobs = zs_knobs(h, coll);
-        const bool bulk = !reduce && h->atom == PURLIN_ATOM_BULK;
+        // The TMA bulk Atom copies 16-byte aligned streams; a layout whose
+        // sources and destinations sit on different alignments goes to the
+        // vector kernels, whose shifted bodies realign it in registers.
+        const bool bulk = !reduce && h->atom == PURLIN_ATOM_BULK &&
+                          !needs_shift(pieces, np, R, in, out, esz, zs_knobs(h, coll, false));
+        const ZsKnobs knobs = zs_knobs(h, coll, bulk);
         const bool by_destination =
             coll == Coll::AllToAllV ||
             (coll == Coll::AllGather &&
@@ -694,8 +714,7 @@ purlin_status_t run(purlin_handle_t h, Coll coll, const void* const in_[], void*
             plan_copy_engine(c, L);
         else if (by_destination)
             st = plan_by_destination(c, knobs, bulk, L);
-        else if (coll == Coll::AllReduce && np == 1 && R > 1 && h->order == 0 &&
-                 !outputs_share_grid(out, R))
+        else if (coll == Coll::AllReduce && np == 1 && R > 1 && !outputs_share_grid(out, R))
             st = plan_all_reduce_split(c, knobs, L);
         else
             st = plan_zs(c, knobs, bulk, L);

@@ -82,6 +82,14 @@ size_t default_chunk(Coll coll, bool stage_y)
     }
 }
 
+// Widest unit of a launch: a sum launch holding a shifted body is planned
+// with 16-byte units throughout (plan_into), so its kernel carries no 32-byte
+// path (the shifted sums need the registers).
+__host__ __device__ constexpr int snac_max_unit(int kind, bool shifted)
+{
+    return (shifted && kind != kAG && kind != kA2A) ? 4 : 5;
+}
+
 constexpr int kDefaultDepth = 2;
 constexpr int kMaxChannels = 256;
 constexpr size_t kMinAutoChunk = 1024;
@@ -252,13 +260,18 @@ __device__ __forceinline__ void cta_copy(const SnacParams& p, char* dst, uint64_
     }
 }
 
-template <bool SRC_CG, bool FAN>
+// MAXU: the widest unit a launch's plan holds (5: 32 bytes; 4: 16 bytes, the
+// sums of launches that hold a shifted body), so that the kernels serving
+// those launches carry no 32-byte paths and keep their registers.
+template <bool SRC_CG, bool FAN, int MAXU = 5>
 __device__ void cta_copy_any(const SnacParams& p, int unit_log2, char* dst, uint64_t dst_off,
                              const char* src, uint64_t len, uintptr_t skip, uint64_t lpol,
                              uint64_t spol)
 {
     switch (unit_log2) {
-    case 5: cta_copy<32, SRC_CG, FAN>(p, dst, dst_off, src, len, skip, lpol, spol); break;
+    case 5:
+        if constexpr (MAXU >= 5) cta_copy<32, SRC_CG, FAN>(p, dst, dst_off, src, len, skip, lpol, spol);
+        break;
     case 4: cta_copy<16, SRC_CG, FAN>(p, dst, dst_off, src, len, skip, lpol, spol); break;
     case 3: cta_copy<8, SRC_CG, FAN>(p, dst, dst_off, src, len, skip, lpol, spol); break;
     case 2: cta_copy<4, SRC_CG, FAN>(p, dst, dst_off, src, len, skip, lpol, spol); break;
@@ -286,11 +299,14 @@ __device__ __forceinline__ void cta_stage_ranks(const SnacParams& p, char* stage
     }
 }
 
+template <int MAXU = 5>
 __device__ void cta_stage_any(const SnacParams& p, int unit_log2, char* staged, uint64_t src_off,
                               uint64_t len, uint64_t lpol)
 {
     switch (unit_log2) {
-    case 5: cta_stage_ranks<32>(p, staged, src_off, len, lpol); break;
+    case 5:
+        if constexpr (MAXU >= 5) cta_stage_ranks<32>(p, staged, src_off, len, lpol);
+        break;
     case 4: cta_stage_ranks<16>(p, staged, src_off, len, lpol); break;
     case 3: cta_stage_ranks<8>(p, staged, src_off, len, lpol); break;
     case 2: cta_stage_ranks<4>(p, staged, src_off, len, lpol); break;
@@ -329,11 +345,13 @@ __device__ __forceinline__ void cta_reduce_elem(const SnacParams& p, char* dst, 
     }
 }
 
-template <typename T, int ORDER>
+template <typename T, int ORDER, int MAXU = 5>
 __device__ void cta_reduce(const SnacParams& p, int unit_log2, char* dst, const char* staged,
                            uint64_t len, uint64_t spol)
 {
-    if (unit_log2 == 5) cta_reduce_vec<T, ORDER, 32>(p, dst, staged, len, spol);
+    if (unit_log2 == 5) {
+        if constexpr (MAXU >= 5) cta_reduce_vec<T, ORDER, 32>(p, dst, staged, len, spol);
+    }
     else if (unit_log2 == 4) cta_reduce_vec<T, ORDER, 16>(p, dst, staged, len, spol);
     else cta_reduce_elem<T, ORDER>(p, dst, staged, len);
 }
@@ -370,11 +388,13 @@ __device__ __forceinline__ void cta_reduce_src_elem(const SnacParams& p, char* d
     }
 }
 
-template <typename T, int ORDER>
+template <typename T, int ORDER, int MAXU = 5>
 __device__ void cta_reduce_src(const SnacParams& p, int unit_log2, char* dst, uint64_t src_off,
                                uint64_t len, uint64_t lpol, uint64_t spol)
 {
-    if (unit_log2 == 5) cta_reduce_src_vec<T, ORDER, 32>(p, dst, src_off, len, lpol, spol);
+    if (unit_log2 == 5) {
+        if constexpr (MAXU >= 5) cta_reduce_src_vec<T, ORDER, 32>(p, dst, src_off, len, lpol, spol);
+    }
     else if (unit_log2 == 4) cta_reduce_src_vec<T, ORDER, 16>(p, dst, src_off, len, lpol, spol);
     else cta_reduce_src_elem<T, ORDER>(p, dst, src_off, len);
 }
@@ -388,34 +408,46 @@ __device__ void cta_reduce_src(const SnacParams& p, int unit_log2, char* dst, ui
 // segment's last one, which holds its last bytes): within the segment.  A
 // shifted step is a whole number of units.
 
-// Copy a step's len bytes from src (any offset) to dst (unit-aligned).
+// Copy a step's len bytes from src (any offset) to dst (unit-aligned).  The
+// step's word offset is fixed at compile time (one branch per step), so a unit
+// is realigned with one shuffle per word it needs from the next lane and one
+// funnel shift per word; each thread has two units in flight.
 template <int B>
 __device__ void cta_copy_shifted(const char* src, char* dst, uint64_t len, uint64_t lpol,
                                  uint64_t spol)
 {
     constexpr int W = B / 4;
     constexpr int WARPS = kThreads / 32;
+    constexpr int U = 2;
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int shift = (int)(reinterpret_cast<uintptr_t>(src) & (B - 1));
     const uint64_t n = len / B;
     const uint64_t nblocks = shift ? n + 1 : n;
-    for (uint64_t row = 0; row < n; row += (uint64_t)WARPS * 31) {
-        const uint64_t q = row + (uint64_t)warp * 31 + lane;
-        atom::Vec<B> v, next, out;
-        if (q < nblocks) {
-            atom::load(v, at(src, q * B, shift), lpol);
-        } else {
+    const uint32_t bits = (uint32_t)(shift & 3) * 8;
+    with_word_offset<W>(shift >> 2, [&](auto A) {
+        for (uint64_t row = 0; row < n; row += (uint64_t)WARPS * 31 * U) {
+            atom::Vec<B> v[U];
 #pragma unroll
-            for (int i = 0; i < W; ++i) v.w[i] = 0u;
+            for (int k = 0; k < U; ++k) {
+                const uint64_t q = row + (uint64_t)(k * WARPS + warp) * 31 + lane;
+                if (q < nblocks) {
+                    atom::load(v[k], at(src, q * B, shift), lpol);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < W; ++i) v[k].w[i] = 0u;
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < U; ++k) {
+                const uint64_t q = row + (uint64_t)(k * WARPS + warp) * 31 + lane;
+                atom::Vec<B> out;
+                realign_from_next<W, decltype(A)::value>(v[k].w, bits, out.w);
+                if (lane == 31 || q >= n) continue;
+                atom::store(dst + q * B, out, spol);
+            }
         }
-#pragma unroll
-        for (int i = 0; i < W; ++i) next.w[i] = __shfl_down_sync(0xffffffffu, v.w[i], 1);
-        if (lane == 31 || q >= n) continue;
-        if (shift) realign<W>(v.w, next.w, shift, out.w);
-        else out = v;
-        atom::store(dst + q * B, out, spol);
-    }
+    });
 }
 
 __device__ void cta_copy_shifted_any(int unit_log2, const char* src, char* dst, uint64_t len,
@@ -425,11 +457,13 @@ __device__ void cta_copy_shifted_any(int unit_log2, const char* src, char* dst, 
     else cta_copy_shifted<16>(src, dst, len, lpol, spol);
 }
 
-// Fold a step of the R sources into dst (unit-aligned), each rank realigned on
-// its own offset before the fold (16-byte units: a shifted sum's width).
-template <typename T, int ORDER>
-__device__ void cta_reduce_src_shifted(const SnacParams& p, char* dst, uint64_t src_off,
-                                       uint64_t len, uint64_t lpol, uint64_t spol)
+// STAGE of a shifted step of a sum with the inputs staged: every rank's chunk
+// realigned into its part of the slot (16-byte units, a shifted sum's width),
+// the R ranks' blocks of a unit loaded before the first store.  Sources on one
+// offset realign with the word offset fixed at compile time; sources on
+// different offsets each on their own.
+__device__ void cta_stage_ranks_shifted(const SnacParams& p, const Segment& s, char* staged,
+                                        uint64_t src_off, uint64_t len, uint64_t lpol)
 {
     constexpr int B = 16;
     constexpr int W = B / 4;
@@ -438,6 +472,114 @@ __device__ void cta_reduce_src_shifted(const SnacParams& p, char* dst, uint64_t 
     const int warp = threadIdx.x >> 5;
     const int R = (int)p.R;
     const uint64_t n = len / B;
+    if (!(s.shift & kShiftPerRank)) {
+        const int shift = (int)((reinterpret_cast<uintptr_t>(p.in[0]) + src_off) & (B - 1));
+        const uint32_t bits = (uint32_t)(shift & 3) * 8;
+        with_word_offset<W>(shift >> 2, [&](auto A) {
+            for (uint64_t row = 0; row < n; row += (uint64_t)WARPS * 31) {
+                const uint64_t q = row + (uint64_t)warp * 31 + lane;
+                atom::Vec<B> v[kMaxRanks];
+#pragma unroll
+                for (int r = 0; r < kMaxRanks; ++r) {
+                    if (r < R && q < n + 1) {
+                        atom::load(v[r], at(p.in[r], src_off + q * B, shift), lpol);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < W; ++i) v[r].w[i] = 0u;
+                    }
+                }
+#pragma unroll
+                for (int r = 0; r < kMaxRanks; ++r) {
+                    if (r >= R) continue;
+                    atom::Vec<B> out;
+                    realign_from_next<W, decltype(A)::value>(v[r].w, bits, out.w);
+                    if (lane != 31 && q < n) atom::store(staged + r * p.chunk + q * B, out);
+                }
+            }
+        });
+        return;
+    }
+    int sh[kMaxRanks];
+#pragma unroll
+    for (int r = 0; r < kMaxRanks; ++r)
+        sh[r] = r < R ? (int)((reinterpret_cast<uintptr_t>(p.in[r]) + src_off) & (B - 1)) : 0;
+    for (uint64_t row = 0; row < n; row += (uint64_t)WARPS * 31) {
+        const uint64_t q = row + (uint64_t)warp * 31 + lane;
+        atom::Vec<B> v[kMaxRanks];
+#pragma unroll
+        for (int r = 0; r < kMaxRanks; ++r) {
+            if (r < R && q < (sh[r] ? n + 1 : n)) {
+                atom::load(v[r], at(p.in[r], src_off + q * B, sh[r]), lpol);
+            } else {
+#pragma unroll
+                for (int i = 0; i < W; ++i) v[r].w[i] = 0u;
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < kMaxRanks; ++r) {
+            if (r >= R) continue;
+            atom::Vec<B> next, out;
+#pragma unroll
+            for (int i = 0; i < W; ++i) next.w[i] = __shfl_down_sync(0xffffffffu, v[r].w[i], 1);
+            if (sh[r]) realign<W>(v[r].w, next.w, sh[r], out.w);
+            else out = v[r];
+            if (lane != 31 && q < n) atom::store(staged + r * p.chunk + q * B, out);
+        }
+    }
+}
+
+// Fold a step of the R sources into dst (unit-aligned; 16-byte units, a
+// shifted sum's width).  Sources on one offset: the R ranks' aligned blocks
+// are folded first (the offset is a multiple of the element size, so a block
+// holds whole elements of every rank at the same positions) and the sum is
+// realigned once, with the word offset fixed at compile time; two units per
+// thread in flight.  Sources on different offsets: each rank's block is
+// realigned on its own offset before the fold.
+template <typename T, int ORDER>
+__device__ void cta_reduce_src_shifted(const SnacParams& p, const Segment& s, char* dst,
+                                       uint64_t src_off, uint64_t len, uint64_t lpol, uint64_t spol)
+{
+    constexpr int B = 16;
+    constexpr int W = B / 4;
+    constexpr int WARPS = kThreads / 32;
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int R = (int)p.R;
+    const uint64_t n = len / B;
+    if (!(s.shift & kShiftPerRank)) {
+        constexpr int U = 1;
+        const int shift = (int)((reinterpret_cast<uintptr_t>(p.in[0]) + src_off) & (B - 1));
+        const uint32_t bits = (uint32_t)(shift & 3) * 8;
+        with_word_offset<W>(shift >> 2, [&](auto A) {
+            for (uint64_t row = 0; row < n; row += (uint64_t)WARPS * 31 * U) {
+                atom::Vec<B> y[U];
+#pragma unroll
+                for (int k = 0; k < U; ++k) {
+                    const uint64_t q = row + (uint64_t)(k * WARPS + warp) * 31 + lane;
+                    atom::Vec<B> v[kMaxRanks];
+#pragma unroll
+                    for (int r = 0; r < kMaxRanks; ++r) {
+                        if (r < R && q < n + 1) {
+                            atom::load(v[r], at(p.in[r], src_off + q * B, shift), lpol);
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < W; ++i) v[r].w[i] = 0u;
+                        }
+                    }
+                    atom::reduce_unit<T, ORDER, B>(v, R, y[k]);
+                }
+#pragma unroll
+                for (int k = 0; k < U; ++k) {
+                    const uint64_t q = row + (uint64_t)(k * WARPS + warp) * 31 + lane;
+                    atom::Vec<B> out;
+                    realign_from_next<W, decltype(A)::value>(y[k].w, bits, out.w);
+                    if (lane == 31 || q >= n) continue;
+                    atom::store(dst + q * B, out, spol);
+                }
+            }
+        });
+        return;
+    }
     int sh[kMaxRanks];
 #pragma unroll
     for (int r = 0; r < kMaxRanks; ++r)
@@ -491,6 +633,7 @@ __device__ __forceinline__ void st_relaxed(uint64_t* w, uint64_t v)
 template <typename T, int ORDER, int KIND, bool SHIFTED>
 __device__ void producer_dynamic(const SnacParams& p, uint32_t ch, uint64_t epoch)
 {
+    constexpr int MAXU = snac_max_unit(KIND, SHIFTED);
     __shared__ uint64_t step_s;
     const uint64_t lpol = atom::l2_policy(kL2EvictFirst);
     const uint64_t spol = atom::l2_policy(kL2Normal);
@@ -521,11 +664,10 @@ __device__ void producer_dynamic(const SnacParams& p, uint32_t ch, uint64_t epoc
                 // realigned to the destinations' grid while staged
                 char* slot_p = slot_data(p, ch, slot);
                 if (KIND == kRSY || KIND == kARY) {
-                    cta_reduce_src_shifted<T, ORDER>(p, slot_p, s.src_off + off, len, lpol, spol);
+                    cta_reduce_src_shifted<T, ORDER>(p, s, slot_p, s.src_off + off, len, lpol,
+                                                     spol);
                 } else if (KIND == kRS || KIND == kAR) {
-                    for (int r = 0; r < (int)p.R; ++r)
-                        cta_copy_shifted_any(s.unit_log2, p.in[r] + s.src_off + off,
-                                             slot_p + (uint64_t)r * p.chunk, len, lpol, spol);
+                    cta_stage_ranks_shifted(p, s, slot_p, s.src_off + off, len, lpol);
                 } else {
                     cta_copy_shifted_any(s.unit_log2, p.in[s.src] + s.src_off + off, slot_p, len,
                                          lpol, spol);
@@ -535,10 +677,11 @@ __device__ void producer_dynamic(const SnacParams& p, uint32_t ch, uint64_t epoc
         }
         if (!staged) {
             if (KIND == kRSY || KIND == kARY) {
-                cta_reduce_src<T, ORDER>(p, s.unit_log2, slot_data(p, ch, slot), s.src_off + off,
+                cta_reduce_src<T, ORDER, MAXU>(p, s.unit_log2, slot_data(p, ch, slot), s.src_off + off,
                                          len, lpol, spol);
             } else if (KIND == kRS || KIND == kAR) {
-                cta_stage_any(p, s.unit_log2, slot_data(p, ch, slot), s.src_off + off, len, lpol);
+                cta_stage_any<MAXU>(p, s.unit_log2, slot_data(p, ch, slot), s.src_off + off, len,
+                                    lpol);
             } else {
                 cta_copy_any<false, false>(p, s.unit_log2, slot_data(p, ch, slot), 0,
                                            p.in[s.src] + s.src_off + off, len, 0, lpol, spol);
@@ -550,7 +693,7 @@ __device__ void producer_dynamic(const SnacParams& p, uint32_t ch, uint64_t epoc
     }
 }
 
-template <typename T, int ORDER, int KIND>
+template <typename T, int ORDER, int KIND, int MAXU>
 __device__ void consumer_dynamic(const SnacParams& p, uint32_t ch, uint64_t epoch)
 {
     __shared__ uint64_t step_s;
@@ -574,18 +717,18 @@ __device__ void consumer_dynamic(const SnacParams& p, uint32_t ch, uint64_t epoc
         const uint64_t len = min(p.chunk, s.bytes - off);
         const char* staged = slot_data(p, ch, slot);
         if (KIND == kRS) {
-            cta_reduce<T, ORDER>(p, s.unit_log2, p.out[s.dst] + s.dst_off + off, staged, len,
+            cta_reduce<T, ORDER, MAXU>(p, s.unit_log2, p.out[s.dst] + s.dst_off + off, staged, len,
                                  spol);
         } else if (KIND == kARY) {
             // In-place AllReduce (out[r] == in[r]): this step's input range was
             // read by the producer before the ready tag was published.
-            cta_copy_any<true, true>(p, s.unit_log2, nullptr, s.dst_off + off, staged, len, 0,
-                                     lpol, spol);
+            cta_copy_any<true, true, MAXU>(p, s.unit_log2, nullptr, s.dst_off + off, staged, len,
+                                           0, lpol, spol);
         } else if (KIND == kAG) {
-            cta_copy_any<true, true>(p, s.unit_log2, nullptr, s.dst_off + off, staged, len,
+            cta_copy_any<true, true, MAXU>(p, s.unit_log2, nullptr, s.dst_off + off, staged, len,
                                      (uintptr_t)(p.in[s.src] + s.src_off + off), lpol, spol);
         } else {
-            cta_copy_any<true, false>(p, s.unit_log2, p.out[s.dst] + s.dst_off + off, 0, staged,
+            cta_copy_any<true, false, MAXU>(p, s.unit_log2, p.out[s.dst] + s.dst_off + off, 0, staged,
                                       len, 0, lpol, spol);
         }
         cta_notify(f + kFree, tag_of(epoch, n));
@@ -595,7 +738,7 @@ __device__ void consumer_dynamic(const SnacParams& p, uint32_t ch, uint64_t epoc
 // The three-role AllReduce (the R input chunks staged): the consumer sums them
 // into the slot's y part and records the step there; the gatherer copies y to
 // all R outputs.
-template <typename T, int ORDER>
+template <typename T, int ORDER, int MAXU>
 __device__ void consumer_ar(const SnacParams& p, uint32_t ch, uint64_t epoch)
 {
     __shared__ uint64_t step_s;
@@ -616,7 +759,7 @@ __device__ void consumer_ar(const SnacParams& p, uint32_t ch, uint64_t epoch)
             const uint64_t off = (uint64_t)((uint32_t)i - s.tile0) * p.chunk;
             const uint64_t len = min(p.chunk, s.bytes - off);
             char* staged = slot_data(p, ch, slot);
-            cta_reduce<T, ORDER>(p, s.unit_log2, staged + (uint64_t)p.R * p.chunk, staged, len,
+            cta_reduce<T, ORDER, MAXU>(p, s.unit_log2, staged + (uint64_t)p.R * p.chunk, staged, len,
                                  spol);
         }
         if (threadIdx.x == 0) st_relaxed(f + kYStepOf, i);  // kNoStep passes through
@@ -626,6 +769,7 @@ __device__ void consumer_ar(const SnacParams& p, uint32_t ch, uint64_t epoch)
     }
 }
 
+template <int MAXU>
 __device__ void gatherer(const SnacParams& p, uint32_t ch, uint64_t epoch)
 {
     __shared__ uint64_t step_s;
@@ -647,7 +791,8 @@ __device__ void gatherer(const SnacParams& p, uint32_t ch, uint64_t epoch)
         const char* y = slot_data(p, ch, slot) + (uint64_t)p.R * p.chunk;
         // In-place AllReduce writes out[r] == in[r]; this step's input range
         // was staged before the y tag was published, so the writes are safe.
-        cta_copy_any<true, true>(p, s.unit_log2, nullptr, s.dst_off + off, y, len, 0, lpol, spol);
+        cta_copy_any<true, true, MAXU>(p, s.unit_log2, nullptr, s.dst_off + off, y, len, 0, lpol,
+                                       spol);
         cta_notify(f + kYFree, tag_of(epoch, n));
     }
 }
@@ -664,15 +809,16 @@ __global__ void __launch_bounds__(kThreads, 2) snac_kernel(const __grid_constant
     }
     __syncthreads();
     const uint64_t epoch = epoch_s;
+    constexpr int MAXU = snac_max_unit(KIND, SHIFTED);
     const uint32_t role = blockIdx.x / p.nch;
     const uint32_t ch = blockIdx.x % p.nch;
     if (role == 0) {
         producer_dynamic<T, ORDER, KIND, SHIFTED>(p, ch, epoch);
     } else if constexpr (KIND == kAR) {
-        if (role == 1) consumer_ar<T, ORDER>(p, ch, epoch);
-        else gatherer(p, ch, epoch);
+        if (role == 1) consumer_ar<T, ORDER, MAXU>(p, ch, epoch);
+        else gatherer<MAXU>(p, ch, epoch);
     } else {
-        consumer_dynamic<T, ORDER, KIND>(p, ch, epoch);
+        consumer_dynamic<T, ORDER, KIND, MAXU>(p, ch, epoch);
     }
     // Whatever path a role left by (done, or an error seen), the last CTA to
     // get here publishes the epoch for the next call and resets the counter.
@@ -695,8 +841,7 @@ using SnacKernel = void (*)(SnacParams);
 template <typename T, int KIND, bool SH>
 SnacKernel pick_order(int order)
 {
-    // the pairwise order never has shifted bodies
-    return order == 0 ? snac_kernel<T, 0, KIND, SH> : snac_kernel<T, 1, KIND, false>;
+    return order == 0 ? snac_kernel<T, 0, KIND, SH> : snac_kernel<T, 1, KIND, SH>;
 }
 
 template <int KIND, bool SH>
@@ -794,15 +939,20 @@ purlin_status_t plan_into(KernelLaunch& k, const SnacRequest& rq, const SnacConf
     k.grid = 0;
     const bool reduce = rq.coll == Coll::ReduceScatter || rq.coll == Coll::AllReduce;
     uint32_t ntiles = 0;
-    // shifted bodies for the fixed rank order and for copies: the producer
-    // realigns them while staging
-    const bool allow_shift = !reduce || rq.order == 0;
+    // shifted bodies: the producer realigns them while staging
+    const bool allow_shift = true;
     int nseg = layout_segments(rq.pieces, rq.npieces, rq.R, rq.in, rq.out, rq.esz, reduce,
                                reduce ? kTileUnitsReduce : kTileUnitsCopy, snac_unit_log2(),
                                allow_shift, p.seg, kSegsLarge, &ntiles);
     if (nseg < 0) return PURLIN_ERR_UNSUPPORTED;
     bool shifted = false;
     for (int i = 0; i < nseg; ++i) shifted |= p.seg[i].shift != 0;
+    if (shifted && reduce && snac_unit_log2() > 4) {
+        // the kernels serving shifted sums take 16-byte vector bodies only
+        nseg = layout_segments(rq.pieces, rq.npieces, rq.R, rq.in, rq.out, rq.esz, reduce,
+                               kTileUnitsReduce, 4, allow_shift, p.seg, kSegsLarge, &ntiles);
+        if (nseg < 0) return PURLIN_ERR_UNSUPPORTED;
+    }
 
     SnacKernel kernel = kernel_for(rq.coll, rq.dtype, rq.order, rq.stage_y, shifted);
     const int resident = resident_ctas_of(reinterpret_cast<const void*>(kernel), kThreads);

@@ -14,16 +14,16 @@ namespace {
 using ReduceKernel = void (*)(ZsParams<kSegsSmall>);
 
 // NR = kMaxRanks / units per thread.  The pairwise rank order keeps one unit
-// per thread (NR = kMaxRanks) and has no shifted segments (SH: 0 none, 1 one
-// offset, 2 one per rank).
+// per thread (NR = kMaxRanks).  SH: 0 no shifted segment, 1 shifted segments
+// on one offset, 2 a sum whose ranks' sources sit on different offsets.
 template <typename T, int THREADS, int NR, int SH>
 ReduceKernel pick_reduce(int order, bool fan_all)
 {
     if (order == 0)
         return fan_all ? zs_reduce_kernel<T, 0, true, THREADS, NR, SH>
                        : zs_reduce_kernel<T, 0, false, THREADS, NR, SH>;
-    return fan_all ? zs_reduce_kernel<T, 1, true, THREADS, kMaxRanks, 0>
-                   : zs_reduce_kernel<T, 1, false, THREADS, kMaxRanks, 0>;
+    return fan_all ? zs_reduce_kernel<T, 1, true, THREADS, kMaxRanks, SH>
+                   : zs_reduce_kernel<T, 1, false, THREADS, kMaxRanks, SH>;
 }
 
 template <int THREADS, int NR, int SH>

@@ -356,6 +356,75 @@ def test_tree_order(policy, dtype, R):
             assert np.all(np.abs(g - f) <= ulp + reorder)
 
 
+@pytest.mark.parametrize("policy", ["zs", "zs_large", "zs_small", "snac_default", "snac_tiny_chunks",
+                                    "snac_y_default", "snac_y_tiny_chunks"])
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("R", [3, 5, 8])
+@pytest.mark.parametrize("layout", ["partitions_off_grid", "ranks_on_different_grids"])
+def test_tree_order_shifted_bodies(policy, dtype, R, layout):
+    """The pairwise order on layouts off the vector grid (shifted bodies):
+    partitions whose starts sit off the outputs' 16-byte grid, or ranks' inputs
+    r % 4 elements into their allocations.  Bit-exact to the oracle's pairwise
+    fold, for a ReduceScatter and an AllReduce."""
+    h = handle(R)
+    set_variant(h, *POLICIES[policy])
+    c = 5 * 1024 + 3
+    n = R * c
+    off = (lambda r: r % 4) if layout == "ranks_on_different_grids" else (lambda r: 0)
+    x = [inputs(1, n, dtype, seed=1200 + 7 * R + r, offset=off(r))[0] for r in range(R)]
+    xin = oracle_in(x)
+    rs_out = [Guarded(c, dtype) for _ in range(R)]
+    ar_out = [Guarded(n, dtype, offset=1) for _ in range(R)]
+    rd.purlin_set_reduce_order(h, rd.ORDER_TREE)
+    try:
+        rd.purlin_reduce_scatter(h, x, [o.view for o in rs_out], [c] * R, None, dtype)
+        rd.purlin_all_reduce(h, x, [o.view for o in ar_out], n, dtype)
+        run_ok(h)
+    finally:
+        rd.purlin_set_reduce_order(h, rd.ORDER_FIXED)
+    want = oracle.reduce_scatter(xin, [c] * R, dtype=dtype, order="tree")
+    whole = np.concatenate(want)
+    for k in range(R):
+        assert same_bits(host_bits(rs_out[k].view), want[k]), k
+        assert rs_out[k].guards_intact()
+    for j in range(R):
+        assert same_bits(host_bits(ar_out[j].view), whole), j
+        assert ar_out[j].guards_intact()
+
+
+@pytest.mark.parametrize("coll", ["all_gather", "all_to_all_v"])
+def test_bulk_atom_hands_off_grid_layouts_to_shifted_bodies(coll):
+    """Under the TMA bulk Atom a layout whose sources and destinations sit on
+    different 16-byte alignments runs on the vector kernels (shifted bodies,
+    256-thread CTAs); an aligned layout stays on the one-warp bulk CTAs."""
+    R = 4
+    h = handle(R)
+    # 256-thread CTAs at every size, so that the vector kernels are told apart
+    # from the one-warp bulk CTAs
+    set_variant(h, rd.VARIANT_ZS, 0, 0, 0, rd.ATOM_BULK, rd.DIRECTION_AUTO, rd.SMALL_TILES_NEVER)
+    try:
+        for counts, want_block in (([20000 + 13 * k + 3 for k in range(R)], 256),
+                                   ([16384] * R, 32)):
+            if coll == "all_gather":
+                x = [inputs(1, c, "bf16", seed=70 + k)[0] for k, c in enumerate(counts)]
+                outs = [Guarded(sum(counts), "bf16") for _ in range(R)]
+                rd.purlin_all_gather(h, x, [o.view for o in outs], counts, None, "bf16")
+                want = oracle.all_gather(oracle_in(x))
+            else:
+                C = np.array([[counts[(s + j) % R] // R for j in range(R)] for s in range(R)])
+                x = [inputs(1, int(C[s].sum()), "bf16", seed=80 + s)[0] for s in range(R)]
+                outs = [Guarded(int(C[:, j].sum()), "bf16") for j in range(R)]
+                rd.purlin_all_to_all_v(h, x, [o.view for o in outs], C, None, None, "bf16")
+                want = oracle.all_to_all_v(oracle_in(x), C)
+            run_ok(h)
+            assert rd.purlin_last_launch(h)["block"] == want_block
+            for j in range(R):
+                assert same_bits(host_bits(outs[j].view), want[j]), j
+                assert outs[j].guards_intact()
+    finally:
+        set_variant(h, *POLICIES["zs"])
+
+
 # ------------------------------------------------------------ argument errors
 
 def test_argument_errors_enqueue_nothing():
