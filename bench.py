@@ -656,6 +656,7 @@ def bench_purlin(args):
 
         # ---- AllReduce size sweep: zero staging vs SNAC (default policy)
         sweep = allreduce_sweep(rd, torch, dev, stream, peak)
+        configs["allreduce_noalloc"] = noalloc_allreduce(rd, torch, dev, stream, peak)
 
     # ---- end to end: inputs from pinned host memory, outputs back to it; with
     # several ranks the job's figure is all ranks' bytes over the slowest rank
@@ -1188,6 +1189,31 @@ def allreduce_sweep(rd, torch, dev, stream, peak):
     finally:
         rd.purlin_destroy(h)
         torch.cuda.empty_cache()
+    return out
+
+
+def noalloc_allreduce(rd, torch, dev, stream, peak):
+    """The AllReduce that allocates nothing (its staged kernel runs from a
+    fixed static device array), R=8, bf16, 64 MiB and 4 KiB per rank."""
+    out = []
+    for nbytes in (64 << 20, 4096):
+        n = nbytes // 2
+        x = [torch.randn(n, device=dev).to(torch.bfloat16) for _ in range(R)]
+        o = [torch.empty_like(t) for t in x]
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+        fn = lambda: rd.purlin_all_reduce_noalloc(x, o, n, "bf16", device_status=status,
+                                                  stream=stream)
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                fn()
+        torch.cuda.synchronize()
+        us = _events_us(torch, stream, fn, 10 if nbytes > 4096 else 200)
+        if int(status.item()) != 0:
+            raise RuntimeError("allocation-free AllReduce: device status not ok")
+        gbs = 2 * R * nbytes / (us / 1e6) / 1e9
+        out.append({"bytes_per_rank": nbytes, "us": round(us, 2), "gbs": round(gbs, 1),
+                    "frac_of_peak": round(gbs / peak, 3)})
+        del x, o
     return out
 
 

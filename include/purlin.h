@@ -233,20 +233,22 @@ PURLIN_API purlin_status_t purlin_all_to_all_v(purlin_handle_t h, const void* co
  * accounting), a plugin that may not own device memory, or a latency-critical
  * path that cannot take the synchronization cudaMalloc/cudaFree may cause.  The
  * handle-based calls above allocate their scratch in purlin_create(); this one
- * needs no handle.  It runs the staged (SNAC) AllReduce kernel -- same result,
- * bit for bit, as purlin_all_reduce -- with its staging ring, flags and status
- * word in one static device array of PURLIN_NOALLOC_SCRATCH_BYTES (8 MiB) that
- * every GPU which loads this library holds until the process exits.  It calls no
+ * needs no handle.  It runs the staged (SNAC) AllReduce kernel that stages the
+ * reduced chunk (PURLIN_VARIANT_STAGED_Y) -- same result, bit for bit, as
+ * purlin_all_reduce -- with its staging ring, flags and status word in one
+ * static device array of PURLIN_NOALLOC_SCRATCH_BYTES (8 MiB) that every GPU
+ * which loads this library holds until the process exits.  It calls no
  * cudaMalloc, cudaFree or other allocating routine.
  *   in, out      R device pointers each; out[r] == in[r] (in-place) is allowed,
  *                any other overlap is PURLIN_ERR_INVALID_ARG.
  *   R            1..PURLIN_MAX_RANKS;  count: elements per rank.
  *   dtype        PURLIN_F32, PURLIN_BF16 or PURLIN_F16.
  *   chunk_bytes  staged bytes per rank per pipeline step, a multiple of 256
- *                (0 = 32 KiB); depth: ring slots, 0..8 (0 = 2).  A ring that
- *                cannot fit in the static array -- depth * (R + 1) * chunk_bytes
+ *                (0 = 32 KiB); depth: ring slots, 0..8 (0 = 2).  A channel's
+ *                ring that cannot fit in the static array -- depth * chunk_bytes
  *                above PURLIN_NOALLOC_SCRATCH_BYTES - 64 KiB -- is rejected with
- *                PURLIN_ERR_INVALID_ARG before anything is enqueued.
+ *                PURLIN_ERR_INVALID_ARG before anything is enqueued; the array
+ *                holds as many channels as fit (127 at the defaults).
  *   device_status  optional DEVICE int: set to 0 on the stream, then to
  *                PURLIN_ERR_TIMEOUT if a bounded wait of the kernel ran out
  *                (NULL: the library's own word inside the static array is used

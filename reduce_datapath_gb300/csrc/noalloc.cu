@@ -1,5 +1,5 @@
-// noalloc.cu -- purlin_all_reduce_noalloc: the staged (SNAC) AllReduce for
-// callers that must not allocate device memory.
+// noalloc.cu -- purlin_all_reduce_noalloc: the staged (SNAC) AllReduce, with
+// the reduced chunk staged, for callers that must not allocate device memory.
 //
 // Some callers cannot call cudaMalloc: a host framework that has reserved the
 // GPU's memory for its own pool allocator (a direct cudaMalloc would fail, or
@@ -94,8 +94,9 @@ extern "C" PURLIN_API purlin_status_t purlin_all_reduce_noalloc(
     if (depth < 0 || depth > 8 || chunk_bytes % 256) return PURLIN_ERR_INVALID_ARG;
     const size_t chunk = chunk_bytes ? chunk_bytes : kDefaultChunk;
     const int dep = depth ? depth : kDefaultDepth;
-    // One channel's ring must fit in the static staging area.
-    if (chunk > kStagingBytes / ((size_t)dep * (R + 1))) return PURLIN_ERR_INVALID_ARG;
+    // One channel's ring -- depth slots of one reduced chunk each -- must fit in
+    // the static staging area.
+    if (chunk > kStagingBytes / (size_t)dep) return PURLIN_ERR_INVALID_ARG;
     const size_t esz = dtype == PURLIN_F32 ? 4 : 2;
     if (count > UINT64_MAX / esz) return PURLIN_ERR_INVALID_ARG;
     const uint64_t bytes = (uint64_t)count * esz;
@@ -134,6 +135,10 @@ extern "C" PURLIN_API purlin_status_t purlin_all_reduce_noalloc(
     rq.esz = esz;
     rq.pieces = &piece;
     rq.npieces = 1;
+    // The producers reduce the R inputs and stage the reduced chunk, the
+    // consumers copy it to the R outputs: a slot holds one part, so the 8 MiB
+    // array fits R + 1 times the channels that staging the R inputs would.
+    rq.stage_y = true;
     for (int r = 0; r < R; ++r) { rq.in[r] = inp[r]; rq.out[r] = outp[r]; }
     SnacConfig cfg{};
     cfg.staging = d.base + kStagingOffset;

@@ -457,11 +457,59 @@ __device__ void cta_copy_shifted_any(int unit_log2, const char* src, char* dst, 
     else cta_copy_shifted<16>(src, dst, len, lpol, spol);
 }
 
+// Rows of a shifted step of a sum with the inputs staged, sources on one
+// offset: every rank's chunk realigned into its part of the slot with the word
+// offset fixed at compile time, the R ranks' blocks of kMaxRanks / NR units
+// loaded before the first store (R <= NR).
+template <int NR>
+__device__ void stage_ranks_shifted_rows(const SnacParams& p, char* staged, uint64_t src_off,
+                                         uint64_t len, uint64_t lpol)
+{
+    constexpr int B = 16;
+    constexpr int W = B / 4;
+    constexpr int WARPS = kThreads / 32;
+    constexpr int U = kMaxRanks / NR;
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int R = (int)p.R;
+    const uint64_t n = len / B;
+    const int shift = (int)((reinterpret_cast<uintptr_t>(p.in[0]) + src_off) & (B - 1));
+    const uint32_t bits = (uint32_t)(shift & 3) * 8;
+    with_word_offset<W>(shift >> 2, [&](auto A) {
+        for (uint64_t row = 0; row < n; row += (uint64_t)WARPS * 31 * U) {
+            atom::Vec<B> v[U][NR];
+#pragma unroll
+            for (int k = 0; k < U; ++k) {
+                const uint64_t q = row + (uint64_t)(k * WARPS + warp) * 31 + lane;
+#pragma unroll
+                for (int r = 0; r < NR; ++r) {
+                    if (r < R && q < n + 1) {
+                        atom::load(v[k][r], at(p.in[r], src_off + q * B, shift), lpol);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < W; ++i) v[k][r].w[i] = 0u;
+                    }
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < U; ++k) {
+                const uint64_t q = row + (uint64_t)(k * WARPS + warp) * 31 + lane;
+#pragma unroll
+                for (int r = 0; r < NR; ++r) {
+                    if (r >= R) continue;
+                    atom::Vec<B> out;
+                    realign_from_next<W, decltype(A)::value>(v[k][r].w, bits, out.w);
+                    if (lane != 31 && q < n) atom::store(staged + r * p.chunk + q * B, out);
+                }
+            }
+        }
+    });
+}
+
 // STAGE of a shifted step of a sum with the inputs staged: every rank's chunk
-// realigned into its part of the slot (16-byte units, a shifted sum's width),
-// the R ranks' blocks of a unit loaded before the first store.  Sources on one
-// offset realign with the word offset fixed at compile time; sources on
-// different offsets each on their own.
+// realigned into its part of the slot (16-byte units, a shifted sum's width).
+// Sources on one offset: stage_ranks_shifted_rows; sources on different
+// offsets: each rank's blocks realigned on their own offset.
 __device__ void cta_stage_ranks_shifted(const SnacParams& p, const Segment& s, char* staged,
                                         uint64_t src_off, uint64_t len, uint64_t lpol)
 {
@@ -473,30 +521,9 @@ __device__ void cta_stage_ranks_shifted(const SnacParams& p, const Segment& s, c
     const int R = (int)p.R;
     const uint64_t n = len / B;
     if (!(s.shift & kShiftPerRank)) {
-        const int shift = (int)((reinterpret_cast<uintptr_t>(p.in[0]) + src_off) & (B - 1));
-        const uint32_t bits = (uint32_t)(shift & 3) * 8;
-        with_word_offset<W>(shift >> 2, [&](auto A) {
-            for (uint64_t row = 0; row < n; row += (uint64_t)WARPS * 31) {
-                const uint64_t q = row + (uint64_t)warp * 31 + lane;
-                atom::Vec<B> v[kMaxRanks];
-#pragma unroll
-                for (int r = 0; r < kMaxRanks; ++r) {
-                    if (r < R && q < n + 1) {
-                        atom::load(v[r], at(p.in[r], src_off + q * B, shift), lpol);
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < W; ++i) v[r].w[i] = 0u;
-                    }
-                }
-#pragma unroll
-                for (int r = 0; r < kMaxRanks; ++r) {
-                    if (r >= R) continue;
-                    atom::Vec<B> out;
-                    realign_from_next<W, decltype(A)::value>(v[r].w, bits, out.w);
-                    if (lane != 31 && q < n) atom::store(staged + r * p.chunk + q * B, out);
-                }
-            }
-        });
+        if (R <= 2) stage_ranks_shifted_rows<2>(p, staged, src_off, len, lpol);
+        else if (R <= 4) stage_ranks_shifted_rows<4>(p, staged, src_off, len, lpol);
+        else stage_ranks_shifted_rows<kMaxRanks>(p, staged, src_off, len, lpol);
         return;
     }
     int sh[kMaxRanks];
@@ -528,13 +555,59 @@ __device__ void cta_stage_ranks_shifted(const SnacParams& p, const Segment& s, c
     }
 }
 
+// Rows of a shifted sum whose sources sit on one offset: the R ranks' aligned
+// blocks are folded first (the offset is a multiple of the element size, so a
+// block holds whole elements of every rank at the same positions) and the sum
+// is realigned once, with the word offset fixed at compile time.  NR bounds the
+// rank count (R <= NR) and each thread folds kMaxRanks / NR units at once, so a
+// sum of few ranks keeps as many loads in flight as one of eight.
+template <typename T, int ORDER, int NR>
+__device__ void reduce_src_shifted_rows(const SnacParams& p, char* dst, uint64_t src_off,
+                                        uint64_t len, uint64_t lpol, uint64_t spol)
+{
+    constexpr int B = 16;
+    constexpr int W = B / 4;
+    constexpr int WARPS = kThreads / 32;
+    constexpr int U = kMaxRanks / NR;
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int R = (int)p.R;
+    const uint64_t n = len / B;
+    const int shift = (int)((reinterpret_cast<uintptr_t>(p.in[0]) + src_off) & (B - 1));
+    const uint32_t bits = (uint32_t)(shift & 3) * 8;
+    with_word_offset<W>(shift >> 2, [&](auto A) {
+        for (uint64_t row = 0; row < n; row += (uint64_t)WARPS * 31 * U) {
+            atom::Vec<B> v[U][NR];
+#pragma unroll
+            for (int k = 0; k < U; ++k) {
+                const uint64_t q = row + (uint64_t)(k * WARPS + warp) * 31 + lane;
+#pragma unroll
+                for (int r = 0; r < NR; ++r) {
+                    if (r < R && q < n + 1) {
+                        atom::load(v[k][r], at(p.in[r], src_off + q * B, shift), lpol);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < W; ++i) v[k][r].w[i] = 0u;
+                    }
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < U; ++k) {
+                const uint64_t q = row + (uint64_t)(k * WARPS + warp) * 31 + lane;
+                atom::Vec<B> y, out;
+                atom::reduce_unit<T, ORDER, B, NR>(v[k], R, y);
+                realign_from_next<W, decltype(A)::value>(y.w, bits, out.w);
+                if (lane == 31 || q >= n) continue;
+                atom::store(dst + q * B, out, spol);
+            }
+        }
+    });
+}
+
 // Fold a step of the R sources into dst (unit-aligned; 16-byte units, a
-// shifted sum's width).  Sources on one offset: the R ranks' aligned blocks
-// are folded first (the offset is a multiple of the element size, so a block
-// holds whole elements of every rank at the same positions) and the sum is
-// realigned once, with the word offset fixed at compile time; two units per
-// thread in flight.  Sources on different offsets: each rank's block is
-// realigned on its own offset before the fold.
+// shifted sum's width).  Sources on one offset: reduce_src_shifted_rows.
+// Sources on different offsets: each rank's block is realigned on its own
+// offset before the fold.
 template <typename T, int ORDER>
 __device__ void cta_reduce_src_shifted(const SnacParams& p, const Segment& s, char* dst,
                                        uint64_t src_off, uint64_t len, uint64_t lpol, uint64_t spol)
@@ -547,37 +620,9 @@ __device__ void cta_reduce_src_shifted(const SnacParams& p, const Segment& s, ch
     const int R = (int)p.R;
     const uint64_t n = len / B;
     if (!(s.shift & kShiftPerRank)) {
-        constexpr int U = 1;
-        const int shift = (int)((reinterpret_cast<uintptr_t>(p.in[0]) + src_off) & (B - 1));
-        const uint32_t bits = (uint32_t)(shift & 3) * 8;
-        with_word_offset<W>(shift >> 2, [&](auto A) {
-            for (uint64_t row = 0; row < n; row += (uint64_t)WARPS * 31 * U) {
-                atom::Vec<B> y[U];
-#pragma unroll
-                for (int k = 0; k < U; ++k) {
-                    const uint64_t q = row + (uint64_t)(k * WARPS + warp) * 31 + lane;
-                    atom::Vec<B> v[kMaxRanks];
-#pragma unroll
-                    for (int r = 0; r < kMaxRanks; ++r) {
-                        if (r < R && q < n + 1) {
-                            atom::load(v[r], at(p.in[r], src_off + q * B, shift), lpol);
-                        } else {
-#pragma unroll
-                            for (int i = 0; i < W; ++i) v[r].w[i] = 0u;
-                        }
-                    }
-                    atom::reduce_unit<T, ORDER, B>(v, R, y[k]);
-                }
-#pragma unroll
-                for (int k = 0; k < U; ++k) {
-                    const uint64_t q = row + (uint64_t)(k * WARPS + warp) * 31 + lane;
-                    atom::Vec<B> out;
-                    realign_from_next<W, decltype(A)::value>(y[k].w, bits, out.w);
-                    if (lane == 31 || q >= n) continue;
-                    atom::store(dst + q * B, out, spol);
-                }
-            }
-        });
+        if (R <= 2) reduce_src_shifted_rows<T, ORDER, 2>(p, dst, src_off, len, lpol, spol);
+        else if (R <= 4) reduce_src_shifted_rows<T, ORDER, 4>(p, dst, src_off, len, lpol, spol);
+        else reduce_src_shifted_rows<T, ORDER, kMaxRanks>(p, dst, src_off, len, lpol, spol);
         return;
     }
     int sh[kMaxRanks];

@@ -77,7 +77,7 @@ def test_rejects_a_ring_beyond_the_static_array():
     R, n = 8, 1024
     x = [torch.zeros(n, dtype=torch.bfloat16, device="cuda") for _ in range(R)]
     out = [torch.zeros_like(t) for t in x]
-    # 8 slots * (8 + 1) parts * 1 MiB = 72 MiB > the 8 MiB array
+    # 8 slots * 1 MiB = 8 MiB > the 8 MiB array less its 64 KiB of flags
     with pytest.raises(rd.PurlinError) as e:
         rd.purlin_all_reduce_noalloc(x, out, n, "bf16", chunk_bytes=1 << 20, depth=8)
     assert e.value.status == rd.ERR_INVALID_ARG
