@@ -380,9 +380,44 @@ KERNEL_SOURCES = {
 }
 
 
+def product_source(text):
+    """The source as the product build compiles it: the checked build's parts
+    left out -- blocks under `#if defined(PURLIN_CHECKED)` (their `#else`
+    branch is kept), and the PURLIN_CHECK_* macros, which the product build
+    defines to nothing."""
+    out = []
+    stack = []   # per open #if: "checked" (inside the checked branch), "else" or "other"
+    for line in text.splitlines():
+        t = line.strip()
+        in_checked = "checked" in stack
+        if t.startswith("#if"):
+            stack.append("checked" if t.startswith("#if defined(PURLIN_CHECKED)") else "other")
+            if stack[-1] == "other" and not in_checked:
+                out.append(line)
+            continue
+        if t.startswith("#else") and stack:
+            if stack[-1] == "checked":
+                stack[-1] = "else"
+            elif not in_checked:
+                out.append(line)
+            continue
+        if t.startswith("#endif") and stack:
+            kind = stack.pop()
+            if kind == "other" and "checked" not in stack:
+                out.append(line)
+            continue
+        if in_checked:
+            continue
+        if t.startswith("PURLIN_CHECK_") or t.startswith("#define PURLIN_CHECK_"):
+            continue
+        out.append(line)
+    return "\n".join(out)
+
+
 def code_tokens(text):
     """C/C++ source with comments removed and whitespace runs collapsed (string
     and character literals kept as written): what the compiler sees."""
+    text = product_source(text)
     out, i, n = [], 0, len(text)
     while i < n:
         c = text[i]

@@ -27,7 +27,8 @@
  *   - Errors.  Argument errors return PURLIN_ERR_INVALID_ARG or
  *     PURLIN_ERR_UNSUPPORTED synchronously and enqueue nothing.  A failed launch
  *     returns PURLIN_ERR_CUDA.  Errors detected by a kernel (a bounded wait that
- *     timed out) are recorded in the handle's device status word and reported by
+ *     timed out; in a checked build, an access outside the call's buffers) are
+ *     recorded in the handle's device status word and reported by
  *     purlin_query_status() after the stream has been synchronized.
  *   - Aliasing.  Outputs must not overlap each other or any input, except for
  *     the in-place forms named at each entry point.
@@ -67,7 +68,10 @@ typedef enum {
     PURLIN_ERR_UNSUPPORTED = 2,  /* valid request this library does not serve   */
     PURLIN_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed        */
     PURLIN_ERR_TIMEOUT = 4,      /* a bounded device-side wait ran out          */
-    PURLIN_ERR_OOM = 5           /* device allocation failed (purlin_create)    */
+    PURLIN_ERR_OOM = 5,          /* device allocation failed (purlin_create)    */
+    PURLIN_ERR_BOUNDS = 6        /* checked builds only: a kernel met an address
+                                    outside the call's buffers and skipped it
+                                    (purlin_debug.h)                           */
 } purlin_status_t;
 
 typedef enum {

@@ -21,10 +21,13 @@ import os
 import threading
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "lib", "libpurlin.so")
+# PURLIN_LIBRARY=checked selects the checked build (every kernel access tested
+# against the call's buffers; for tests) in place of the product build.
+LIB_PATH = os.path.join(_HERE, "lib", "libpurlin_checked.so"
+                        if os.environ.get("PURLIN_LIBRARY") == "checked" else "libpurlin.so")
 
 # purlin_status_t
-OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_OOM = range(6)
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_OOM, ERR_BOUNDS = range(7)
 # purlin_dtype_t
 F32, BF16, F16, U8 = range(4)
 DTYPES = {"f32": F32, "bf16": BF16, "f16": F16, "u8": U8}
@@ -53,7 +56,8 @@ EXPORTED = (
     "purlin_set_timeout", "purlin_query_status", "purlin_plan_begin", "purlin_plan_end",
     "purlin_plan_launch", "purlin_plan_destroy",
     "purlin_last_launch", "purlin_status_string", "purlin_version", "purlin_plan_segments",
-    "purlin_debug_inject", "purlin_all_reduce_noalloc",
+    "purlin_debug_inject", "purlin_debug_checked", "purlin_debug_violation",
+    "purlin_all_reduce_noalloc",
 )
 
 
@@ -87,10 +91,11 @@ _lock = threading.Lock()
 _lib = None
 
 
-def build(force: bool = False) -> str:
-    """Compile libpurlin.so in-tree (nvcc, sm_103a)."""
+def build(force: bool = False, checked: bool = False) -> str:
+    """Compile libpurlin.so in-tree (nvcc, sm_103a); checked=True: the checked
+    build libpurlin_checked.so instead."""
     from . import _build
-    return _build.build(force=force)
+    return _build.build(force=force, checked=checked)
 
 
 def lib():
@@ -136,6 +141,8 @@ def lib():
                                      ctypes.POINTER(Segment), i32, ctypes.POINTER(i32),
                                      ctypes.POINTER(ctypes.c_uint32)],
             "purlin_debug_inject": [vp, i32],
+            "purlin_debug_checked": [],
+            "purlin_debug_violation": [vp, u64p],
             "purlin_all_reduce_noalloc": [pp, pp, i32, sz, i32, sz, i32, vp, vp],
         }
         for name, args in sigs.items():
@@ -425,6 +432,16 @@ def purlin_status_string(status) -> str:
 
 def purlin_debug_inject(h, what: int) -> None:
     _check(lib().purlin_debug_inject(h, int(what)), "purlin_debug_inject")
+
+
+def purlin_debug_checked() -> bool:
+    return bool(lib().purlin_debug_checked())
+
+
+def purlin_debug_violation(h) -> int:
+    v = ctypes.c_uint64(0)
+    _check(lib().purlin_debug_violation(h, ctypes.byref(v)), "purlin_debug_violation")
+    return int(v.value)
 
 
 def purlin_all_reduce_noalloc(ins, outs, count, dtype="bf16", chunk_bytes=0, depth=0,

@@ -39,6 +39,12 @@ def nvcc() -> str:
     raise RuntimeError("nvcc not found (set CUDA_HOME)")
 
 
+# The checked build: the same sources with PURLIN_CHECKED (every kernel access
+# tested against the call's buffers), for tests.
+BUILD_CHECKED = os.path.join(HERE, "_build_checked")
+LIB_CHECKED = os.path.join(LIBDIR, "libpurlin_checked.so")
+
+
 def _inputs():
     files = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
     files += [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE)]
@@ -46,50 +52,73 @@ def _inputs():
     return files
 
 
-def is_fresh() -> bool:
-    if not os.path.exists(LIB):
+def is_fresh(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(f) <= t for f in _inputs())
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile and link libpurlin.so unless it is newer than every source."""
-    if not force and is_fresh():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
-    os.makedirs(LIBDIR, exist_ok=True)
+def _compile_jobs(build_dir: str, defines: list, verbose: bool):
+    """Start one nvcc per translation unit; returns [(src, obj, process)]."""
+    os.makedirs(build_dir, exist_ok=True)
     cc = nvcc()
-    procs = []
-    objs = []
+    jobs = []
     for src in SOURCES:
-        obj = os.path.join(BUILD, src.rsplit(".", 1)[0] + ".o")
-        objs.append(obj)
-        cmd = [cc, *COMMON]
+        obj = os.path.join(build_dir, src.rsplit(".", 1)[0] + ".o")
+        cmd = [cc, *COMMON, *defines]
         if src.endswith(".cu"):
             cmd += CUDA_ONLY
         cmd += ["-c", os.path.join(CSRC, src), "-o", obj]
         if verbose:
             print(" ".join(cmd), file=sys.stderr)
-        procs.append((src, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT,
-                                            text=True)))
+        jobs.append((src, obj, subprocess.Popen(cmd, stdout=subprocess.PIPE,
+                                                 stderr=subprocess.STDOUT, text=True)))
+    return jobs
+
+
+def _finish(jobs, lib: str, verbose: bool) -> None:
     failed = []
-    for src, p in procs:
+    for src, _, p in jobs:
         out, _ = p.communicate()
         if p.returncode != 0:
             failed.append(f"--- {src}\n{out}")
         elif verbose and out.strip():
             print(out, file=sys.stderr)
     if failed:
-        raise RuntimeError("libpurlin build failed:\n" + "\n".join(failed))
-    tmp = LIB + ".%d.tmp" % os.getpid()
-    link = [cc, "-shared", *ARCH, "-o", tmp, *objs]
+        raise RuntimeError(f"{os.path.basename(lib)} build failed:\n" + "\n".join(failed))
+    tmp = lib + ".%d.tmp" % os.getpid()
+    link = [nvcc(), "-shared", *ARCH, "-o", tmp, *[obj for _, obj, _ in jobs]]
     r = subprocess.run(link, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True)
     if r.returncode != 0:
-        raise RuntimeError("libpurlin link failed:\n" + r.stdout)
-    os.replace(tmp, LIB)
-    return LIB
+        raise RuntimeError(f"{os.path.basename(lib)} link failed:\n" + r.stdout)
+    os.replace(tmp, lib)
+
+
+def build(force: bool = False, verbose: bool = False, checked: bool = False) -> str:
+    """Compile and link libpurlin.so (checked=True: libpurlin_checked.so)
+    unless it is newer than every source."""
+    lib = LIB_CHECKED if checked else LIB
+    if not force and is_fresh(lib):
+        return lib
+    os.makedirs(LIBDIR, exist_ok=True)
+    jobs = _compile_jobs(BUILD_CHECKED if checked else BUILD,
+                         ["-DPURLIN_CHECKED"] if checked else [], verbose)
+    _finish(jobs, lib, verbose)
+    return lib
+
+
+def build_all(force: bool = False, verbose: bool = False) -> None:
+    """Both libraries, every translation unit compiled at once."""
+    os.makedirs(LIBDIR, exist_ok=True)
+    pending = []
+    for lib, d, defs in ((LIB, BUILD, []), (LIB_CHECKED, BUILD_CHECKED, ["-DPURLIN_CHECKED"])):
+        if force or not is_fresh(lib):
+            pending.append((lib, _compile_jobs(d, defs, verbose)))
+    for lib, jobs in pending:
+        _finish(jobs, lib, verbose)
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose=True))
+    build_all(force="--force" in sys.argv, verbose=True)
+    print(LIB, LIB_CHECKED)

@@ -15,9 +15,65 @@
 #include <cuda_fp16.h>
 
 #include "plan.h"
+#if defined(PURLIN_CHECKED)
+#include "purlin.h"
+#endif
 
 namespace purlin {
 namespace atom {
+
+// ------------------------------------------------------------ checked builds
+// With PURLIN_CHECKED every global access below is first tested against the
+// launch's address ranges (CheckRanges, copied into shared memory when the
+// kernel starts): one outside all of them is skipped (a load returns zeros),
+// and the kernel records PURLIN_ERR_BOUNDS and the first such address (a
+// misaligned access too, which the kernels never make).  A store must lie
+// inside a range.  A load of a block aligned to its size need
+// only hold a byte of one: the shifted bodies read the aligned blocks around a
+// segment's ends, which stay within the pages the buffer lies in, while a
+// block wholly outside every buffer is still caught.  A debug build for tests;
+// the product build compiles none of it.
+#if defined(PURLIN_CHECKED)
+static __shared__ CheckRanges s_check;
+static __shared__ int* s_check_status;
+
+__device__ __forceinline__ void check_begin(const CheckRanges& c, int* status)
+{
+    if (threadIdx.x == 0) {
+        s_check = c;
+        s_check_status = status;
+    }
+    __syncthreads();
+}
+
+// bytes at p, which must be aligned to `align` (a misaligned access is
+// reported rather than made); block: an aligned block that need only hold a
+// byte of a range.
+static __device__ __noinline__ bool access_ok(const void* p, uint32_t bytes, uint32_t align,
+                                              bool block)
+{
+    const uint64_t a = reinterpret_cast<uint64_t>(p);
+    const uint64_t e = a + bytes;
+    const bool aligned = (a & (uint64_t)(align - 1)) == 0;
+    for (uint32_t i = 0; aligned && i < s_check.n; ++i) {
+        if (block ? (a < s_check.hi[i] && e > s_check.lo[i])
+                  : (a >= s_check.lo[i] && e <= s_check.hi[i] && e >= a))
+            return true;
+    }
+    atomicCAS(s_check_status, 0, (int)PURLIN_ERR_BOUNDS);
+    if (s_check.bad) atomicCAS(s_check.bad, 0ull, (unsigned long long)a);
+    return false;
+}
+#define PURLIN_CHECK_BEGIN(params) ::purlin::atom::check_begin((params).check, (params).status)
+#define PURLIN_CHECK_LOAD(p, bytes, zero) \
+    if (!::purlin::atom::access_ok((p), (bytes), (bytes), true)) { zero; return; }
+#define PURLIN_CHECK_STORE(p, bytes) \
+    if (!::purlin::atom::access_ok((p), (bytes), (bytes), false)) return;
+#else
+#define PURLIN_CHECK_BEGIN(params) ((void)0)
+#define PURLIN_CHECK_LOAD(p, bytes, zero)
+#define PURLIN_CHECK_STORE(p, bytes)
+#endif
 
 // ---------------------------------------------------------------- raw accesses
 
@@ -28,6 +84,7 @@ template <> struct Vec<32> { uint32_t w[8]; };
 // Loads skip L1 allocation: every source byte is read exactly once.
 __device__ __forceinline__ void load(Vec<16>& v, const char* p)
 {
+    PURLIN_CHECK_LOAD(p, 16, v = Vec<16>{})
     asm volatile("ld.global.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
                  : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3])
                  : "l"(p));
@@ -35,6 +92,7 @@ __device__ __forceinline__ void load(Vec<16>& v, const char* p)
 
 __device__ __forceinline__ void load(Vec<32>& v, const char* p)
 {
+    PURLIN_CHECK_LOAD(p, 32, v = Vec<32>{})
     asm volatile("ld.global.L1::no_allocate.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
                  : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3]),
                    "=r"(v.w[4]), "=r"(v.w[5]), "=r"(v.w[6]), "=r"(v.w[7])
@@ -43,6 +101,7 @@ __device__ __forceinline__ void load(Vec<32>& v, const char* p)
 
 __device__ __forceinline__ void store(char* p, const Vec<16>& v)
 {
+    PURLIN_CHECK_STORE(p, 16)
     asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};"
                  :: "l"(p), "r"(v.w[0]), "r"(v.w[1]), "r"(v.w[2]), "r"(v.w[3])
                  : "memory");
@@ -50,6 +109,7 @@ __device__ __forceinline__ void store(char* p, const Vec<16>& v)
 
 __device__ __forceinline__ void store(char* p, const Vec<32>& v)
 {
+    PURLIN_CHECK_STORE(p, 32)
     asm volatile("st.global.v8.u32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
                  :: "l"(p), "r"(v.w[0]), "r"(v.w[1]), "r"(v.w[2]), "r"(v.w[3]),
                     "r"(v.w[4]), "r"(v.w[5]), "r"(v.w[6]), "r"(v.w[7])
@@ -73,6 +133,7 @@ __device__ __forceinline__ uint64_t l2_policy(uint32_t kind)
 
 __device__ __forceinline__ void load(Vec<16>& v, const char* p, uint64_t pol)
 {
+    PURLIN_CHECK_LOAD(p, 16, v = Vec<16>{})
     asm volatile("ld.global.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
                  : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3])
                  : "l"(p), "l"(pol));
@@ -80,6 +141,7 @@ __device__ __forceinline__ void load(Vec<16>& v, const char* p, uint64_t pol)
 
 __device__ __forceinline__ void load(Vec<32>& v, const char* p, uint64_t pol)
 {
+    PURLIN_CHECK_LOAD(p, 32, v = Vec<32>{})
     asm volatile("ld.global.L1::no_allocate.L2::cache_hint.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7},"
                  " [%8], %9;"
                  : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3]),
@@ -89,6 +151,7 @@ __device__ __forceinline__ void load(Vec<32>& v, const char* p, uint64_t pol)
 
 __device__ __forceinline__ void store(char* p, const Vec<16>& v, uint64_t pol)
 {
+    PURLIN_CHECK_STORE(p, 16)
     asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1,%2,%3,%4}, %5;"
                  :: "l"(p), "r"(v.w[0]), "r"(v.w[1]), "r"(v.w[2]), "r"(v.w[3]), "l"(pol)
                  : "memory");
@@ -96,6 +159,7 @@ __device__ __forceinline__ void store(char* p, const Vec<16>& v, uint64_t pol)
 
 __device__ __forceinline__ void store(char* p, const Vec<32>& v, uint64_t pol)
 {
+    PURLIN_CHECK_STORE(p, 32)
     asm volatile("st.global.L2::cache_hint.v8.u32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8}, %9;"
                  :: "l"(p), "r"(v.w[0]), "r"(v.w[1]), "r"(v.w[2]), "r"(v.w[3]),
                     "r"(v.w[4]), "r"(v.w[5]), "r"(v.w[6]), "r"(v.w[7]), "l"(pol)
@@ -106,6 +170,7 @@ __device__ __forceinline__ void store(char* p, const Vec<32>& v, uint64_t pol)
 // cached in L2 only (.cg), so no stale L1 line can be returned.
 __device__ __forceinline__ void load_cg(Vec<16>& v, const char* p)
 {
+    PURLIN_CHECK_LOAD(p, 16, v = Vec<16>{})
     asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];"
                  : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3])
                  : "l"(p));
@@ -113,6 +178,7 @@ __device__ __forceinline__ void load_cg(Vec<16>& v, const char* p)
 
 __device__ __forceinline__ void load_cg(Vec<32>& v, const char* p)
 {
+    PURLIN_CHECK_LOAD(p, 32, v = Vec<32>{})
     asm volatile("ld.global.cg.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
                  : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3]),
                    "=r"(v.w[4]), "=r"(v.w[5]), "=r"(v.w[6]), "=r"(v.w[7])
@@ -133,6 +199,7 @@ template <> struct Unit<8> { uint2 v; };
 template <int BYTES, bool CG = false>
 __device__ __forceinline__ void load_unit(Unit<BYTES>& u, const char* p)
 {
+    PURLIN_CHECK_LOAD(p, BYTES, u = Unit<BYTES>{})
     if constexpr (BYTES >= 16) {
         if constexpr (CG) load_cg(u.v, p);
         else load(u.v, p);
@@ -159,6 +226,7 @@ __device__ __forceinline__ void load_unit(Unit<BYTES>& u, const char* p)
 template <int BYTES>
 __device__ __forceinline__ void store_unit(char* p, const Unit<BYTES>& u)
 {
+    PURLIN_CHECK_STORE(p, BYTES)
     if constexpr (BYTES >= 16) store(p, u.v);
     else if constexpr (BYTES == 8) *reinterpret_cast<uint2*>(p) = u.v;
     else if constexpr (BYTES == 4) *reinterpret_cast<uint32_t*>(p) = u.v;
@@ -174,14 +242,27 @@ struct F32 {
     static constexpr int kBytes = 4;
     __device__ static float widen(uint32_t w, int) { return __uint_as_float(w); }
     __device__ static uint32_t narrow(const float* f) { return __float_as_uint(f[0]); }
-    __device__ static float load1(const char* p) { return *reinterpret_cast<const float*>(p); }
+    __device__ static float load1(const char* p)
+    {
+#if defined(PURLIN_CHECKED)
+        if (!access_ok(p, 4, 4, false)) return 0.0f;
+#endif
+        return *reinterpret_cast<const float*>(p);
+    }
     __device__ static float load1_cg(const char* p)
     {
+#if defined(PURLIN_CHECKED)
+        if (!access_ok(p, 4, 4, false)) return 0.0f;
+#endif
         float f;
         asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(f) : "l"(p));
         return f;
     }
-    __device__ static void store1(char* p, float f) { *reinterpret_cast<float*>(p) = f; }
+    __device__ static void store1(char* p, float f)
+    {
+        PURLIN_CHECK_STORE(p, 4)
+        *reinterpret_cast<float*>(p) = f;
+    }
 };
 
 struct BF16 {
@@ -201,16 +282,23 @@ struct BF16 {
     }
     __device__ static float load1(const char* p)
     {
+#if defined(PURLIN_CHECKED)
+        if (!access_ok(p, 2, 2, false)) return 0.0f;
+#endif
         return __uint_as_float((uint32_t)(*reinterpret_cast<const uint16_t*>(p)) << 16);
     }
     __device__ static float load1_cg(const char* p)
     {
+#if defined(PURLIN_CHECKED)
+        if (!access_ok(p, 2, 2, false)) return 0.0f;
+#endif
         uint16_t h;
         asm volatile("ld.global.cg.u16 %0, [%1];" : "=h"(h) : "l"(p));
         return __uint_as_float((uint32_t)h << 16);
     }
     __device__ static void store1(char* p, float f)
     {
+        PURLIN_CHECK_STORE(p, 2)
         float two[2] = {f, 0.0f};
         *reinterpret_cast<uint16_t*>(p) = (uint16_t)(narrow(two) & 0xffffu);
     }
@@ -231,16 +319,23 @@ struct F16 {
     }
     __device__ static float load1(const char* p)
     {
+#if defined(PURLIN_CHECKED)
+        if (!access_ok(p, 2, 2, false)) return 0.0f;
+#endif
         return __half2float(__ushort_as_half(*reinterpret_cast<const unsigned short*>(p)));
     }
     __device__ static float load1_cg(const char* p)
     {
+#if defined(PURLIN_CHECKED)
+        if (!access_ok(p, 2, 2, false)) return 0.0f;
+#endif
         unsigned short h;
         asm volatile("ld.global.cg.u16 %0, [%1];" : "=h"(h) : "l"(p));
         return __half2float(__ushort_as_half(h));
     }
     __device__ static void store1(char* p, float f)
     {
+        PURLIN_CHECK_STORE(p, 2)
         float two[2] = {f, 0.0f};
         *reinterpret_cast<uint16_t*>(p) = (uint16_t)(narrow(two) & 0xffffu);
     }

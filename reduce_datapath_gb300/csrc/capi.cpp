@@ -176,6 +176,32 @@ purlin_status_t check_buffers(Coll coll, int R, const uint64_t* in, const uint64
     return PURLIN_OK;
 }
 
+}  // namespace
+
+void purlin::add_range(CheckRanges& c, uint64_t lo, uint64_t bytes)
+{
+    if (bytes == 0 || c.n >= (uint32_t)kMaxCheckRanges) return;
+    c.lo[c.n] = lo;
+    c.hi[c.n] = lo + bytes;
+    ++c.n;
+}
+
+CheckRanges purlin::call_ranges(int R, const uint64_t* in, const uint64_t* out,
+                                const uint64_t* in_ext, const uint64_t* out_ext,
+                                unsigned long long* bad)
+{
+    CheckRanges c;
+    std::memset(&c, 0, sizeof(c));
+    c.bad = bad;
+    for (int r = 0; r < R; ++r) {
+        add_range(c, in[r], in_ext[r]);
+        add_range(c, out[r], out_ext[r]);
+    }
+    return c;
+}
+
+namespace {
+
 // Launch-wide knobs of the zero-staging kernels.
 struct ZsKnobs {
     int tile_units;
@@ -219,10 +245,15 @@ ZsKnobs zs_knobs(const purlin_handle* h, Coll coll, bool bulk)
 template <int MAXSEG>
 purlin_status_t make_params(ZsParams<MAXSEG>& p, const Piece* pieces, int npieces, int R,
                             const uint64_t* in, const uint64_t* out, size_t esz, bool reduce,
-                            const ZsKnobs& k, int* status)
+                            const ZsKnobs& k, int* status, const CheckRanges& check)
 {
     const int max_unit_log2 = k.max_unit_log2;
     std::memset(&p, 0, sizeof(p));
+#if defined(PURLIN_CHECKED)
+    p.check = check;
+#else
+    (void)check;
+#endif
     p.l2_load = k.l2_load;
     p.l2_store = k.l2_store;
     p.pdl = k.pdl ? 1u : 0u;
@@ -271,7 +302,7 @@ int has_shift(const ZsParams<MAXSEG>& p)
 template <int MAXSEG>
 bool replan_small(const purlin_handle* h, Coll coll, ZsParams<MAXSEG>& p, const Piece* pieces,
                   int npieces, int R, const uint64_t* in, const uint64_t* out, size_t esz,
-                  bool reduce, ZsKnobs& k)
+                  bool reduce, ZsKnobs& k, const CheckRanges& check)
 {
     const long threshold = h->small_tiles >= 0 ? h->small_tiles : small_tiles_default(coll);
     // counted in tiles of one unit per thread for sums, whatever reduce_unroll
@@ -287,10 +318,11 @@ bool replan_small(const purlin_handle* h, Coll coll, ZsParams<MAXSEG>& p, const 
     const int ci = (int)coll;
     if (h->l2_load < 0 && h->l2_coll_load[ci] < 0) ks.l2_load = kL2Normal;
     if (h->l2_store < 0 && h->l2_coll_store[ci] < 0) ks.l2_store = kL2Normal;
-    if (make_params(p, pieces, npieces, R, in, out, esz, reduce, ks, p.status) != PURLIN_OK) {
+    if (make_params(p, pieces, npieces, R, in, out, esz, reduce, ks, p.status, check) !=
+        PURLIN_OK) {
         // cannot happen (same segments, more tiles of a smaller size fit in
         // 32 bits only if the large plan did); keep the large plan
-        make_params(p, pieces, npieces, R, in, out, esz, reduce, k, p.status);
+        make_params(p, pieces, npieces, R, in, out, esz, reduce, k, p.status, check);
         return false;
     }
     k = ks;
@@ -391,6 +423,9 @@ struct Call {
     const uint64_t* out;
     const Piece* pieces;
     int np;
+    const CheckRanges* check;  // the call's buffers (checked builds test against them)
+    const uint64_t* in_ext;    // bytes read from each input
+    const uint64_t* out_ext;   // bytes touched in each output
 };
 
 // What a call launches: nothing (kind 0), kernel k (1), copy-engine copies
@@ -428,11 +463,14 @@ purlin_status_t plan_staged(const Call& c, Launches& L)
     cfg.channels = h->ctas;
     cfg.sms = h->sms;
     cfg.timeout_ns = h->timeout_ns;
-    cfg.inject_skip_notify = h->inject;
+    cfg.inject_skip_notify = h->inject == 1;
+#if defined(PURLIN_CHECKED)
+    rq.check = c.check;
+#endif
     SnacLaunch sl{};
     purlin_status_t st = snac_plan(rq, cfg, L.k, &sl);
     if (st != PURLIN_OK) return st;
-    h->inject = 0;
+    if (h->inject == 1) h->inject = 0;
     L.kind = L.k.grid > 0 ? 1 : 0;
     L.info.variant = h->variant;
     L.info.kernels = sl.kernels;
@@ -483,7 +521,8 @@ purlin_status_t plan_by_destination(const Call& c, ZsKnobs knobs, bool bulk, Lau
         plan = pulled;
         if (h->l2_load < 0 && h->l2_coll_load[(int)c.coll] < 0) knobs.l2_load = kL2Normal;
     }
-    purlin_status_t st = make_params(p, plan, nplan, c.R, c.in, c.out, c.esz, false, knobs, h->status);
+    purlin_status_t st =
+        make_params(p, plan, nplan, c.R, c.in, c.out, c.esz, false, knobs, h->status, *c.check);
     if (st != PURLIN_OK) return st;
     int grid;
     if (bulk) {
@@ -492,7 +531,7 @@ purlin_status_t plan_by_destination(const Call& c, ZsKnobs knobs, bool bulk, Lau
         L.info.block = kBulkThreads;
     } else {
         const bool small = replan_small(h, c.coll, p, plan, nplan, c.R, c.in, c.out, c.esz, false,
-                                        knobs);
+                                        knobs, *c.check);
         const bool sh = has_shift(p) != 0;
         grid = zs_grid(h, p.ntiles, zs_copy_resident_ctas(true, false, small, sh));
         zs_copy_select(L.k, true, false, small, sh);
@@ -521,9 +560,11 @@ purlin_status_t plan_all_reduce_split(const Call& c, const ZsKnobs& knobs, Launc
     sum.dst = 0;
     ZsKnobs ks = knobs;
     if (h->l2_store < 0 && h->l2_coll_store[(int)c.coll] < 0) ks.l2_store = kL2Normal;
-    purlin_status_t st = make_params(p, &sum, 1, R, c.in, c.out, c.esz, true, ks, h->status);
+    purlin_status_t st =
+        make_params(p, &sum, 1, R, c.in, c.out, c.esz, true, ks, h->status, *c.check);
     if (st != PURLIN_OK) return st;
-    const bool small = replan_small(h, c.coll, p, &sum, 1, R, c.in, c.out, c.esz, true, ks);
+    const bool small = replan_small(h, c.coll, p, &sum, 1, R, c.in, c.out, c.esz, true, ks,
+                                    *c.check);
     const int sh = has_shift(p);
     const int grid =
         zs_grid(h, p.ntiles, zs_reduce_resident_ctas(c.dtype, h->order, false, small, R, sh));
@@ -541,10 +582,10 @@ purlin_status_t plan_all_reduce_split(const Call& c, const ZsKnobs& knobs, Launc
         copies[nc++] = Piece{sum.dst_off, sum.dst_off, sum.bytes, 0, (uint8_t)j};
     }
     ZsKnobs kc = zs_knobs(h, Coll::AllToAllV, false);  // vector copies
-    st = make_params(p2, copies, nc, R, from, c.out, c.esz, false, kc, h->status);
+    st = make_params(p2, copies, nc, R, from, c.out, c.esz, false, kc, h->status, *c.check);
     if (st != PURLIN_OK) return st;
     const bool small2 = replan_small(h, Coll::AllToAllV, p2, copies, nc, R, from, c.out, c.esz,
-                                     false, kc);
+                                     false, kc, *c.check);
     const bool sh2 = has_shift(p2) != 0;
     const int grid2 = zs_grid(h, p2.ntiles, zs_copy_resident_ctas(false, false, small2, sh2));
     zs_copy_select(L.k2, false, false, small2, sh2);
@@ -567,7 +608,7 @@ purlin_status_t plan_zs(const Call& c, const ZsKnobs& knobs, bool bulk, Launches
     ZsKnobs kn = knobs;
     ZsParams<kSegsSmall>& p = *reinterpret_cast<ZsParams<kSegsSmall>*>(L.k.params);
     purlin_status_t st = make_params(p, c.pieces, c.np, c.R, c.in, c.out, c.esz, c.reduce, kn,
-                                     h->status);
+                                     h->status, *c.check);
     if (st != PURLIN_OK) return st;
     const bool fan_all = c.coll == Coll::AllGather || c.coll == Coll::AllReduce;
     int grid;
@@ -577,7 +618,7 @@ purlin_status_t plan_zs(const Call& c, const ZsKnobs& knobs, bool bulk, Launches
         L.info.block = kBulkThreads;
     } else {
         const bool small = replan_small(h, c.coll, p, c.pieces, c.np, c.R, c.in, c.out, c.esz,
-                                        c.reduce, kn);
+                                        c.reduce, kn, *c.check);
         if (c.reduce) {
             const int sh = has_shift(p);
             grid = zs_grid(h, p.ntiles,
@@ -589,6 +630,22 @@ purlin_status_t plan_zs(const Call& c, const ZsKnobs& knobs, bool bulk, Launches
             zs_copy_select(L.k, false, fan_all, small, sh);
         }
         if (small) L.info.block = kSmallThreads;
+#if defined(PURLIN_CHECKED)
+        if ((h->inject == 2 || h->inject == 3) && p.nseg > 0) {
+            // purlin_debug_inject: the first segment's destination (2) or
+            // sources (3) one extent too far (every access past the call's
+            // buffers is then skipped)
+            if (h->inject == 2) {
+                const int d = p.seg[0].dst == kEveryRank ? 0 : p.seg[0].dst;
+                p.seg[0].dst_off += c.out_ext[d];
+            } else {
+                uint64_t ext = c.reduce ? 0 : c.in_ext[p.seg[0].src];
+                for (int r = 0; c.reduce && r < c.R; ++r) ext = std::max(ext, c.in_ext[r]);
+                p.seg[0].src_off += ext;
+            }
+            h->inject = 0;
+        }
+#endif
     }
     L.k.grid = (unsigned)grid;
     L.k.pdl = p.pdl != 0;
@@ -693,7 +750,8 @@ purlin_status_t run(purlin_handle_t h, Coll coll, const void* const in_[], void*
     tl_k2.grid = 0;
     tl_copies.clear();
     Launches L{tl_k, tl_k2, tl_copies, info};
-    const Call c{h, coll, R, dtype, esz, reduce, in, out, pieces, np};
+    const CheckRanges check = call_ranges(R, in, out, in_ext, out_ext, violation_word(h->status));
+    const Call c{h, coll, R, dtype, esz, reduce, in, out, pieces, np, &check, in_ext, out_ext};
 
     if (wants_staged(h) && np > 0) {
         st = plan_staged(c, L);
@@ -742,6 +800,7 @@ const char* purlin_status_string(purlin_status_t s)
     case PURLIN_ERR_CUDA: return "CUDA runtime error";
     case PURLIN_ERR_TIMEOUT: return "device-side wait timed out";
     case PURLIN_ERR_OOM: return "device out of memory";
+    case PURLIN_ERR_BOUNDS: return "an access outside the call's buffers was skipped";
     }
     return "unknown status";
 }
@@ -772,13 +831,13 @@ purlin_status_t purlin_create(purlin_handle_t* out, int R, size_t staging_bytes,
     h->flag_words = kFlagWords;
     if (cudaMalloc(&h->staging, h->staging_bytes) != cudaSuccess ||
         cudaMalloc(&h->flags, h->flag_words * sizeof(uint64_t)) != cudaSuccess ||
-        cudaMalloc(&h->status, sizeof(int)) != cudaSuccess) {
+        cudaMalloc(&h->status, kStatusBytes) != cudaSuccess) {
         cudaGetLastError();
         purlin_destroy(h);
         return PURLIN_ERR_OOM;
     }
     if (cudaMemset(h->flags, 0, h->flag_words * sizeof(uint64_t)) != cudaSuccess ||
-        cudaMemset(h->status, 0, sizeof(int)) != cudaSuccess ||
+        cudaMemset(h->status, 0, kStatusBytes) != cudaSuccess ||
         cudaDeviceSynchronize() != cudaSuccess) {
         purlin_destroy(h);
         return PURLIN_ERR_CUDA;
@@ -963,8 +1022,39 @@ purlin_status_t purlin_set_small_tiles(purlin_handle_t h, int tiles)
 
 purlin_status_t purlin_debug_inject(purlin_handle_t h, int what)
 {
-    if (!h || what < 0 || what > 1) return PURLIN_ERR_INVALID_ARG;
+    if (!h || what < 0 || what > 3) return PURLIN_ERR_INVALID_ARG;
+#if !defined(PURLIN_CHECKED)
+    if (what >= 2) return PURLIN_ERR_UNSUPPORTED;  // only a checked build catches it
+#endif
     h->inject = what;
+    return PURLIN_OK;
+}
+
+int purlin_debug_checked(void)
+{
+#if defined(PURLIN_CHECKED)
+    return 1;
+#else
+    return 0;
+#endif
+}
+
+purlin_status_t purlin_debug_violation(purlin_handle_t h, uint64_t* address)
+{
+    if (!h || !address) return PURLIN_ERR_INVALID_ARG;
+    DeviceGuard guard(h->device);
+    if (!guard.ok) return PURLIN_ERR_CUDA;
+    unsigned long long v = 0;
+    if (cudaMemcpy(&v, violation_word(h->status), sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return PURLIN_ERR_CUDA;
+    if (v != 0) {
+        const unsigned long long zero = 0;
+        if (cudaMemcpy(violation_word(h->status), &zero, sizeof zero, cudaMemcpyHostToDevice) !=
+                cudaSuccess ||
+            cudaDeviceSynchronize() != cudaSuccess)
+            return PURLIN_ERR_CUDA;
+    }
+    *address = (uint64_t)v;
     return PURLIN_OK;
 }
 

@@ -4,6 +4,7 @@
 
 #include <cuda_runtime.h>
 
+#include "check.h"
 #include "plan.h"
 
 namespace purlin {
@@ -36,6 +37,24 @@ cudaError_t launch_kernel(const KernelLaunch& k, cudaStream_t stream);
 // memory, on the current device (occupancy API, cached without allocating; 1
 // if the query fails).
 int resident_ctas_of(const void* kernel, int threads);
+
+// ---- device status area and checked builds ----------------------------------
+// A handle's (or the allocation-free call's) status area: the status word, then
+// the first address a checked kernel met outside the call's buffers.
+constexpr size_t kStatusBytes = 16;
+
+inline unsigned long long* violation_word(int* status)
+{
+    return reinterpret_cast<unsigned long long*>(reinterpret_cast<char*>(status) + 8);
+}
+
+// The address ranges of a call's buffers: input r is [in[r], in[r] + in_ext[r]),
+// output r [out[r], out[r] + out_ext[r]) (empty extents left out).
+CheckRanges call_ranges(int R, const uint64_t* in, const uint64_t* out, const uint64_t* in_ext,
+                        const uint64_t* out_ext, unsigned long long* bad);
+
+// Appends [lo, lo + bytes) to c (if there is room).
+void add_range(CheckRanges& c, uint64_t lo, uint64_t bytes);
 
 // ---- zero-staging Atom kernels (zs_kernels.cu) -----------------------------
 

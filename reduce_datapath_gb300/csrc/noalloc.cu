@@ -135,6 +135,13 @@ extern "C" PURLIN_API purlin_status_t purlin_all_reduce_noalloc(
     rq.esz = esz;
     rq.pieces = &piece;
     rq.npieces = 1;
+#if defined(PURLIN_CHECKED)
+    uint64_t ext[kMaxRanks];
+    for (int r = 0; r < R; ++r) ext[r] = bytes;
+    const CheckRanges check = call_ranges(
+        R, inp, outp, ext, ext, violation_word(reinterpret_cast<int*>(d.base + kStatusOffset)));
+    rq.check = &check;
+#endif
     // The producers reduce the R inputs and stage the reduced chunk, the
     // consumers copy it to the R outputs: a slot holds one part, so the 8 MiB
     // array fits R + 1 times the channels that staging the R inputs would.

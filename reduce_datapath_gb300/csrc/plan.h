@@ -17,6 +17,10 @@
 #include <cstddef>
 #include <cstdint>
 
+#if defined(PURLIN_CHECKED)
+#include "check.h"
+#endif
+
 #if defined(__CUDACC__)
 #define PURLIN_HD __host__ __device__
 #else
@@ -58,6 +62,10 @@ struct Segment {
 constexpr uint8_t kShiftPerRank = 0x80;
 static_assert(sizeof(Segment) == 32, "Segment is passed by value to kernels");
 
+#if defined(PURLIN_CHECKED)
+static_assert(kMaxCheckRanges >= 2 * kMaxRanks + 1, "check ranges");
+#endif
+
 // Kernel parameter block of the zero-staging Atom kernels (passed as a
 // __grid_constant__ argument: no host-to-device copy per call).
 // L2 eviction priority of a stream (PTX createpolicy).
@@ -75,6 +83,9 @@ struct ZsParams {
     uint32_t nseg;
     uint32_t ntiles;
     uint32_t tile_units;  // units per tile
+#if defined(PURLIN_CHECKED)
+    CheckRanges check;
+#endif
     Segment seg[MAXSEG];
 };
 

@@ -38,6 +38,9 @@ struct SnacRequest {
     uint64_t in[kMaxRanks];
     uint64_t out[kMaxRanks];
     bool stage_y;  // sums: the producer reduces and stages the reduced chunk
+#if defined(PURLIN_CHECKED)
+    const CheckRanges* check;  // the call's buffers
+#endif
 };
 
 struct SnacConfig {

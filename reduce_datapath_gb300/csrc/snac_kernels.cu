@@ -114,6 +114,9 @@ struct SnacParams {
     uint32_t nseg;
     uint32_t nsteps;
     uint32_t inject;
+#if defined(PURLIN_CHECKED)
+    CheckRanges check;
+#endif
     Segment seg[kSegsLarge];  // tile0 = first step of the segment
 };
 
@@ -846,6 +849,7 @@ __device__ void gatherer(const SnacParams& p, uint32_t ch, uint64_t epoch)
 template <typename T, int ORDER, int KIND, bool SHIFTED>
 __global__ void __launch_bounds__(kThreads, 2) snac_kernel(const __grid_constant__ SnacParams p)
 {
+    PURLIN_CHECK_BEGIN(p);
     __shared__ uint64_t epoch_s;
     if (threadIdx.x == 0) {
         uint64_t prev;
@@ -1044,6 +1048,11 @@ purlin_status_t plan_into(KernelLaunch& k, const SnacRequest& rq, const SnacConf
     p.nseg = (uint32_t)nseg;
     p.nsteps = (uint32_t)steps;
     p.inject = (uint32_t)cfg.inject_skip_notify;
+#if defined(PURLIN_CHECKED)
+    // the call's buffers and the staging ring
+    if (rq.check) p.check = *rq.check;
+    add_range(p.check, reinterpret_cast<uint64_t>(cfg.staging), cfg.staging_bytes);
+#endif
 
     const int grid = nch * roles_of(rq.coll, rq.stage_y);
     k.func = reinterpret_cast<const void*>(kernel);

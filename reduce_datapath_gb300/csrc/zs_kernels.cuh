@@ -377,6 +377,7 @@ zs_reduce_kernel(const __grid_constant__ ZsParams<kSegsSmall> p)
 {
     constexpr int U = kMaxRanks / NR;
     pdl_enter();
+    PURLIN_CHECK_BEGIN(p);
     const int R = (int)p.R;
     const uint64_t lpol = atom::l2_policy(p.l2_load);
     const uint64_t spol = atom::l2_policy(p.l2_store);
@@ -483,6 +484,7 @@ __global__ void __launch_bounds__(THREADS, THREADS == kThreads ? 2 : 16)
 zs_copy_kernel(const __grid_constant__ ZsParams<MAXSEG> p)
 {
     pdl_enter();
+    PURLIN_CHECK_BEGIN(p);
     const uint64_t lpol = atom::l2_policy(p.l2_load);
     const uint64_t spol = atom::l2_policy(p.l2_store);
     for (uint32_t t = blockIdx.x; t < p.ntiles; t += gridDim.x) {
@@ -575,6 +577,9 @@ __device__ __forceinline__ void bulk_load(void* smem, const char* gmem, uint32_t
 
 __device__ __forceinline__ void bulk_store(char* gmem, const void* smem, uint32_t bytes)
 {
+#if defined(PURLIN_CHECKED)
+    if (!atom::access_ok(gmem, bytes, 16, false)) return;  // a bulk copy's run: 16-byte aligned
+#endif
     asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
                  ::"l"(gmem), "r"(smem_u32(smem)), "r"(bytes) : "memory");
 }
@@ -622,6 +627,7 @@ zs_copy_bulk_kernel(const __grid_constant__ ZsParams<MAXSEG> p)
     __shared__ __align__(8) uint64_t bar[STAGES];
     const uint32_t G = gridDim.x;
     pdl_enter();
+    PURLIN_CHECK_BEGIN(p);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) mbar_init(&bar[s]);
@@ -641,6 +647,12 @@ zs_copy_bulk_kernel(const __grid_constant__ ZsParams<MAXSEG> p)
             uint64_t base;
             const uint32_t len = tile_len(t, s, base);
             const int st = (int)(n % STAGES);
+#if defined(PURLIN_CHECKED)
+            if (!atom::access_ok(p.in[s.src] + s.src_off + base, len, 16, false)) {
+                mbar_expect_tx(&bar[st], 0);  // skipped: the stage completes with no bytes
+                return;
+            }
+#endif
             mbar_expect_tx(&bar[st], len);
             bulk_load(ring + (size_t)st * kBulkStageBytes, p.in[s.src] + s.src_off + base, len,
                       &bar[st]);

@@ -193,3 +193,20 @@ def test_reference_line_is_short_and_shares_the_config():
     ours = bench.bench_config(1)
     assert ours["workload"] == bench.WORKLOAD_SHORT
     assert len(json.dumps(bench.bench_config(8))) < 200
+
+
+def test_sources_digest_leaves_out_the_checked_build():
+    """Code that only the checked build compiles (blocks under
+    `#if defined(PURLIN_CHECKED)`, PURLIN_CHECK_* lines) does not move the
+    digest; the `#else` branch of such a block and every other conditional do."""
+    import bench
+    base = "int f(int x) { return x + 1; }\n#if defined(FOO)\nint g;\n#endif\n"
+    checked = ("#if defined(PURLIN_CHECKED)\nint chk;\n#if X\nint y;\n#endif\n#endif\n"
+               "int f(int x) {\n    PURLIN_CHECK_STORE(p, 4)\n    return x + 1; }\n"
+               "#if defined(FOO)\nint g;\n#endif\n")
+    with_else = "#if defined(PURLIN_CHECKED)\nint chk;\n#else\nint prod;\n#endif\n" + base
+    other = base.replace("FOO", "BAR")
+    assert bench.code_tokens(base) == bench.code_tokens(checked)
+    assert bench.code_tokens(base) != bench.code_tokens(with_else)
+    assert "int prod;" in bench.code_tokens(with_else)
+    assert bench.code_tokens(base) != bench.code_tokens(other)

@@ -43,8 +43,8 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_version_and_status_strings(lib):
     assert rd.purlin_version() >> 16 == 1
-    for s in range(6):
-        assert rd.purlin_status_string(s)
+    for s in range(7):
+        assert rd.purlin_status_string(s) != "unknown status"
     assert rd.purlin_status_string(99) == "unknown status"
 
 
@@ -63,6 +63,13 @@ def test_null_handle_is_invalid(lib):
     assert lib.purlin_plan_end(None, None) == rd.ERR_INVALID_ARG
     assert lib.purlin_plan_launch(None, None) == rd.ERR_INVALID_ARG
     assert lib.purlin_plan_destroy(None) == rd.OK
+
+
+def test_product_build_is_not_the_checked_one(lib):
+    # the checked build (bounds tests in every kernel access) is a separate
+    # library; the product one reports itself as unchecked
+    assert lib.purlin_debug_checked() == 0
+    assert lib.purlin_debug_violation(None, None) == rd.ERR_INVALID_ARG
 
 
 # ----------------------------------------------------------------- plan tests

@@ -195,6 +195,27 @@ def test_allreduce_sweep_r8(sweep_handle, nbytes, variant, chunk):
     _check_allreduce(x, out, n, sampled=nbytes > 16 * MiB, seed=nbytes)
 
 
+@pytest.mark.parametrize("variant", [rd.VARIANT_ZS, rd.VARIANT_STAGED_Y])
+def test_allreduce_sweep_256MiB_full(sweep_handle, variant):
+    """The largest point of the AllReduce sweep (256 MiB per rank, R=8, bf16)
+    compared in full with the oracle, not on a sample."""
+    R, n = 8, 256 * MiB // 2
+    h = sweep_handle
+    rd.purlin_set_policy(h, 0, 0, 0, variant)
+    x = workloads.rank_buffers("allreduce_sweep_r8", R, n, "bf16", device="cuda",
+                               role=(256 * MiB).bit_length())
+    out = [torch.empty_like(t) for t in x]
+    rd.purlin_all_reduce(h, x, out, n, "bf16")
+    _ok(h)
+    for j in range(1, R):
+        assert torch.equal(out[j].view(torch.int16), out[0].view(torch.int16)), j
+    xs = [host_bits(t) for t in x]
+    del x
+    want = oracle.all_reduce(xs, dtype="bf16")
+    del xs
+    assert _bits_equal(host_bits(out[0]), want[0])
+
+
 # ---------------------------------------------------------------- moe_a2av_r8
 
 ATOMS = [(rd.VARIANT_ZS, rd.ATOM_VECTOR), (rd.VARIANT_ZS, rd.ATOM_BULK),
