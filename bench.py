@@ -289,7 +289,7 @@ def run_cpu_oracle(xh, budget_s, max_reps=20):
     return {"value": reps * (rs + ag) / el / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": f"{reps} full step(s) of the workload (RS then AG, R=8, 8 x 64 MiB bf16) "
                       f"in {el:.1f} s, single-threaded C, {cpu_model()}",
-            "short": f"{reps} steps, {el:.1f} s, {cpu_model()[:16]}",
+            "short": f"{reps} full steps, {el:.1f} s, {cpu_model().split(' (')[0][:24]}",
             "seconds": el}, y, z
 
 
