@@ -152,8 +152,9 @@ typedef struct {
 /* ------------------------------------------------------------------------- */
 
 /* Create a handle for R virtual ranks (1..PURLIN_MAX_RANKS) on CUDA device
- * `device`.  The handle owns the SNAC staging ring (staging_bytes; 0 picks a
- * default sized well below the L2 cache), its ready/free flags and a device
+ * `device`.  The handle owns the SNAC staging ring (staging_bytes; 0 picks
+ * 64 MiB, half the L2 cache: room for a channel on every resident CTA pair at
+ * the default chunks of 8 ranks), its ready/free flags and a device
  * status word, all allocated here with cudaMalloc (PURLIN_ERR_OOM on failure).
  * On success *h receives the handle; on failure *h is set to NULL. */
 PURLIN_API purlin_status_t purlin_create(purlin_handle_t* h, int R, size_t staging_bytes, int device);

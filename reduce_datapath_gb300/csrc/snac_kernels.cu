@@ -63,22 +63,26 @@ enum : int { kReady = 0, kFree = 1, kYReady = 2, kYFree = 3, kStepOf = 4, kYStep
 constexpr uint64_t kNoStep = 0xffffffffull;  // no step left; steps are < 2^32 - 1 (plan_into)
 
 // Default chunk per rank per step, measured best on GB300 at 64 MiB per rank,
-// R = 8, 32 MiB ring, depth 2:
+// R = 8, 64 MiB ring, depth 2 (event-timed, 20 launches; the time is not
+// monotonic in the chunk, so each default is the best of a sweep that was
+// the same at a 48 MiB ring):
 //   - sums with the inputs staged put R + 1 parts in a slot and favour many
-//     channels of small chunks (AllReduce 3468 GB/s at 16 KiB vs 2102 at 64 KiB);
+//     channels of small chunks: ReduceScatter 186.9 us at 24 KiB (196.5 at 16,
+//     198.7 at 32 KiB), AllReduce 291.4 us at 24 KiB (311.6 at 16, 352.9 at 12);
 //   - sums with the reduced chunk staged put one part in a slot: AllReduce
-//     198.4 us at 64 KiB (200.4 at 32 KiB, 218.6 at 128 KiB), ReduceScatter
-//     122.5 us at 64 KiB (130.2 at 128 KiB);
+//     193.7 us at 48 KiB and 194.5 at 64 KiB, ReduceScatter 120.5 us at 64 KiB
+//     (123.7 at 56, 125.4 at 80 KiB);
 //   - copies put one part in a slot; with steps handed out from a counter the
-//     AllGather runs 115.0 us at 64 KiB (135.4 at 128 KiB, 169.1 at 256 KiB),
-//     the AllToAllV 270.3 us at 128 KiB (301.6 at 64 KiB, 343.7 at 256 KiB).
+//     AllGather runs 120.4 us at 64 KiB (116.2 at 48 and 96 KiB, 122.6 at 80,
+//     129.7 at 112 KiB), the AllToAllV 253.9 us at 192 KiB (267.1 at 128,
+//     259.3 at 208 KiB).
 size_t default_chunk(Coll coll, bool stage_y)
 {
     if (stage_y && (coll == Coll::ReduceScatter || coll == Coll::AllReduce)) return 64 * 1024;
     switch (coll) {
     case Coll::AllGather: return 64 * 1024;
-    case Coll::AllToAllV: return 128 * 1024;
-    default: return 16 * 1024;
+    case Coll::AllToAllV: return 192 * 1024;
+    default: return 24 * 1024;
     }
 }
 
