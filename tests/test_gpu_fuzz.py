@@ -6,7 +6,9 @@ displacements, a datapath (zero staging with one of three copy Atoms, or SNAC
 with a random chunk, depth and channel count), the launch shape (one-warp or
 256-thread CTAs) and, for sums, the rank order.
 The outputs must equal the oracle's bit for bit and the canary guards around
-every output must survive.
+every output must survive.  Run with PURLIN_LIBRARY=checked (after
+reduce_datapath_gb300.build(checked=True)) the same cases also assert that no
+kernel access left the call's buffers.
 """
 import os
 
@@ -130,6 +132,9 @@ def _case(seed, scale):
             want = oracle.all_to_all_v([host_bits(t) for t in x], C)
         torch.cuda.synchronize()
         assert rd.purlin_query_status(h) == rd.OK
+        # under the checked build (PURLIN_LIBRARY=checked) no access may leave
+        # the call's buffers; the product build reports 0
+        assert rd.purlin_debug_violation(h) == 0
         for j in range(R):
             assert same_bits(host_bits(outs[j].view), want[j]), (coll, R, dtype, j)
             assert outs[j].guards_intact()
