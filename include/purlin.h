@@ -249,11 +249,11 @@ PURLIN_API purlin_status_t purlin_all_to_all_v(purlin_handle_t h, const void* co
  *   R            1..PURLIN_MAX_RANKS;  count: elements per rank.
  *   dtype        PURLIN_F32, PURLIN_BF16 or PURLIN_F16.
  *   chunk_bytes  staged bytes per rank per pipeline step, a multiple of 256
- *                (0 = 32 KiB); depth: ring slots, 0..8 (0 = 2).  A channel's
+ *                (0 = 8 KiB); depth: ring slots, 0..8 (0 = 2).  A channel's
  *                ring that cannot fit in the static array -- depth * chunk_bytes
  *                above PURLIN_NOALLOC_SCRATCH_BYTES - 64 KiB -- is rejected with
  *                PURLIN_ERR_INVALID_ARG before anything is enqueued; the array
- *                holds as many channels as fit (127 at the defaults).
+ *                holds as many channels as fit (508 at the defaults).
  *   device_status  optional DEVICE int: set to 0 on the stream, then to
  *                PURLIN_ERR_TIMEOUT if a bounded wait of the kernel ran out
  *                (NULL: the library's own word inside the static array is used

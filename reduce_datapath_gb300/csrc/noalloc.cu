@@ -29,10 +29,10 @@ namespace {
 constexpr size_t kScratchBytes = PURLIN_NOALLOC_SCRATCH_BYTES;
 constexpr size_t kStatusOffset = 0;               // one int, padded to 256 bytes
 constexpr size_t kFlagsOffset = 256;
-constexpr size_t kFlagWords = 4096;               // 32 KiB of uint64 flags
+constexpr size_t kFlagWords = (64 * 1024 - 256) / 8;  // the rest of the header: 8160 flags
 constexpr size_t kStagingOffset = 64 * 1024;      // the rest is the staging ring
 constexpr size_t kStagingBytes = kScratchBytes - kStagingOffset;
-constexpr size_t kDefaultChunk = 32 * 1024;
+constexpr size_t kDefaultChunk = 8 * 1024;  // 508 channels of 64-thread role CTAs
 constexpr int kDefaultDepth = 2;
 constexpr uint64_t kTimeoutNs = 1000000000ull;
 constexpr int kMaxDevices = 64;

@@ -63,26 +63,26 @@ enum : int { kReady = 0, kFree = 1, kYReady = 2, kYFree = 3, kStepOf = 4, kYStep
 constexpr uint64_t kNoStep = 0xffffffffull;  // no step left; steps are < 2^32 - 1 (plan_into)
 
 // Default chunk per rank per step, measured best on GB300 at 64 MiB per rank,
-// R = 8, 64 MiB ring, depth 2 (event-timed, 20 launches; the time is not
-// monotonic in the chunk, so each default is the best of a sweep that was
-// the same at a 48 MiB ring):
+// R = 8, depth 2, 64-thread role CTAs (event-timed, 20 launches; the time is not
+// monotonic in the chunk, so each default is the best of a sweep):
 //   - sums with the inputs staged put R + 1 parts in a slot and favour many
-//     channels of small chunks: ReduceScatter 186.9 us at 24 KiB (196.5 at 16,
-//     198.7 at 32 KiB), AllReduce 291.4 us at 24 KiB (311.6 at 16, 352.9 at 12);
-//   - sums with the reduced chunk staged put one part in a slot: AllReduce
-//     193.7 us at 48 KiB and 194.5 at 64 KiB, ReduceScatter 120.5 us at 64 KiB
-//     (123.7 at 56, 125.4 at 80 KiB);
-//   - copies put one part in a slot; with steps handed out from a counter the
-//     AllGather runs 120.4 us at 64 KiB (116.2 at 48 and 96 KiB, 122.6 at 80,
-//     129.7 at 112 KiB), the AllToAllV 253.9 us at 192 KiB (267.1 at 128,
-//     259.3 at 208 KiB).
+//     channels of small chunks: ReduceScatter 176.0 us at 6 KiB (185.7 at 8,
+//     231.0 at 12 KiB), AllReduce 264.4 us at 8 KiB (285.1 at 12, 331.0 at 16);
+//   - sums with the reduced chunk staged put one part in a slot: ReduceScatter
+//     117.9 us at 16 KiB (121.4 at 24, 127.0 at 32 KiB), AllReduce 186.2 us at
+//     12 KiB (188.2 at 16, 189.9 at 24 KiB);
+//   - copies put one part in a slot: AllGather 104.7 us at 16 KiB (106.4 at 12,
+//     108.7 at 24, 114.5 at 32 KiB), AllToAllV 241.3 us at 48 KiB (247.0 at 32,
+//     254.1 at 64 KiB).
 size_t default_chunk(Coll coll, bool stage_y)
 {
-    if (stage_y && (coll == Coll::ReduceScatter || coll == Coll::AllReduce)) return 64 * 1024;
+    const bool sum = coll == Coll::ReduceScatter || coll == Coll::AllReduce;
+    if (stage_y && sum) return coll == Coll::ReduceScatter ? 16 * 1024 : 12 * 1024;
     switch (coll) {
-    case Coll::AllGather: return 64 * 1024;
-    case Coll::AllToAllV: return 192 * 1024;
-    default: return 24 * 1024;
+    case Coll::AllGather: return 16 * 1024;
+    case Coll::AllToAllV: return 48 * 1024;
+    case Coll::ReduceScatter: return 6 * 1024;
+    default: return 8 * 1024;
     }
 }
 
@@ -94,8 +94,16 @@ __host__ __device__ constexpr int snac_max_unit(int kind, bool shifted)
     return (shifted && kind != kAG && kind != kA2A) ? 4 : 5;
 }
 
+// Role CTAs of two warps, eight per SM (128 registers a thread, as 256-thread
+// CTAs at two per SM have): more, narrower channels.  At 64 MiB per rank, R = 8,
+// bf16, each kind at its best chunk, 256 / 128 / 64 / 32 threads per CTA:
+// AllGather 115-120 / 109.8 / 104.7 / 104.1 us, AllReduce with the inputs staged
+// 290 / 266.3 / 264.4 / 285.8, ReduceScatter with the inputs staged 185 / 174.7 /
+// 176.0 / 185.7, AllToAllV 251 / 240.8 / 241.3 / 247.8.
+constexpr int kSnacThreads = 64;
+constexpr int kSnacCtasPerSm = 8;
 constexpr int kDefaultDepth = 2;
-constexpr int kMaxChannels = 256;
+constexpr int kMaxChannels = 640;
 constexpr size_t kMinAutoChunk = 1024;
 
 struct SnacParams {
@@ -244,16 +252,16 @@ __device__ __forceinline__ void cta_copy(const SnacParams& p, char* dst, uint64_
                                          uint64_t lpol, uint64_t spol)
 {
     constexpr int U = 4;
-    for (uint64_t base = 0; base < len; base += (uint64_t)kThreads * B * U) {
+    for (uint64_t base = 0; base < len; base += (uint64_t)kSnacThreads * B * U) {
         atom::Unit<B> u[U];
 #pragma unroll
         for (int k = 0; k < U; ++k) {
-            const uint64_t o = base + (uint64_t)(k * kThreads + threadIdx.x) * B;
+            const uint64_t o = base + (uint64_t)(k * kSnacThreads + threadIdx.x) * B;
             if (o < len) load_pol<B, SRC_CG>(u[k], src + o, lpol);
         }
 #pragma unroll
         for (int k = 0; k < U; ++k) {
-            const uint64_t o = base + (uint64_t)(k * kThreads + threadIdx.x) * B;
+            const uint64_t o = base + (uint64_t)(k * kSnacThreads + threadIdx.x) * B;
             if (o >= len) continue;
             if (FAN) {
                 for (int r = 0; r < (int)p.R; ++r) {
@@ -295,7 +303,7 @@ __device__ __forceinline__ void cta_stage_ranks(const SnacParams& p, char* stage
                                                 uint64_t src_off, uint64_t len, uint64_t lpol)
 {
     const int R = (int)p.R;
-    for (uint64_t o = (uint64_t)threadIdx.x * B; o < len; o += (uint64_t)kThreads * B) {
+    for (uint64_t o = (uint64_t)threadIdx.x * B; o < len; o += (uint64_t)kSnacThreads * B) {
         atom::Unit<B> u[kMaxRanks];
 #pragma unroll
         for (int r = 0; r < kMaxRanks; ++r)
@@ -328,7 +336,7 @@ __device__ __forceinline__ void cta_reduce_vec(const SnacParams& p, char* dst, c
                                                uint64_t len, uint64_t spol)
 {
     const int R = (int)p.R;
-    for (uint64_t o = (uint64_t)threadIdx.x * B; o < len; o += (uint64_t)kThreads * B) {
+    for (uint64_t o = (uint64_t)threadIdx.x * B; o < len; o += (uint64_t)kSnacThreads * B) {
         atom::Vec<B> v[kMaxRanks];
 #pragma unroll
         for (int r = 0; r < kMaxRanks; ++r)
@@ -344,7 +352,7 @@ __device__ __forceinline__ void cta_reduce_elem(const SnacParams& p, char* dst, 
                                                 uint64_t len)
 {
     const int R = (int)p.R;
-    for (uint64_t o = (uint64_t)threadIdx.x * T::kBytes; o < len; o += (uint64_t)kThreads * T::kBytes) {
+    for (uint64_t o = (uint64_t)threadIdx.x * T::kBytes; o < len; o += (uint64_t)kSnacThreads * T::kBytes) {
         float v[kMaxRanks];
 #pragma unroll
         for (int r = 0; r < kMaxRanks; ++r) v[r] = (r < R) ? T::load1_cg(staged + r * p.chunk + o) : 0.0f;
@@ -371,7 +379,7 @@ __device__ __forceinline__ void cta_reduce_src_vec(const SnacParams& p, char* ds
                                                    uint64_t spol)
 {
     const int R = (int)p.R;
-    for (uint64_t o = (uint64_t)threadIdx.x * B; o < len; o += (uint64_t)kThreads * B) {
+    for (uint64_t o = (uint64_t)threadIdx.x * B; o < len; o += (uint64_t)kSnacThreads * B) {
         atom::Vec<B> v[kMaxRanks];
 #pragma unroll
         for (int r = 0; r < kMaxRanks; ++r)
@@ -387,7 +395,7 @@ __device__ __forceinline__ void cta_reduce_src_elem(const SnacParams& p, char* d
                                                     uint64_t src_off, uint64_t len)
 {
     const int R = (int)p.R;
-    for (uint64_t o = (uint64_t)threadIdx.x * T::kBytes; o < len; o += (uint64_t)kThreads * T::kBytes) {
+    for (uint64_t o = (uint64_t)threadIdx.x * T::kBytes; o < len; o += (uint64_t)kSnacThreads * T::kBytes) {
         float v[kMaxRanks];
 #pragma unroll
         for (int r = 0; r < kMaxRanks; ++r) v[r] = (r < R) ? T::load1(p.in[r] + src_off + o) : 0.0f;
@@ -424,7 +432,7 @@ __device__ void cta_copy_shifted(const char* src, char* dst, uint64_t len, uint6
                                  uint64_t spol)
 {
     constexpr int W = B / 4;
-    constexpr int WARPS = kThreads / 32;
+    constexpr int WARPS = kSnacThreads / 32;
     constexpr int U = 2;
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -474,7 +482,7 @@ __device__ void stage_ranks_shifted_rows(const SnacParams& p, char* staged, uint
 {
     constexpr int B = 16;
     constexpr int W = B / 4;
-    constexpr int WARPS = kThreads / 32;
+    constexpr int WARPS = kSnacThreads / 32;
     constexpr int U = kMaxRanks / NR;
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -522,7 +530,7 @@ __device__ void cta_stage_ranks_shifted(const SnacParams& p, const Segment& s, c
 {
     constexpr int B = 16;
     constexpr int W = B / 4;
-    constexpr int WARPS = kThreads / 32;
+    constexpr int WARPS = kSnacThreads / 32;
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int R = (int)p.R;
@@ -574,7 +582,7 @@ __device__ void reduce_src_shifted_rows(const SnacParams& p, char* dst, uint64_t
 {
     constexpr int B = 16;
     constexpr int W = B / 4;
-    constexpr int WARPS = kThreads / 32;
+    constexpr int WARPS = kSnacThreads / 32;
     constexpr int U = kMaxRanks / NR;
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -621,7 +629,7 @@ __device__ void cta_reduce_src_shifted(const SnacParams& p, const Segment& s, ch
 {
     constexpr int B = 16;
     constexpr int W = B / 4;
-    constexpr int WARPS = kThreads / 32;
+    constexpr int WARPS = kSnacThreads / 32;
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int R = (int)p.R;
@@ -851,7 +859,7 @@ __device__ void gatherer(const SnacParams& p, uint32_t ch, uint64_t epoch)
 
 // SHIFTED: the plan holds a shifted body (only such launches carry that path).
 template <typename T, int ORDER, int KIND, bool SHIFTED>
-__global__ void __launch_bounds__(kThreads, 2) snac_kernel(const __grid_constant__ SnacParams p)
+__global__ void __launch_bounds__(kSnacThreads, kSnacCtasPerSm) snac_kernel(const __grid_constant__ SnacParams p)
 {
     PURLIN_CHECK_BEGIN(p);
     __shared__ uint64_t epoch_s;
@@ -1008,7 +1016,7 @@ purlin_status_t plan_into(KernelLaunch& k, const SnacRequest& rq, const SnacConf
     }
 
     SnacKernel kernel = kernel_for(rq.coll, rq.dtype, rq.order, rq.stage_y, shifted);
-    const int resident = resident_ctas_of(reinterpret_cast<const void*>(kernel), kThreads);
+    const int resident = resident_ctas_of(reinterpret_cast<const void*>(kernel), kSnacThreads);
     if (resident < 1) return PURLIN_ERR_CUDA;
     size_t chunk = 0;
     int depth = 0, nch = 0;
@@ -1026,7 +1034,7 @@ purlin_status_t plan_into(KernelLaunch& k, const SnacRequest& rq, const SnacConf
         if (steps > 0xffffffffull) return PURLIN_ERR_UNSUPPORTED;
     }
     if (steps == 0) {
-        *launch = SnacLaunch{0, 0, kThreads, depth, 0, chunk};
+        *launch = SnacLaunch{0, 0, kSnacThreads, depth, 0, chunk};
         return PURLIN_OK;
     }
     nch = (int)std::min<uint64_t>((uint64_t)nch, steps);
@@ -1061,12 +1069,12 @@ purlin_status_t plan_into(KernelLaunch& k, const SnacRequest& rq, const SnacConf
     const int grid = nch * roles_of(rq.coll, rq.stage_y);
     k.func = reinterpret_cast<const void*>(kernel);
     k.grid = (unsigned)grid;
-    k.block = kThreads;
+    k.block = kSnacThreads;
     k.smem = 0;
     k.pdl = false;
     k.cooperative = true;  // every waiter's partner must be resident
     k.params_bytes = sizeof(SnacParams);
-    *launch = SnacLaunch{1, grid, kThreads, depth, nch, chunk};
+    *launch = SnacLaunch{1, grid, kSnacThreads, depth, nch, chunk};
     return PURLIN_OK;
 }
 
