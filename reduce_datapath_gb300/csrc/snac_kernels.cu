@@ -184,7 +184,7 @@ __device__ bool cta_wait(const SnacParams& p, const uint64_t* flag, uint64_t wan
                     break;
                 }
             }
-            __nanosleep(100);
+            if (spins > 64) __nanosleep(100);
         }
         go = ok;
     }
@@ -689,7 +689,10 @@ __device__ __forceinline__ void st_relaxed(uint64_t* w, uint64_t v)
 // Every kind hands out steps from a counter instead of dealing them
 // round-robin: a channel whose SM drains faster takes more steps, so the
 // slowest SMs do not set the time.  The producer records the step in the slot's step
-// word before notifying; the consumer reads it after the acquire.
+// word before notifying; the consumer reads it after the acquire.  When the plan
+// has one step per channel (nsteps == nch: channel ch's step is ch, and the
+// counter has nothing left), every role leaves after that step instead of
+// passing an end-of-steps marker down the pipeline.
 template <typename T, int ORDER, int KIND, bool SHIFTED>
 __device__ void producer_dynamic(const SnacParams& p, uint32_t ch, uint64_t epoch)
 {
@@ -750,6 +753,7 @@ __device__ void producer_dynamic(const SnacParams& p, uint32_t ch, uint64_t epoc
         if (threadIdx.x == 0) st_relaxed(f + kStepOf, i);
         if (p.inject && ch == 0 && n == 0) continue;  // testing: this notify never happens
         cta_notify(f + kReady, tag_of(epoch, n));
+        if (p.nsteps == p.nch) return;  // one step per channel: no end-of-steps round
     }
 }
 
@@ -792,6 +796,7 @@ __device__ void consumer_dynamic(const SnacParams& p, uint32_t ch, uint64_t epoc
                                       len, 0, lpol, spol);
         }
         cta_notify(f + kFree, tag_of(epoch, n));
+        if (p.nsteps == p.nch) return;
     }
 }
 
@@ -825,7 +830,7 @@ __device__ void consumer_ar(const SnacParams& p, uint32_t ch, uint64_t epoch)
         if (threadIdx.x == 0) st_relaxed(f + kYStepOf, i);  // kNoStep passes through
         cta_notify(f + kFree, tag_of(epoch, n));
         if (threadIdx.x == 0) st_release(f + kYReady, tag_of(epoch, n));
-        if (i >= p.nsteps) return;
+        if (i >= p.nsteps || p.nsteps == p.nch) return;
     }
 }
 
@@ -854,6 +859,7 @@ __device__ void gatherer(const SnacParams& p, uint32_t ch, uint64_t epoch)
         cta_copy_any<true, true, MAXU>(p, s.unit_log2, nullptr, s.dst_off + off, y, len, 0, lpol,
                                        spol);
         cta_notify(f + kYFree, tag_of(epoch, n));
+        if (p.nsteps == p.nch) return;
     }
 }
 
