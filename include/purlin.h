@@ -156,7 +156,15 @@ typedef struct {
  * 64 MiB, half the L2 cache: room for a channel on every resident CTA pair at
  * the default chunks of 8 ranks), its ready/free flags and a device
  * status word, all allocated here with cudaMalloc (PURLIN_ERR_OOM on failure).
- * On success *h receives the handle; on failure *h is set to NULL. */
+ * On success *h receives the handle; on failure *h is set to NULL.
+ * Environment, read here, for measurements and sweeps only (the defaults are the
+ * measured best; a value out of range is ignored): PURLIN_CHUNK, PURLIN_DEPTH,
+ * PURLIN_CTAS and PURLIN_VARIANT set the initial policy as purlin_set_policy
+ * would; PURLIN_SMALL_TILES as purlin_set_small_tiles; PURLIN_PDL (0 turns
+ * programmatic dependent launch off); PURLIN_L2_LOAD / PURLIN_L2_STORE and
+ * PURLIN_L2_<RS|AG|AR|A2A>_<LOAD|STORE> (0 normal, 1 evict-first, 2 evict-last)
+ * set the L2 priority of the zero-staging kernels' streams; PURLIN_MAX_UNIT
+ * (2..32 bytes) caps their vector unit. */
 PURLIN_API purlin_status_t purlin_create(purlin_handle_t* h, int R, size_t staging_bytes, int device);
 
 /* Synchronize the device, free everything the handle owns, free the handle.

@@ -866,6 +866,24 @@ purlin_status_t purlin_create(purlin_handle_t* out, int R, size_t staging_bytes,
         for (int l = 1; l <= 5; ++l)
             if (v == (1 << l)) h->max_unit_log2 = l;
     }
+    // The handle's initial policy, for sweeps: each value that purlin_set_policy
+    // would accept replaces the default; anything else is ignored.
+    if (const char* u = std::getenv("PURLIN_CHUNK")) {
+        const long long v = std::atoll(u);
+        if (v > 0 && v % 16 == 0) h->chunk_bytes = (size_t)v;
+    }
+    if (const char* u = std::getenv("PURLIN_DEPTH")) {
+        const int v = std::atoi(u);
+        if (v >= 1 && v <= 8) h->depth = v;
+    }
+    if (const char* u = std::getenv("PURLIN_CTAS")) {
+        const int v = std::atoi(u);
+        if (v >= 1 && v <= 65535) h->ctas = v;
+    }
+    if (const char* u = std::getenv("PURLIN_VARIANT")) {
+        const int v = std::atoi(u);
+        if (v >= PURLIN_VARIANT_AUTO && v <= PURLIN_VARIANT_STAGED_Y) h->variant = v;
+    }
     *out = h;
     return PURLIN_OK;
 }
