@@ -163,9 +163,11 @@ __device__ __forceinline__ int ld_status(const int* s)
     return v;
 }
 
-// Bounded wait of one CTA for *flag >= want.  Thread 0 spins; the outcome is
-// shared through shared memory.  Returns false if the CTA must leave (this
-// wait timed out, or another CTA recorded an error).
+// Bounded wait of one CTA for *flag >= want.  Thread 0 polls, the first 64
+// times back to back (a short message's next step is usually a round trip
+// away) and then with a 100 ns sleep between polls; the outcome is shared
+// through shared memory.  Returns false if the CTA must leave (this wait timed
+// out, or another CTA recorded an error).
 __device__ bool cta_wait(const SnacParams& p, const uint64_t* flag, uint64_t want)
 {
     __shared__ int go;
