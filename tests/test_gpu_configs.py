@@ -166,9 +166,10 @@ def _check_allreduce(x, out, n, sampled, seed):
 
 
 SWEEP = [(b, v, ch) for b in workloads.SWEEP_BYTES for (v, ch) in
-         [(rd.VARIANT_ZS, 0), (rd.VARIANT_STAGED, 64 * 1024), (rd.VARIANT_STAGED, 256 * 1024),
-          (rd.VARIANT_STAGED, 1 * MiB), (rd.VARIANT_STAGED, 2 * MiB),
-          (rd.VARIANT_STAGED_Y, 64 * 1024), (rd.VARIANT_STAGED_Y, 2 * MiB)]]
+         [(rd.VARIANT_ZS, 0), (rd.VARIANT_STAGED, 0), (rd.VARIANT_STAGED, 64 * 1024),
+          (rd.VARIANT_STAGED, 256 * 1024), (rd.VARIANT_STAGED, 1 * MiB), (rd.VARIANT_STAGED, 2 * MiB),
+          (rd.VARIANT_STAGED_Y, 0), (rd.VARIANT_STAGED_Y, 64 * 1024),
+          (rd.VARIANT_STAGED_Y, 2 * MiB)]]
 
 
 @pytest.fixture(scope="module")
@@ -195,7 +196,7 @@ def test_allreduce_sweep_r8(sweep_handle, nbytes, variant, chunk):
     _check_allreduce(x, out, n, sampled=nbytes > 16 * MiB, seed=nbytes)
 
 
-@pytest.mark.parametrize("variant", [rd.VARIANT_ZS, rd.VARIANT_STAGED_Y])
+@pytest.mark.parametrize("variant", [rd.VARIANT_ZS, rd.VARIANT_STAGED, rd.VARIANT_STAGED_Y])
 def test_allreduce_sweep_256MiB_full(sweep_handle, variant):
     """The largest point of the AllReduce sweep (256 MiB per rank, R=8, bf16)
     compared in full with the oracle, not on a sample."""
