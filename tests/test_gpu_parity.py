@@ -817,3 +817,49 @@ def test_all_reduce_in_place_on_different_grids(dtype):
     run_ok(h)
     for j in range(R):
         assert same_bits(host_bits(x[j]), want[j]), j
+
+
+# ------------------------------------------------- staged steps vs channels
+
+@pytest.mark.parametrize("variant", [rd.VARIANT_STAGED, rd.VARIANT_STAGED_Y])
+@pytest.mark.parametrize("steps", [3, 4, 5, 8, 9])
+def test_staged_steps_around_the_channel_count(variant, steps):
+    """A staged call on 4 channels of 4 KiB chunks whose step count sits below,
+    at and above the channel count: with one step per channel every role leaves
+    after its step, otherwise the channels take further steps from the device
+    counter.  AllReduce (the whole vector in `steps` chunks), ReduceScatter and
+    AllGather (one piece per rank, `steps` chunks in all where R divides it)."""
+    R, chunk = 4, 4096
+    h = handle(R)
+    set_variant(h, variant, chunk=chunk, depth=2, ctas=4)
+    try:
+        _staged_steps_case(h, R, chunk, steps)
+    finally:
+        set_variant(h, rd.VARIANT_AUTO)
+
+
+def _staged_steps_case(h, R, chunk, steps):
+    n = steps * chunk // 2 - 3   # bf16 elements: the last chunk is ragged
+    x = inputs(R, n, "bf16", seed=300 + steps)
+    out = [Guarded(n, "bf16") for _ in range(R)]
+    rd.purlin_all_reduce(h, x, [o.view for o in out], n, "bf16")
+    run_ok(h)
+    assert rd.purlin_last_launch(h)["chunk_bytes"] == chunk
+    want = oracle.all_reduce(oracle_in(x), dtype="bf16")
+    for j in range(R):
+        assert same_bits(host_bits(out[j].view), want[j]) and out[j].guards_intact()
+    # one piece of ceil(steps / R) chunks per rank
+    c = -(-steps // R) * chunk // 2 - 1
+    x = inputs(R, R * c, "bf16", seed=400 + steps)
+    rs = [Guarded(c, "bf16") for _ in range(R)]
+    rd.purlin_reduce_scatter(h, x, [o.view for o in rs], [c] * R, None, "bf16")
+    run_ok(h)
+    want = oracle.reduce_scatter(oracle_in(x), [c] * R, dtype="bf16")
+    for j in range(R):
+        assert same_bits(host_bits(rs[j].view), want[j]) and rs[j].guards_intact()
+    ag = [Guarded(R * c, "bf16") for _ in range(R)]
+    rd.purlin_all_gather(h, [o.view for o in rs], [o.view for o in ag], [c] * R, None, "bf16")
+    run_ok(h)
+    want = np.concatenate([host_bits(o.view) for o in rs])
+    for j in range(R):
+        assert same_bits(host_bits(ag[j].view), want) and ag[j].guards_intact()
