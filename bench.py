@@ -524,7 +524,8 @@ def compact_line(*, world, steps, warmup, value, ms_per_step, variant, roofline,
         "e2e": {"value": _r(e2e["value"], 1), "unit": e2e["unit"],
                 "h2d_bytes_per_step": e2e["h2d_bytes_per_step"],
                 "d2h_bytes_per_step": e2e["d2h_bytes_per_step"],
-                "ms_per_step": _r(e2e.get("ms_per_step"), 3), "steps": e2e.get("steps")},
+                "ms_per_step": _r(e2e.get("ms_per_step"), 2),
+                "link_frac": _r(e2e.get("link_frac"), 2)},
         "cpu_baseline": None if cpu is None else
         {"value": _r(cpu["value"], 3), "unit": cpu["unit"], "cores": cpu["cores"],
          "kind": cpu["kind"], "sample": cpu.get("short", "full steps")},
@@ -1399,14 +1400,39 @@ def bench_e2e(args, rd, torch, h, x, y, z, counts, stream):
         torch.cuda.synchronize()
         return start.elapsed_time(end)
 
+    def link_gbs(upload, download, reps=3):
+        """This machine's host link on the same pinned buffers: the step's uploads,
+        its downloads, or both at once on their two streams."""
+        nbytes = 0
+        torch.cuda.synchronize()
+        t = time.perf_counter()
+        for _ in range(reps):
+            if upload:
+                with torch.cuda.stream(up):
+                    for a, src in zip(xs[0], xh):
+                        a.copy_(src, non_blocking=True)
+                nbytes += sum(t_.numel() * t_.element_size() for t_ in xh)
+            if download:
+                with torch.cuda.stream(down):
+                    for dst, a in zip(zh, zs[0]):
+                        dst.copy_(a, non_blocking=True)
+                nbytes += sum(t_.numel() * t_.element_size() for t_ in zh)
+        torch.cuda.synchronize()
+        return nbytes / (time.perf_counter() - t) / 1e9
+
     run(2)
     K = max(1, args.e2e_steps)
     ms = run(K) / K
     rs_b, ag_b = step_bytes()
+    h2d = sum(t.numel() * t.element_size() for t in xh)
+    d2h = sum(t.numel() * t.element_size() for t in zh)
+    link = {"h2d_gbs": round(link_gbs(True, False), 1), "d2h_gbs": round(link_gbs(False, True), 1),
+            "both_gbs": round(link_gbs(True, True), 1)}
     return {"value": (rs_b + ag_b) / (ms / 1e3) / 1e9, "unit": UNIT,
-            "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in xh),
-            "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in zh),
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "ms_per_step": ms, "steps": K,
+            # the step's transfers over the link's rate with both directions busy
+            "link_frac": (h2d + d2h) / (ms / 1e3) / 1e9 / link["both_gbs"], "link": link,
             "note": "pinned host buffers; upload, compute and download pipelined across steps"}
 
 

@@ -121,6 +121,8 @@ def _worst_case_line(bench):
                                     551648256, "in step")
     e2e = {"value": 363.61234567, "unit": "GB/s", "h2d_bytes_per_step": 536870912,
            "d2h_bytes_per_step": 536870912, "ms_per_step": 3.3212345678, "steps": 20,
+           "link_frac": 0.9612345678, "link": {"h2d_gbs": 209.7, "d2h_gbs": 192.3,
+                                               "both_gbs": 335.1},
            "note": "a long note that must not reach the line " * 4}
     cpu = {"value": 1.7871234567, "unit": "GB/s", "cores": 1, "kind": "oracle",
            "sample": "a long sample description " * 10,
@@ -166,8 +168,9 @@ def test_result_line_is_last_short_and_parses():
     assert rf["dram_frac"] == pytest.approx(551648256 / 97.12345678e-6 / 1e9 / 6785.9, rel=1e-3)
     assert got["step_dram_frac"] == pytest.approx(1141000000 / 0.17212345678e-3 / 1e9 / 6785.9,
                                                   rel=1e-3)
-    for key in ("value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step"):
+    for key in ("value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step", "link_frac"):
         assert key in got["e2e"]
+    assert "link" not in got["e2e"] and "note" not in got["e2e"]
     for key in ("value", "unit", "cores", "kind", "sample"):
         assert key in got["cpu_baseline"]
     assert json.loads(out[0])["studies"] == studies
