@@ -320,12 +320,16 @@ PURLIN_API purlin_status_t purlin_plan_destroy(purlin_plan_t plan);
  *   chunk_bytes  SNAC bytes per rank per pipeline step, a multiple of 16 (the
  *                staged kernels round it up to a multiple of 256).  A staged call
  *                whose ring cannot hold one channel -- depth x chunk x (R + 1 for
- *                AllReduce, R for ReduceScatter, 1 for copies) above the
- *                handle's staging bytes -- returns PURLIN_ERR_UNSUPPORTED.
+ *                an AllReduce staging its inputs, R for a ReduceScatter staging
+ *                its inputs, 1 for copies and for sums staging the reduced
+ *                chunk) above the handle's staging bytes -- returns
+ *                PURLIN_ERR_UNSUPPORTED.
  *   depth        SNAC ring slots per channel, 1..8.
  *   ctas         0..65535: CTAs per zero-staging launch (automatic: 16 per
  *                resident CTA slot of the device, 4 for the TMA bulk Atom, at
- *                most one per tile), or SNAC channels (CTAs per role).
+ *                most one per tile), or SNAC channels (CTAs per role; a role
+ *                CTA has 64 threads, up to 8 per SM: automatic is every channel
+ *                the residency, the ring and the flags allow).
  *   variant      a purlin_variant_t.
  * Out-of-range values: PURLIN_ERR_INVALID_ARG. */
 PURLIN_API purlin_status_t purlin_set_policy(purlin_handle_t h, size_t chunk_bytes, int depth,
