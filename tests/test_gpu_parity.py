@@ -863,3 +863,35 @@ def _staged_steps_case(h, R, chunk, steps):
     want = np.concatenate([host_bits(o.view) for o in rs])
     for j in range(R):
         assert same_bits(host_bits(ag[j].view), want) and ag[j].guards_intact()
+
+
+@pytest.mark.parametrize("variant", [rd.VARIANT_STAGED, rd.VARIANT_STAGED_Y])
+def test_staged_calls_on_two_handles_at_once(variant):
+    """Two handles (each with its own ring, flags and status word) run staged
+    AllReduces on two streams at the same time, several calls deep: every call
+    must finish and give the oracle's bits.  (The allocation-free AllReduce,
+    whose one static array all calls share, is the documented exception.)"""
+    R, n = 8, (4 << 20) // 2 + 5
+    hs = [rd.purlin_create(R), rd.purlin_create(R)]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    try:
+        xs = [inputs(R, n, "bf16", seed=500 + k) for k in range(2)]
+        wants = [oracle.all_reduce(oracle_in(x), dtype="bf16") for x in xs]
+        outs = [[[torch.empty_like(t) for t in xs[k]] for _ in range(3)] for k in range(2)]
+        for h in hs:
+            set_variant(h, variant)
+        torch.cuda.synchronize()
+        for rep in range(3):
+            for k in range(2):
+                with torch.cuda.stream(streams[k]):
+                    rd.purlin_all_reduce(hs[k], xs[k], outs[k][rep], n, "bf16",
+                                         stream=streams[k])
+        torch.cuda.synchronize()
+        for k in range(2):
+            run_ok(hs[k])
+            for rep in range(3):
+                for j in range(R):
+                    assert same_bits(host_bits(outs[k][rep][j]), wants[k][j]), (k, rep, j)
+    finally:
+        for h in hs:
+            rd.purlin_destroy(h)
