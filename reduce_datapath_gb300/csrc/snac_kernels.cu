@@ -63,26 +63,32 @@ enum : int { kReady = 0, kFree = 1, kYReady = 2, kYFree = 3, kStepOf = 4, kYStep
 constexpr uint64_t kNoStep = 0xffffffffull;  // no step left; steps are < 2^32 - 1 (plan_into)
 
 // Default chunk per rank per step, measured best on GB300 at 64 MiB per rank,
-// R = 8, depth 2, 64-thread role CTAs (event-timed, 20 launches; the time is not
+// depth 2, 64-thread role CTAs (event-timed, 20 launches; the time is not
 // monotonic in the chunk, so each default is the best of a sweep):
-//   - sums with the inputs staged put R + 1 parts in a slot and favour many
-//     channels of small chunks: ReduceScatter 176.0 us at 6 KiB (185.7 at 8,
-//     231.0 at 12 KiB), AllReduce 264.4 us at 8 KiB (285.1 at 12, 331.0 at 16);
+//   - sums with the inputs staged put R (+ 1 for the AllReduce's y part) parts
+//     in a slot and do best with a slot of about 48 KiB (ReduceScatter) or
+//     72 KiB (AllReduce) whatever R: at R = 8 the ReduceScatter runs 176.0 us at
+//     6 KiB (185.7 at 8, 231.0 at 12 KiB) and the AllReduce 264.4 us at 8 KiB
+//     (285.1 at 12, 331.0 at 16); at R = 2 82.5 us at 16 KiB (100.6 at 6) and
+//     118.1 us at 24 KiB (148.6 at 8); at R = 3 131.0 us at 12 KiB and 141.9 us
+//     at 16 KiB; at R = 4 114.4 us at 12 KiB and 167.0 us at 16 KiB;
 //   - sums with the reduced chunk staged put one part in a slot: ReduceScatter
-//     117.9 us at 16 KiB (121.4 at 24, 127.0 at 32 KiB), AllReduce 186.2 us at
-//     12 KiB (188.2 at 16, 189.9 at 24 KiB);
+//     117.9 us at 16 KiB (121.4 at 24, 127.0 at 32 KiB; 16 KiB is also best at
+//     R = 2, 3 and 4), AllReduce 186.2 us at 12 KiB (188.2 at 16, 189.9 at 24);
 //   - copies put one part in a slot: AllGather 104.7 us at 16 KiB (106.4 at 12,
 //     108.7 at 24, 114.5 at 32 KiB), AllToAllV 241.3 us at 48 KiB (247.0 at 32,
 //     254.1 at 64 KiB).
-size_t default_chunk(Coll coll, bool stage_y)
+size_t default_chunk(Coll coll, int R, bool stage_y)
 {
     const bool sum = coll == Coll::ReduceScatter || coll == Coll::AllReduce;
     if (stage_y && sum) return coll == Coll::ReduceScatter ? 16 * 1024 : 12 * 1024;
+    const size_t k512 = 512;
     switch (coll) {
     case Coll::AllGather: return 16 * 1024;
     case Coll::AllToAllV: return 48 * 1024;
-    case Coll::ReduceScatter: return 6 * 1024;
-    default: return 8 * 1024;
+    case Coll::ReduceScatter:
+        return std::min<size_t>(16 * 1024, (48 * 1024 / (size_t)R) / k512 * k512);
+    default: return (72 * 1024 / (size_t)(R + 1)) / k512 * k512;
     }
 }
 
@@ -973,7 +979,7 @@ purlin_status_t snac_geometry(int R, Coll coll, bool stage_y, const SnacConfig& 
         // spreads over every channel the GPU can hold (at least 1 KiB)
         const long target = std::max<long>(1, std::min<long>(resident_channels, kMaxChannels));
         const uint64_t spread = (total_bytes + (uint64_t)target - 1) / (uint64_t)target;
-        chunk = std::min<size_t>(default_chunk(coll, stage_y),
+        chunk = std::min<size_t>(default_chunk(coll, R, stage_y),
                                  std::max<size_t>(kMinAutoChunk, (size_t)spread));
     }
     chunk = std::max<size_t>(256, (chunk + 255) & ~(size_t)255);
